@@ -1,0 +1,574 @@
+#!/usr/bin/env python
+"""Benchmark of decode-step KV-cache attention on GB300.
+
+One step = one decode step of one attention layer for the whole batch:
+kvc_append of the new token's K/V (fused RoPE) followed by
+kvc_decode_attention (split-K attention + in-launch combine).  Steps cycle
+over `layers` cache layers so the working set (>= 1 GiB) is far larger than
+the 126 MiB L2: every step reads its KV from HBM.
+
+Prints one JSON line.  `value` = algorithmic bytes per step (attended K/V
+rows + q + out + the appended row) / device time per step, in GB/s;
+`roofline` relates the decode kernel's own time to the measured HBM copy peak;
+`e2e` repeats the metric with host-resident inputs copied in and the output
+copied out every step; `cpu_baseline` times the CPU oracle on a bounded
+sample.  `--impl reference` times the CPU oracle as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import kvc_synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "ring_bf16"
+DEFAULT_LAYERS = {"tiny_ring_sink_f32": 1, "ring_bf16": 8, "sink_window_bf16": 2,
+                  "paged_shared_prefix_bf16": 2, "long_context_pool_bf16": 4}
+
+
+def _kvc():
+    import sliding_window_attention_kvc_gb300 as kvc
+    return kvc
+
+
+# ---------------------------------------------------------------------------
+# workload -> library descriptor, algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def workload_desc(wl, layers=None, num_splits=0, batch=None):
+    kvc = _kvc()
+    L = wl.layers if layers is None else layers
+    B = wl.batch if batch is None else batch
+    if wl.layout == "window":
+        layout = "sink_ring" if wl.sinks > 0 else "ring"
+        return kvc.make_desc(layout, wl.rope, wl.dtype, L, B, wl.q_heads, wl.kv_heads, wl.head_dim,
+                             window=wl.window, sinks=wl.sinks, num_splits=num_splits, rope_base=wl.rope_base)
+    return kvc.make_desc("paged", wl.rope, wl.dtype, L, B, wl.q_heads, wl.kv_heads, wl.head_dim,
+                         block_size=wl.block_size, num_blocks=wl.num_blocks,
+                         max_blocks_per_seq=wl.max_blocks_per_seq, num_splits=num_splits,
+                         rope_base=wl.rope_base)
+
+
+def attended_rows(wl):
+    """Per sequence: number of cached rows the step at t_b attends, and for the
+    paged layout the (physical block -> rows read) map (for unique bytes)."""
+    t = wl.positions
+    if wl.layout == "window":
+        return np.minimum(t + 1, wl.capacity), None
+    rows = np.zeros(wl.batch, dtype=np.int64)
+    touched = {}
+    for b in range(wl.batch):
+        tb = int(t[b])
+        for lb in range(tb // wl.block_size + 1):
+            phys = int(wl.block_table[b, lb])
+            if phys < 0 or (wl.valid is not None and not wl.valid[phys]):
+                continue
+            n = wl.block_size if lb < tb // wl.block_size else tb - lb * wl.block_size + 1
+            rows[b] += n
+            touched[phys] = max(touched.get(phys, 0), n)
+    return rows, touched
+
+
+def step_bytes(wl):
+    """Algorithmic bytes of one decode step (whole batch, one layer)."""
+    rows, touched = attended_rows(wl)
+    row_bytes = wl.kv_heads * 2 * wl.head_dim * wl.elt_bytes     # K and V of one token
+    logical_kv = int(rows.sum()) * row_bytes
+    unique_kv = logical_kv if touched is None else sum(touched.values()) * row_bytes
+    qo = 2 * wl.batch * wl.q_heads * wl.head_dim * wl.elt_bytes   # q in, out
+    appended = 2 * wl.batch * wl.kv_heads * 2 * wl.head_dim * wl.elt_bytes  # new K/V read + written
+    return {"kv_logical": logical_kv, "kv_unique": unique_kv, "qo": qo, "append": appended,
+            "decode_algorithmic": unique_kv + qo, "step_algorithmic": unique_kv + qo + appended}
+
+
+# ---------------------------------------------------------------------------
+# cache set-up through kvc_append
+# ---------------------------------------------------------------------------
+
+def _raw_rows_device(shape, dtype, seed_key):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(kvc_synth.derive_seed(*seed_key))
+    return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(kvc_synth.to_dtype(dtype))
+
+
+def _window_fill_inputs(wl, layer, source):
+    """K/V rows for positions before t_b that the cache holds at step t_b:
+    sinks [0, min(S, t_b)) and the last W positions [t_b - W, t_b), both
+    left-padded to fixed lengths (negative positions are skipped by kvc_append)."""
+    calls = []
+    t = wl.positions
+    parts = [("sinks", wl.sinks, np.minimum(wl.sinks, t) - wl.sinks)] if wl.sinks > 0 else []
+    parts.append(("window", wl.window, t - wl.window))
+    for name, n, start in parts:
+        if source == "cpu":
+            k = torch.zeros((wl.batch, n, wl.kv_heads, wl.head_dim), dtype=kvc_synth.to_dtype(wl.dtype))
+            v = torch.zeros_like(k)
+            for b in range(wl.batch):
+                p = np.arange(start[b], start[b] + n)
+                keep = p >= 0
+                kb, vb = wl.kv_history(layer, b, p[keep])
+                k[b, keep] = kb
+                v[b, keep] = vb
+            k, v = k.cuda(), v.cuda()
+        else:
+            k = _raw_rows_device((wl.batch, n, wl.kv_heads, wl.head_dim), wl.dtype,
+                                 (wl.seed, layer, 101 if name == "sinks" else 102))
+            v = _raw_rows_device((wl.batch, n, wl.kv_heads, wl.head_dim), wl.dtype,
+                                 (wl.seed, layer, 103 if name == "sinks" else 104))
+        calls.append((k, v, torch.from_numpy(start.astype(np.int32)).cuda()))
+    return calls
+
+
+def _paged_runs(wl, b):
+    """Runs [p0, p1) of positions before t_b whose logical blocks are mapped."""
+    bs, tb = wl.block_size, int(wl.positions[b])
+    mapped = wl.block_table[b] >= 0
+    runs, lb, nlb = [], 0, tb // bs + 1
+    while lb < nlb:
+        if not mapped[lb]:
+            lb += 1
+            continue
+        lb1 = lb
+        while lb1 < nlb and mapped[lb1]:
+            lb1 += 1
+        p0, p1 = lb * bs, min(lb1 * bs, tb)
+        if p1 > p0:
+            runs.append((p0, p1))
+        lb = lb1
+    return runs
+
+
+class DecodeState:
+    """Device state of one workload: cache, workspace, per-layer step inputs."""
+
+    def __init__(self, wl, layers, source="device", num_splits=0, poison=True):
+        kvc = _kvc()
+        self.wl = wl
+        self.layers = layers
+        self.desc = workload_desc(wl, layers, num_splits)
+        self.cache = kvc.alloc_cache(self.desc, fill=float("nan") if poison else 0.0)
+        self.ws = kvc.alloc_workspace(self.desc)
+        self.pos = torch.from_numpy(wl.positions.astype(np.int32)).cuda()
+        self.table = None
+        self.valid_bits = None
+        if wl.layout == "paged":
+            self.table = torch.from_numpy(wl.block_table.astype(np.int32)).contiguous().cuda()
+            if wl.valid is not None:
+                self.valid_bits = kvc.pack_valid_bits(torch.from_numpy(wl.valid)).cuda()
+        self.q, self.k_new, self.v_new = [], [], []
+        for layer in range(layers):
+            self._fill_layer(layer, source)
+            if source == "cpu":
+                q = wl.queries(layer)
+                kn, vn = wl.new_kv(layer)
+            else:
+                q = _raw_rows_device((wl.batch, wl.q_heads, wl.head_dim), wl.dtype, (wl.seed, layer, 105))
+                kn = _raw_rows_device((wl.batch, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, 106))
+                vn = _raw_rows_device((wl.batch, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, 107))
+            self.q.append(q.contiguous().cuda())
+            self.k_new.append(kn.contiguous().cuda())
+            self.v_new.append(vn.contiguous().cuda())
+        if wl.layout == "paged" and wl.valid is not None and poison:
+            # non-resident slots hold no data: poison them, they must never be read
+            bad = torch.from_numpy(~wl.valid).cuda()
+            self.cache[:, :, bad] = float("nan")
+        self.out = torch.empty((wl.batch, wl.q_heads, wl.head_dim), dtype=kvc.desc_dtype(self.desc),
+                               device="cuda")
+        torch.cuda.synchronize()
+        err = kvc.get_error(self.ws)
+        if err:
+            raise RuntimeError(f"device error bits {err:#x} while filling the cache")
+
+    def _fill_layer(self, layer, source):
+        kvc = _kvc()
+        wl = self.wl
+        if wl.layout == "window":
+            for k, v, start in _window_fill_inputs(wl, layer, source):
+                kvc.append(self.desc, self.cache, layer, k, v, start, self.ws)
+            return
+        d1 = workload_desc(wl, self.layers, batch=1)
+        ws1 = kvc.alloc_workspace(d1)
+        elt = self.table.element_size()
+        for b in range(wl.batch):
+            row_ptr = self.table.data_ptr() + b * wl.max_blocks_per_seq * elt
+            for p0, p1 in _paged_runs(wl, b):
+                n = p1 - p0
+                if source == "cpu":
+                    k, v = wl.kv_history(layer, b, np.arange(p0, p1))
+                    k, v = k[None].cuda(), v[None].cuda()
+                else:
+                    k = _raw_rows_device((1, n, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, b, p0, 108))
+                    v = _raw_rows_device((1, n, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, b, p0, 109))
+                start = torch.tensor([p0], dtype=torch.int32, device="cuda")
+                rc = kvc.lib().kvc_append(ctypes.byref(d1), self.cache.data_ptr(), layer, k.data_ptr(),
+                                          v.data_ptr(), n, start.data_ptr(), row_ptr, ws1.data_ptr(),
+                                          ws1.numel(), torch.cuda.current_stream().cuda_stream)
+                if rc != 0:
+                    raise kvc.KvcError(rc, "kvc_append (fill)")
+        torch.cuda.synchronize()
+        if kvc.get_error(ws1):
+            raise RuntimeError("device error while filling the paged cache")
+
+    # one decode step on `layer`, through the C ABI with device buffers
+    def step(self, layer, out=None):
+        kvc = _kvc()
+        kvc.append(self.desc, self.cache, layer, self.k_new[layer], self.v_new[layer], self.pos, self.ws,
+                   block_table=self.table)
+        return kvc.decode_attention(self.desc, self.cache, layer, self.q[layer], self.pos, self.ws,
+                                    block_table=self.table, valid_bits=self.valid_bits,
+                                    out=self.out if out is None else out)
+
+
+class FastCalls:
+    """Pre-marshalled ctypes calls of kvc_append / kvc_decode_attention for the
+    timed loop (same C entry points as the binding, minus per-call checks)."""
+
+    def __init__(self, st: DecodeState):
+        kvc = _kvc()
+        L = kvc.lib()
+        self.L = L
+        s = torch.cuda.current_stream().cuda_stream
+        d = ctypes.byref(st.desc)
+        tb = st.table.data_ptr() if st.table is not None else None
+        vb = st.valid_bits.data_ptr() if st.valid_bits is not None else None
+        ws, wsn = st.ws.data_ptr(), st.ws.numel()
+        self.app = [(d, st.cache.data_ptr(), l, st.k_new[l].data_ptr(), st.v_new[l].data_ptr(), 1,
+                     st.pos.data_ptr(), tb, ws, wsn, s) for l in range(st.layers)]
+        self.dec = [(d, st.cache.data_ptr(), l, st.q[l].data_ptr(), st.pos.data_ptr(), tb, vb,
+                     st.out.data_ptr(), ws, wsn, s) for l in range(st.layers)]
+
+    def append(self, layer):
+        rc = self.L.kvc_append(*self.app[layer])
+        if rc:
+            raise RuntimeError(f"kvc_append: {rc}")
+
+    def decode(self, layer):
+        rc = self.L.kvc_decode_attention(*self.dec[layer])
+        if rc:
+            raise RuntimeError(f"kvc_decode_attention: {rc}")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0, period_ms=50):
+        self.proc = None
+        self.lines = []
+        self.device_index = device_index
+        self.period_ms = period_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a timed baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, budget_s, max_rows=None):
+    """Run the CPU oracle on (sequence, kv head) units of layer 0 until
+    `budget_s` seconds of oracle time are spent; returns (bytes, seconds, desc)."""
+    import oracle
+    spec = dict(rope=wl.rope, base=wl.rope_base, storage=wl.dtype, sinks=wl.sinks, window=wl.window)
+    row_bytes = 2 * wl.head_dim * wl.elt_bytes
+    g = wl.group_size
+    done_bytes, spent, units = 0, 0.0, 0
+    for b in range(wl.batch):
+        t = int(wl.positions[b])
+        if wl.layout == "window":
+            pos = oracle.window_attended(t, wl.sinks, wl.window)
+        else:
+            pos = oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size)
+        if max_rows is not None:
+            pos = pos[-max_rows:]
+        k, v = wl.kv_history(0, b, pos)
+        q = wl.query(0, b)
+        for h in range(wl.kv_heads):
+            qf = q[h * g:(h + 1) * g].double().numpy()
+            kf, vf = k[:, h].double().numpy(), v[:, h].double().numpy()
+            t0 = time.perf_counter()
+            oracle.decode_reference(qf, kf, vf, pos, t, **spec)
+            spent += time.perf_counter() - t0
+            done_bytes += len(pos) * row_bytes
+            units += 1
+            if spent >= budget_s:
+                return done_bytes, spent, units
+    return done_bytes, spent, units
+
+
+def cpu_baseline(wl, budget_s=10.0):
+    nbytes, secs, units = oracle_sample(wl, budget_s)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units} (sequence, kv head) units of one layer-step of {wl.name}, "
+                      f"{nbytes / 1e6:.1f} MB of attended K/V, {secs:.1f} s single-threaded fp64"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return None
+    wl = kvc_synth.make_workload(args.workload)
+    per_step = max(0.002, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    # rows per step sized to the per-step budget (about 25k rows/s for D=128)
+    rows = max(64, int(per_step * 25000 * 128 / wl.head_dim))
+    for _ in range(args.warmup):
+        oracle_sample(wl, per_step, max_rows=rows)
+    tot_b, tot_s, tot_u = 0, 0.0, 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        b, s, u = oracle_sample(wl, per_step, max_rows=rows)
+        tot_b, tot_s, tot_u = tot_b + b, tot_s + s, tot_u + u
+    wall = time.perf_counter() - t0
+    val = tot_b / tot_s / 1e9
+    return {"impl": "reference", "metric": "decode-attention KV GB/s", "value": val, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_s / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: up to {rows} attended rows of (sequence, kv head) units, "
+                                       f"~{per_step:.3f} s of fp64 oracle time; {tot_u} units, wall {wall:.1f} s"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args):
+    kvc = _kvc()
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    wl = kvc_synth.make_workload(args.workload)
+    layers = args.layers or DEFAULT_LAYERS[args.workload]
+    st = DecodeState(wl, layers, source="device", num_splits=args.num_splits)
+    fc = FastCalls(st)
+    nb = step_bytes(wl)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up
+    for i in range(args.warmup):
+        fc.append(i % layers)
+        fc.decode(i % layers)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)      # ~10 ms head start: the host enqueues ahead of the GPU
+    start.record()
+    for i in range(K):
+        layer = i % layers
+        fc.append(layer)
+        ev[i][0].record()
+        fc.decode(layer)
+        ev[i][1].record()
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * nb["step_algorithmic"] / (ms_per_step * 1e-3) / 1e9
+    dec_mean = sum(dec_ms) / len(dec_ms)
+    achieved = nb["decode_algorithmic"] / (dec_mean * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    err = kvc.get_error(st.ws)
+    if err:
+        raise RuntimeError(f"device error bits {err:#x} during the timed region")
+
+    # end to end: host inputs copied in, host output copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(st, fc, args, nb)
+
+    line = {
+        "metric": "decode-attention KV HBM GB/s",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
+                   "head_dim": wl.head_dim, "window": wl.window, "sinks": wl.sinks,
+                   "block_size": wl.block_size, "layers_cycled": layers, "rope": wl.rope,
+                   "l2": f"inputs larger than L2: {layers} layers cycled, "
+                         f"{layers * nb['kv_unique'] / 2**20:.0f} MiB of attended K/V",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "steps_per_s": 1e3 / ms_per_step,
+        "bytes_per_step": nb,
+        "decode_kernel_ms": dec_mean,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": args.traffic, "kernel": "decode_kernel",
+                     "algorithmic_bytes_per_launch": nb["decode_algorithmic"]},
+        "frac_of_8tbs": value / 8000.0,
+        "clocks": clk,
+        "gpu_launches": 2 * K + (K if wl.layout == "paged" else 0),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def run_e2e(st, fc, args, nb):
+    wl = st.wl
+    layers = st.layers
+    K = max(10, min(args.steps, 2000))
+    hq = [st.q[l].cpu().pin_memory() for l in range(layers)]
+    hk = [st.k_new[l].cpu().pin_memory() for l in range(layers)]
+    hv = [st.v_new[l].cpu().pin_memory() for l in range(layers)]
+    hp = st.pos.cpu().pin_memory()
+    hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = hq[0].numel() * hq[0].element_size() + 2 * hk[0].numel() * hk[0].element_size() + \
+        hp.numel() * hp.element_size()
+    d2h = hout.numel() * hout.element_size()
+    for i in range(3):
+        _e2e_step(st, fc, i % layers, hq, hk, hv, hp, hout)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(K):
+        _e2e_step(st, fc, i % layers, hq, hk, hv, hp, hout)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / K
+    return {"value": nb["step_algorithmic"] / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "per step: pinned host q/k/v/pos -> device, append + attention, out -> pinned host, "
+                    "host waits for the result"}
+
+
+def _e2e_step(st, fc, layer, hq, hk, hv, hp, hout):
+    st.q[layer].copy_(hq[layer], non_blocking=True)
+    st.k_new[layer].copy_(hk[layer], non_blocking=True)
+    st.v_new[layer].copy_(hv[layer], non_blocking=True)
+    st.pos.copy_(hp, non_blocking=True)
+    fc.append(layer)
+    fc.decode(layer)
+    hout.copy_(st.out, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(kvc_synth.WORKLOAD_NAMES), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per decode launch from an ncu capture of the current kernel")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * kvc.h - C ABI of the decode-step KV-cache attention library (libkvc.so).
+ *
+ * One new query per sequence attends over a fixed-capacity KV cache kept in
+ * one of three layouts, and the new token's K/V is appended to that cache.
+ * The operations follow these pages (cited by title and section):
+ *
+ *   [ring]   "Why sliding-window attention decodes with a ring KV cache"
+ *            (2kiu.com/news/4318096)
+ *   [share]  "Shared state, isolated problems: KV cache and batching"
+ *            (pwwt.cn/news/6215824)
+ *   [sink]   "Attention sinks and StreamingLLM" (openeuler.csdn.net)
+ *   [primer] "KV cache primer" (pwwt.cn/news/5010196)
+ *   [pool]   "KV cache paging" (cloudlnk.cn/blog/kv-cache-paging)
+ *
+ * Conventions shared by every entry point
+ *   - Every buffer argument is a DEVICE pointer owned by the caller (cache,
+ *     queries, outputs, tables, workspace); the library allocates nothing and
+ *     keeps no state between calls.  `stream` is a cudaStream_t (NULL = the
+ *     legacy default stream); every call except kvc_get_error only enqueues
+ *     work on it and returns.
+ *   - Return value: KVC_OK (0) or a negative KVC_ERR_* code.  On a negative
+ *     code nothing was launched.  Errors that only the device can see (a
+ *     block id out of range, an append into an unmapped block, a bad
+ *     position) set bits in the workspace's error word; the kernel skips the
+ *     offending access and carries on.  kvc_get_error() reads and clears them.
+ *   - Element types: the cache, q, out, k_new and v_new share one element
+ *     type (kvc_desc.dtype).  All arithmetic is fp32.
+ *   - Alignment: cache, q, out, k_new, v_new and workspace must be 16-byte
+ *     aligned (KVC_ERR_ALIGN otherwise).
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+/* Cache layouts.
+ *  RING       [ring] 3.2-3.3, 5.1: W slots per (sequence, kv head); token p
+ *             goes to slot p mod W.  Token t attends t-W+1 .. t ([ring] 2.2,
+ *             6), itself included.
+ *  SINK_RING  [sink] cache-set equation: S pinned sink slots, then a W-slot
+ *             ring.  Token p goes to slot p (p < S) or S + ((p - S) mod W).
+ *             Token t attends {0 .. S-1} U {t-W+1 .. t}.
+ *  PAGED      [share] 3.1-3.2, [pool] "kernel forgets absent blocks": a pool
+ *             of fixed-size blocks; block_table[b][p / block_size] names the
+ *             physical block of token p (-1 = not mapped); a per-block valid
+ *             bit drops non-resident blocks.  Token t attends every p <= t
+ *             whose block is mapped and valid. */
+typedef enum { KVC_LAYOUT_RING = 0, KVC_LAYOUT_SINK_RING = 1, KVC_LAYOUT_PAGED = 2 } kvc_layout;
+
+/* RoPE handling (rotate-half pairs (i, i + D/2), theta_i = base^(-2i/D)).
+ *  NONE          no rotation.
+ *  BAKED         [primer] 4.5, [pool] "RoPE baked into K rows": K is rotated
+ *                at its absolute position when appended; q is rotated at t.
+ *  READ_INCACHE  [sink] "RoPE cache position shifting": K is stored raw and
+ *                rotated when read, at its index in the compacted cache
+ *                (sinks 0..S-1; window token p at p - max(0, t - C + 1),
+ *                C = S + W); q at min(t, C - 1).  RING and SINK_RING only. */
+typedef enum { KVC_ROPE_NONE = 0, KVC_ROPE_BAKED = 1, KVC_ROPE_READ_INCACHE = 2 } kvc_rope;
+
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
+
+/* Cache geometry.  Cache memory layout ([primer] 3.1, K at index 0, V at 1):
+ *   RING / SINK_RING: [layers, 2, batch, kv_heads, capacity, head_dim],
+ *                     capacity = sinks + window;
+ *   PAGED:            [layers, 2, num_blocks, kv_heads, block_size, head_dim].
+ * q_heads must be a multiple of kv_heads; q head h reads kv head
+ * h / (q_heads / kv_heads) ([share] 2.2 and 4.1, grouped-query attention). */
+typedef struct kvc_desc {
+    int32_t layout;             /* kvc_layout */
+    int32_t rope;               /* kvc_rope */
+    int32_t dtype;              /* kvc_dtype */
+    int32_t layers;
+    int32_t batch;              /* sequences (rows of block_table for PAGED) */
+    int32_t q_heads;
+    int32_t kv_heads;
+    int32_t head_dim;           /* 64, 128 or 256 */
+    int32_t window;             /* RING / SINK_RING: W */
+    int32_t sinks;              /* SINK_RING: S >= 1; RING: 0 */
+    int32_t block_size;         /* PAGED */
+    int32_t num_blocks;         /* PAGED: physical blocks in the pool */
+    int32_t max_blocks_per_seq; /* PAGED: columns of block_table */
+    int32_t num_splits;         /* 0 = library choice; else KV splits per (sequence, kv head)
+                                   for RING / SINK_RING, work items for PAGED */
+    float rope_base;            /* e.g. 10000 */
+    float softmax_scale;        /* 0 => 1 / sqrt(head_dim) */
+} kvc_desc;
+
+/* Host-detected status codes (nothing launched). */
+#define KVC_OK 0
+#define KVC_ERR_NULL (-1)        /* a required pointer is NULL */
+#define KVC_ERR_DESC (-2)        /* inconsistent descriptor */
+#define KVC_ERR_UNSUPPORTED (-3) /* combination not built (e.g. PAGED + READ_INCACHE) */
+#define KVC_ERR_ALIGN (-4)       /* pointer not 16-byte aligned */
+#define KVC_ERR_WORKSPACE (-5)   /* workspace smaller than kvc_workspace_bytes() */
+#define KVC_ERR_ARG (-6)         /* argument out of range (layer, n_new, n) */
+#define KVC_ERR_CUDA (-7)        /* a CUDA runtime call or launch failed */
+
+/* Device-detected error bits, returned by kvc_get_error(). */
+#define KVC_DEV_BAD_BLOCK 0x1u       /* block_table entry >= num_blocks (access skipped) */
+#define KVC_DEV_UNMAPPED_APPEND 0x2u /* append into a logical block whose entry is -1 */
+#define KVC_DEV_BAD_POSITION 0x4u    /* decode position < 0, or beyond the block table */
+#define KVC_DEV_TIMEOUT 0x8u         /* a bounded wait inside a kernel gave up */
+#define KVC_DEV_BAD_ENTRY 0x10u      /* kvc_block_table_write / kvc_valid_write entry out of range */
+
+/* Bytes of the cache tensor described by `d` (0 if `d` is invalid). */
+KVC_API size_t kvc_cache_bytes(const kvc_desc* d);
+
+/* Bytes of workspace that kvc_append / kvc_decode_attention /
+ * kvc_block_table_write / kvc_valid_write need for `d` (0 if `d` is invalid).
+ * The workspace holds the device error word, split-K partial results and
+ * per-(sequence, kv head) completion counters.  It must be zero-filled once
+ * before first use (kvc_workspace_init); every call leaves it ready for the
+ * next one.  Calls that share a workspace must not overlap on the GPU. */
+KVC_API size_t kvc_workspace_bytes(const kvc_desc* d);
+
+/* Zero-fill `workspace` (cudaMemsetAsync on `stream`). */
+KVC_API int kvc_workspace_init(const kvc_desc* d, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Append n_new tokens per sequence to layer `layer` of the cache
+ * ([ring] 3.3 and 5.1, [primer] 4.4: write in place, no allocation).
+ *   k_new, v_new  [batch, n_new, kv_heads, head_dim], pre-RoPE.
+ *   pos           [batch] int32: position of token 0 of each sequence; token
+ *                 i is at pos[b] + i.  Tokens at negative positions are
+ *                 skipped (left padding).
+ *   block_table   PAGED: [batch, max_blocks_per_seq] int32; else NULL.
+ * BAKED rotates K at its absolute position (angle reduced in fp64, rotated in
+ * fp32, stored rounded to nearest-even); V is never rotated ([pool]).  For
+ * RING / SINK_RING the cache ends as if the tokens were appended one at a
+ * time in order: a token that a later token of the same call overwrites is
+ * not written.  Ring appends must come in position order, one call per step,
+ * before the attention call that reads them.  PAGED: an unmapped target
+ * block sets KVC_DEV_UNMAPPED_APPEND; a block shared by several sequences
+ * must be copied first by the caller (copy-on-write, [share] 3.2). */
+KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer,
+                       const void* k_new, const void* v_new, int32_t n_new,
+                       const int32_t* pos, const int32_t* block_table,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Decode attention for one layer ([primer] 2.2 and 4.2, [sink] softmax
+ * equations): out = softmax(q . K^T * scale) . V over the attended set of
+ * each sequence, fp32 online softmax, split over the KV length and combined
+ * in the same launch.
+ *   q       [batch, q_heads, head_dim], pre-RoPE.
+ *   pos     [batch] int32: position t of the token being decoded (already
+ *           appended, so t attends to itself; [ring] 4.3).
+ *   block_table, valid_bits  PAGED only (else NULL): block_table as in
+ *           kvc_append; valid_bits [ceil(num_blocks / 32)] uint32, bit
+ *           (k & 31) of word k / 32 set when physical block k is resident.
+ *           valid_bits NULL = every block resident.
+ *   out     [batch, q_heads, head_dim], same element type as q.
+ * An empty attended set (a fully masked PAGED sequence) gives zeros. */
+KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t layer,
+                                 const void* q, const int32_t* pos,
+                                 const int32_t* block_table, const uint32_t* valid_bits,
+                                 void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Batched block-table update ([share] 3.1 block table, 5.1 block manager):
+ * for each i < n, block_table[seq[i]][logical_block[i]] = physical_block[i];
+ * -1 unmaps.  When valid_bits is not NULL, each mapped physical block gets its
+ * valid bit set (the data is in place); unmapping does not touch valid bits,
+ * since other sequences may still map that block.  Entries out of range set
+ * KVC_DEV_BAD_ENTRY and are skipped.  Two entries naming the same
+ * (seq, logical_block) in one call: which one lands is unspecified. */
+KVC_API int kvc_block_table_write(const kvc_desc* d, int32_t* block_table, uint32_t* valid_bits,
+                                  int32_t n, const int32_t* seq, const int32_t* logical_block,
+                                  const int32_t* physical_block,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Batched residency update ([pool] "kernel forgets absent blocks"): for each
+ * i < n, set (value[i] != 0) or clear the valid bit of physical block slot[i]. */
+KVC_API int kvc_valid_write(const kvc_desc* d, uint32_t* valid_bits, int32_t n,
+                            const int32_t* slot, const int32_t* value,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Wait for `stream`, then return the workspace's device error bits
+ * (KVC_DEV_*, 0 = none) and clear them.  Negative KVC_ERR_* on failure. */
+KVC_API int kvc_get_error(void* workspace, void* stream);
+
+/* Static description of a status code or device error bit. */
+KVC_API const char* kvc_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

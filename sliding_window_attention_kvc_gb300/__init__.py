@@ -1,0 +1,271 @@
+"""Decode-step KV-cache attention on GB300: Python binding of libkvc.so.
+
+Thin ctypes wrappers with the names of the C ABI in include/kvc.h.  They only
+marshal arguments (torch tensors -> device pointers, the current CUDA stream)
+and raise `KvcError` on a non-zero status; every step of the computation runs
+in the library's CUDA kernels.  There is no CPU fallback: if libkvc.so is
+missing or cannot be loaded, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+LAYOUTS = {"ring": 0, "sink_ring": 1, "paged": 2}
+ROPES = {"none": 0, "baked": 1, "read_time": 2}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+DTYPE_NAMES = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+KVC_OK = 0
+KVC_ERR_NULL, KVC_ERR_DESC, KVC_ERR_UNSUPPORTED = -1, -2, -3
+KVC_ERR_ALIGN, KVC_ERR_WORKSPACE, KVC_ERR_ARG, KVC_ERR_CUDA = -4, -5, -6, -7
+KVC_DEV_BAD_BLOCK, KVC_DEV_UNMAPPED_APPEND, KVC_DEV_BAD_POSITION = 0x1, 0x2, 0x4
+KVC_DEV_TIMEOUT, KVC_DEV_BAD_ENTRY = 0x8, 0x10
+
+ABI_FUNCTIONS = (
+    "kvc_cache_bytes", "kvc_workspace_bytes", "kvc_workspace_init", "kvc_append",
+    "kvc_decode_attention", "kvc_block_table_write", "kvc_valid_write", "kvc_get_error",
+    "kvc_strerror",
+)
+
+
+class KvcDesc(ctypes.Structure):
+    """Mirror of `kvc_desc` in include/kvc.h."""
+    _fields_ = [
+        ("layout", ctypes.c_int32), ("rope", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("layers", ctypes.c_int32), ("batch", ctypes.c_int32), ("q_heads", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32),
+        ("sinks", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+        ("rope_base", ctypes.c_float), ("softmax_scale", ctypes.c_float),
+    ]
+
+
+class KvcError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: kvc status {code} ({strerror(code)})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvc.so (built in-tree by build.py); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not built: run sliding_window_attention_kvc_gb300/build.py "
+                               "(or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        dp = ctypes.POINTER(KvcDesc)
+        L.kvc_cache_bytes.argtypes = [dp]
+        L.kvc_cache_bytes.restype = sz
+        L.kvc_workspace_bytes.argtypes = [dp]
+        L.kvc_workspace_bytes.restype = sz
+        L.kvc_workspace_init.argtypes = [dp, vp, sz, vp]
+        L.kvc_append.argtypes = [dp, vp, i32, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.kvc_decode_attention.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.kvc_block_table_write.argtypes = [dp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.kvc_valid_write.argtypes = [dp, vp, i32, vp, vp, vp, sz, vp]
+        L.kvc_get_error.argtypes = [vp, vp]
+        L.kvc_strerror.argtypes = [ctypes.c_int]
+        L.kvc_strerror.restype = ctypes.c_char_p
+        for name in ABI_FUNCTIONS:
+            if name not in ("kvc_cache_bytes", "kvc_workspace_bytes", "kvc_strerror"):
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().kvc_strerror(int(code)).decode()
+    except Exception:  # the library itself is unavailable
+        return "unknown"
+
+
+def make_desc(layout: str, rope: str, dtype, layers: int, batch: int, q_heads: int, kv_heads: int,
+              head_dim: int, window: int = 0, sinks: int = 0, block_size: int = 0, num_blocks: int = 0,
+              max_blocks_per_seq: int = 0, num_splits: int = 0, rope_base: float = 10000.0,
+              softmax_scale: float = 0.0) -> KvcDesc:
+    if isinstance(dtype, str):
+        dtype = DTYPE_NAMES[dtype]
+    return KvcDesc(LAYOUTS[layout], ROPES[rope], DTYPES[dtype], layers, batch, q_heads, kv_heads, head_dim,
+                   window, sinks, block_size, num_blocks, max_blocks_per_seq, num_splits,
+                   float(rope_base), float(softmax_scale))
+
+
+def desc_dtype(d: KvcDesc) -> torch.dtype:
+    return torch.float32 if d.dtype == 0 else torch.bfloat16
+
+
+def cache_shape(d: KvcDesc) -> tuple:
+    """[layers, 2, batch, kv_heads, sinks + window, D] or [layers, 2, num_blocks, kv_heads, block_size, D]."""
+    if d.layout == LAYOUTS["paged"]:
+        return (d.layers, 2, d.num_blocks, d.kv_heads, d.block_size, d.head_dim)
+    return (d.layers, 2, d.batch, d.kv_heads, d.window + d.sinks, d.head_dim)
+
+
+def cache_bytes(d: KvcDesc) -> int:
+    return int(lib().kvc_cache_bytes(ctypes.byref(d)))
+
+
+def workspace_bytes(d: KvcDesc) -> int:
+    return int(lib().kvc_workspace_bytes(ctypes.byref(d)))
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise KvcError(rc, what)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, numel=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+
+
+def alloc_cache(d: KvcDesc, device="cuda", fill=None) -> torch.Tensor:
+    """Caller-owned cache tensor of the layout's shape (uninitialised unless `fill`)."""
+    shape = cache_shape(d)
+    if fill is None:
+        return torch.empty(shape, dtype=desc_dtype(d), device=device)
+    return torch.full(shape, fill, dtype=desc_dtype(d), device=device)
+
+
+def alloc_workspace(d: KvcDesc, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace of kvc_workspace_bytes(d) bytes."""
+    n = workspace_bytes(d)
+    if n == 0:
+        raise KvcError(KVC_ERR_DESC, "kvc_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def workspace_init(d: KvcDesc, workspace: torch.Tensor, stream=None):
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib().kvc_workspace_init(ctypes.byref(d), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvc_workspace_init")
+
+
+def append(d: KvcDesc, cache: torch.Tensor, layer: int, k_new: torch.Tensor, v_new: torch.Tensor,
+           pos: torch.Tensor, workspace: torch.Tensor, block_table: torch.Tensor | None = None, stream=None):
+    """kvc_append: k_new / v_new [batch, n_new, kv_heads, D] (or [batch, kv_heads, D] for one token)."""
+    dt = desc_dtype(d)
+    _need(cache, "cache", dt)
+    _need(k_new, "k_new", dt)
+    _need(v_new, "v_new", dt)
+    _need(pos, "pos", torch.int32, d.batch)
+    _need(workspace, "workspace", torch.uint8)
+    per_tok = d.kv_heads * d.head_dim
+    if k_new.numel() % (d.batch * per_tok) or v_new.numel() != k_new.numel():
+        raise ValueError("k_new / v_new must be [batch, n_new, kv_heads, head_dim]")
+    n_new = k_new.numel() // (d.batch * per_tok)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, d.batch * d.max_blocks_per_seq)
+    _check(lib().kvc_append(ctypes.byref(d), _ptr(cache), int(layer), _ptr(k_new), _ptr(v_new), int(n_new),
+                            _ptr(pos), _ptr(block_table), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvc_append")
+
+
+def decode_attention(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, pos: torch.Tensor,
+                     workspace: torch.Tensor, block_table: torch.Tensor | None = None,
+                     valid_bits: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """kvc_decode_attention: q [batch, q_heads, D] -> out [batch, q_heads, D]."""
+    dt = desc_dtype(d)
+    _need(cache, "cache", dt)
+    _need(q, "q", dt, d.batch * d.q_heads * d.head_dim)
+    _need(pos, "pos", torch.int32, d.batch)
+    _need(workspace, "workspace", torch.uint8)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, d.batch * d.max_blocks_per_seq)
+    if valid_bits is not None:
+        _need(valid_bits, "valid_bits", torch.int32, (d.num_blocks + 31) // 32)
+    if out is None:
+        out = torch.empty((d.batch, d.q_heads, d.head_dim), dtype=dt, device=q.device)
+    _need(out, "out", dt, d.batch * d.q_heads * d.head_dim)
+    _check(lib().kvc_decode_attention(ctypes.byref(d), _ptr(cache), int(layer), _ptr(q), _ptr(pos),
+                                      _ptr(block_table), _ptr(valid_bits), _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)),
+           "kvc_decode_attention")
+    return out
+
+
+def block_table_write(d: KvcDesc, block_table: torch.Tensor, seq: torch.Tensor, logical_block: torch.Tensor,
+                      physical_block: torch.Tensor, workspace: torch.Tensor,
+                      valid_bits: torch.Tensor | None = None, stream=None):
+    n = seq.numel()
+    _need(block_table, "block_table", torch.int32, d.batch * d.max_blocks_per_seq)
+    for name, t in (("seq", seq), ("logical_block", logical_block), ("physical_block", physical_block)):
+        _need(t, name, torch.int32, n)
+    if valid_bits is not None:
+        _need(valid_bits, "valid_bits", torch.int32, (d.num_blocks + 31) // 32)
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib().kvc_block_table_write(ctypes.byref(d), _ptr(block_table), _ptr(valid_bits), int(n), _ptr(seq),
+                                       _ptr(logical_block), _ptr(physical_block), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)),
+           "kvc_block_table_write")
+
+
+def valid_write(d: KvcDesc, valid_bits: torch.Tensor, slot: torch.Tensor, value: torch.Tensor,
+                workspace: torch.Tensor, stream=None):
+    n = slot.numel()
+    _need(valid_bits, "valid_bits", torch.int32, (d.num_blocks + 31) // 32)
+    _need(slot, "slot", torch.int32, n)
+    _need(value, "value", torch.int32, n)
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib().kvc_valid_write(ctypes.byref(d), _ptr(valid_bits), int(n), _ptr(slot), _ptr(value),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvc_valid_write")
+
+
+def get_error(workspace: torch.Tensor, stream=None) -> int:
+    """Device error bits (KVC_DEV_*) since the last call; synchronises the stream and clears them."""
+    _need(workspace, "workspace", torch.uint8)
+    rc = lib().kvc_get_error(_ptr(workspace), _stream(stream))
+    if rc < 0:
+        raise KvcError(rc, "kvc_get_error")
+    return rc
+
+
+def pack_valid_bits(mask: torch.Tensor) -> torch.Tensor:
+    """bool [num_blocks] -> int32 words, bit (k & 31) of word k // 32 = mask[k] (the layout valid_bits uses)."""
+    m = mask.to(torch.int64).flatten()
+    n = m.numel()
+    words = (n + 31) // 32
+    pad = torch.zeros(words * 32, dtype=torch.int64, device=m.device)
+    pad[:n] = m
+    w = (pad.view(words, 32) << torch.arange(32, device=m.device, dtype=torch.int64)).sum(dim=1)
+    w = torch.where(w >= 2 ** 31, w - 2 ** 32, w)
+    return w.to(torch.int32)

@@ -1,0 +1,19 @@
+// Explicit instantiation of the decode launchers for one element type and
+// layout family; included by the decode_*.cu translation units so the heavy
+// template code compiles in parallel.
+#pragma once
+#include "kvc_decode.cuh"
+
+#define KVC_INST(E, D, GH, PG, RD) \
+    template cudaError_t kvc::launch_decode_t<E, D, GH, PG, RD>(const kvc::DecodeParams&, dim3, cudaStream_t);
+
+#define KVC_INST_ALL_D(E, PG, RD)   \
+    KVC_INST(E, 64, 1, PG, RD)      \
+    KVC_INST(E, 64, 2, PG, RD)      \
+    KVC_INST(E, 64, 4, PG, RD)      \
+    KVC_INST(E, 128, 1, PG, RD)     \
+    KVC_INST(E, 128, 2, PG, RD)     \
+    KVC_INST(E, 128, 4, PG, RD)     \
+    KVC_INST(E, 256, 1, PG, RD)     \
+    KVC_INST(E, 256, 2, PG, RD)     \
+    KVC_INST(E, 256, 4, PG, RD)

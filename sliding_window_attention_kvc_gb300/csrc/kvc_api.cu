@@ -1,0 +1,358 @@
+// Host side of the C ABI declared in include/kvc.h: descriptor checks,
+// workspace carve-up, launch configuration and dispatch to the kernels.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include <cuda_bf16.h>
+
+#include "kvc.h"
+#include "kvc_params.h"
+
+namespace kvc {
+
+template <typename Elt, int D, int GH, bool PAGED, bool READ>
+cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t stream);
+
+namespace {
+
+struct Geo {
+    int elt;        // bytes per element
+    int C;          // window layouts: slots per (sequence, kv head)
+    int G, GH, nsub;
+    long long half_elems;   // elements of one K (or V) half of one layer
+};
+
+int rows_per_stage(int elt, int D) { return 8192 / (D * elt); }
+
+int check_desc(const kvc_desc* d, Geo* g) {
+    if (!d) return KVC_ERR_NULL;
+    if (d->layout < 0 || d->layout > 2 || d->rope < 0 || d->rope > 2 || d->dtype < 0 || d->dtype > 1)
+        return KVC_ERR_DESC;
+    if (d->layers < 1 || d->batch < 1 || d->kv_heads < 1 || d->q_heads < 1 || d->q_heads % d->kv_heads)
+        return KVC_ERR_DESC;
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return KVC_ERR_UNSUPPORTED;
+    if (d->num_splits < 0) return KVC_ERR_DESC;
+    if (d->rope != KVC_ROPE_NONE && !(d->rope_base > 0.f)) return KVC_ERR_DESC;
+    if (d->softmax_scale < 0.f) return KVC_ERR_DESC;
+    g->elt = d->dtype == KVC_F32 ? 4 : 2;
+    g->G = d->q_heads / d->kv_heads;
+    g->GH = (g->G % 4 == 0) ? 4 : ((g->G % 2 == 0) ? 2 : 1);
+    g->nsub = g->G / g->GH;
+    if (d->batch > 65535 || d->kv_heads > 65535 || g->nsub > 65535) return KVC_ERR_DESC;
+    if (d->layout == KVC_LAYOUT_PAGED) {
+        if (d->block_size < 1 || d->num_blocks < 1 || d->max_blocks_per_seq < 1) return KVC_ERR_DESC;
+        if ((long long)d->block_size * d->max_blocks_per_seq > 0x7fffffffLL) return KVC_ERR_DESC;
+        if (d->rope == KVC_ROPE_READ_INCACHE) return KVC_ERR_UNSUPPORTED;
+        g->C = 0;
+        g->half_elems = (long long)d->num_blocks * d->kv_heads * d->block_size * d->head_dim;
+    } else {
+        if (d->window < 1) return KVC_ERR_DESC;
+        if (d->layout == KVC_LAYOUT_RING && d->sinks != 0) return KVC_ERR_DESC;
+        if (d->layout == KVC_LAYOUT_SINK_RING && d->sinks < 1) return KVC_ERR_DESC;
+        if ((long long)d->window + d->sinks > 0x3fffffffLL) return KVC_ERR_DESC;
+        g->C = d->window + d->sinks;
+        g->half_elems = (long long)d->batch * d->kv_heads * g->C * d->head_dim;
+    }
+    return KVC_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
+    WorkspaceLayout w{};
+    const int units = d->batch * d->kv_heads * g.nsub;
+    if (d->layout == KVC_LAYOUT_PAGED) {
+        const int target = (kTargetCtas + d->kv_heads * g.nsub - 1) / (d->kv_heads * g.nsub);
+        w.items = d->num_splits > 0 ? (d->num_splits > d->batch ? d->num_splits : d->batch) : d->batch + target;
+        w.nsplit = 0;
+    } else {
+        const int T = rows_per_stage(g.elt, d->head_dim);
+        int maxs = g.C / (2 * T);
+        if (maxs < 1) maxs = 1;
+        int ns = d->num_splits > 0 ? d->num_splits : (kTargetCtas + units - 1) / units;
+        if (d->num_splits <= 0 && ns > maxs) ns = maxs;
+        if (ns < 1) ns = 1;
+        w.nsplit = ns;
+        w.items = d->batch * ns;
+    }
+    size_t off = 0;
+    w.err = off;
+    off += 256;
+    w.counters = off;
+    off = align_up(off + (size_t)units * 4, 256);
+    w.part_ml = off;
+    off = align_up(off + (size_t)w.items * d->q_heads * 8, 256);
+    w.part_o = off;
+    off = align_up(off + (size_t)w.items * d->q_heads * d->head_dim * 4, 256);
+    w.plan_rows = w.plan_seq = w.plan_items = w.plan_total = off;
+    if (d->layout == KVC_LAYOUT_PAGED) {
+        w.plan_rows = off;
+        off = align_up(off + (size_t)d->batch * d->max_blocks_per_seq * 4, 256);
+        w.plan_seq = off;
+        off = align_up(off + (size_t)d->batch * 8, 256);
+        w.plan_items = off;
+        off = align_up(off + (size_t)w.items * 16, 256);
+        w.plan_total = off;
+        off += 256;
+    }
+    w.total = off;
+    return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void fill_theta(int D, float base, double* theta, float* theta_f) {
+    for (int i = 0; i < D / 2; ++i) {
+        theta[i] = std::pow((double)base, -2.0 * i / D);
+        if (theta_f) theta_f[i] = (float)theta[i];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int dtype, int D, int gh, bool paged, bool rd, const DecodeParams& p, dim3 grid,
+                          cudaStream_t s) {
+#define KVC_CASE(E, DD, GG, PG, RD) \
+    if (D == DD && gh == GG && paged == PG && rd == RD) return launch_decode_t<E, DD, GG, PG, RD>(p, grid, s);
+#define KVC_CASES(E, PG, RD)                                                         \
+    KVC_CASE(E, 64, 1, PG, RD) KVC_CASE(E, 64, 2, PG, RD) KVC_CASE(E, 64, 4, PG, RD)    \
+    KVC_CASE(E, 128, 1, PG, RD) KVC_CASE(E, 128, 2, PG, RD) KVC_CASE(E, 128, 4, PG, RD) \
+    KVC_CASE(E, 256, 1, PG, RD) KVC_CASE(E, 256, 2, PG, RD) KVC_CASE(E, 256, 4, PG, RD)
+    if (dtype == KVC_F32) {
+        KVC_CASES(float, false, false)
+        KVC_CASES(float, false, true)
+        KVC_CASES(float, true, false)
+    } else {
+        KVC_CASES(__nv_bfloat16, false, false)
+        KVC_CASES(__nv_bfloat16, false, true)
+        KVC_CASES(__nv_bfloat16, true, false)
+    }
+#undef KVC_CASES
+#undef KVC_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+KVC_API size_t kvc_cache_bytes(const kvc_desc* d) {
+    Geo g;
+    if (check_desc(d, &g) != KVC_OK) return 0;
+    return (size_t)d->layers * 2 * (size_t)g.half_elems * g.elt;
+}
+
+KVC_API size_t kvc_workspace_bytes(const kvc_desc* d) {
+    Geo g;
+    if (check_desc(d, &g) != KVC_OK) return 0;
+    return ws_layout(d, g).total;
+}
+
+KVC_API int kvc_workspace_init(const kvc_desc* d, void* workspace, size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (!workspace) return KVC_ERR_NULL;
+    const size_t need = ws_layout(d, g).total;
+    if (workspace_bytes < need) return KVC_ERR_WORKSPACE;
+    if (cudaMemsetAsync(workspace, 0, need, (cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer, const void* k_new, const void* v_new,
+                       int32_t n_new, const int32_t* pos, const int32_t* block_table, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (!cache || !k_new || !v_new || !pos || !workspace) return KVC_ERR_NULL;
+    if (d->layout == KVC_LAYOUT_PAGED && !block_table) return KVC_ERR_NULL;
+    if (!aligned16(cache) || !aligned16(workspace)) return KVC_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & (uintptr_t)(g.elt - 1))
+        return KVC_ERR_ALIGN;
+    if (layer < 0 || layer >= d->layers || n_new < 1 || n_new > 0x7fffffff / 2) return KVC_ERR_ARG;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
+    AppendParams p{};
+    p.cache = cache;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.pos = pos;
+    p.table = block_table;
+    p.err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + w.err);
+    p.layer_off = (long long)layer * 2 * g.half_elems;
+    p.kv_off = g.half_elems;
+    p.B = d->batch;
+    p.Hkv = d->kv_heads;
+    p.D = d->head_dim;
+    p.n_new = n_new;
+    p.layout = d->layout;
+    p.window = d->window;
+    p.sinks = d->layout == KVC_LAYOUT_SINK_RING ? d->sinks : 0;
+    p.capacity = g.C;
+    p.bs = d->block_size;
+    p.num_blocks = d->num_blocks;
+    p.maxb = d->max_blocks_per_seq;
+    p.rope = d->rope;
+    if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, p.theta, nullptr);
+    if (launch_append(d->dtype, p, (cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t layer, const void* q,
+                                 const int32_t* pos, const int32_t* block_table, const uint32_t* valid_bits,
+                                 void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (!cache || !q || !pos || !out || !workspace) return KVC_ERR_NULL;
+    const bool paged = d->layout == KVC_LAYOUT_PAGED;
+    if (paged && !block_table) return KVC_ERR_NULL;
+    if (!aligned16(cache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVC_ERR_ALIGN;
+    if (layer < 0 || layer >= d->layers) return KVC_ERR_ARG;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    DecodeParams p{};
+    p.cache = cache;
+    p.q = q;
+    p.pos = pos;
+    p.table = block_table;
+    p.valid = valid_bits;
+    p.out = out;
+    p.err = reinterpret_cast<uint32_t*>(ws + w.err);
+    p.counters = reinterpret_cast<uint32_t*>(ws + w.counters);
+    p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+    p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+    p.layer_off = (long long)layer * 2 * g.half_elems;
+    p.kv_off = g.half_elems;
+    p.B = d->batch;
+    p.Hq = d->q_heads;
+    p.Hkv = d->kv_heads;
+    p.G = g.G;
+    p.nsub = g.nsub;
+    p.window = d->window;
+    p.sinks = d->layout == KVC_LAYOUT_SINK_RING ? d->sinks : 0;
+    p.capacity = g.C;
+    p.bs = d->block_size;
+    p.num_blocks = d->num_blocks;
+    p.maxb = d->max_blocks_per_seq;
+    p.nsplit = w.nsplit;
+    p.rope = d->rope;
+    const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+    p.q_scale = scale * 1.4426950408889634f;   // log2(e): softmax in base 2
+    if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
+
+    dim3 grid(w.items, d->kv_heads, g.nsub);
+    if (paged) {
+        PlanParams pp{};
+        pp.pos = pos;
+        pp.table = block_table;
+        pp.valid = valid_bits;
+        pp.err = p.err;
+        pp.rows = reinterpret_cast<int32_t*>(ws + w.plan_rows);
+        pp.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
+        pp.items = reinterpret_cast<int4*>(ws + w.plan_items);
+        pp.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
+        pp.B = d->batch;
+        pp.bs = d->block_size;
+        pp.num_blocks = d->num_blocks;
+        pp.maxb = d->max_blocks_per_seq;
+        pp.max_items = w.items;
+        if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
+        p.items = pp.items;
+        p.seq_items = pp.seq_items;
+        p.n_items = pp.n_items;
+    }
+    const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
+    if (launch_decode(d->dtype, d->head_dim, g.GH, paged, rd, p, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+KVC_API int kvc_block_table_write(const kvc_desc* d, int32_t* block_table, uint32_t* valid_bits, int32_t n,
+                                  const int32_t* seq, const int32_t* logical_block, const int32_t* physical_block,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (d->layout != KVC_LAYOUT_PAGED) return KVC_ERR_DESC;
+    if (n < 0) return KVC_ERR_ARG;
+    if (n == 0) return KVC_OK;
+    if (!block_table || !seq || !logical_block || !physical_block || !workspace) return KVC_ERR_NULL;
+    if (!aligned16(workspace)) return KVC_ERR_ALIGN;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
+    TableParams p{};
+    p.table = block_table;
+    p.valid = valid_bits;
+    p.seq = seq;
+    p.lb = logical_block;
+    p.phys = physical_block;
+    p.err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + w.err);
+    p.n = n;
+    p.B = d->batch;
+    p.maxb = d->max_blocks_per_seq;
+    p.num_blocks = d->num_blocks;
+    if (launch_table_write(p, (cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+KVC_API int kvc_valid_write(const kvc_desc* d, uint32_t* valid_bits, int32_t n, const int32_t* slot,
+                            const int32_t* value, void* workspace, size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (d->layout != KVC_LAYOUT_PAGED) return KVC_ERR_DESC;
+    if (n < 0) return KVC_ERR_ARG;
+    if (n == 0) return KVC_OK;
+    if (!valid_bits || !slot || !value || !workspace) return KVC_ERR_NULL;
+    if (!aligned16(workspace)) return KVC_ERR_ALIGN;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
+    TableParams p{};
+    p.valid = valid_bits;
+    p.phys = slot;
+    p.value = value;
+    p.err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + w.err);
+    p.n = n;
+    p.num_blocks = d->num_blocks;
+    if (launch_valid_write(p, (cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+KVC_API int kvc_get_error(void* workspace, void* stream) {
+    if (!workspace) return KVC_ERR_NULL;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t bits = 0;
+    if (cudaMemcpyAsync(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ERR_CUDA;
+    if (bits && cudaMemsetAsync(workspace, 0, sizeof(bits), s) != cudaSuccess) return KVC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ERR_CUDA;
+    return (int)(bits & 0x7fffffffu);
+}
+
+KVC_API const char* kvc_strerror(int code) {
+    switch (code) {
+        case KVC_OK: return "ok";
+        case KVC_ERR_NULL: return "a required pointer is NULL";
+        case KVC_ERR_DESC: return "inconsistent cache descriptor";
+        case KVC_ERR_UNSUPPORTED: return "unsupported combination (head_dim not 64/128/256, or PAGED with READ_INCACHE)";
+        case KVC_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case KVC_ERR_WORKSPACE: return "workspace smaller than kvc_workspace_bytes()";
+        case KVC_ERR_ARG: return "argument out of range";
+        case KVC_ERR_CUDA: return "CUDA launch or runtime call failed";
+        case (int)KVC_DEV_BAD_BLOCK: return "device: block table entry >= num_blocks";
+        case (int)KVC_DEV_UNMAPPED_APPEND: return "device: append into an unmapped block";
+        case (int)KVC_DEV_BAD_POSITION: return "device: position < 0 or beyond the block table";
+        case (int)KVC_DEV_TIMEOUT: return "device: a bounded wait timed out";
+        case (int)KVC_DEV_BAD_ENTRY: return "device: table/valid update entry out of range";
+        default: return "unknown code";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// Kernel parameter blocks and launch entry points shared by the host-side
+// ABI (kvc_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvc {
+
+constexpr int kMaxHalfDim = 128;                 // head_dim <= 256
+constexpr long long kWaitCycles = 2000000000LL;  // bounded mbarrier wait (~1 s)
+constexpr int kConsumerWarps = 4;                // decode kernel: 4 compute warps
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;  // + 1 copy-issuing warp
+constexpr int kStages = 4;                       // bulk-copy pipeline depth
+constexpr int kTargetCtas = 608;                 // 152 SMs x 2 CTAs x 2 waves
+
+enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
+enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
+
+// Workspace carve-up (byte offsets from the workspace base).
+struct WorkspaceLayout {
+    size_t err;          // uint32 error word
+    size_t counters;     // uint32 [batch * kv_heads * nsub]
+    size_t part_ml;      // float2 [items * q_heads]: running max (log2 units), sum of weights
+    size_t part_o;       // float  [items * q_heads * head_dim]: unnormalised output
+    size_t plan_rows;    // PAGED: int32 [batch * max_blocks]: attended rows per block, then prefix
+    size_t plan_seq;     // PAGED: int2  [batch]: first item, item count
+    size_t plan_items;   // PAGED: int4  [items]: (seq, first block, first row, rows)
+    size_t plan_total;   // PAGED: int32 number of items used
+    size_t total;
+    int items;           // partial slots per (q head): batch * nsplit, or paged items
+    int nsplit;          // RING / SINK_RING: splits per (sequence, kv head)
+};
+
+struct DecodeParams {
+    const void* cache;          // whole cache tensor
+    const void* q;              // [B, Hq, D]
+    const int32_t* pos;         // [B]
+    const int32_t* table;       // PAGED [B, maxb]
+    const uint32_t* valid;      // PAGED, may be null
+    void* out;                  // [B, Hq, D]
+    uint32_t* err;
+    uint32_t* counters;
+    float2* part_ml;
+    float* part_o;
+    const int4* items;          // PAGED plan
+    const int2* seq_items;      // PAGED plan
+    const int32_t* n_items;     // PAGED plan
+    long long layer_off;        // elements from cache base to this layer's K half
+    long long kv_off;           // elements from the K half to the V half
+    int B, Hq, Hkv, G, nsub;
+    int window, sinks, capacity;
+    int bs, num_blocks, maxb;
+    int nsplit;
+    int rope;                   // kRopeNone / kRopeBaked / kRopeRead
+    float q_scale;              // softmax scale * log2(e)
+    float theta_f[kMaxHalfDim];     // RoPE frequencies, fp32 (small in-tile angles)
+    double theta[kMaxHalfDim];      // RoPE frequencies, fp64 (absolute positions)
+};
+
+struct PlanParams {
+    const int32_t* pos;
+    const int32_t* table;
+    const uint32_t* valid;
+    uint32_t* err;
+    int32_t* rows;        // [B * maxb]
+    int2* seq_items;      // [B]
+    int4* items;          // [max_items]
+    int32_t* n_items;
+    int B, bs, num_blocks, maxb, max_items;
+};
+
+struct AppendParams {
+    void* cache;
+    const void* k_new;    // [B, n_new, Hkv, D]
+    const void* v_new;
+    const int32_t* pos;
+    const int32_t* table;
+    uint32_t* err;
+    long long layer_off;
+    long long kv_off;
+    int B, Hkv, D, n_new;
+    int layout, window, sinks, capacity;
+    int bs, num_blocks, maxb;
+    int rope;
+    double theta[kMaxHalfDim];
+};
+
+struct TableParams {
+    int32_t* table;
+    uint32_t* valid;
+    const int32_t* seq;
+    const int32_t* lb;
+    const int32_t* phys;
+    const int32_t* value;
+    uint32_t* err;
+    int n, B, maxb, num_blocks;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_decode(int dtype, int head_dim, int gh, bool paged, bool read_rope,
+                          const DecodeParams& p, dim3 grid, cudaStream_t stream);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
+cudaError_t launch_valid_write(const TableParams& p, cudaStream_t stream);
+
+}  // namespace kvc

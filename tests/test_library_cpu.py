@@ -1,0 +1,137 @@
+"""Host-side checks that need no GPU: the library builds and loads, exports
+every entry point of include/kvc.h, and validates its arguments before any
+CUDA call; host logic of the binding and the benchmark."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import kvc_synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sliding_window_attention_kvc_gb300 as m
+    return m
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "kvc.h")) as f:
+        src = f.read()
+    return re.findall(r"KVC_API\s+[\w\s\*]+?\b(kvc_\w+)\s*\(", src)
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for n in ("kvc_append", "kvc_decode_attention", "kvc_block_table_write", "kvc_get_error",
+              "kvc_cache_bytes", "kvc_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kvc):
+    L = kvc.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert set(_declared()) == set(kvc.ABI_FUNCTIONS)
+    nm = subprocess.run(["nm", "-D", "--defined-only", kvc.LIB_PATH], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = {ln.split()[-1] for ln in nm.stdout.splitlines() if " T " in ln}
+        assert set(_declared()) <= exported
+        assert not [s for s in exported if s.startswith("cuda")], "CUDA runtime symbols leak out"
+
+
+def _desc(kvc, **kw):
+    base = dict(layout="ring", rope="baked", dtype="bf16", layers=2, batch=3, q_heads=8, kv_heads=2,
+                head_dim=128, window=100)
+    base.update(kw)
+    return kvc.make_desc(**base)
+
+
+def test_cache_and_workspace_sizes(kvc):
+    for name in kvc_synth.WORKLOAD_NAMES:
+        wl = kvc_synth.make_workload(name)
+        d = bench.workload_desc(wl, layers=2)
+        elt = 4 if wl.dtype == "f32" else 2
+        assert kvc.cache_bytes(d) == int(np.prod(wl.cache_shape(2))) * elt
+        assert kvc.workspace_bytes(d) > 0
+        assert tuple(kvc.cache_shape(d)) == wl.cache_shape(2)
+
+
+def test_invalid_descriptors_are_rejected(kvc):
+    bad = [
+        dict(head_dim=96),                    # unsupported head_dim
+        dict(q_heads=6, kv_heads=4),          # not a multiple
+        dict(window=0),
+        dict(layout="sink_ring", sinks=0),
+        dict(layout="ring", sinks=2),
+        dict(layout="paged", block_size=0, num_blocks=4, max_blocks_per_seq=4),
+        dict(layers=0),
+    ]
+    for kw in bad:
+        assert kvc.cache_bytes(_desc(kvc, **kw)) == 0, kw
+        assert kvc.workspace_bytes(_desc(kvc, **kw)) == 0, kw
+    L = kvc.lib()
+    assert L.kvc_cache_bytes(None) == 0
+
+
+def test_argument_errors_return_codes_without_launching(kvc):
+    L = kvc.lib()
+    d = _desc(kvc)
+    ws_n = kvc.workspace_bytes(d)
+    A = 1 << 20   # fake, 16-byte aligned "device" addresses: never dereferenced on these paths
+    dp = ctypes.byref(d)
+    assert L.kvc_append(dp, None, 0, A, A, 1, A, None, A, ws_n, None) == kvc.KVC_ERR_NULL
+    assert L.kvc_append(dp, A + 8, 0, A, A, 1, A, None, A, ws_n, None) == kvc.KVC_ERR_ALIGN
+    assert L.kvc_append(dp, A, 5, A, A, 1, A, None, A, ws_n, None) == kvc.KVC_ERR_ARG
+    assert L.kvc_append(dp, A, 0, A, A, 0, A, None, A, ws_n, None) == kvc.KVC_ERR_ARG
+    assert L.kvc_append(dp, A, 0, A, A, 1, A, None, A, ws_n - 1, None) == kvc.KVC_ERR_WORKSPACE
+    assert L.kvc_decode_attention(dp, A, 0, A, A, None, None, A + 4, A, ws_n, None) == kvc.KVC_ERR_ALIGN
+    assert L.kvc_decode_attention(dp, A, -1, A, A, None, None, A, A, ws_n, None) == kvc.KVC_ERR_ARG
+    assert L.kvc_decode_attention(dp, A, 0, None, A, None, None, A, A, ws_n, None) == kvc.KVC_ERR_NULL
+    dpg = _desc(kvc, layout="paged", rope="baked", block_size=16, num_blocks=10, max_blocks_per_seq=4)
+    nws = kvc.workspace_bytes(dpg)
+    assert L.kvc_decode_attention(ctypes.byref(dpg), A, 0, A, A, None, None, A, A, nws, None) == kvc.KVC_ERR_NULL
+    dpr = _desc(kvc, layout="paged", rope="read_time", block_size=16, num_blocks=10, max_blocks_per_seq=4)
+    assert L.kvc_decode_attention(ctypes.byref(dpr), A, 0, A, A, A, None, A, A, 1 << 30, None) == \
+        kvc.KVC_ERR_UNSUPPORTED
+    assert L.kvc_block_table_write(dp, A, None, 1, A, A, A, A, ws_n, None) == kvc.KVC_ERR_DESC
+    assert L.kvc_block_table_write(ctypes.byref(dpg), A, None, 0, None, None, None, None, 0, None) == kvc.KVC_OK
+    assert L.kvc_get_error(None, None) == kvc.KVC_ERR_NULL
+    assert kvc.strerror(kvc.KVC_ERR_ALIGN).startswith("pointer")
+
+
+def test_pack_valid_bits(kvc):
+    rng = np.random.default_rng(0)
+    for n in (1, 31, 32, 33, 1024, 1000):
+        m = rng.random(n) < 0.5
+        w = kvc.pack_valid_bits(torch.from_numpy(m)).numpy().view(np.uint32)
+        for k in range(n):
+            assert bool((w[k // 32] >> (k % 32)) & 1) == bool(m[k])
+
+
+def test_step_bytes_formula():
+    # KV bytes per token: 2 (K and V) x layers x kv_heads x head_dim x element bytes;
+    # the pages' example (32 layers, 32 heads, D 128, FP16) is 524288 bytes.
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "window_examples.json")) as f:
+        ex = json.load(f)["kv_bytes_per_token"]
+    wl = kvc_synth.Workload(name="x", layout="window", dtype="bf16", rope="none", batch=1,
+                            q_heads=ex["kv_heads"], kv_heads=ex["kv_heads"], head_dim=ex["head_dim"],
+                            window=10, positions=[0])
+    per_layer = bench.step_bytes(wl)["kv_logical"]      # t = 0: one attended token, one layer
+    assert per_layer * ex["layers"] == ex["bytes"]
+    wl = kvc_synth.make_workload("ring_bf16")
+    assert bench.step_bytes(wl)["kv_logical"] == 8 * 8 * 4096 * 2 * 128 * 2      # 128 MiB
+    wl = kvc_synth.make_workload("paged_shared_prefix_bf16")
+    nb = bench.step_bytes(wl)
+    assert nb["kv_unique"] < nb["kv_logical"]
