@@ -106,6 +106,8 @@ typedef struct kvc_desc {
 #define KVC_ERR_WORKSPACE (-5)   /* workspace smaller than kvc_workspace_bytes() */
 #define KVC_ERR_ARG (-6)         /* argument out of range (layer, n_new, n) */
 #define KVC_ERR_CUDA (-7)        /* a CUDA runtime call or launch failed */
+#define KVC_ERR_TOO_LARGE (-8)   /* kvc_decode_attention_noalloc: the call needs more than
+                                    KVC_NOALLOC_SCRATCH_BYTES of scratch */
 
 /* Device-detected error bits, returned by kvc_get_error(). */
 #define KVC_DEV_BAD_BLOCK 0x1u       /* block_table entry >= num_blocks (access skipped) */
@@ -183,6 +185,42 @@ KVC_API int kvc_block_table_write(const kvc_desc* d, int32_t* block_table, uint3
 KVC_API int kvc_valid_write(const kvc_desc* d, uint32_t* valid_bits, int32_t n,
                             const int32_t* slot, const int32_t* value,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Size of the library's own fixed scratch array used by
+ * kvc_decode_attention_noalloc: 8 MiB of device memory, reserved on every GPU
+ * that loads the library, from the first use until the process exits. */
+#define KVC_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* kvc_decode_attention for callers that cannot allocate device memory.
+ *
+ * Same operation, arguments and results as kvc_decode_attention, except that
+ * the caller passes no workspace: the split-K partial results, completion
+ * counters and (PAGED) work plan live in a fixed scratch array inside the
+ * library (KVC_NOALLOC_SCRATCH_BYTES).  It is meant for code that must not
+ * call cudaMalloc once it is running - a serving loop whose device memory is
+ * fixed when it starts, or a plugin inside a host framework that owns all
+ * device memory and offers no way to allocate - and so has nowhere to put a
+ * workspace.  The pages have no counterpart of this entry point.
+ *
+ *   - It allocates nothing: no cudaMalloc / cudaFree, no allocating library
+ *     call.  Inputs and outputs are still the caller's device buffers.
+ *   - The first call on a device (with that device current) looks up the
+ *     scratch array's device address; make that first call before any stream
+ *     capture.  Later calls only enqueue work on `stream`.
+ *   - Every call on a device shares the one scratch array and finds it as the
+ *     previous call left it; the call clears the parts that must start at
+ *     zero (error word, completion counters) on `stream` before its kernels.
+ *     Calls that overlap on the GPU (different streams, no ordering between
+ *     them) race on the scratch and give wrong results: order them.
+ *   - A problem whose workspace (kvc_workspace_bytes) exceeds
+ *     KVC_NOALLOC_SCRATCH_BYTES is rejected with KVC_ERR_TOO_LARGE before
+ *     anything is launched.
+ *   - Device-detected errors are not reported: the kernels still skip bad
+ *     accesses, but there is no workspace for kvc_get_error to read. */
+KVC_API int kvc_decode_attention_noalloc(const kvc_desc* d, const void* cache, int32_t layer,
+                                         const void* q, const int32_t* pos,
+                                         const int32_t* block_table, const uint32_t* valid_bits,
+                                         void* out, void* stream);
 
 /* Wait for `stream`, then return the workspace's device error bits
  * (KVC_DEV_*, 0 = none) and clear them.  Negative KVC_ERR_* on failure. */

@@ -25,13 +25,15 @@ DTYPE_NAMES = {"f32": torch.float32, "bf16": torch.bfloat16}
 KVC_OK = 0
 KVC_ERR_NULL, KVC_ERR_DESC, KVC_ERR_UNSUPPORTED = -1, -2, -3
 KVC_ERR_ALIGN, KVC_ERR_WORKSPACE, KVC_ERR_ARG, KVC_ERR_CUDA = -4, -5, -6, -7
+KVC_ERR_TOO_LARGE = -8
+KVC_NOALLOC_SCRATCH_BYTES = 8 << 20
 KVC_DEV_BAD_BLOCK, KVC_DEV_UNMAPPED_APPEND, KVC_DEV_BAD_POSITION = 0x1, 0x2, 0x4
 KVC_DEV_TIMEOUT, KVC_DEV_BAD_ENTRY = 0x8, 0x10
 
 ABI_FUNCTIONS = (
     "kvc_cache_bytes", "kvc_workspace_bytes", "kvc_workspace_init", "kvc_append",
     "kvc_decode_attention", "kvc_block_table_write", "kvc_valid_write", "kvc_get_error",
-    "kvc_strerror",
+    "kvc_strerror", "kvc_decode_attention_noalloc",
 )
 
 
@@ -76,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.kvc_block_table_write.argtypes = [dp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.kvc_valid_write.argtypes = [dp, vp, i32, vp, vp, vp, sz, vp]
         L.kvc_get_error.argtypes = [vp, vp]
+        L.kvc_decode_attention_noalloc.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.kvc_strerror.argtypes = [ctypes.c_int]
         L.kvc_strerror.restype = ctypes.c_char_p
         for name in ABI_FUNCTIONS:

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_bf16.h>
 
@@ -346,6 +347,7 @@ KVC_API const char* kvc_strerror(int code) {
         case KVC_ERR_WORKSPACE: return "workspace smaller than kvc_workspace_bytes()";
         case KVC_ERR_ARG: return "argument out of range";
         case KVC_ERR_CUDA: return "CUDA launch or runtime call failed";
+        case KVC_ERR_TOO_LARGE: return "problem needs more scratch than KVC_NOALLOC_SCRATCH_BYTES";
         case (int)KVC_DEV_BAD_BLOCK: return "device: block table entry >= num_blocks";
         case (int)KVC_DEV_UNMAPPED_APPEND: return "device: append into an unmapped block";
         case (int)KVC_DEV_BAD_POSITION: return "device: position < 0 or beyond the block table";
@@ -356,3 +358,53 @@ KVC_API const char* kvc_strerror(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// kvc_decode_attention_noalloc: kvc_decode_attention with the library's own
+// fixed scratch array in place of a caller workspace, for callers that cannot
+// allocate device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Device scratch shared by every kvc_decode_attention_noalloc call on a GPU.
+static __device__ __align__(256) unsigned char kvc_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mutex;
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device with that device current.
+int scratch_on_current_device(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, kvc_noalloc_scratch) != cudaSuccess || !ptr) return KVC_ERR_CUDA;
+        g_scratch_addr[dev] = ptr;
+    }
+    *out = g_scratch_addr[dev];
+    return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" KVC_API int kvc_decode_attention_noalloc(const kvc_desc* d, const void* cache, int32_t layer,
+                                                    const void* q, const int32_t* pos,
+                                                    const int32_t* block_table, const uint32_t* valid_bits,
+                                                    void* out, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (w.total > (size_t)KVC_NOALLOC_SCRATCH_BYTES) return KVC_ERR_TOO_LARGE;
+    void* scratch = nullptr;
+    rc = scratch_on_current_device(&scratch);
+    if (rc) return rc;
+    // error word and completion counters must start at zero
+    if (cudaMemsetAsync(scratch, 0, w.part_ml, (cudaStream_t)stream) != cudaSuccess) return KVC_ERR_CUDA;
+    return kvc_decode_attention(d, cache, layer, q, pos, block_table, valid_bits, out, scratch,
+                                (size_t)KVC_NOALLOC_SCRATCH_BYTES, stream);
+}
