@@ -115,6 +115,8 @@ typedef struct kvc_desc {
 #define KVC_DEV_BAD_POSITION 0x4u    /* decode position < 0, or beyond the block table */
 #define KVC_DEV_TIMEOUT 0x8u         /* a bounded wait inside a kernel gave up */
 #define KVC_DEV_BAD_ENTRY 0x10u      /* kvc_block_table_write / kvc_valid_write entry out of range */
+#define KVC_DEV_INTERNAL 0x20u       /* an index computed inside a kernel failed its bounds check
+                                        (access skipped); a library bug, please report */
 
 /* Bytes of the cache tensor described by `d` (0 if `d` is invalid). */
 KVC_API size_t kvc_cache_bytes(const kvc_desc* d);

@@ -1,9 +1,9 @@
-// Explicit instantiation of the decode launchers for one element type and
-// layout family; included by the decode_*.cu translation units so the heavy
-// template code compiles in parallel.
+// Explicit instantiation of the decode launchers; included by the decode_*.cu
+// translation units so the heavy template code compiles in parallel.
 #pragma once
-#include "kvc_decode.cuh"
+#include "kvc_decode_mma.cuh"
 
+// fp32 caches: CUDA-core kernel (kvc_decode.cuh)
 #define KVC_INST(E, D, GH, PG, RD) \
     template cudaError_t kvc::launch_decode_t<E, D, GH, PG, RD>(const kvc::DecodeParams&, dim3, cudaStream_t);
 
@@ -17,3 +17,19 @@
     KVC_INST(E, 256, 1, PG, RD)     \
     KVC_INST(E, 256, 2, PG, RD)     \
     KVC_INST(E, 256, 4, PG, RD)
+
+// bf16 caches: tensor-core kernel (kvc_decode_mma.cuh)
+#define KVC_INST_MMA(D, GH, PG, RD)                                                                  \
+    template cudaError_t kvc::launch_decode_mma_t<D, GH, PG, RD>(const kvc::DecodeParams&, const void*, \
+                                                                 dim3, cudaStream_t);
+
+#define KVC_INST_MMA_ALL_D(PG, RD) \
+    KVC_INST_MMA(64, 1, PG, RD)    \
+    KVC_INST_MMA(64, 2, PG, RD)    \
+    KVC_INST_MMA(64, 4, PG, RD)    \
+    KVC_INST_MMA(128, 1, PG, RD)   \
+    KVC_INST_MMA(128, 2, PG, RD)   \
+    KVC_INST_MMA(128, 4, PG, RD)   \
+    KVC_INST_MMA(256, 1, PG, RD)   \
+    KVC_INST_MMA(256, 2, PG, RD)   \
+    KVC_INST_MMA(256, 4, PG, RD)

@@ -1,3 +1,3 @@
-// Decode kernels: PAGED layout, bf16 cache.
+// Decode kernels: PAGED layout, bf16 cache (tensor cores).
 #include "decode_inst.cuh"
-KVC_INST_ALL_D(__nv_bfloat16, true, false)
+KVC_INST_MMA_ALL_D(true, false)

@@ -1,4 +1,4 @@
-// Decode kernels: RING / SINK_RING layouts, bf16 cache.
+// Decode kernels: RING / SINK_RING layouts, bf16 cache (tensor cores).
 #include "decode_inst.cuh"
-KVC_INST_ALL_D(__nv_bfloat16, false, false)
-KVC_INST_ALL_D(__nv_bfloat16, false, true)
+KVC_INST_MMA_ALL_D(false, false)
+KVC_INST_MMA_ALL_D(false, true)

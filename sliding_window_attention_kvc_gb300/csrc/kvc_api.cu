@@ -5,6 +5,7 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "kvc.h"
@@ -14,6 +15,8 @@ namespace kvc {
 
 template <typename Elt, int D, int GH, bool PAGED, bool READ>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t stream);
+template <int D, int GH, bool PAGED, bool READ>
+cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 grid, cudaStream_t stream);
 
 namespace {
 
@@ -24,7 +27,9 @@ struct Geo {
     long long half_elems;   // elements of one K (or V) half of one layer
 };
 
-int rows_per_stage(int elt, int D) { return 8192 / (D * elt); }
+// rows of K/V one pipeline stage holds: fp32 kernel 8 KiB per K stage;
+// bf16 tensor-core kernel 4 (2 for head_dim 256) sub-tiles of 16 rows
+int rows_per_stage(int elt, int D) { return elt == 4 ? 8192 / (D * elt) : (D == 256 ? 32 : 64); }
 
 int check_desc(const kvc_desc* d, Geo* g) {
     if (!d) return KVC_ERR_NULL;
@@ -63,9 +68,11 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     WorkspaceLayout w{};
     const int units = d->batch * d->kv_heads * g.nsub;
-    if (d->layout == KVC_LAYOUT_PAGED) {
-        const int target = (kTargetCtas + d->kv_heads * g.nsub - 1) / (d->kv_heads * g.nsub);
-        w.items = d->num_splits > 0 ? (d->num_splits > d->batch ? d->num_splits : d->batch) : d->batch + target;
+    const int groups = d->kv_heads * g.nsub;
+    // stream-K CTAs per (kv head, q-head group): bf16 kernels, and the paged plan
+    w.ctas = d->num_splits > 0 ? d->num_splits : (kStreamCtas + groups - 1) / groups;
+    if (d->layout == KVC_LAYOUT_PAGED || d->dtype == KVC_BF16) {
+        w.items = w.ctas + d->batch;       // slot x + b of segment (share x, sequence b)
         w.nsplit = 0;
     } else {
         const int T = rows_per_stage(g.elt, d->head_dim);
@@ -86,7 +93,7 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     off = align_up(off + (size_t)w.items * d->q_heads * 8, 256);
     w.part_o = off;
     off = align_up(off + (size_t)w.items * d->q_heads * d->head_dim * 4, 256);
-    w.plan_rows = w.plan_seq = w.plan_items = w.plan_total = off;
+    w.plan_rows = w.plan_seq = w.plan_items = w.plan_total = w.plan_cta = off;
     if (d->layout == KVC_LAYOUT_PAGED) {
         w.plan_rows = off;
         off = align_up(off + (size_t)d->batch * d->max_blocks_per_seq * 4, 256);
@@ -94,6 +101,8 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
         off = align_up(off + (size_t)d->batch * 8, 256);
         w.plan_items = off;
         off = align_up(off + (size_t)w.items * 16, 256);
+        w.plan_cta = off;
+        off = align_up(off + (size_t)w.ctas * 8, 256);
         w.plan_total = off;
         off += 256;
     }
@@ -124,15 +133,69 @@ cudaError_t launch_decode(int dtype, int D, int gh, bool paged, bool rd, const D
         KVC_CASES(float, false, false)
         KVC_CASES(float, false, true)
         KVC_CASES(float, true, false)
-    } else {
-        KVC_CASES(__nv_bfloat16, false, false)
-        KVC_CASES(__nv_bfloat16, false, true)
-        KVC_CASES(__nv_bfloat16, true, false)
     }
 #undef KVC_CASES
 #undef KVC_CASE
     return cudaErrorInvalidValue;
 }
+
+cudaError_t launch_decode_mma(int D, int gh, bool paged, bool rd, const DecodeParams& p, const void* tmap,
+                              dim3 grid, cudaStream_t s) {
+#define KVC_CASE(DD, GG, PG, RD) \
+    if (D == DD && gh == GG && paged == PG && rd == RD) return launch_decode_mma_t<DD, GG, PG, RD>(p, tmap, grid, s);
+#define KVC_CASES(PG, RD)                                                   \
+    KVC_CASE(64, 1, PG, RD) KVC_CASE(64, 2, PG, RD) KVC_CASE(64, 4, PG, RD)    \
+    KVC_CASE(128, 1, PG, RD) KVC_CASE(128, 2, PG, RD) KVC_CASE(128, 4, PG, RD) \
+    KVC_CASE(256, 1, PG, RD) KVC_CASE(256, 2, PG, RD) KVC_CASE(256, 4, PG, RD)
+    KVC_CASES(false, false)
+    KVC_CASES(false, true)
+    KVC_CASES(true, false)
+#undef KVC_CASES
+#undef KVC_CASE
+    return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
+// point (no link against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// The whole bf16 cache as a 2-D tensor [rows, head_dim]: boxes of 16 rows x 64
+// columns (128 bytes), 128-byte swizzle.  Row of (layer, K|V, unit row) =
+// (layer * 2 + kv) * rows_per_half + unit row.
+int make_kv_tensor_map(const kvc_desc* d, const Geo& g, const void* cache, CUtensorMap* map) {
+    const unsigned long long rows = (unsigned long long)d->layers * 2 * (unsigned long long)g.half_elems / d->head_dim;
+    if (rows >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return KVC_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVC_OK : KVC_ERR_CUDA;
+}
+
+}  // namespace
 
 }  // namespace kvc
 
@@ -244,12 +307,13 @@ KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t l
     p.num_blocks = d->num_blocks;
     p.maxb = d->max_blocks_per_seq;
     p.nsplit = w.nsplit;
+    p.max_items = w.items;
     p.rope = d->rope;
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
     p.q_scale = scale * 1.4426950408889634f;   // log2(e): softmax in base 2
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
 
-    dim3 grid(w.items, d->kv_heads, g.nsub);
+    dim3 grid(d->dtype == KVC_BF16 ? w.ctas : w.items, d->kv_heads, g.nsub);
     if (paged) {
         PlanParams pp{};
         pp.pos = pos;
@@ -260,6 +324,8 @@ KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t l
         pp.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
         pp.items = reinterpret_cast<int4*>(ws + w.plan_items);
         pp.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
+        pp.cta_items = reinterpret_cast<int2*>(ws + w.plan_cta);
+        pp.ctas = w.ctas;
         pp.B = d->batch;
         pp.bs = d->block_size;
         pp.num_blocks = d->num_blocks;
@@ -269,8 +335,16 @@ KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t l
         p.items = pp.items;
         p.seq_items = pp.seq_items;
         p.n_items = pp.n_items;
+        p.cta_items = pp.cta_items;
     }
     const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
+    if (d->dtype == KVC_BF16) {
+        CUtensorMap map;
+        rc = make_kv_tensor_map(d, g, cache, &map);
+        if (rc) return rc;
+        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, p, &map, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
+        return KVC_OK;
+    }
     if (launch_decode(d->dtype, d->head_dim, g.GH, paged, rd, p, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
     return KVC_OK;
 }
@@ -353,6 +427,7 @@ KVC_API const char* kvc_strerror(int code) {
         case (int)KVC_DEV_BAD_POSITION: return "device: position < 0 or beyond the block table";
         case (int)KVC_DEV_TIMEOUT: return "device: a bounded wait timed out";
         case (int)KVC_DEV_BAD_ENTRY: return "device: table/valid update entry out of range";
+        case (int)KVC_DEV_INTERNAL: return "device: an internal index check failed (access skipped)";
         default: return "unknown code";
     }
 }

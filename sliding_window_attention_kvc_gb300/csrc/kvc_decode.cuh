@@ -82,6 +82,12 @@ __device__ __forceinline__ int paged_block_rows(const int32_t* table_row, const 
     return lb == last ? (t - lb * bs + 1) : bs;
 }
 
+// Share holding unit u of a stream-K partition of `total` units into
+// `shares` contiguous ranges [floor(x total / shares), floor((x + 1) total / shares)).
+__device__ __forceinline__ int streamk_share_of(long long u, long long total, int shares) {
+    return (int)(((u + 1) * shares - 1) / total);
+}
+
 __device__ __forceinline__ int clamp_paged_t(int t, int maxb, int bs) {
     const long long lim = (long long)maxb * bs - 1;
     return t > lim ? (int)lim : t;
@@ -128,6 +134,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     if constexpr (PAGED) {
         if (item >= *p.n_items) return;
         pitem = p.items[item];
+        if (pitem.x < 0) return;          // index left unused by the plan
         b = pitem.x;
         const int2 si = p.seq_items[b];
         first_item = si.x;

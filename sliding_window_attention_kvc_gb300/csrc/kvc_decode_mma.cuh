@@ -1,0 +1,729 @@
+// Split-K decode attention for bf16 caches on the tensor cores, stream-K.
+//
+// Work decomposition.  For each (kv head, q-head group) the attended rows of
+// all sequences, laid end to end, are cut into gridDim.x nearly equal
+// contiguous shares, one per CTA (a persistent grid of two CTAs per SM).  A
+// share covers one or more *segments* (its intersection with one sequence);
+// a CTA reduces each segment to a partial (m, l, o) and the last CTA to
+// finish a sequence - found with an atomic ticket, never by waiting - merges
+// that sequence's few partials:
+//     M = max m_i,  out = sum o_i 2^(m_i - M) / sum l_i 2^(m_i - M).
+// With shares in sequence order, segment (CTA x, sequence b) gets partial
+// slot x + b: consecutive, unique, and a sequence's slots are consecutive.
+//
+// Contractions of a GQA group by mma.sync m16n8k16 (bf16 in, fp32 acc):
+//     S = Q K^T   A = the group's q heads (rows 0..GH-1 of 16; the rest zero),
+//                 B = K rows of a 16-token sub-tile, k = head_dim;
+//     O += P V    A = exp2(S - m) rounded to bf16, B = V rows, k = 16 tokens.
+// On a q head group of 4 the CUDA-core formulation spent ~97 warp
+// instructions per cached token (measured); these two products cost ~4.
+//
+// Data movement.  K and V arrive through 2-D TMA tensor copies
+// (cp.async.bulk.tensor) of 16-row x 64-column boxes with the 128-byte
+// swizzle, so that ldmatrix reads of 8 rows at one column are bank-conflict
+// free.  Warp 4 issues the copies into a ring of shared-memory stages guarded
+// by mbarriers and walks the CTA's segments; warps 0..3 compute.  A stage
+// holds up to NSUB sub-tiles of one segment; each sub-tile is one box per 64
+// columns and carries its own row count (ragged ends, partial paged blocks)
+// and, for READ_INCACHE, its first in-cache position.  Rows of a sub-tile past
+// its row count are masked out of the softmax and their V rows zeroed before
+// P V (they may hold any bits, NaN included).
+#pragma once
+
+#include <cuda.h>
+
+#include <atomic>
+
+#include "kvc_decode.cuh"
+
+namespace kvc {
+
+template <int D, bool READ>
+struct MmaShape {
+    static constexpr int kSub = 16;                           // rows per sub-tile
+    static constexpr int kBoxCols = 64;                       // bf16 columns per TMA box (128 bytes)
+    static constexpr int kBoxes = D / kBoxCols;               // boxes per row of K (or V)
+    static constexpr int kBoxBytes = kSub * 128;              // one 16-row box
+    static constexpr int kSubBytes = kBoxes * kBoxBytes;      // K (or V) of one sub-tile
+    static constexpr int kDsplit = D == 256 ? 2 : 1;          // warps sharing one sub-tile (split over dims)
+    static constexpr int kTokenGroups = kConsumerWarps / kDsplit;
+    static constexpr int kNsub = kTokenGroups;                // sub-tiles per stage (one per token group)
+    static constexpr int kStageBytes = 2 * kNsub * kSubBytes; // K sub-tiles, then V sub-tiles
+    static constexpr int kStages = D == 64 ? 6 : (READ ? 5 : 3);
+    static constexpr int kDl = D / kDsplit;                   // output columns per warp
+    static constexpr int kNt = kDl / 8;                       // 8-column output tiles per warp
+    static constexpr int kKsteps = D / 16;                    // k-steps of Q K^T
+    static constexpr int kHalf = D / 2;
+};
+
+// Segment header, carried by the first stage of each segment.
+struct MmaSegment {
+    int b;           // sequence
+    int t;           // its current position
+    int slot;        // partial slot of this segment
+    int first_slot;  // first partial slot of the sequence
+    int nparts;      // partials of the sequence
+    int pad[3];
+};
+
+struct alignas(16) MmaStageMeta {
+    int nsub;        // sub-tiles in the stage (0 allowed); -1 = end of the stream
+    int flags;       // kSegBegin | kSegEnd
+    int pad[2];
+    int nrows[4];    // rows of each sub-tile (1..16)
+    int ip0[4];      // READ_INCACHE: in-cache position of row 0 of each sub-tile
+    MmaSegment seg;  // valid with kSegBegin
+};
+constexpr int kSegBegin = 1, kSegEnd = 2;
+
+template <int D, int GH, bool READ>
+struct MmaSmem {
+    using S = MmaShape<D, READ>;
+    static constexpr size_t kStage = 0;                                        // 1024-aligned stages
+    static constexpr size_t kBars = kStage + (size_t)S::kStages * S::kStageBytes;
+    static constexpr size_t kMeta = kBars + 2 * S::kStages * sizeof(uint64_t);
+    static constexpr size_t kRot = kMeta + S::kStages * sizeof(MmaStageMeta);  // [stage][sub][D/2] float2
+    static constexpr size_t kTab = kRot + (READ ? (size_t)S::kStages * S::kNsub * S::kHalf * 8 : 0);
+    static constexpr size_t kQcs = kTab + (READ ? (size_t)S::kSub * S::kHalf * 8 : 0);   // [16][D/2] float2
+    static constexpr size_t kMergeO = kQcs + (size_t)S::kHalf * 8;
+    static constexpr size_t kMergeML = kMergeO + (size_t)S::kTokenGroups * GH * D * 4;
+    static constexpr size_t kFlag = kMergeML + (size_t)S::kTokenGroups * GH * 8;
+    static constexpr size_t kCbar = kFlag + 16;           // 3 mbarriers: all compute warps, 2 warp pairs
+    static constexpr size_t kTotal = kCbar + 32 + 1024;   // + slack to align the base to 1024
+};
+
+// Barrier among a fixed set of threads built on an mbarrier, so that waiting
+// is bounded like every other wait in these kernels (a hardware named barrier
+// would wait forever for a warp that gave up and left).
+struct BoundedBarrier {
+    uint64_t* bar;
+    uint32_t phase;
+    __device__ __forceinline__ bool sync(uint32_t* err) {
+        mbar_arrive(bar);
+        const bool ok = mbar_wait(bar, phase);
+        phase ^= 1u;
+        if (!ok) set_error(err, 0x8u /* KVC_DEV_TIMEOUT */);
+        return ok;
+    }
+};
+
+template <int D, int GH, bool PAGED, bool READ>
+__global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
+    decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmap) {
+    using S = MmaShape<D, READ>;
+    using SM = MmaSmem<D, GH, READ>;
+    constexpr int NST = S::kStages, NSUB = S::kNsub, HALF = S::kHalf;
+
+    extern __shared__ unsigned char smem_raw[];
+    // the 128-byte swizzle pattern repeats every 1024 bytes: align the stages to it
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* stage_base = smem + SM::kStage;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+    uint64_t* empty = full + NST;
+    MmaStageMeta* meta = reinterpret_cast<MmaStageMeta*>(smem + SM::kMeta);
+    float2* rot = reinterpret_cast<float2*>(smem + SM::kRot);
+    float2* tab = reinterpret_cast<float2*>(smem + SM::kTab);
+    float2* qcs = reinterpret_cast<float2*>(smem + SM::kQcs);
+    float* merge_o = reinterpret_cast<float*>(smem + SM::kMergeO);
+    float2* merge_ml = reinterpret_cast<float2*>(smem + SM::kMergeML);
+    int* flag = reinterpret_cast<int*>(smem + SM::kFlag);
+    uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + SM::kCbar);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int x = blockIdx.x, kvh = blockIdx.y, z = blockIdx.z;
+    const int nctas = gridDim.x;
+
+    int2 my_items = make_int2(0, 0);      // PAGED: first item, item count of this CTA
+    if constexpr (PAGED) {
+        my_items = p.cta_items[x];
+        if (my_items.y <= 0) return;
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(&cbar[0], kConsumerWarps * 32);
+        mbar_init(&cbar[1], 64);
+        mbar_init(&cbar[2], 64);
+        mbar_fence_init();
+        tma_prefetch_desc(&tmap);
+    }
+    __syncthreads();
+
+    // tensor-map rows: [layers][K | V][rows of the half][D]
+    const long long layer_row0 = p.layer_off / D;
+    const long long half_rows = p.kv_off / D;
+
+    if (warp == kConsumerWarps) {
+        // =================== copy-issuing warp ==============================
+        int it = 0, fill = 0;
+        bool ok = true, open = false;
+        auto open_stage = [&]() -> bool {
+            const int s = it % NST;
+            if (it >= NST && !mbar_wait(&empty[s], ((it / NST) - 1) & 1)) {
+                if (lane == 0) set_error(p.err, 0x8u /* KVC_DEV_TIMEOUT */);
+                return false;
+            }
+            open = true;
+            fill = 0;
+            if (lane == 0) meta[s].flags = 0;
+            return true;
+        };
+        auto commit = [&](int extra_flags) {
+            const int s = it % NST;
+            __syncwarp();
+            if (lane == 0) {
+                meta[s].nsub = fill;
+                meta[s].flags |= extra_flags;
+                mbar_arrive(&full[s]);
+            }
+            open = false;
+            ++it;
+        };
+        // a segment starts on a fresh stage that carries its header
+        auto begin_segment = [&](const MmaSegment& hdr) -> bool {
+            if (open) commit(0);
+            if (!open_stage()) return false;
+            if (lane == 0) {
+                meta[it % NST].flags = kSegBegin;
+                meta[it % NST].seg = hdr;
+            }
+            return true;
+        };
+        // A full stage is published only when the next sub-tile needs room, so
+        // the last stage of a segment is still open here and carries kSegEnd.
+        auto end_segment = [&]() { commit(kSegEnd); };
+        // one sub-tile: `n` rows starting at tensor-map row `krow` (K half)
+        auto emit = [&](long long krow, int n, int ip0) -> bool {
+            if (open && fill == NSUB) commit(0);
+            if (!open && !open_stage()) return false;
+            const int s = it % NST;
+            if constexpr (READ) {
+                for (int i = lane; i < HALF; i += 32) {
+                    float cs, sn;
+                    rope_cos_sin((double)ip0, p.theta[i], &cs, &sn);
+                    rot[(s * NSUB + fill) * HALF + i] = make_float2(cs, sn);
+                }
+            }
+            if (lane == 0) {
+                meta[s].nrows[fill] = n;
+                meta[s].ip0[fill] = ip0;
+                unsigned char* kdst = stage_base + (size_t)s * S::kStageBytes + (size_t)fill * S::kSubBytes;
+                unsigned char* vdst = kdst + (size_t)NSUB * S::kSubBytes;
+                mbar_expect_tx(&full[s], 2 * S::kSubBytes);
+#pragma unroll
+                for (int bx = 0; bx < S::kBoxes; ++bx) {
+                    tma_load_2d(kdst + bx * S::kBoxBytes, &tmap, bx * S::kBoxCols, (int)krow, &full[s]);
+                    tma_load_2d(vdst + bx * S::kBoxBytes, &tmap, bx * S::kBoxCols, (int)(krow + half_rows),
+                                &full[s]);
+                }
+            }
+            ++fill;
+            return true;
+        };
+
+        if constexpr (!PAGED) {
+            // stream-K over the sequences: sequence b contributes
+            // max(1, ceil(n_live(b) / 16)) sub-tiles (an empty one when t < 0)
+            const int C = p.capacity;
+            auto seq_tiles = [&](int bb, int* t_out, int* nl_out) -> long long {
+                if (bb >= p.B) return 0;
+                const int tb = p.pos[bb];
+                const int nl = tb < 0 ? 0 : (tb + 1 < C ? tb + 1 : C);
+                *t_out = tb;
+                *nl_out = nl;
+                return nl > 0 ? (nl + 15) / 16 : 1;
+            };
+            long long total = 0;
+            for (int base = 0; base < p.B; base += 32) {
+                int tb = 0, nl = 0;
+                long long st = seq_tiles(base + lane, &tb, &nl);
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) st += __shfl_xor_sync(0xffffffffu, st, off);
+                total += st;
+            }
+            // no more shares than units, so that every share is non-empty and a
+            // sequence's partial count is exactly the shares it overlaps
+            const int G = (int)(total < nctas ? total : nctas);
+            const long long lo = x < G ? (long long)x * total / G : total;
+            const long long hi = x < G ? (long long)(x + 1) * total / G : total;
+            long long run = 0;
+            for (int base = 0; base < p.B && ok && run < hi; base += 32) {
+                int tb = 0, nl = 0;
+                const long long st = seq_tiles(base + lane, &tb, &nl);
+                long long incl = st;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const long long u = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += u;
+                }
+                for (int j = 0; j < 32 && ok; ++j) {
+                    const int b = base + j;
+                    if (b >= p.B) break;
+                    const long long Sb = __shfl_sync(0xffffffffu, st, j);
+                    const long long Ob = run + __shfl_sync(0xffffffffu, incl, j) - Sb;
+                    const int t_b = __shfl_sync(0xffffffffu, tb, j);
+                    const int nl_b = __shfl_sync(0xffffffffu, nl, j);
+                    if (Ob >= hi) break;
+                    if (Ob + Sb <= lo) continue;
+                    const int fx = streamk_share_of(Ob, total, G);
+                    const int lx = streamk_share_of(Ob + Sb - 1, total, G);
+                    MmaSegment hdr;
+                    hdr.b = b;
+                    hdr.t = t_b;
+                    hdr.slot = x + b;
+                    hdr.first_slot = fx + b;
+                    hdr.nparts = lx - fx + 1;
+                    if (!(ok = begin_segment(hdr))) break;
+                    const int r0 = (int)((lo > Ob ? lo : Ob) - Ob) * 16;
+                    const int r1 = min((int)((hi < Ob + Sb ? hi : Ob + Sb) - Ob) * 16, nl_b);
+                    const long long base_row = layer_row0 + ((long long)b * p.Hkv + kvh) * C;
+                    int h_slot = 0;
+                    if constexpr (READ) {
+                        if (t_b >= 0)
+                            h_slot = t_b < p.sinks ? t_b : p.sinks + (int)(((long long)t_b - p.sinks) % p.window);
+                    }
+                    for (int r = r0; r < r1 && ok;) {
+                        int n = min(16, r1 - r);
+                        int ip0 = 0;
+                        if constexpr (READ) {
+                            // a sub-tile never straddles the sink/window boundary or the ring's wrap
+                            const int seg_end = r < p.sinks ? p.sinks : (r <= h_slot ? h_slot + 1 : C);
+                            n = min(n, seg_end - r);
+                            ip0 = incache_of_slot(r, t_b, p.sinks, p.window, C);
+                        }
+                        ok = emit(base_row + r, n, ip0);
+                        r += n;
+                    }
+                    if (ok) end_segment();
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        } else {
+            for (int k = 0; k < my_items.y && ok; ++k) {
+                const int item = my_items.x + k;
+                if (item < 0 || item >= p.max_items) {
+                    if (lane == 0) index_fault(p.err, 1, item);
+                    break;
+                }
+                const int4 itv = p.items[item];
+                const int b = itv.x;
+                if (b < 0 || b >= p.B) {
+                    if (lane == 0) index_fault(p.err, 2, b);
+                    break;
+                }
+                const int2 si = p.seq_items[b];
+                MmaSegment hdr;
+                hdr.b = b;
+                hdr.t = p.pos[b];
+                hdr.slot = item;
+                hdr.first_slot = si.x;
+                hdr.nparts = si.y;
+                if (!(ok = begin_segment(hdr))) break;
+                const int tt = clamp_paged_t(hdr.t, p.maxb, p.bs);
+                const int32_t* trow = p.table + (long long)b * p.maxb;
+                int lb = itv.y;
+                int rem = itv.w;
+                const int last_lb = tt < 0 ? -1 : tt / p.bs;
+                while (rem > 0 && lb <= last_lb && ok) {
+                    const int my_lb = lb + lane;
+                    int my_phys = -1, my_rows = 0;
+                    if (my_lb <= last_lb)
+                        my_rows = paged_block_rows(trow, p.valid, p.err, my_lb, tt, p.bs, p.num_blocks, &my_phys);
+                    unsigned mask = __ballot_sync(0xffffffffu, my_rows > 0);
+                    while (mask && rem > 0 && ok) {
+                        const int src = __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const int phys = __shfl_sync(0xffffffffu, my_phys, src);
+                        const int brows = __shfl_sync(0xffffffffu, my_rows, src);
+                        int row = (lb + src == itv.y) ? itv.z : 0;
+                        int take = min(brows - row, rem);
+                        const long long blk = layer_row0 + ((long long)phys * p.Hkv + kvh) * p.bs;
+                        while (take > 0 && ok) {
+                            const int n = min(16, take);
+                            ok = emit(blk + row, n, 0);
+                            take -= n;
+                            rem -= n;
+                            row += n;
+                        }
+                    }
+                    lb += 32;
+                }
+                if (ok) end_segment();
+            }
+        }
+        if (ok) {
+            if (open) commit(0);
+            if ((ok = open_stage())) {
+                __syncwarp();
+                if (lane == 0) {
+                    meta[it % NST].nsub = -1;
+                    mbar_arrive(&full[it % NST]);
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            // never leave with copies still landing in this CTA's shared memory;
+            // a stage left open has issued copies: arrive so its phase can end
+            if (open) {
+                mbar_arrive(&full[it % NST]);
+                ++it;
+            }
+            for (int k = (it > NST ? it - NST : 0); k < it; ++k) mbar_wait(&full[k % NST], (k / NST) & 1);
+        }
+        return;
+    }
+
+    // ====================== compute warps (0 .. 3) ==========================
+    const int ctid = tid;
+    const int tg = warp / S::kDsplit;     // token group: which sub-tile of each stage
+    const int hd = warp % S::kDsplit;     // which half of the output columns (D = 256)
+    const int g = lane >> 2, c = lane & 3;
+    constexpr int NCT = kConsumerWarps * 32;
+    BoundedBarrier csync{&cbar[0], 0u};           // the four compute warps
+    BoundedBarrier psync{&cbar[1 + (tg & 1)], 0u}; // the two warps sharing a sub-tile (head_dim 256)
+
+    if constexpr (READ) {
+        // R(r theta_i) for the rows r = 0..15 of a sub-tile
+        for (int idx = ctid; idx < S::kSub * HALF; idx += NCT) {
+            const int r = idx / HALF, i = idx % HALF;
+            float cs, sn;
+            sincosf((float)r * p.theta_f[i], &sn, &cs);
+            tab[idx] = make_float2(cs, sn);
+        }
+    }
+
+    MmaSegment seg;
+    seg.b = seg.t = seg.slot = seg.first_slot = seg.nparts = 0;
+    uint32_t qa[S::kKsteps][2];
+    float o[S::kNt][4];
+    float m_run = -INFINITY, l_run = 0.f;
+
+    // q of sequence seg.b as mma A fragments: row g = q head (zero for g >= GH),
+    // per k-step columns 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1); rotated,
+    // scaled by softmax_scale * log2(e), rounded to bf16
+    auto load_q = [&]() {
+        int qpos = seg.t;
+        if constexpr (PAGED) {
+            qpos = clamp_paged_t(seg.t, p.maxb, p.bs);
+            if ((seg.t < 0 || seg.t != qpos) && seg.slot == seg.first_slot && kvh == 0 && z == 0 && ctid == 0)
+                set_error(p.err, 0x4u /* KVC_DEV_BAD_POSITION */);
+        } else {
+            if (seg.t < 0 && seg.slot == seg.first_slot && kvh == 0 && z == 0 && ctid == 0)
+                set_error(p.err, 0x4u);
+            if (READ) qpos = min(seg.t, p.capacity - 1);
+        }
+        csync.sync(p.err);                      // everyone is done with the previous qcs
+        if (p.rope != kRopeNone) {
+            for (int i = ctid; i < HALF; i += NCT) {
+                float cs, sn;
+                rope_cos_sin((double)qpos, p.theta[i], &cs, &sn);
+                qcs[i] = make_float2(cs, sn);
+            }
+        }
+        csync.sync(p.err);
+        float qf[S::kKsteps][4];
+        if (g < GH) {
+            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                        ((long long)seg.b * p.Hq + kvh * p.G + z * GH + g) * D;
+#pragma unroll
+            for (int ks = 0; ks < S::kKsteps; ++ks) {
+                const uint32_t lo = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c);
+                const uint32_t hi = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c);
+                qf[ks][0] = __uint_as_float(lo << 16);
+                qf[ks][1] = __uint_as_float(lo & 0xffff0000u);
+                qf[ks][2] = __uint_as_float(hi << 16);
+                qf[ks][3] = __uint_as_float(hi & 0xffff0000u);
+            }
+            if (p.rope != kRopeNone) {
+#pragma unroll
+                for (int ks = 0; ks < S::kKsteps / 2; ++ks) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 16 * ks + 2 * c + (e & 1) + 8 * (e >> 1);
+                        const float2 cs = qcs[i];
+                        const float x1 = qf[ks][e], x2 = qf[ks + S::kKsteps / 2][e];
+                        qf[ks][e] = x1 * cs.x - x2 * cs.y;
+                        qf[ks + S::kKsteps / 2][e] = x1 * cs.y + x2 * cs.x;
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < S::kKsteps; ++ks) qf[ks][0] = qf[ks][1] = qf[ks][2] = qf[ks][3] = 0.f;
+        }
+#pragma unroll
+        for (int ks = 0; ks < S::kKsteps; ++ks) {
+            qa[ks][0] = pack_bf16x2(qf[ks][0] * p.q_scale, qf[ks][1] * p.q_scale);
+            qa[ks][1] = pack_bf16x2(qf[ks][2] * p.q_scale, qf[ks][3] * p.q_scale);
+        }
+#pragma unroll
+        for (int j = 0; j < S::kNt; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+    };
+
+    // end of a segment: merge the warps, write the segment's partial, and let
+    // the last CTA of the sequence combine all its partials
+    auto finish_segment = [&]() {
+        if (seg.b < 0) {                          // rejected segment: keep the barrier sequence
+            csync.sync(p.err);
+            csync.sync(p.err);
+            csync.sync(p.err);
+            csync.sync(p.err);
+            return;
+        }
+        float lq = l_run;
+        lq += __shfl_xor_sync(0xffffffffu, lq, 1);
+        lq += __shfl_xor_sync(0xffffffffu, lq, 2);
+        csync.sync(p.err);                     // merge buffers free (previous segment done with them)
+        if (g < GH) {
+            float* mo = merge_o + (tg * GH + g) * D;
+#pragma unroll
+            for (int j = 0; j < S::kNt; ++j) {
+                const int col = (hd * S::kNt + j) * 8 + 2 * c;
+                mo[col] = o[j][0];
+                mo[col + 1] = o[j][1];
+            }
+            if (c == 0 && hd == 0) merge_ml[tg * GH + g] = make_float2(m_run, lq);
+        }
+        csync.sync(p.err);
+        const int qh0 = kvh * p.G + z * GH;
+        for (int idx = ctid; idx < GH * D; idx += NCT) {
+            const int h = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < S::kTokenGroups; ++w) M = fmaxf(M, merge_ml[w * GH + h].x);
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < S::kTokenGroups; ++w) {
+                const float2 ml = merge_ml[w * GH + h];
+                const float e = (ml.x == M) ? 1.f : exp2f(ml.x - M);
+                L += ml.y * e;
+                O += merge_o[(w * GH + h) * D + d] * e;
+            }
+            const long long slot = (long long)seg.slot * p.Hq + qh0 + h;
+            p.part_o[slot * D + d] = O;
+            if (d == 0) p.part_ml[slot] = make_float2(M, L);
+        }
+        __threadfence();
+        csync.sync(p.err);
+        const long long cidx = ((long long)seg.b * p.Hkv + kvh) * p.nsub + z;
+        if (ctid == 0) {
+            const unsigned ticket = atomicAdd(&p.counters[cidx], 1u);
+            *flag = (ticket == (unsigned)(seg.nparts - 1));
+        }
+        csync.sync(p.err);
+        if (*flag) {
+            __threadfence();
+            // (m, l) of every partial staged in shared memory (merge_o is free now)
+            float2* sml = reinterpret_cast<float2*>(merge_o);
+            constexpr int kCap = S::kTokenGroups * GH * D / 2;
+            const int npl = seg.nparts * GH;
+            const bool staged = npl <= kCap;
+            if (staged) {
+                for (int i = ctid; i < npl; i += NCT)
+                    sml[i] = __ldcg(&p.part_ml[(long long)(seg.first_slot + i / GH) * p.Hq + qh0 + i % GH]);
+            }
+            csync.sync(p.err);
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+            for (int o4 = ctid; o4 < GH * D / 4; o4 += NCT) {
+                const int h = (o4 * 4) / D, d0 = (o4 * 4) % D;
+                auto ml_of = [&](int k) -> float2 {
+                    return staged ? sml[k * GH + h]
+                                  : __ldcg(&p.part_ml[(long long)(seg.first_slot + k) * p.Hq + qh0 + h]);
+                };
+                float M = -INFINITY;
+                for (int k = 0; k < seg.nparts; ++k) M = fmaxf(M, ml_of(k).x);
+                float L = 0.f;
+                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                for (int k = 0; k < seg.nparts; ++k) {
+                    const float2 ml = ml_of(k);
+                    const float e = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                        p.part_o + ((long long)(seg.first_slot + k) * p.Hq + qh0 + h) * D + d0));
+                    L += ml.y * e;
+                    O.x += v.x * e;
+                    O.y += v.y * e;
+                    O.z += v.z * e;
+                    O.w += v.w * e;
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                __nv_bfloat16* dst = out + ((long long)seg.b * p.Hq + qh0 + h) * D + d0;
+                *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(O.x * inv, O.y * inv),
+                                                            pack_bf16x2(O.z * inv, O.w * inv));
+            }
+            if (ctid == 0) p.counters[cidx] = 0u;
+        }
+    };
+
+    for (int it = 0;; ++it) {
+        const int s = it % NST;
+        if (!mbar_wait(&full[s], (it / NST) & 1)) {
+            if (lane == 0) set_error(p.err, 0x8u);
+            break;
+        }
+        const int nsub = meta[s].nsub;
+        if (nsub < 0) break;
+        if (nsub > NSUB) {                        // cannot happen: stop rather than read past the stage
+            if (ctid == 0) index_fault(p.err, 12, nsub);
+            break;
+        }
+        const int flags = meta[s].flags;
+        if (flags & kSegBegin) {
+            seg = meta[s].seg;
+            if (seg.b < 0 || seg.b >= p.B || seg.slot < 0 || seg.slot >= p.max_items || seg.first_slot < 0 ||
+                seg.nparts < 1 || seg.first_slot + seg.nparts > p.max_items || seg.slot < seg.first_slot ||
+                seg.slot >= seg.first_slot + seg.nparts) {
+                if (ctid == 0) index_fault(p.err, 3 + (seg.b < 0 || seg.b >= p.B ? 0 : 8), seg.slot);
+                seg.b = -1;                       // this segment writes nothing
+            }
+            if (seg.b >= 0) load_q(); else csync.sync(p.err), csync.sync(p.err);
+        }
+        if (tg < nsub) {
+            const int nrows = meta[s].nrows[tg];
+            unsigned char* Ks = stage_base + (size_t)s * S::kStageBytes + (size_t)tg * S::kSubBytes;
+            unsigned char* Vs = Ks + (size_t)NSUB * S::kSubBytes;
+            const uint32_t ku = smem_u32(Ks), vu = smem_u32(Vs);
+            bool wrote = false;
+
+            if constexpr (READ) {
+                // rotate the stored (raw) K rows in place by R((ip0 + r) theta),
+                // R(ip0 theta) from the stage table times R(r theta) from `tab`
+                constexpr int CPR = D / 16;   // 16-byte chunk pairs (i, i + D/2) per row
+                const float2* rs = rot + (s * NSUB + tg) * HALF;
+                const int nmine = (nrows - hd + S::kDsplit - 1) / S::kDsplit;
+                for (int idx = lane; idx < nmine * CPR; idx += 32) {
+                    const int r = hd + (idx / CPR) * S::kDsplit;
+                    const int cp = idx % CPR;
+                    const int chi = cp + CPR;
+                    unsigned char* plo = Ks + (cp >> 3) * S::kBoxBytes + r * 128 + ((((cp & 7) ^ (r & 7))) << 4);
+                    unsigned char* phi = Ks + (chi >> 3) * S::kBoxBytes + r * 128 + ((((chi & 7) ^ (r & 7))) << 4);
+                    uint4 wl = *reinterpret_cast<uint4*>(plo);
+                    uint4 wh = *reinterpret_cast<uint4*>(phi);
+                    float xl[8], xh[8];
+                    EltTraits<__nv_bfloat16>::unpack(wl, xl);
+                    EltTraits<__nv_bfloat16>::unpack(wh, xh);
+                    float yl[8], yh[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int i = cp * 8 + j;
+                        const float2 a = rs[i], bb = tab[r * HALF + i];
+                        const float cs = a.x * bb.x - a.y * bb.y;
+                        const float sn = a.y * bb.x + a.x * bb.y;
+                        yl[j] = xl[j] * cs - xh[j] * sn;
+                        yh[j] = xl[j] * sn + xh[j] * cs;
+                    }
+                    wl = make_uint4(pack_bf16x2(yl[0], yl[1]), pack_bf16x2(yl[2], yl[3]),
+                                    pack_bf16x2(yl[4], yl[5]), pack_bf16x2(yl[6], yl[7]));
+                    wh = make_uint4(pack_bf16x2(yh[0], yh[1]), pack_bf16x2(yh[2], yh[3]),
+                                    pack_bf16x2(yh[4], yh[5]), pack_bf16x2(yh[6], yh[7]));
+                    *reinterpret_cast<uint4*>(plo) = wl;
+                    *reinterpret_cast<uint4*>(phi) = wh;
+                }
+                wrote = true;
+                if constexpr (S::kDsplit == 2) psync.sync(p.err); else __syncwarp();
+            }
+            if (nrows < S::kSub) {
+                // rows past nrows may hold anything (NaN): zero this warp's V columns there
+                constexpr int BPW = S::kBoxes / S::kDsplit;
+                const int per_box = (S::kSub - nrows) * 8;
+                for (int idx = lane; idx < per_box * BPW; idx += 32) {
+                    const int bxl = idx / per_box, rem = idx % per_box;
+                    const int r = nrows + rem / 8, ch = rem % 8;
+                    *reinterpret_cast<uint4*>(Vs + (hd * BPW + bxl) * S::kBoxBytes + r * 128 + ch * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                wrote = true;
+                __syncwarp();
+            }
+
+            // ---- S = Q K^T over the 16 rows: two 8-token n-tiles --------------
+            float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int tok = ((lane >> 4) << 3) + (lane & 7);
+                const int chs = (lane >> 3) & 1;
+#pragma unroll
+                for (int ks = 0; ks < S::kKsteps; ++ks) {
+                    const int bx = ks >> 2;
+                    const int ch = ((ks & 3) << 1) + chs;
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(ku + bx * S::kBoxBytes + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+                    mma_bf16_16816(sa[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+                    mma_bf16_16816(sa[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+                }
+            }
+
+            // ---- online softmax on row g (this lane's q head) ----------------
+            float sv[4] = {sa[0][0], sa[0][1], sa[1][0], sa[1][1]};
+            const int tk0 = 2 * c;
+            if (tk0 >= nrows) sv[0] = -INFINITY;
+            if (tk0 + 1 >= nrows) sv[1] = -INFINITY;
+            if (tk0 + 8 >= nrows) sv[2] = -INFINITY;
+            if (tk0 + 9 >= nrows) sv[3] = -INFINITY;
+            float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mn = fmaxf(m_run, mx);
+            const float alpha = (mn == m_run || g >= GH) ? 1.f : exp2f(m_run - mn);
+            float pe[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pe[e] = (sv[e] == -INFINITY || g >= GH) ? 0.f : exp2f(sv[e] - mn);
+            l_run = l_run * alpha + ((pe[0] + pe[1]) + (pe[2] + pe[3]));
+            m_run = mn;
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int j = 0; j < S::kNt; ++j) {
+                    o[j][0] *= alpha;
+                    o[j][1] *= alpha;
+                }
+            }
+            const uint32_t pa0 = pack_bf16x2(pe[0], pe[1]);
+            const uint32_t pa2 = pack_bf16x2(pe[2], pe[3]);
+
+            // ---- O += P V over this warp's output columns ---------------------
+            {
+                const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
+                const int chs = lane >> 4;
+#pragma unroll
+                for (int j = 0; j < S::kNt; j += 2) {
+                    const int dt = hd * S::kNt + j;        // global 8-column tile
+                    const int bx = dt >> 3;
+                    const int ch = (dt & 7) + chs;
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_trans(vu + bx * S::kBoxBytes + tok * 128 + ((ch ^ (tok & 7)) << 4), v0, v1, v2, v3);
+                    mma_bf16_16816(o[j], pa0, 0u, pa2, 0u, v0, v1);
+                    mma_bf16_16816(o[j + 1], pa0, 0u, pa2, 0u, v2, v3);
+                }
+            }
+            if (wrote) fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (flags & kSegEnd) finish_segment();
+    }
+}
+
+template <int D, int GH, bool PAGED, bool READ>
+cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 grid, cudaStream_t stream) {
+    using SM = MmaSmem<D, GH, READ>;
+    auto kern = decode_mma_kernel<D, GH, PAGED, READ>;
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_relaxed) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::kTotal);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_relaxed);
+    }
+    kern<<<grid, kDecodeThreads, SM::kTotal, stream>>>(p, *static_cast<const CUtensorMap*>(tmap));
+    return cudaGetLastError();
+}
+
+}  // namespace kvc

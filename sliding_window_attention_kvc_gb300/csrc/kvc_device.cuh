@@ -45,6 +45,17 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
 
+// An index computed in a kernel failed its bounds check: KVC_DEV_INTERNAL,
+// and the first failure's (site, value) kept in err[1], err[2].  The caller
+// skips the access.
+__device__ __forceinline__ void index_fault(uint32_t* err, uint32_t site, long long value) {
+    if (!err) return;
+    if ((atomicOr(err, 0x20u) & 0x20u) == 0u) {
+        err[1] = site;
+        err[2] = (uint32_t)value;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // RoPE angle: pos * theta reduced to [-pi, pi] in fp64 (two-constant
 // Cody-Waite reduction), then sin/cos in fp32.  Keeps the rotation accurate at
@@ -126,5 +137,59 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 }
 
 __device__ __forceinline__ float exp2_approx(float x) { return exp2f(x); }
+
+}  // namespace kvc
+
+namespace kvc {
+
+// ---------------------------------------------------------------------------
+// 2-D tensor copies (TMA) and tensor-core fragments for the bf16 kernel
+// ---------------------------------------------------------------------------
+
+// Box load of a 2-D tensor map at element coordinates (x, y) into shared
+// memory; completion counted on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst_smem)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> one 32-bit register of two bf16 (lo = first), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 }  // namespace kvc

@@ -79,115 +79,122 @@ cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream)
 }
 
 // ---------------------------------------------------------------------------
-// Paged work plan: split each sequence's attended rows into work items of
-// nearly equal size, in proportion to its length, so one long sequence (a
-// 256K-token pool) or a batch of mixed lengths keeps every SM busy.
+// Paged work plan (stream-K).  The attended rows of all sequences, laid end
+// to end, are cut into `ctas` nearly equal contiguous shares; the
+// intersection of share x with sequence b is work item x + b (items of one
+// sequence, and of one share, get consecutive indices; a share boundary that
+// falls exactly on a sequence boundary leaves one index unused, marked -1).
 //   1. rows[b][lb] = attended rows of logical block lb (0 if unmapped, not
-//      valid, or past t), then an inclusive prefix sum per sequence;
-//   2. n_b = 1 + floor(R_b * extra / R) items for sequence b (R_b its rows,
-//      R the batch total, extra = max_items - B), first item by prefix sum;
-//   3. item k of b starts at row floor(k R_b / n_b) of b's attended rows,
-//      located by binary search in the prefix.
+//      valid, or past t); a block-wide inclusive scan over the flattened
+//      [B][max_blocks] array turns it into P, so sequence b starts at
+//      O_b = P[b * maxb - 1] and holds R_b = P[(b + 1) * maxb - 1] - O_b rows;
+//   2. per sequence: the shares overlapping [O_b, O_b + R_b) (a sequence with
+//      no attended row still gets one empty item, for its zero output), each
+//      item's first block and row by binary search in P.
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanPerThread = 8;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
-    __shared__ long long s_total;
-    __shared__ int s_carry;
     __shared__ int s_warp[32];
+    __shared__ int s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long n = (long long)p.B * p.maxb;
 
-    // 1. rows per block
-    for (long long idx = tid; idx < (long long)p.B * p.maxb; idx += kPlanThreads) {
-        const int b = (int)(idx / p.maxb), lb = (int)(idx % p.maxb);
-        const int t = clamp_paged_t(p.pos[b], p.maxb, p.bs);
-        int phys = -1;
-        p.rows[idx] = paged_block_rows(p.table + (long long)b * p.maxb, p.valid, p.err, lb, t, p.bs,
-                                       p.num_blocks, &phys);
-    }
-    if (tid == 0) {
-        s_total = 0;
-        s_carry = 0;
-    }
+    for (int i = tid; i < p.max_items; i += kPlanThreads) p.items[i] = make_int4(-1, 0, 0, 0);
+    for (int i = tid; i < p.ctas; i += kPlanThreads) p.cta_items[i] = make_int2(0x7fffffff, 0);
+    if (tid == 0) s_carry = 0;
     __syncthreads();
-    // inclusive prefix per sequence: one warp per sequence
-    for (int b = warp; b < p.B; b += kPlanThreads / 32) {
-        int run = 0;
-        int32_t* r = p.rows + (long long)b * p.maxb;
-        for (int base = 0; base < p.maxb; base += 32) {
-            const int lb = base + lane;
-            int v = lb < p.maxb ? r[lb] : 0;
+
+    // 1. rows per block and their block-wide inclusive scan, in chunks
+    for (long long base = 0; base < n; base += (long long)kPlanThreads * kPlanPerThread) {
+        int v[kPlanPerThread];
+        int tsum = 0;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += u;
+        for (int j = 0; j < kPlanPerThread; ++j) {
+            const long long idx = base + (long long)tid * kPlanPerThread + j;
+            int r = 0;
+            if (idx < n) {
+                const int b = (int)(idx / p.maxb), lb = (int)(idx % p.maxb);
+                const int t = clamp_paged_t(p.pos[b], p.maxb, p.bs);
+                int phys = -1;
+                r = paged_block_rows(p.table + (long long)b * p.maxb, p.valid, p.err, lb, t, p.bs, p.num_blocks,
+                                     &phys);
             }
-            if (lb < p.maxb) r[lb] = run + v;
-            run += __shfl_sync(0xffffffffu, v, 31);
+            tsum += r;
+            v[j] = tsum;
         }
-        if (lane == 0) atomicAdd((unsigned long long*)&s_total, (unsigned long long)run);
-    }
-    __syncthreads();
-
-    // 2. items per sequence and first item (block-wide exclusive scan)
-    const long long R = s_total;
-    const int extra = p.max_items - p.B;
-    for (int base = 0; base < p.B; base += kPlanThreads) {
-        const int b = base + tid;
-        int n = 0;
-        if (b < p.B) {
-            const long long Rb = p.rows[(long long)b * p.maxb + p.maxb - 1];
-            n = 1 + (R > 0 ? (int)((Rb * (long long)extra) / R) : 0);
-        }
-        // exclusive scan of n over the block
-        int v = n;
+        int w = tsum;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) v += u;
+            const int u = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += u;
         }
-        if (lane == 31) s_warp[warp] = v;
+        if (lane == 31) s_warp[warp] = w;
         __syncthreads();
         if (warp == 0) {
-            int w = s_warp[lane];
+            int x = s_warp[lane];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, w, off);
-                if (lane >= off) w += u;
+                const int u = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += u;
             }
-            s_warp[lane] = w;
+            s_warp[lane] = x;
         }
         __syncthreads();
-        const int incl = v + (warp > 0 ? s_warp[warp - 1] : 0) + s_carry;
-        if (b < p.B) p.seq_items[b] = make_int2(incl - n, n);
+        const int before = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + (w - tsum);
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) {
+            const long long idx = base + (long long)tid * kPlanPerThread + j;
+            if (idx < n) p.rows[idx] = before + v[j];
+        }
         __syncthreads();
-        if (tid == kPlanThreads - 1) s_carry = incl;
+        if (tid == 0) s_carry += s_warp[31];
         __syncthreads();
     }
-    if (tid == 0) *p.n_items = s_carry;
+    const long long R = s_carry;
+    const int G = (int)(R < p.ctas ? (R > 0 ? R : 1) : p.ctas);   // no empty shares
 
-    // 3. item boundaries: one warp per sequence, lanes over its items
-    for (int b = warp; b < p.B; b += kPlanThreads / 32) {
-        const int32_t* pre = p.rows + (long long)b * p.maxb;
-        const long long Rb = pre[p.maxb - 1];
-        const int2 si = p.seq_items[b];
-        for (int k = lane; k < si.y; k += 32) {
-            const long long start = (long long)k * Rb / si.y;
-            const long long stop = (long long)(k + 1) * Rb / si.y;
+    // 2. items, one thread per sequence
+    for (int b = tid; b < p.B; b += kPlanThreads) {
+        const int32_t* P = p.rows;
+        const long long Ob = b > 0 ? P[(long long)b * p.maxb - 1] : 0;
+        const long long Rb = P[(long long)(b + 1) * p.maxb - 1] - Ob;
+        int fx, lx;
+        if (Rb > 0) {
+            fx = streamk_share_of(Ob, R, G);
+            lx = streamk_share_of(Ob + Rb - 1, R, G);
+        } else {
+            fx = lx = R > 0 ? streamk_share_of(Ob < R ? Ob : R - 1, R, G) : 0;
+        }
+        p.seq_items[b] = make_int2(fx + b, lx - fx + 1);
+        for (int x = fx; x <= lx; ++x) {
+            const long long lo = (long long)x * R / G, hi = (long long)(x + 1) * R / G;
+            const long long s0 = (lo > Ob ? lo : Ob) - Ob;
+            const long long s1 = (hi < Ob + Rb ? hi : Ob + Rb) - Ob;
             int lb = 0, off = 0;
-            if (stop > start) {
-                // first block whose inclusive prefix exceeds `start`
-                int lo = 0, hi = p.maxb - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    if (pre[mid] > start) hi = mid; else lo = mid + 1;
+            if (s1 > s0) {
+                // first block whose (sequence-local) inclusive prefix exceeds s0
+                int lo_b = 0, hi_b = p.maxb - 1;
+                const int32_t* Pb = P + (long long)b * p.maxb;
+                while (lo_b < hi_b) {
+                    const int mid = (lo_b + hi_b) >> 1;
+                    if (Pb[mid] - Ob > s0) hi_b = mid; else lo_b = mid + 1;
                 }
-                lb = lo;
-                off = (int)(start - (lb > 0 ? pre[lb - 1] : 0));
+                lb = lo_b;
+                off = (int)(s0 - ((lb > 0 ? Pb[lb - 1] : Ob) - Ob));
             }
-            p.items[si.x + k] = make_int4(b, lb, off, (int)(stop - start));
+            const int item = x + b;
+            if (item >= p.max_items || x >= p.ctas) {
+                index_fault(p.err, 6, item);
+                continue;
+            }
+            p.items[item] = make_int4(b, lb, off, (int)(s1 > s0 ? s1 - s0 : 0));
+            atomicMin(&p.cta_items[x].x, item);
+            atomicAdd(&p.cta_items[x].y, 1);
         }
     }
+    if (tid == 0) *p.n_items = G + p.B;
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {

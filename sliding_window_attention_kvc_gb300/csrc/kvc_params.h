@@ -13,6 +13,7 @@ constexpr int kConsumerWarps = 4;                // decode kernel: 4 compute war
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;  // + 1 copy-issuing warp
 constexpr int kStages = 4;                       // bulk-copy pipeline depth
 constexpr int kTargetCtas = 608;                 // 152 SMs x 2 CTAs x 2 waves
+constexpr int kStreamCtas = 304;                 // stream-K grid: 152 SMs x 2 CTAs
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
 enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
@@ -27,9 +28,11 @@ struct WorkspaceLayout {
     size_t plan_seq;     // PAGED: int2  [batch]: first item, item count
     size_t plan_items;   // PAGED: int4  [items]: (seq, first block, first row, rows)
     size_t plan_total;   // PAGED: int32 number of items used
+    size_t plan_cta;     // PAGED: int2 [ctas]: first item, item count
     size_t total;
     int items;           // partial slots per (q head): batch * nsplit, or paged items
-    int nsplit;          // RING / SINK_RING: splits per (sequence, kv head)
+    int nsplit;          // RING / SINK_RING fp32: splits per (sequence, kv head)
+    int ctas;            // stream-K CTAs per (kv head, q-head group)
 };
 
 struct DecodeParams {
@@ -46,12 +49,14 @@ struct DecodeParams {
     const int4* items;          // PAGED plan
     const int2* seq_items;      // PAGED plan
     const int32_t* n_items;     // PAGED plan
+    const int2* cta_items;      // PAGED plan: first item, item count of each CTA (stream-K kernel)
     long long layer_off;        // elements from cache base to this layer's K half
     long long kv_off;           // elements from the K half to the V half
     int B, Hq, Hkv, G, nsub;
     int window, sinks, capacity;
     int bs, num_blocks, maxb;
     int nsplit;
+    int max_items;              // partial slots per q head (bound for every slot index)
     int rope;                   // kRopeNone / kRopeBaked / kRopeRead
     float q_scale;              // softmax scale * log2(e)
     float theta_f[kMaxHalfDim];     // RoPE frequencies, fp32 (small in-tile angles)
@@ -64,10 +69,11 @@ struct PlanParams {
     const uint32_t* valid;
     uint32_t* err;
     int32_t* rows;        // [B * maxb]
-    int2* seq_items;      // [B]
-    int4* items;          // [max_items]
-    int32_t* n_items;
-    int B, bs, num_blocks, maxb, max_items;
+    int2* seq_items;      // [B]: first item, item count
+    int4* items;          // [max_items]: (seq, first block, first row, rows); seq -1 = unused
+    int2* cta_items;      // [ctas]: first item, item count
+    int32_t* n_items;     // one past the last item used
+    int B, bs, num_blocks, maxb, max_items, ctas;
 };
 
 struct AppendParams {
@@ -100,6 +106,10 @@ struct TableParams {
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode(int dtype, int head_dim, int gh, bool paged, bool read_rope,
                           const DecodeParams& p, dim3 grid, cudaStream_t stream);
+// bf16 caches: tensor-core kernel fed by 2-D TMA copies through `tmap`
+// (a CUtensorMap over the cache viewed as [rows, head_dim]).
+cudaError_t launch_decode_mma(int head_dim, int gh, bool paged, bool read_rope, const DecodeParams& p,
+                              const void* tmap, dim3 grid, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
