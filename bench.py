@@ -2,8 +2,8 @@
 """Benchmark of decode-step KV-cache attention on GB300.
 
 One step = one decode step of one attention layer for the whole batch:
-kvc_append of the new token's K/V (fused RoPE) followed by
-kvc_decode_attention (split-K attention + in-launch combine).  Steps cycle
+kvc_decode_step: the new token's K/V appended (RoPE fused; fused into the
+attention kernel for bf16 ring caches), then split-K attention.  Steps cycle
 over `layers` cache layers so the working set (>= 1 GiB) is far larger than
 the 126 MiB L2: every step reads its KV from HBM.
 
@@ -225,14 +225,23 @@ class DecodeState:
         if kvc.get_error(ws1):
             raise RuntimeError("device error while filling the paged cache")
 
-    # one decode step on `layer`, through the C ABI with device buffers
+    # one decode step on `layer` (append the token at pos, attend), through the
+    # C ABI with device buffers
     def step(self, layer, out=None):
         kvc = _kvc()
-        kvc.append(self.desc, self.cache, layer, self.k_new[layer], self.v_new[layer], self.pos, self.ws,
-                   block_table=self.table)
-        return kvc.decode_attention(self.desc, self.cache, layer, self.q[layer], self.pos, self.ws,
-                                    block_table=self.table, valid_bits=self.valid_bits,
-                                    out=self.out if out is None else out)
+        return kvc.decode_step(self.desc, self.cache, layer, self.q[layer], self.k_new[layer], self.v_new[layer],
+                               self.pos, self.ws, block_table=self.table, valid_bits=self.valid_bits,
+                               out=self.out if out is None else out)
+
+    def launches_per_step(self):
+        """Kernels one kvc_decode_step launches (fused append for bf16 ring layouts)."""
+        bf16 = self.wl.dtype == "bf16"
+        paged = self.wl.layout == "paged"
+        n = 1                              # decode kernel
+        n += 1 if bf16 else 0              # combine kernel (bf16 stream-K)
+        n += 1 if paged else 0             # work plan
+        n += 1 if (paged or not bf16) else 0   # separate append kernel
+        return n
 
 
 class FastCalls:
@@ -252,6 +261,8 @@ class FastCalls:
                      st.pos.data_ptr(), tb, ws, wsn, s) for l in range(st.layers)]
         self.dec = [(d, st.cache.data_ptr(), l, st.q[l].data_ptr(), st.pos.data_ptr(), tb, vb,
                      st.out.data_ptr(), ws, wsn, s) for l in range(st.layers)]
+        self.stp = [(d, st.cache.data_ptr(), l, st.q[l].data_ptr(), st.k_new[l].data_ptr(), st.v_new[l].data_ptr(),
+                     st.pos.data_ptr(), tb, vb, st.out.data_ptr(), ws, wsn, s) for l in range(st.layers)]
 
     def append(self, layer):
         rc = self.L.kvc_append(*self.app[layer])
@@ -262,6 +273,11 @@ class FastCalls:
         rc = self.L.kvc_decode_attention(*self.dec[layer])
         if rc:
             raise RuntimeError(f"kvc_decode_attention: {rc}")
+
+    def step(self, layer):
+        rc = self.L.kvc_decode_step(*self.stp[layer])
+        if rc:
+            raise RuntimeError(f"kvc_decode_step: {rc}")
 
 
 # ---------------------------------------------------------------------------
@@ -433,32 +449,55 @@ def run_ours(args):
 
     # warm-up
     for i in range(args.warmup):
-        fc.append(i % layers)
-        fc.decode(i % layers)
+        fc.step(i % layers)
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # The timed region replays CUDA graphs of the K steps (the launches keep
+    # their programmatic-dependency edges); without --eager the host's launch
+    # cost stays out of the device timeline.  Graph A holds n steps (a whole
+    # number of layer cycles), graph B the remaining K mod n steps.
+    graphs = []
+    timing = "eager"
+    if not args.eager:
+        try:
+            n = min(K, max(layers, (512 // layers) * layers))
+            reps, rest = divmod(K, n)
+            for count in (n, rest):
+                if count == 0 or (count == n and reps == 0):
+                    continue
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fcg = FastCalls(st)           # binds the capture stream
+                    for i in range(count):
+                        fcg.step(i % layers)
+                graphs.append((g, reps if count == n else 1))
+            timing = "cuda_graph"
+        except Exception as exc:                  # capture unsupported: time eagerly
+            graphs = []
+            timing = f"eager (graph capture failed: {type(exc).__name__})"
+        torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
-    torch.cuda._sleep(20_000_000)      # ~10 ms head start: the host enqueues ahead of the GPU
+    if not graphs:
+        torch.cuda._sleep(20_000_000)      # ~10 ms head start: the host enqueues ahead of the GPU
     start.record()
-    for i in range(K):
-        layer = i % layers
-        fc.append(layer)
-        ev[i][0].record()
-        fc.decode(layer)
-        ev[i][1].record()
+    if graphs:
+        for g, r in graphs:
+            for _ in range(r):
+                g.replay()
+    else:
+        for i in range(K):
+            fc.step(i % layers)
     end.record()
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device="cuda")
@@ -466,12 +505,29 @@ def run_ours(args):
         total_ms = float(t.item())
     ms_per_step = total_ms / K
     value = world * nb["step_algorithmic"] / (ms_per_step * 1e-3) / 1e9
-    dec_mean = sum(dec_ms) / len(dec_ms)
-    achieved = nb["decode_algorithmic"] / (dec_mean * 1e-3) / 1e9
+    # the step's kernels (decode + combine, fused append) take the whole step:
+    # per launch of the step, algorithmic bytes / device time per step
+    dec_mean = ms_per_step
+    achieved = nb["step_algorithmic"] / (dec_mean * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     err = kvc.get_error(st.ws)
     if err:
         raise RuntimeError(f"device error bits {err:#x} during the timed region")
+
+    # the same steps launched one by one (untimed for the headline): what a
+    # caller without graphs sees per step
+    eager_ms = None
+    if graphs:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ne = min(K, 2000)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        e0.record()
+        for i in range(ne):
+            fc.step(i % layers)
+        e1.record()
+        torch.cuda.synchronize()
+        eager_ms = e0.elapsed_time(e1) / ne
 
     # end to end: host inputs copied in, host output copied out, every step
     e2e = None
@@ -492,13 +548,18 @@ def run_ours(args):
         "steps_per_s": 1e3 / ms_per_step,
         "bytes_per_step": nb,
         "decode_kernel_ms": dec_mean,
+        "timing": timing,
+        "eager_ms_per_step": eager_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": args.traffic, "kernel": "decode_kernel",
-                     "algorithmic_bytes_per_launch": nb["decode_algorithmic"]},
+                     "traffic": args.traffic,
+                     "kernel": "kvc_decode_step: " + ("decode_mma_kernel + combine_streamk_kernel"
+                                                      if wl.dtype == "bf16" else "append + decode"),
+                     "timer": "CUDA events around the timed region (K kvc_decode_step calls); per step",
+                     "algorithmic_bytes_per_launch": nb["step_algorithmic"]},
         "frac_of_8tbs": value / 8000.0,
         "clocks": clk,
-        "gpu_launches": 2 * K + (K if wl.layout == "paged" else 0),
+        "gpu_launches": st.launches_per_step() * K,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -542,8 +603,7 @@ def _e2e_step(st, fc, layer, hq, hk, hv, hp, hout):
     st.k_new[layer].copy_(hk[layer], non_blocking=True)
     st.v_new[layer].copy_(hv[layer], non_blocking=True)
     st.pos.copy_(hp, non_blocking=True)
-    fc.append(layer)
-    fc.decode(layer)
+    fc.step(layer)
     hout.copy_(st.out, non_blocking=True)
     torch.cuda.current_stream().synchronize()
 
@@ -551,7 +611,7 @@ def _e2e_step(st, fc, layer, hq, hk, hv, hp, hout):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(kvc_synth.WORKLOAD_NAMES), default=DEFAULT_WORKLOAD)
@@ -559,6 +619,7 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode launch from an ncu capture of the current kernel")

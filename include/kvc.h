@@ -170,6 +170,18 @@ KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t l
                                  const int32_t* block_table, const uint32_t* valid_bits,
                                  void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step: kvc_append of the token at pos[b] (n_new = 1), then
+ * kvc_decode_attention at pos[b], with the same arguments and results as
+ * that pair of calls.  For bf16 RING / SINK_RING caches the append is fused
+ * into the attention kernel (the CTA that reads the token's slot writes it,
+ * with RoPE baked when BAKED, to the cache and to its own copy of the tile);
+ * otherwise the two calls are made in turn.
+ *   k_new, v_new  [batch, kv_heads, head_dim], pre-RoPE, 16-byte aligned. */
+KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const void* q,
+                            const void* k_new, const void* v_new, const int32_t* pos,
+                            const int32_t* block_table, const uint32_t* valid_bits,
+                            void* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Batched block-table update ([share] 3.1 block table, 5.1 block manager):
  * for each i < n, block_table[seq[i]][logical_block[i]] = physical_block[i];
  * -1 unmaps.  When valid_bits is not NULL, each mapped physical block gets its

@@ -33,7 +33,7 @@ KVC_DEV_TIMEOUT, KVC_DEV_BAD_ENTRY = 0x8, 0x10
 ABI_FUNCTIONS = (
     "kvc_cache_bytes", "kvc_workspace_bytes", "kvc_workspace_init", "kvc_append",
     "kvc_decode_attention", "kvc_block_table_write", "kvc_valid_write", "kvc_get_error",
-    "kvc_strerror", "kvc_decode_attention_noalloc",
+    "kvc_strerror", "kvc_decode_attention_noalloc", "kvc_decode_step",
 )
 
 
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.kvc_valid_write.argtypes = [dp, vp, i32, vp, vp, vp, sz, vp]
         L.kvc_get_error.argtypes = [vp, vp]
         L.kvc_decode_attention_noalloc.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kvc_decode_step.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.kvc_strerror.argtypes = [ctypes.c_int]
         L.kvc_strerror.restype = ctypes.c_char_p
         for name in ABI_FUNCTIONS:
@@ -222,6 +223,32 @@ def decode_attention(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tenso
                                       _ptr(block_table), _ptr(valid_bits), _ptr(out), _ptr(workspace),
                                       workspace.numel(), _stream(stream)),
            "kvc_decode_attention")
+    return out
+
+
+def decode_step(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, k_new: torch.Tensor,
+                v_new: torch.Tensor, pos: torch.Tensor, workspace: torch.Tensor,
+                block_table: torch.Tensor | None = None, valid_bits: torch.Tensor | None = None,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvc_decode_step: append the token at pos (k_new / v_new [batch, kv_heads, D]) and attend."""
+    dt = desc_dtype(d)
+    _need(cache, "cache", dt)
+    _need(q, "q", dt, d.batch * d.q_heads * d.head_dim)
+    _need(k_new, "k_new", dt, d.batch * d.kv_heads * d.head_dim)
+    _need(v_new, "v_new", dt, d.batch * d.kv_heads * d.head_dim)
+    _need(pos, "pos", torch.int32, d.batch)
+    _need(workspace, "workspace", torch.uint8)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, d.batch * d.max_blocks_per_seq)
+    if valid_bits is not None:
+        _need(valid_bits, "valid_bits", torch.int32, (d.num_blocks + 31) // 32)
+    if out is None:
+        out = torch.empty((d.batch, d.q_heads, d.head_dim), dtype=dt, device=q.device)
+    _need(out, "out", dt, d.batch * d.q_heads * d.head_dim)
+    _check(lib().kvc_decode_step(ctypes.byref(d), _ptr(cache), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                 _ptr(pos), _ptr(block_table), _ptr(valid_bits), _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)),
+           "kvc_decode_step")
     return out
 
 

@@ -112,10 +112,15 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-void fill_theta(int D, float base, double* theta, float* theta_f) {
+// theta_i = base^(-2i/D); passed as fp32 (small in-tile angles) and as the
+// 64-bit fixed-point fraction of a turn theta_i / (2 pi) * 2^64 used for
+// exact reduction of pos * theta_i on the device.
+void fill_theta(int D, float base, unsigned long long* turns, float* theta_f) {
+    const double two_pi = 6.283185307179586476925286766559;
     for (int i = 0; i < D / 2; ++i) {
-        theta[i] = std::pow((double)base, -2.0 * i / D);
-        if (theta_f) theta_f[i] = (float)theta[i];
+        const double th = std::pow((double)base, -2.0 * i / D);
+        turns[i] = (unsigned long long)std::ldexp(th / two_pi, 64);
+        if (theta_f) theta_f[i] = (float)th;
     }
 }
 
@@ -201,6 +206,97 @@ int make_kv_tensor_map(const kvc_desc* d, const Geo& g, const void* cache, CUten
 
 using namespace kvc;
 
+extern "C" KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer, const void* k_new, const void* v_new,
+                                  int32_t n_new, const int32_t* pos, const int32_t* block_table, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, const void* q, const void* k_new,
+                       const void* v_new, const int32_t* pos, const int32_t* block_table,
+                       const uint32_t* valid_bits, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (!cache || !q || !pos || !out || !workspace) return KVC_ERR_NULL;
+    const bool paged = d->layout == KVC_LAYOUT_PAGED;
+    if (paged && !block_table) return KVC_ERR_NULL;
+    if (!aligned16(cache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVC_ERR_ALIGN;
+    if (layer < 0 || layer >= d->layers) return KVC_ERR_ARG;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    DecodeParams p{};
+    p.cache = cache;
+    p.q = q;
+    p.pos = pos;
+    p.table = block_table;
+    p.valid = valid_bits;
+    p.out = out;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.err = reinterpret_cast<uint32_t*>(ws + w.err);
+    p.counters = reinterpret_cast<uint32_t*>(ws + w.counters);
+    p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+    p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+    p.layer_off = (long long)layer * 2 * g.half_elems;
+    p.kv_off = g.half_elems;
+    p.B = d->batch;
+    p.Hq = d->q_heads;
+    p.Hkv = d->kv_heads;
+    p.G = g.G;
+    p.nsub = g.nsub;
+    p.window = d->window;
+    p.sinks = d->layout == KVC_LAYOUT_SINK_RING ? d->sinks : 0;
+    p.capacity = g.C;
+    p.bs = d->block_size;
+    p.num_blocks = d->num_blocks;
+    p.maxb = d->max_blocks_per_seq;
+    p.nsplit = d->dtype == KVC_BF16 ? w.ctas : w.nsplit;   // bf16: stream-K CTAs per (kv head, group)
+    p.max_items = w.items;
+    p.rope = d->rope;
+    const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+    p.q_scale = scale * 1.4426950408889634f;   // log2(e): softmax in base 2
+    if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
+
+    dim3 grid(d->dtype == KVC_BF16 ? w.ctas : w.items, d->kv_heads, g.nsub);
+    if (paged) {
+        PlanParams pp{};
+        pp.pos = pos;
+        pp.table = block_table;
+        pp.valid = valid_bits;
+        pp.err = p.err;
+        pp.rows = reinterpret_cast<int32_t*>(ws + w.plan_rows);
+        pp.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
+        pp.items = reinterpret_cast<int4*>(ws + w.plan_items);
+        pp.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
+        pp.cta_items = reinterpret_cast<int2*>(ws + w.plan_cta);
+        pp.ctas = w.ctas;
+        pp.B = d->batch;
+        pp.bs = d->block_size;
+        pp.num_blocks = d->num_blocks;
+        pp.maxb = d->max_blocks_per_seq;
+        pp.max_items = w.items;
+        if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
+        p.items = pp.items;
+        p.seq_items = pp.seq_items;
+        p.n_items = pp.n_items;
+        p.cta_items = pp.cta_items;
+    }
+    const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
+    if (d->dtype == KVC_BF16) {
+        CUtensorMap map;
+        rc = make_kv_tensor_map(d, g, cache, &map);
+        if (rc) return rc;
+        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, p, &map, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
+        return KVC_OK;
+    }
+    if (launch_decode(d->dtype, d->head_dim, g.GH, paged, rd, p, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
+
 extern "C" {
 
 KVC_API size_t kvc_cache_bytes(const kvc_desc* d) {
@@ -269,84 +365,28 @@ KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer, const void
 KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t layer, const void* q,
                                  const int32_t* pos, const int32_t* block_table, const uint32_t* valid_bits,
                                  void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return decode_impl(d, cache, layer, q, nullptr, nullptr, pos, block_table, valid_bits, out, workspace,
+                       workspace_bytes, stream);
+}
+
+KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const void* q, const void* k_new,
+                            const void* v_new, const int32_t* pos, const int32_t* block_table,
+                            const uint32_t* valid_bits, void* out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
     Geo g;
     int rc = check_desc(d, &g);
     if (rc) return rc;
-    if (!cache || !q || !pos || !out || !workspace) return KVC_ERR_NULL;
-    const bool paged = d->layout == KVC_LAYOUT_PAGED;
-    if (paged && !block_table) return KVC_ERR_NULL;
-    if (!aligned16(cache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVC_ERR_ALIGN;
-    if (layer < 0 || layer >= d->layers) return KVC_ERR_ARG;
-    const WorkspaceLayout w = ws_layout(d, g);
-    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
-    char* ws = static_cast<char*>(workspace);
-    cudaStream_t s = (cudaStream_t)stream;
-
-    DecodeParams p{};
-    p.cache = cache;
-    p.q = q;
-    p.pos = pos;
-    p.table = block_table;
-    p.valid = valid_bits;
-    p.out = out;
-    p.err = reinterpret_cast<uint32_t*>(ws + w.err);
-    p.counters = reinterpret_cast<uint32_t*>(ws + w.counters);
-    p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
-    p.part_o = reinterpret_cast<float*>(ws + w.part_o);
-    p.layer_off = (long long)layer * 2 * g.half_elems;
-    p.kv_off = g.half_elems;
-    p.B = d->batch;
-    p.Hq = d->q_heads;
-    p.Hkv = d->kv_heads;
-    p.G = g.G;
-    p.nsub = g.nsub;
-    p.window = d->window;
-    p.sinks = d->layout == KVC_LAYOUT_SINK_RING ? d->sinks : 0;
-    p.capacity = g.C;
-    p.bs = d->block_size;
-    p.num_blocks = d->num_blocks;
-    p.maxb = d->max_blocks_per_seq;
-    p.nsplit = w.nsplit;
-    p.max_items = w.items;
-    p.rope = d->rope;
-    const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
-    p.q_scale = scale * 1.4426950408889634f;   // log2(e): softmax in base 2
-    if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
-
-    dim3 grid(d->dtype == KVC_BF16 ? w.ctas : w.items, d->kv_heads, g.nsub);
-    if (paged) {
-        PlanParams pp{};
-        pp.pos = pos;
-        pp.table = block_table;
-        pp.valid = valid_bits;
-        pp.err = p.err;
-        pp.rows = reinterpret_cast<int32_t*>(ws + w.plan_rows);
-        pp.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
-        pp.items = reinterpret_cast<int4*>(ws + w.plan_items);
-        pp.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
-        pp.cta_items = reinterpret_cast<int2*>(ws + w.plan_cta);
-        pp.ctas = w.ctas;
-        pp.B = d->batch;
-        pp.bs = d->block_size;
-        pp.num_blocks = d->num_blocks;
-        pp.maxb = d->max_blocks_per_seq;
-        pp.max_items = w.items;
-        if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
-        p.items = pp.items;
-        p.seq_items = pp.seq_items;
-        p.n_items = pp.n_items;
-        p.cta_items = pp.cta_items;
+    if (!k_new || !v_new) return KVC_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGN;
+    if (d->dtype == KVC_BF16 && d->layout != KVC_LAYOUT_PAGED) {
+        // one launch pair: the decode kernel writes the new token itself
+        return decode_impl(d, cache, layer, q, k_new, v_new, pos, block_table, valid_bits, out, workspace,
+                           workspace_bytes, stream);
     }
-    const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
-    if (d->dtype == KVC_BF16) {
-        CUtensorMap map;
-        rc = make_kv_tensor_map(d, g, cache, &map);
-        if (rc) return rc;
-        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, p, &map, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
-        return KVC_OK;
-    }
-    if (launch_decode(d->dtype, d->head_dim, g.GH, paged, rd, p, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
-    return KVC_OK;
+    rc = kvc_append(d, cache, layer, k_new, v_new, 1, pos, block_table, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+    return decode_impl(d, cache, layer, q, nullptr, nullptr, pos, block_table, valid_bits, out, workspace,
+                       workspace_bytes, stream);
 }
 
 KVC_API int kvc_block_table_write(const kvc_desc* d, int32_t* block_table, uint32_t* valid_bits, int32_t n,

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
                 if constexpr (READ) {
                     for (int i = lane; i < HALF; i += 32) {
                         float c, sn;
-                        rope_cos_sin((double)ipb, p.theta[i], &c, &sn);
+                        rope_cos_sin((long long)ipb, p.theta[i], &c, &sn);
                         rot[s * HALF + i] = make_float2(c, sn);
                     }
                 }
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const __grid_
     if (p.rope != kRopeNone) {
         for (int i = ctid; i < HALF; i += kConsumerWarps * 32) {
             float c, sn;
-            rope_cos_sin((double)qpos, p.theta[i], &c, &sn);
+            rope_cos_sin((long long)qpos, p.theta[i], &c, &sn);
             qcs[i] = make_float2(c, sn);
         }
     }

@@ -72,6 +72,7 @@ struct alignas(16) MmaStageMeta {
     int pad[2];
     int nrows[4];    // rows of each sub-tile (1..16)
     int ip0[4];      // READ_INCACHE: in-cache position of row 0 of each sub-tile
+    int newrow[4];   // fused append: row of the sub-tile that holds the new token, else -1
     MmaSegment seg;  // valid with kSegBegin
 };
 constexpr int kSegBegin = 1, kSegEnd = 2;
@@ -107,6 +108,153 @@ struct BoundedBarrier {
     }
 };
 
+// Programmatic dependent launch: wait for the preceding kernel in the stream
+// to complete (its writes visible), and let the next one start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Stream-K partition of a window layout for one (kv head, q-head group):
+// sequence b contributes max(1, ceil(n_live(b) / 16)) sub-tiles.  Returns the
+// grand total and b's offset and size to every lane of the calling warp.
+__device__ __forceinline__ void window_partition(const DecodeParams& p, int b, long long* total, long long* Ob,
+                                                 long long* Sb) {
+    const int lane = threadIdx.x & 31;
+    const int C = p.capacity;
+    long long tot = 0, before = 0, sb = 0;
+    for (int base = 0; base < p.B; base += 32) {
+        const int bb = base + lane;
+        long long st = 0;
+        if (bb < p.B) {
+            const int tb = p.pos[bb];
+            const int nl = tb < 0 ? 0 : (tb + 1 < C ? tb + 1 : C);
+            st = nl > 0 ? (nl + 15) / 16 : 1;
+        }
+        long long pre = bb < b ? st : 0;
+        long long me = bb == b ? st : 0;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            st += __shfl_xor_sync(0xffffffffu, st, off);
+            pre += __shfl_xor_sync(0xffffffffu, pre, off);
+            me += __shfl_xor_sync(0xffffffffu, me, off);
+        }
+        tot += st;
+        before += pre;
+        sb += me;
+    }
+    *total = tot;
+    *Ob = before;
+    *Sb = sb;
+}
+
+// ---------------------------------------------------------------------------
+// Combine kernel for the stream-K decode: one CTA per (sequence, kv head,
+// q-head group, 32-column chunk).  out = sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)
+// over the sequence's partials, M = max m_i; an empty attended set gives 0.
+// Threads split the partials four ways and reduce through shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kCombineThreads = 128;
+constexpr int kCombineCols = 32;
+
+template <int D, int GH, bool PAGED>
+__global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int C4 = kCombineCols / 4;           // float4 columns per chunk
+    constexpr int PAIRS = GH * C4;                 // (head, float4) outputs of the chunk
+    constexpr int PG = kCombineThreads / PAIRS;    // partial groups
+    constexpr int kMaxStaged = 1024;
+    __shared__ float2 s_ml[kMaxStaged];
+    __shared__ float s_M[GH], s_L[GH];
+    __shared__ float4 s_part[kCombineThreads];
+
+    const int b = blockIdx.x;
+    const int kvh = blockIdx.y / p.nsub, z = blockIdx.y % p.nsub;
+    const int col0 = blockIdx.z * kCombineCols;
+    const int tid = threadIdx.x;
+    const int qh0 = kvh * p.G + z * GH;
+
+    // which partial slots belong to sequence b (inputs that the decode kernel does not write)
+    int first = 0, nparts = 0;
+    if constexpr (PAGED) {
+        pdl_wait();                                 // the plan is written by an earlier kernel
+        const int2 si = p.seq_items[b];
+        first = si.x;
+        nparts = si.y;
+    } else {
+        __shared__ int s_fn[2];
+        if (tid < 32) {
+            long long total, Ob, Sb;
+            window_partition(p, b, &total, &Ob, &Sb);
+            const int G = (int)(total < p.nsplit ? total : p.nsplit);
+            const int fx = streamk_share_of(Ob, total, G);
+            const int lx = streamk_share_of(Ob + Sb - 1, total, G);
+            if (tid == 0) {
+                s_fn[0] = fx + b;
+                s_fn[1] = lx - fx + 1;
+            }
+        }
+        __syncthreads();
+        first = s_fn[0];
+        nparts = s_fn[1];
+        pdl_wait();                                 // the decode kernel's partials
+    }
+    if (first < 0 || nparts < 1 || first + nparts > p.max_items) {
+        if (tid == 0) index_fault(p.err, 20, first);
+        return;
+    }
+    const int npl = nparts * GH;
+    const bool staged = npl <= kMaxStaged;
+    if (staged)
+        for (int i = tid; i < npl; i += kCombineThreads)
+            s_ml[i] = __ldcg(&p.part_ml[(long long)(first + i / GH) * p.Hq + qh0 + i % GH]);
+    __syncthreads();
+    auto ml_of = [&](int k, int h) -> float2 {
+        return staged ? s_ml[k * GH + h] : __ldcg(&p.part_ml[(long long)(first + k) * p.Hq + qh0 + h]);
+    };
+    if (tid < GH) {
+        float M = -INFINITY;
+        for (int k = 0; k < nparts; ++k) M = fmaxf(M, ml_of(k, tid).x);
+        float L = 0.f;
+        for (int k = 0; k < nparts; ++k) {
+            const float2 ml = ml_of(k, tid);
+            L += (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
+        }
+        s_M[tid] = M;
+        s_L[tid] = L;
+    }
+    __syncthreads();
+    const int pair = tid % PAIRS, grp = tid / PAIRS;
+    const int h = pair / C4, c4 = pair % C4;
+    const int d0 = col0 + c4 * 4;
+    const float M = s_M[h];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int k = grp; k < nparts; k += PG) {
+        const float2 ml = ml_of(k, h);
+        const float e = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+        const float4 v =
+            __ldcg(reinterpret_cast<const float4*>(p.part_o + ((long long)(first + k) * p.Hq + qh0 + h) * D + d0));
+        acc.x += v.x * e;
+        acc.y += v.y * e;
+        acc.z += v.z * e;
+        acc.w += v.w * e;
+    }
+    s_part[tid] = acc;
+    __syncthreads();
+    if (grp == 0) {
+        for (int gI = 1; gI < PG; ++gI) {
+            const float4 o = s_part[gI * PAIRS + pair];
+            acc.x += o.x;
+            acc.y += o.y;
+            acc.z += o.z;
+            acc.w += o.w;
+        }
+        const float L = s_L[h];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + ((long long)b * p.Hq + qh0 + h) * D + d0;
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
+}
+
 template <int D, int GH, bool PAGED, bool READ>
 __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmap) {
@@ -126,7 +274,6 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
     float2* qcs = reinterpret_cast<float2*>(smem + SM::kQcs);
     float* merge_o = reinterpret_cast<float*>(smem + SM::kMergeO);
     float2* merge_ml = reinterpret_cast<float2*>(smem + SM::kMergeML);
-    int* flag = reinterpret_cast<int*>(smem + SM::kFlag);
     uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + SM::kCbar);
 
     const int tid = threadIdx.x;
@@ -151,6 +298,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
         mbar_fence_init();
         tma_prefetch_desc(&tmap);
     }
+    pdl_wait();                 // inputs written by earlier kernels (append, plan) are visible
+    pdl_launch_dependents();    // the combine kernel may start launching
     __syncthreads();
 
     // tensor-map rows: [layers][K | V][rows of the half][D]
@@ -197,20 +346,21 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
         // the last stage of a segment is still open here and carries kSegEnd.
         auto end_segment = [&]() { commit(kSegEnd); };
         // one sub-tile: `n` rows starting at tensor-map row `krow` (K half)
-        auto emit = [&](long long krow, int n, int ip0) -> bool {
+        auto emit = [&](long long krow, int n, int ip0, int newrow) -> bool {
             if (open && fill == NSUB) commit(0);
             if (!open && !open_stage()) return false;
             const int s = it % NST;
             if constexpr (READ) {
                 for (int i = lane; i < HALF; i += 32) {
                     float cs, sn;
-                    rope_cos_sin((double)ip0, p.theta[i], &cs, &sn);
+                    rope_cos_sin((long long)ip0, p.theta[i], &cs, &sn);
                     rot[(s * NSUB + fill) * HALF + i] = make_float2(cs, sn);
                 }
             }
             if (lane == 0) {
                 meta[s].nrows[fill] = n;
                 meta[s].ip0[fill] = ip0;
+                meta[s].newrow[fill] = newrow;
                 unsigned char* kdst = stage_base + (size_t)s * S::kStageBytes + (size_t)fill * S::kSubBytes;
                 unsigned char* vdst = kdst + (size_t)NSUB * S::kSubBytes;
                 mbar_expect_tx(&full[s], 2 * S::kSubBytes);
@@ -281,11 +431,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                     const int r0 = (int)((lo > Ob ? lo : Ob) - Ob) * 16;
                     const int r1 = min((int)((hi < Ob + Sb ? hi : Ob + Sb) - Ob) * 16, nl_b);
                     const long long base_row = layer_row0 + ((long long)b * p.Hkv + kvh) * C;
+                    // slot of the token being decoded: the ring's wrap point, and
+                    // (fused append) the row that receives the new K/V
                     int h_slot = 0;
-                    if constexpr (READ) {
-                        if (t_b >= 0)
-                            h_slot = t_b < p.sinks ? t_b : p.sinks + (int)(((long long)t_b - p.sinks) % p.window);
-                    }
+                    if (t_b >= 0)
+                        h_slot = t_b < p.sinks ? t_b : p.sinks + (int)(((long long)t_b - p.sinks) % p.window);
                     for (int r = r0; r < r1 && ok;) {
                         int n = min(16, r1 - r);
                         int ip0 = 0;
@@ -295,7 +445,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                             n = min(n, seg_end - r);
                             ip0 = incache_of_slot(r, t_b, p.sinks, p.window, C);
                         }
-                        ok = emit(base_row + r, n, ip0);
+                        const int newrow = (p.k_new && t_b >= 0 && h_slot >= r && h_slot < r + n) ? h_slot - r : -1;
+                        ok = emit(base_row + r, n, ip0, newrow);
                         r += n;
                     }
                     if (ok) end_segment();
@@ -344,7 +495,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                         const long long blk = layer_row0 + ((long long)phys * p.Hkv + kvh) * p.bs;
                         while (take > 0 && ok) {
                             const int n = min(16, take);
-                            ok = emit(blk + row, n, 0);
+                            ok = emit(blk + row, n, 0, -1);
                             take -= n;
                             rem -= n;
                             row += n;
@@ -420,7 +571,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
         if (p.rope != kRopeNone) {
             for (int i = ctid; i < HALF; i += NCT) {
                 float cs, sn;
-                rope_cos_sin((double)qpos, p.theta[i], &cs, &sn);
+                rope_cos_sin((long long)qpos, p.theta[i], &cs, &sn);
                 qcs[i] = make_float2(cs, sn);
             }
         }
@@ -466,12 +617,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
         l_run = 0.f;
     };
 
-    // end of a segment: merge the warps, write the segment's partial, and let
-    // the last CTA of the sequence combine all its partials
+    // end of a segment: merge the warps and write the segment's partial
+    // (m, l, o) per q head; the combine kernel merges a sequence's partials
     auto finish_segment = [&]() {
         if (seg.b < 0) {                          // rejected segment: keep the barrier sequence
-            csync.sync(p.err);
-            csync.sync(p.err);
             csync.sync(p.err);
             csync.sync(p.err);
             return;
@@ -485,79 +634,33 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
 #pragma unroll
             for (int j = 0; j < S::kNt; ++j) {
                 const int col = (hd * S::kNt + j) * 8 + 2 * c;
-                mo[col] = o[j][0];
-                mo[col + 1] = o[j][1];
+                *reinterpret_cast<float2*>(mo + col) = make_float2(o[j][0], o[j][1]);
             }
             if (c == 0 && hd == 0) merge_ml[tg * GH + g] = make_float2(m_run, lq);
         }
         csync.sync(p.err);
         const int qh0 = kvh * p.G + z * GH;
-        for (int idx = ctid; idx < GH * D; idx += NCT) {
-            const int h = idx / D, d = idx % D;
+        for (int i4 = ctid; i4 < GH * D / 4; i4 += NCT) {
+            const int h = (i4 * 4) / D, d = (i4 * 4) % D;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < S::kTokenGroups; ++w) M = fmaxf(M, merge_ml[w * GH + h].x);
-            float L = 0.f, O = 0.f;
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < S::kTokenGroups; ++w) {
                 const float2 ml = merge_ml[w * GH + h];
                 const float e = (ml.x == M) ? 1.f : exp2f(ml.x - M);
+                const float4 v = *reinterpret_cast<const float4*>(merge_o + (w * GH + h) * D + d);
                 L += ml.y * e;
-                O += merge_o[(w * GH + h) * D + d] * e;
+                O.x += v.x * e;
+                O.y += v.y * e;
+                O.z += v.z * e;
+                O.w += v.w * e;
             }
             const long long slot = (long long)seg.slot * p.Hq + qh0 + h;
-            p.part_o[slot * D + d] = O;
+            *reinterpret_cast<float4*>(p.part_o + slot * D + d) = O;
             if (d == 0) p.part_ml[slot] = make_float2(M, L);
-        }
-        __threadfence();
-        csync.sync(p.err);
-        const long long cidx = ((long long)seg.b * p.Hkv + kvh) * p.nsub + z;
-        if (ctid == 0) {
-            const unsigned ticket = atomicAdd(&p.counters[cidx], 1u);
-            *flag = (ticket == (unsigned)(seg.nparts - 1));
-        }
-        csync.sync(p.err);
-        if (*flag) {
-            __threadfence();
-            // (m, l) of every partial staged in shared memory (merge_o is free now)
-            float2* sml = reinterpret_cast<float2*>(merge_o);
-            constexpr int kCap = S::kTokenGroups * GH * D / 2;
-            const int npl = seg.nparts * GH;
-            const bool staged = npl <= kCap;
-            if (staged) {
-                for (int i = ctid; i < npl; i += NCT)
-                    sml[i] = __ldcg(&p.part_ml[(long long)(seg.first_slot + i / GH) * p.Hq + qh0 + i % GH]);
-            }
-            csync.sync(p.err);
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-            for (int o4 = ctid; o4 < GH * D / 4; o4 += NCT) {
-                const int h = (o4 * 4) / D, d0 = (o4 * 4) % D;
-                auto ml_of = [&](int k) -> float2 {
-                    return staged ? sml[k * GH + h]
-                                  : __ldcg(&p.part_ml[(long long)(seg.first_slot + k) * p.Hq + qh0 + h]);
-                };
-                float M = -INFINITY;
-                for (int k = 0; k < seg.nparts; ++k) M = fmaxf(M, ml_of(k).x);
-                float L = 0.f;
-                float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int k = 0; k < seg.nparts; ++k) {
-                    const float2 ml = ml_of(k);
-                    const float e = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                        p.part_o + ((long long)(seg.first_slot + k) * p.Hq + qh0 + h) * D + d0));
-                    L += ml.y * e;
-                    O.x += v.x * e;
-                    O.y += v.y * e;
-                    O.z += v.z * e;
-                    O.w += v.w * e;
-                }
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                __nv_bfloat16* dst = out + ((long long)seg.b * p.Hq + qh0 + h) * D + d0;
-                *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(O.x * inv, O.y * inv),
-                                                            pack_bf16x2(O.z * inv, O.w * inv));
-            }
-            if (ctid == 0) p.counters[cidx] = 0u;
         }
     };
 
@@ -590,6 +693,50 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
             unsigned char* Vs = Ks + (size_t)NSUB * S::kSubBytes;
             const uint32_t ku = smem_u32(Ks), vu = smem_u32(Vs);
             bool wrote = false;
+
+            if constexpr (!PAGED) {
+                // fused append (kvc_decode_step): this sub-tile holds the slot of the
+                // token being decoded.  Write its K (RoPE baked at t when BAKED) and V
+                // to the cache, and over the stale row just copied into shared memory.
+                const int nr = meta[s].newrow[tg];
+                if (nr >= 0) {
+                    if (hd == 0) {
+                        const long long unit = (long long)seg.b * p.Hkv + kvh;
+                        const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(p.k_new) + unit * D;
+                        const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(p.v_new) + unit * D;
+                        const int h_slot = seg.t < p.sinks ? seg.t
+                                                           : p.sinks + (int)(((long long)seg.t - p.sinks) % p.window);
+                        __nv_bfloat16* kg = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(p.cache)) +
+                                            p.layer_off + (unit * p.capacity + h_slot) * D;
+                        __nv_bfloat16* vg = kg + p.kv_off;
+                        for (int i = lane; i < HALF; i += 32) {
+                            __nv_bfloat16 k1 = kn[i], k2 = kn[i + HALF];
+                            if (p.rope == kRopeBaked) {
+                                float cs, sn;
+                                rope_cos_sin((long long)seg.t, p.theta[i], &cs, &sn);
+                                const float x1 = __bfloat162float(k1), x2 = __bfloat162float(k2);
+                                k1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
+                                k2 = __float2bfloat16_rn(x1 * sn + x2 * cs);
+                            }
+                            const __nv_bfloat16 v1 = vn[i], v2 = vn[i + HALF];
+                            kg[i] = k1;
+                            kg[i + HALF] = k2;
+                            vg[i] = v1;
+                            vg[i + HALF] = v2;
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int col = i + e * HALF;
+                                const int off = (col >> 6) * S::kBoxBytes + nr * 128 +
+                                                (((((col & 63) >> 3)) ^ (nr & 7)) << 4) + (col & 7) * 2;
+                                *reinterpret_cast<__nv_bfloat16*>(Ks + off) = e ? k2 : k1;
+                                *reinterpret_cast<__nv_bfloat16*>(Vs + off) = e ? v2 : v1;
+                            }
+                        }
+                    }
+                    wrote = true;
+                    if constexpr (S::kDsplit == 2) psync.sync(p.err); else __syncwarp();
+                }
+            }
 
             if constexpr (READ) {
                 // rotate the stored (raw) K rows in place by R((ip0 + r) theta),
@@ -712,6 +859,7 @@ template <int D, int GH, bool PAGED, bool READ>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 grid, cudaStream_t stream) {
     using SM = MmaSmem<D, GH, READ>;
     auto kern = decode_mma_kernel<D, GH, PAGED, READ>;
+    auto comb = combine_streamk_kernel<D, GH, PAGED>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -722,8 +870,28 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 gr
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_relaxed);
     }
-    kern<<<grid, kDecodeThreads, SM::kTotal, stream>>>(p, *static_cast<const CUtensorMap*>(tmap));
-    return cudaGetLastError();
+    // both launches may begin while the previous kernel in the stream drains;
+    // each waits (griddepcontrol.wait) before touching that kernel's outputs
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = SM::kTotal;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, *static_cast<const CUtensorMap*>(tmap));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(p.B, p.Hkv * p.nsub, D / kCombineCols);
+    ccfg.blockDim = dim3(kCombineThreads);
+    ccfg.dynamicSmemBytes = 0;
+    ccfg.stream = stream;
+    ccfg.attrs = &attr;
+    ccfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&ccfg, comb, p);
 }
 
 }  // namespace kvc

@@ -57,20 +57,18 @@ __device__ __forceinline__ void index_fault(uint32_t* err, uint32_t site, long l
 }
 
 // ---------------------------------------------------------------------------
-// RoPE angle: pos * theta reduced to [-pi, pi] in fp64 (two-constant
-// Cody-Waite reduction), then sin/cos in fp32.  Keeps the rotation accurate at
-// positions of 10^5 - 10^6, where an fp32 product pos * theta would already
-// be off by ~1e-2 rad.
+// RoPE angle pos * theta_i, reduced exactly: the host passes
+// F_i = theta_i / (2 pi) * 2^64 as an unsigned 64-bit fixed-point fraction of a
+// turn; pos * F_i mod 2^64 (integer multiply, wraps) is the angle's fraction
+// of a turn, whose top 32 bits, read as a signed number, place it in
+// [-1/2, 1/2) turn.  Error: the rounding of F_i (2^-53 relative, ~1e-11 rad at
+// pos = 2^20) plus one fp32 rounding (~2e-7 rad); fp32 pos * theta would be
+// off by ~1e-2 rad at pos ~ 2.6e5, fp64 is slow on this part.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void rope_cos_sin(double pos, double theta, float* c, float* s) {
-    const double kInv2Pi = 0.15915494309189535;      // 1 / (2 pi)
-    const double k2PiHi = 6.283185307179586;         // 2 pi rounded to fp64
-    const double k2PiLo = 2.4492935982947064e-16;    // 2 pi - k2PiHi
-    double a = pos * theta;
-    double k = rint(a * kInv2Pi);
-    double r = fma(-k, k2PiHi, a);
-    r = fma(-k, k2PiLo, r);
-    sincosf((float)r, s, c);
+__device__ __forceinline__ void rope_cos_sin(long long pos, unsigned long long turn_frac, float* c, float* s) {
+    const unsigned long long ph = (unsigned long long)pos * turn_frac;     // mod 2^64
+    const float turns = (float)(int)(unsigned)(ph >> 32) * 2.3283064365386963e-10f;   // 2^-32
+    sincosf(turns * 6.283185307179586f, s, c);
 }
 
 // ---------------------------------------------------------------------------

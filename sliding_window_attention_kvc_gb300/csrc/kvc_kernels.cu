@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
         const Elt k1 = kr[i], k2 = kr[i + half];
         if (p.rope == kRopeBaked) {
             float c, s;
-            rope_cos_sin((double)pos, p.theta[i], &c, &s);
+            rope_cos_sin((long long)pos, p.theta[i], &c, &s);
             const float x1 = TR::to_f32(k1), x2 = TR::to_f32(k2);
             kd[i] = TR::from_f32(x1 * c - x2 * s);
             kd[i + half] = TR::from_f32(x1 * s + x2 * c);
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const long long R = s_carry;
     const int G = (int)(R < p.ctas ? (R > 0 ? R : 1) : p.ctas);   // no empty shares
 
-    // 2. items, one thread per sequence
+    // 2a. per sequence: offset, rows, first and last share
     for (int b = tid; b < p.B; b += kPlanThreads) {
         const int32_t* P = p.rows;
         const long long Ob = b > 0 ? P[(long long)b * p.maxb - 1] : 0;
@@ -168,31 +168,45 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             fx = lx = R > 0 ? streamk_share_of(Ob < R ? Ob : R - 1, R, G) : 0;
         }
         p.seq_items[b] = make_int2(fx + b, lx - fx + 1);
-        for (int x = fx; x <= lx; ++x) {
-            const long long lo = (long long)x * R / G, hi = (long long)(x + 1) * R / G;
-            const long long s0 = (lo > Ob ? lo : Ob) - Ob;
-            const long long s1 = (hi < Ob + Rb ? hi : Ob + Rb) - Ob;
-            int lb = 0, off = 0;
-            if (s1 > s0) {
-                // first block whose (sequence-local) inclusive prefix exceeds s0
-                int lo_b = 0, hi_b = p.maxb - 1;
-                const int32_t* Pb = P + (long long)b * p.maxb;
-                while (lo_b < hi_b) {
-                    const int mid = (lo_b + hi_b) >> 1;
-                    if (Pb[mid] - Ob > s0) hi_b = mid; else lo_b = mid + 1;
-                }
-                lb = lo_b;
-                off = (int)(s0 - ((lb > 0 ? Pb[lb - 1] : Ob) - Ob));
-            }
-            const int item = x + b;
-            if (item >= p.max_items || x >= p.ctas) {
-                index_fault(p.err, 6, item);
-                continue;
-            }
-            p.items[item] = make_int4(b, lb, off, (int)(s1 > s0 ? s1 - s0 : 0));
-            atomicMin(&p.cta_items[x].x, item);
-            atomicAdd(&p.cta_items[x].y, 1);
+    }
+    __syncthreads();
+    // 2b. one thread per item index i = x + b: its sequence by binary search
+    // over the sequences' first items, then its first block and row
+    for (int i = tid; i < G + p.B && i < p.max_items; i += kPlanThreads) {
+        int lo_s = 0, hi_s = p.B - 1;
+        while (lo_s < hi_s) {                 // last sequence whose first item <= i
+            const int mid = (lo_s + hi_s + 1) >> 1;
+            if (p.seq_items[mid].x <= i) lo_s = mid; else hi_s = mid - 1;
         }
+        const int b = lo_s;
+        const int2 si = p.seq_items[b];
+        if (i < si.x || i >= si.x + si.y) continue;      // unused index (stays -1)
+        const int x = i - b;
+        if (x < 0 || x >= p.ctas) {
+            index_fault(p.err, 6, i);
+            continue;
+        }
+        const int32_t* P = p.rows;
+        const long long Ob = b > 0 ? P[(long long)b * p.maxb - 1] : 0;
+        const long long Rb = P[(long long)(b + 1) * p.maxb - 1] - Ob;
+        const long long lo = (long long)x * R / G, hi = (long long)(x + 1) * R / G;
+        const long long s0 = (lo > Ob ? lo : Ob) - Ob;
+        const long long s1 = (hi < Ob + Rb ? hi : Ob + Rb) - Ob;
+        int lb = 0, off = 0;
+        if (s1 > s0) {
+            // first block whose (sequence-local) inclusive prefix exceeds s0
+            int lo_b = 0, hi_b = p.maxb - 1;
+            const int32_t* Pb = P + (long long)b * p.maxb;
+            while (lo_b < hi_b) {
+                const int mid = (lo_b + hi_b) >> 1;
+                if (Pb[mid] - Ob > s0) hi_b = mid; else lo_b = mid + 1;
+            }
+            lb = lo_b;
+            off = (int)(s0 - ((lb > 0 ? Pb[lb - 1] : Ob) - Ob));
+        }
+        p.items[i] = make_int4(b, lb, off, (int)(s1 > s0 ? s1 - s0 : 0));
+        atomicMin(&p.cta_items[x].x, i);
+        atomicAdd(&p.cta_items[x].y, 1);
     }
     if (tid == 0) *p.n_items = G + p.B;
 }

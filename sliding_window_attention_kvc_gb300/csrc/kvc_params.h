@@ -42,6 +42,8 @@ struct DecodeParams {
     const int32_t* table;       // PAGED [B, maxb]
     const uint32_t* valid;      // PAGED, may be null
     void* out;                  // [B, Hq, D]
+    const void* k_new;          // fused append (kvc_decode_step): [B, Hkv, D] pre-RoPE; null = none
+    const void* v_new;
     uint32_t* err;
     uint32_t* counters;
     float2* part_ml;
@@ -55,12 +57,12 @@ struct DecodeParams {
     int B, Hq, Hkv, G, nsub;
     int window, sinks, capacity;
     int bs, num_blocks, maxb;
-    int nsplit;
+    int nsplit;                 // fp32 window: splits per (sequence, kv head); bf16: stream-K CTAs
     int max_items;              // partial slots per q head (bound for every slot index)
     int rope;                   // kRopeNone / kRopeBaked / kRopeRead
     float q_scale;              // softmax scale * log2(e)
     float theta_f[kMaxHalfDim];     // RoPE frequencies, fp32 (small in-tile angles)
-    double theta[kMaxHalfDim];      // RoPE frequencies, fp64 (absolute positions)
+    unsigned long long theta[kMaxHalfDim];   // RoPE frequencies as turns, fixed point: theta_i / (2 pi) * 2^64
 };
 
 struct PlanParams {
@@ -89,7 +91,7 @@ struct AppendParams {
     int layout, window, sinks, capacity;
     int bs, num_blocks, maxb;
     int rope;
-    double theta[kMaxHalfDim];
+    unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
 };
 
 struct TableParams {

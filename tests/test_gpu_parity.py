@@ -214,6 +214,36 @@ def test_decode_full_size_sampled(kvc, name, seqs):
     assert kvc.get_error(st.ws) == 0
 
 
+@pytest.mark.parametrize("name", SMALL)
+def test_decode_step_three_steps_and_cache(kvc, name):
+    """kvc_decode_step (fused append for bf16 ring layouts) over three
+    consecutive positions: outputs match the oracle, and the cache holds what
+    the separate kvc_append writes (one bf16 ulp for RoPE baked into K)."""
+    wl = kvc_synth.make_workload(name, small=True)
+    st = bench.DecodeState(wl, 1, source="cpu")
+    ref_cache = st.cache.clone()
+    # paged: the next positions may need blocks the table does not map yet
+    for step in range(3 if wl.layout == "window" else 1):
+        pos = wl.positions + step
+        q = wl.queries(0, pos).contiguous().cuda()
+        kn, vn = wl.new_kv(0, pos)
+        kn, vn = kn.contiguous().cuda(), vn.contiguous().cuda()
+        pos_t = torch.from_numpy(pos.astype(np.int32)).cuda()
+        out = kvc.decode_step(st.desc, st.cache, 0, q, kn, vn, pos_t, st.ws, block_table=st.table,
+                              valid_bits=st.valid_bits)
+        kvc.append(st.desc, ref_cache, 0, kn, vn, pos_t, st.ws, block_table=st.table)
+        got = out.float().cpu().numpy()
+        ref = oracle_outputs(wl, 0, positions=pos)
+        assert np.isfinite(got).all()
+        assert _maxerr(got, ref) <= TOL[wl.dtype], (name, step, _maxerr(got, ref))
+        a, r = st.cache.float(), ref_cache.float()
+        both_nan = torch.isnan(a) & torch.isnan(r)
+        diff = (a - r).abs().masked_fill(both_nan, 0.0)
+        assert (diff <= r.abs().masked_fill(both_nan, 0.0) * 2.0 ** -7 + 1e-6).all()
+        assert (diff == 0).float().mean() > 0.999
+    assert kvc.get_error(st.ws) == 0
+
+
 def test_shared_prefix_outputs_depend_on_own_tail(kvc):
     """[share] 3.3: sequences sharing prefix blocks but with different tails
     must give different outputs (no cross-talk through the shared blocks)."""
