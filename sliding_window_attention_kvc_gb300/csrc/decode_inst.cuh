@@ -20,8 +20,8 @@
 
 // bf16 caches: tensor-core kernel (kvc_decode_mma.cuh)
 #define KVC_INST_MMA(D, GH, PG, RD)                                                                  \
-    template cudaError_t kvc::launch_decode_mma_t<D, GH, PG, RD>(const kvc::DecodeParams&, const void*, \
-                                                                 dim3, cudaStream_t);
+    template cudaError_t kvc::launch_decode_mma_t<D, GH, PG, RD>(const kvc::DecodeParams&,              \
+                                                                 const kvc::KvTensorMaps&, dim3, cudaStream_t);
 
 #define KVC_INST_MMA_ALL_D(PG, RD) \
     KVC_INST_MMA(64, 1, PG, RD)    \

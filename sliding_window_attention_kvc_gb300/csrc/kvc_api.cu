@@ -16,7 +16,7 @@ namespace kvc {
 template <typename Elt, int D, int GH, bool PAGED, bool READ>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t stream);
 template <int D, int GH, bool PAGED, bool READ>
-cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 grid, cudaStream_t stream);
+cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps, dim3 grid, cudaStream_t stream);
 
 namespace {
 
@@ -144,10 +144,10 @@ cudaError_t launch_decode(int dtype, int D, int gh, bool paged, bool rd, const D
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_mma(int D, int gh, bool paged, bool rd, const DecodeParams& p, const void* tmap,
+cudaError_t launch_decode_mma(int D, int gh, bool paged, bool rd, const DecodeParams& p, const KvTensorMaps& maps,
                               dim3 grid, cudaStream_t s) {
 #define KVC_CASE(DD, GG, PG, RD) \
-    if (D == DD && gh == GG && paged == PG && rd == RD) return launch_decode_mma_t<DD, GG, PG, RD>(p, tmap, grid, s);
+    if (D == DD && gh == GG && paged == PG && rd == RD) return launch_decode_mma_t<DD, GG, PG, RD>(p, maps, grid, s);
 #define KVC_CASES(PG, RD)                                                   \
     KVC_CASE(64, 1, PG, RD) KVC_CASE(64, 2, PG, RD) KVC_CASE(64, 4, PG, RD)    \
     KVC_CASE(128, 1, PG, RD) KVC_CASE(128, 2, PG, RD) KVC_CASE(128, 4, PG, RD) \
@@ -182,22 +182,95 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// The whole bf16 cache as a 2-D tensor [rows, head_dim]: boxes of 16 rows x 64
-// columns (128 bytes), 128-byte swizzle.  Row of (layer, K|V, unit row) =
-// (layer * 2 + kv) * rows_per_half + unit row.
-int make_kv_tensor_map(const kvc_desc* d, const Geo& g, const void* cache, CUtensorMap* map) {
-    const unsigned long long rows = (unsigned long long)d->layers * 2 * (unsigned long long)g.half_elems / d->head_dim;
-    if (rows >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
+// Tensor maps over a bf16 cache for copies of runs of 16 r consecutive rows of
+// one K half together with the same rows of its V half (r = 1..kRunMaps).
+// The cache [layers][K|V][rows per half][head_dim] is viewed as the 5-D tensor
+// {64 columns, row, K|V, layer, 64-column block} (byte strides: row, half,
+// 2 halves, 128), which brings every column block in one copy; if the driver
+// refuses it, the 4-D tensor {column, row, K|V, layer} takes one copy per
+// 64-column block.  Both land as [column block][K|V][rows][128 bytes] with the
+// 128-byte swizzle.  Rows past the end of a half read as zeros.
+int encode_kv_maps(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps* maps, int* whole) {
+    const unsigned long long half_rows = (unsigned long long)g.half_elems / d->head_dim;
+    if (half_rows >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return KVC_ERR_CUDA;
-    const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? KVC_OK : KVC_ERR_CUDA;
+    const cuuint64_t row_bytes = (cuuint64_t)d->head_dim * 2, half_bytes = half_rows * row_bytes;
+    const cuuint32_t boxes = (cuuint32_t)(d->head_dim / 64);
+    for (int pass = boxes > 1 ? 0 : 1; pass < 2; ++pass) {
+        const bool five = pass == 0;
+        bool ok = true;
+        for (int r = 0; r < kRunMaps && ok; ++r) {
+            const cuuint32_t R = 16u * (cuuint32_t)(r + 1);
+            CUresult e;
+            if (five) {
+                const cuuint64_t dims[5] = {64, half_rows, 2, (cuuint64_t)d->layers, boxes};
+                const cuuint64_t strides[4] = {row_bytes, half_bytes, 2 * half_bytes, 128};
+                const cuuint32_t box[5] = {64, R, 2, 1, boxes};
+                const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+                e = fn(&maps->run[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            } else {
+                const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, half_rows, 2, (cuuint64_t)d->layers};
+                const cuuint64_t strides[3] = {row_bytes, half_bytes, 2 * half_bytes};
+                const cuuint32_t box[4] = {64, R, 2, 1};
+                const cuuint32_t estr[4] = {1, 1, 1, 1};
+                e = fn(&maps->run[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides,
+                       box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            }
+            ok = e == CUDA_SUCCESS;
+        }
+        if (ok) {
+            *whole = five ? 1 : 0;
+            return KVC_OK;
+        }
+    }
+    return KVC_ERR_CUDA;
+}
+
+// The maps depend only on the cache's address and shape: the last few are
+// kept, so that a decode step does not pay for encoding them.
+int kv_maps_for(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps* maps, int* whole) {
+    struct Entry {
+        const void* cache;
+        long long half_elems;
+        int layers, head_dim, device, whole;
+        KvTensorMaps maps;
+    };
+    constexpr int kEntries = 8;
+    static Entry entries[kEntries];
+    static int used = 0, next = 0;
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& e = entries[i];
+            if (e.cache == cache && e.half_elems == g.half_elems && e.layers == d->layers &&
+                e.head_dim == d->head_dim && e.device == dev) {
+                *maps = e.maps;
+                *whole = e.whole;
+                return KVC_OK;
+            }
+        }
+    }
+    const int rc = encode_kv_maps(d, g, cache, maps, whole);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry& e = entries[next];
+    e.cache = cache;
+    e.half_elems = g.half_elems;
+    e.layers = d->layers;
+    e.head_dim = d->head_dim;
+    e.device = dev;
+    e.whole = *whole;
+    e.maps = *maps;
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+    return KVC_OK;
 }
 
 }  // namespace
@@ -241,6 +314,7 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     p.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
     p.part_o = reinterpret_cast<float*>(ws + w.part_o);
     p.layer_off = (long long)layer * 2 * g.half_elems;
+    p.layer = layer;
     p.kv_off = g.half_elems;
     p.B = d->batch;
     p.Hq = d->q_heads;
@@ -286,10 +360,10 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     }
     const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
     if (d->dtype == KVC_BF16) {
-        CUtensorMap map;
-        rc = make_kv_tensor_map(d, g, cache, &map);
+        KvTensorMaps maps;
+        rc = kv_maps_for(d, g, cache, &maps, &p.tma_whole);
         if (rc) return rc;
-        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, p, &map, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
+        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, p, maps, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
         return KVC_OK;
     }
     if (launch_decode(d->dtype, d->head_dim, g.GH, paged, rd, p, grid, s) != cudaSuccess) return KVC_ERR_CUDA;

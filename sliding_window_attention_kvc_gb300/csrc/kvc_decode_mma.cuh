@@ -4,9 +4,9 @@
 // all sequences, laid end to end, are cut into gridDim.x nearly equal
 // contiguous shares, one per CTA (a persistent grid of two CTAs per SM).  A
 // share covers one or more *segments* (its intersection with one sequence);
-// a CTA reduces each segment to a partial (m, l, o) and the last CTA to
-// finish a sequence - found with an atomic ticket, never by waiting - merges
-// that sequence's few partials:
+// a CTA reduces each segment to a partial (m, l, o) per q head, and
+// combine_streamk_kernel, launched behind it with programmatic dependent
+// launch, merges each sequence's few partials:
 //     M = max m_i,  out = sum o_i 2^(m_i - M) / sum l_i 2^(m_i - M).
 // With shares in sequence order, segment (CTA x, sequence b) gets partial
 // slot x + b: consecutive, unique, and a sequence's slots are consecutive.
@@ -18,16 +18,20 @@
 // On a q head group of 4 the CUDA-core formulation spent ~97 warp
 // instructions per cached token (measured); these two products cost ~4.
 //
-// Data movement.  K and V arrive through 2-D TMA tensor copies
-// (cp.async.bulk.tensor) of 16-row x 64-column boxes with the 128-byte
-// swizzle, so that ldmatrix reads of 8 rows at one column are bank-conflict
-// free.  Warp 4 issues the copies into a ring of shared-memory stages guarded
-// by mbarriers and walks the CTA's segments; warps 0..3 compute.  A stage
-// holds up to NSUB sub-tiles of one segment; each sub-tile is one box per 64
-// columns and carries its own row count (ragged ends, partial paged blocks)
-// and, for READ_INCACHE, its first in-cache position.  Rows of a sub-tile past
-// its row count are masked out of the softmax and their V rows zeroed before
-// P V (they may hold any bits, NaN included).
+// Data movement.  Warp 4 walks the CTA's segments and cuts them into *runs*
+// of up to 64 consecutive cache rows (a paged block, or the slots of a ring
+// between its boundaries).  One TMA tensor copy (cp.async.bulk.tensor) per run
+// brings the run's K and V rows, every column, into a ring of shared-memory
+// stages guarded by mbarriers, laid out [64-column block][K|V][rows][128 B]
+// with the 128-byte swizzle, so that ldmatrix reads of 8 rows at one column
+// are bank-conflict free.  Issuing copies was the bottleneck with one 2 KB
+// box per (16 rows, 64 columns, K or V): ~70 cycles per copy instruction plus
+// the bookkeeping around it, against a stage's worth of tensor-core work.
+// Warps 0..3 compute, one 16-row sub-tile of a stage each.  Each sub-tile
+// carries its row count (ragged ends, partial paged blocks), its place in the
+// stage and, for READ_INCACHE, its first in-cache position.  Rows of a
+// sub-tile past its row count are masked out of the softmax and their V rows
+// zeroed before P V (they may hold any bits, NaN included).
 #pragma once
 
 #include <cuda.h>
@@ -48,8 +52,13 @@ struct MmaShape {
     static constexpr int kDsplit = D == 256 ? 2 : 1;          // warps sharing one sub-tile (split over dims)
     static constexpr int kTokenGroups = kConsumerWarps / kDsplit;
     static constexpr int kNsub = kTokenGroups;                // sub-tiles per stage (one per token group)
-    static constexpr int kStageBytes = 2 * kNsub * kSubBytes; // K sub-tiles, then V sub-tiles
-    static constexpr int kStages = D == 64 ? 6 : (READ ? 5 : 3);
+    static constexpr int kStageBytes = 2 * kNsub * kSubBytes; // K and V of kNsub sub-tiles
+    static constexpr int kStages = D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3);
+    // READ_INCACHE rotation: a lane owns one 16-byte chunk pair (8 rotation
+    // pairs) of kRowsPerLane rows of its warp's sub-tile
+    static constexpr int kCpr = D / 16;                       // chunk pairs (i, i + D/2) per row
+    static constexpr int kRowGroups = 32 / kCpr;              // rows a warp visits at once
+    static constexpr int kRowsPerLane = kSub / (kDsplit * kRowGroups);
     static constexpr int kDl = D / kDsplit;                   // output columns per warp
     static constexpr int kNt = kDl / 8;                       // 8-column output tiles per warp
     static constexpr int kKsteps = D / 16;                    // k-steps of Q K^T
@@ -73,6 +82,9 @@ struct alignas(16) MmaStageMeta {
     int nrows[4];    // rows of each sub-tile (1..16)
     int ip0[4];      // READ_INCACHE: in-cache position of row 0 of each sub-tile
     int newrow[4];   // fused append: row of the sub-tile that holds the new token, else -1
+    int base[4];     // byte offset of each sub-tile's K rows (column block 0) in the stage
+    int ld[4];       // rows of the copy the sub-tile belongs to: its K|V and column
+                     // blocks lie 128 * ld bytes apart
     MmaSegment seg;  // valid with kSegBegin
 };
 constexpr int kSegBegin = 1, kSegEnd = 2;
@@ -83,9 +95,10 @@ struct MmaSmem {
     static constexpr size_t kStage = 0;                                        // 1024-aligned stages
     static constexpr size_t kBars = kStage + (size_t)S::kStages * S::kStageBytes;
     static constexpr size_t kMeta = kBars + 2 * S::kStages * sizeof(uint64_t);
-    static constexpr size_t kRot = kMeta + S::kStages * sizeof(MmaStageMeta);  // [stage][sub][D/2] float2
-    static constexpr size_t kTab = kRot + (READ ? (size_t)S::kStages * S::kNsub * S::kHalf * 8 : 0);
-    static constexpr size_t kQcs = kTab + (READ ? (size_t)S::kSub * S::kHalf * 8 : 0);   // [16][D/2] float2
+    // READ_INCACHE: R(ip0 theta_i) of each sub-tile, [stage][sub][4][D/16][2] float2
+    // (pair i = 8 cp + 2 jj + e at [jj][cp][e], so a lane's float4 loads are conflict-free)
+    static constexpr size_t kRot = kMeta + S::kStages * sizeof(MmaStageMeta);
+    static constexpr size_t kQcs = kRot + (READ ? (size_t)S::kStages * S::kNsub * S::kHalf * 8 : 0);  // [D/2] float2
     static constexpr size_t kMergeO = kQcs + (size_t)S::kHalf * 8;
     static constexpr size_t kMergeML = kMergeO + (size_t)S::kTokenGroups * GH * D * 4;
     static constexpr size_t kFlag = kMergeML + (size_t)S::kTokenGroups * GH * 8;
@@ -256,8 +269,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
 }
 
 template <int D, int GH, bool PAGED, bool READ>
-__global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
-    decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256) ? 255 : 200)
+    decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ KvTensorMaps maps) {
     using S = MmaShape<D, READ>;
     using SM = MmaSmem<D, GH, READ>;
     constexpr int NST = S::kStages, NSUB = S::kNsub, HALF = S::kHalf;
@@ -270,7 +283,6 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
     uint64_t* empty = full + NST;
     MmaStageMeta* meta = reinterpret_cast<MmaStageMeta*>(smem + SM::kMeta);
     float2* rot = reinterpret_cast<float2*>(smem + SM::kRot);
-    float2* tab = reinterpret_cast<float2*>(smem + SM::kTab);
     float2* qcs = reinterpret_cast<float2*>(smem + SM::kQcs);
     float* merge_o = reinterpret_cast<float*>(smem + SM::kMergeO);
     float2* merge_ml = reinterpret_cast<float2*>(smem + SM::kMergeML);
@@ -296,19 +308,17 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
         mbar_init(&cbar[1], 64);
         mbar_init(&cbar[2], 64);
         mbar_fence_init();
-        tma_prefetch_desc(&tmap);
+#pragma unroll
+        for (int r = 0; r < kRunMaps; ++r) tma_prefetch_desc(&maps.run[r]);
     }
     pdl_wait();                 // inputs written by earlier kernels (append, plan) are visible
     pdl_launch_dependents();    // the combine kernel may start launching
     __syncthreads();
 
-    // tensor-map rows: [layers][K | V][rows of the half][D]
-    const long long layer_row0 = p.layer_off / D;
-    const long long half_rows = p.kv_off / D;
 
     if (warp == kConsumerWarps) {
         // =================== copy-issuing warp ==============================
-        int it = 0, fill = 0;
+        int it = 0, fill = 0, run_off = 0;
         bool ok = true, open = false;
         auto open_stage = [&]() -> bool {
             const int s = it % NST;
@@ -318,6 +328,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
             }
             open = true;
             fill = 0;
+            run_off = 0;
             if (lane == 0) meta[s].flags = 0;
             return true;
         };
@@ -342,37 +353,79 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
             }
             return true;
         };
-        // A full stage is published only when the next sub-tile needs room, so
-        // the last stage of a segment is still open here and carries kSegEnd.
+        // A full stage is published only when the next run needs room, so the
+        // last stage of a segment is still open here and carries kSegEnd.
         auto end_segment = [&]() { commit(kSegEnd); };
-        // one sub-tile: `n` rows starting at tensor-map row `krow` (K half)
-        auto emit = [&](long long krow, int n, int ip0, int newrow) -> bool {
+        // free sub-tiles in the open stage (opening a stage when none is open or
+        // the open one is full); 0 when the pipeline gave up
+        auto ensure_room = [&]() -> int {
             if (open && fill == NSUB) commit(0);
-            if (!open && !open_stage()) return false;
+            if (!open && !open_stage()) return 0;
+            return NSUB - fill;
+        };
+        // READ_INCACHE: R(ip theta_i) of the last sub-tile emitted, for
+        // i = lane + 32 m, and the step R(16 theta_i) to the next one
+        constexpr int kFpl = (HALF + 31) / 32;        // frequencies per lane
+        float2 ang[kFpl], adv[kFpl];
+        if constexpr (READ) {
+#pragma unroll
+            for (int m = 0; m < kFpl; ++m) {
+                const int i = lane + 32 * m;
+                ang[m] = make_float2(1.f, 0.f);
+                if (i < HALF) rope_cos_sin(16, p.theta[i], &adv[m].x, &adv[m].y);
+            }
+        }
+        // One run: n consecutive rows (1 <= n <= 16 * room) of this layer's K
+        // half from row urow, copied with their V rows by one tensor copy (one
+        // per column block without tma_whole) of 16 ceil(n / 16) rows, as that
+        // many sub-tiles.  ip0: in-cache position of the first row (READ_INCACHE);
+        // exact: its angles computed afresh rather than advanced by 16 from the
+        // previous sub-tile's; newrow: run row of the token being appended or -1.
+        auto emit_run = [&](long long urow, int n, int ip0, int newrow, bool exact) {
             const int s = it % NST;
+            const int nsr = (n + 15) >> 4;
+            const int R = nsr * 16;
             if constexpr (READ) {
-                for (int i = lane; i < HALF; i += 32) {
-                    float cs, sn;
-                    rope_cos_sin((long long)ip0, p.theta[i], &cs, &sn);
-                    rot[(s * NSUB + fill) * HALF + i] = make_float2(cs, sn);
+                for (int j = 0; j < nsr; ++j) {
+#pragma unroll
+                    for (int m = 0; m < kFpl; ++m) {
+                        const int i = lane + 32 * m;
+                        if (i < HALF) {
+                            if (exact && j == 0) {
+                                rope_cos_sin((long long)ip0, p.theta[i], &ang[m].x, &ang[m].y);
+                            } else {
+                                const float2 a = ang[m], d = adv[m];
+                                ang[m] = make_float2(a.x * d.x - a.y * d.y, a.y * d.x + a.x * d.y);
+                            }
+                            const int cp = i >> 3, jj = (i & 7) >> 1, e = i & 1;
+                            rot[(s * NSUB + fill + j) * HALF + (jj * S::kCpr + cp) * 2 + e] = ang[m];
+                        }
+                    }
                 }
+            }
+            if (lane < nsr) {
+                const int f = fill + lane;
+                const int lo = 16 * lane;
+                meta[s].nrows[f] = min(16, n - lo);
+                meta[s].ip0[f] = ip0 + lo;
+                meta[s].newrow[f] = (newrow >= lo && newrow < lo + 16) ? newrow - lo : -1;
+                meta[s].base[f] = run_off + lo * 128;
+                meta[s].ld[f] = R;
             }
             if (lane == 0) {
-                meta[s].nrows[fill] = n;
-                meta[s].ip0[fill] = ip0;
-                meta[s].newrow[fill] = newrow;
-                unsigned char* kdst = stage_base + (size_t)s * S::kStageBytes + (size_t)fill * S::kSubBytes;
-                unsigned char* vdst = kdst + (size_t)NSUB * S::kSubBytes;
-                mbar_expect_tx(&full[s], 2 * S::kSubBytes);
+                unsigned char* dst = stage_base + (size_t)s * S::kStageBytes + run_off;
+                const CUtensorMap* map = &maps.run[nsr - 1];
+                mbar_expect_tx(&full[s], (uint32_t)(S::kBoxes * 2 * R * 128));
+                if (p.tma_whole) {
+                    tma_load_5d(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s]);
+                } else {
 #pragma unroll
-                for (int bx = 0; bx < S::kBoxes; ++bx) {
-                    tma_load_2d(kdst + bx * S::kBoxBytes, &tmap, bx * S::kBoxCols, (int)krow, &full[s]);
-                    tma_load_2d(vdst + bx * S::kBoxBytes, &tmap, bx * S::kBoxCols, (int)(krow + half_rows),
-                                &full[s]);
+                    for (int bx = 0; bx < S::kBoxes; ++bx)
+                        tma_load_4d(dst + bx * 2 * R * 128, map, bx * S::kBoxCols, (int)urow, 0, p.layer, &full[s]);
                 }
             }
-            ++fill;
-            return true;
+            fill += nsr;
+            run_off += S::kBoxes * 2 * R * 128;
         };
 
         if constexpr (!PAGED) {
@@ -430,23 +483,42 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                     if (!(ok = begin_segment(hdr))) break;
                     const int r0 = (int)((lo > Ob ? lo : Ob) - Ob) * 16;
                     const int r1 = min((int)((hi < Ob + Sb ? hi : Ob + Sb) - Ob) * 16, nl_b);
-                    const long long base_row = layer_row0 + ((long long)b * p.Hkv + kvh) * C;
+                    const long long base_row = ((long long)b * p.Hkv + kvh) * C;   // row in the K half
                     // slot of the token being decoded: the ring's wrap point, and
                     // (fused append) the row that receives the new K/V
                     int h_slot = 0;
                     if (t_b >= 0)
                         h_slot = t_b < p.sinks ? t_b : p.sinks + (int)(((long long)t_b - p.sinks) % p.window);
+                    // READ_INCACHE: in-cache positions run on by one per slot between
+                    // the sink/window boundary and the ring's wrap; they (and their
+                    // angles) are computed afresh at those points and every 32 runs
+                    int ip_next = 0, prev_n = 0, since = 0;
                     for (int r = r0; r < r1 && ok;) {
-                        int n = min(16, r1 - r);
+                        const int room = ensure_room();
+                        if (!room) {
+                            ok = false;
+                            break;
+                        }
+                        int n = min(16 * room, r1 - r);
                         int ip0 = 0;
+                        bool exact = true;
                         if constexpr (READ) {
-                            // a sub-tile never straddles the sink/window boundary or the ring's wrap
+                            // a run never straddles the sink/window boundary or the ring's wrap
                             const int seg_end = r < p.sinks ? p.sinks : (r <= h_slot ? h_slot + 1 : C);
                             n = min(n, seg_end - r);
-                            ip0 = incache_of_slot(r, t_b, p.sinks, p.window, C);
+                            exact = r == r0 || r == p.sinks || r == h_slot + 1 || (prev_n & 15) != 0 || since >= 32;
+                            if (exact) {
+                                ip0 = incache_of_slot(r, t_b, p.sinks, p.window, C);
+                                since = 0;
+                            } else {
+                                ip0 = ip_next;
+                            }
+                            ++since;
+                            ip_next = ip0 + n;
+                            prev_n = n;
                         }
                         const int newrow = (p.k_new && t_b >= 0 && h_slot >= r && h_slot < r + n) ? h_slot - r : -1;
-                        ok = emit(base_row + r, n, ip0, newrow);
+                        emit_run(base_row + r, n, ip0, newrow, exact);
                         r += n;
                     }
                     if (ok) end_segment();
@@ -492,10 +564,15 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                         const int brows = __shfl_sync(0xffffffffu, my_rows, src);
                         int row = (lb + src == itv.y) ? itv.z : 0;
                         int take = min(brows - row, rem);
-                        const long long blk = layer_row0 + ((long long)phys * p.Hkv + kvh) * p.bs;
+                        const long long blk = ((long long)phys * p.Hkv + kvh) * p.bs;   // row in the K half
                         while (take > 0 && ok) {
-                            const int n = min(16, take);
-                            ok = emit(blk + row, n, 0, -1);
+                            const int room = ensure_room();
+                            if (!room) {
+                                ok = false;
+                                break;
+                            }
+                            const int n = min(take, 16 * room);
+                            emit_run(blk + row, n, 0, -1, true);
                             take -= n;
                             rem -= n;
                             row += n;
@@ -537,13 +614,28 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
     BoundedBarrier csync{&cbar[0], 0u};           // the four compute warps
     BoundedBarrier psync{&cbar[1 + (tg & 1)], 0u}; // the two warps sharing a sub-tile (head_dim 256)
 
+    // READ_INCACHE: this lane rotates chunk pair rcp (pairs i = 8 rcp + j) of
+    // rows rrow0 + kRowStep k of its sub-tile; R(rrow0 theta_i) and the step
+    // R(kRowStep theta_i) stay in registers (small angles: rrow0, kRowStep < 16)
+    constexpr int kRowStep = S::kDsplit * S::kRowGroups;
+    const int rcp = lane % S::kCpr;
+    const int rrow0 = hd + S::kDsplit * (lane / S::kCpr);
+    // packed over the pair couples (8 rcp + 2 q, 8 rcp + 2 q + 1): cos and sin
+    float2 r0c[4], r0s[4], stc[4], sts[4];
     if constexpr (READ) {
-        // R(r theta_i) for the rows r = 0..15 of a sub-tile
-        for (int idx = ctid; idx < S::kSub * HALF; idx += NCT) {
-            const int r = idx / HALF, i = idx % HALF;
-            float cs, sn;
-            sincosf((float)r * p.theta_f[i], &sn, &cs);
-            tab[idx] = make_float2(cs, sn);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float th = p.theta_f[rcp * 8 + 2 * q + e];
+                float c0, s0, c1, s1;
+                sincosf((float)rrow0 * th, &s0, &c0);
+                sincosf((float)kRowStep * th, &s1, &c1);
+                (e ? r0c[q].y : r0c[q].x) = c0;
+                (e ? r0s[q].y : r0s[q].x) = s0;
+                (e ? stc[q].y : stc[q].x) = c1;
+                (e ? sts[q].y : sts[q].x) = s1;
+            }
         }
     }
 
@@ -689,8 +781,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
         }
         if (tg < nsub) {
             const int nrows = meta[s].nrows[tg];
-            unsigned char* Ks = stage_base + (size_t)s * S::kStageBytes + (size_t)tg * S::kSubBytes;
-            unsigned char* Vs = Ks + (size_t)NSUB * S::kSubBytes;
+            // the sub-tile's copy lands as [column block][K|V][ld rows][128 bytes]
+            const int ld = meta[s].ld[tg];
+            const int bstride = 2 * ld * 128;             // between column blocks
+            unsigned char* Ks = stage_base + (size_t)s * S::kStageBytes + meta[s].base[tg];
+            unsigned char* Vs = Ks + ld * 128;
             const uint32_t ku = smem_u32(Ks), vu = smem_u32(Vs);
             bool wrote = false;
 
@@ -726,7 +821,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
                                 const int col = i + e * HALF;
-                                const int off = (col >> 6) * S::kBoxBytes + nr * 128 +
+                                const int off = (col >> 6) * bstride + nr * 128 +
                                                 (((((col & 63) >> 3)) ^ (nr & 7)) << 4) + (col & 7) * 2;
                                 *reinterpret_cast<__nv_bfloat16*>(Ks + off) = e ? k2 : k1;
                                 *reinterpret_cast<__nv_bfloat16*>(Vs + off) = e ? v2 : v1;
@@ -739,38 +834,48 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
             }
 
             if constexpr (READ) {
-                // rotate the stored (raw) K rows in place by R((ip0 + r) theta),
-                // R(ip0 theta) from the stage table times R(r theta) from `tab`
-                constexpr int CPR = D / 16;   // 16-byte chunk pairs (i, i + D/2) per row
-                const float2* rs = rot + (s * NSUB + tg) * HALF;
-                const int nmine = (nrows - hd + S::kDsplit - 1) / S::kDsplit;
-                for (int idx = lane; idx < nmine * CPR; idx += 32) {
-                    const int r = hd + (idx / CPR) * S::kDsplit;
-                    const int cp = idx % CPR;
-                    const int chi = cp + CPR;
-                    unsigned char* plo = Ks + (cp >> 3) * S::kBoxBytes + r * 128 + ((((cp & 7) ^ (r & 7))) << 4);
-                    unsigned char* phi = Ks + (chi >> 3) * S::kBoxBytes + r * 128 + ((((chi & 7) ^ (r & 7))) << 4);
-                    uint4 wl = *reinterpret_cast<uint4*>(plo);
-                    uint4 wh = *reinterpret_cast<uint4*>(phi);
-                    float xl[8], xh[8];
-                    EltTraits<__nv_bfloat16>::unpack(wl, xl);
-                    EltTraits<__nv_bfloat16>::unpack(wh, xh);
-                    float yl[8], yh[8];
+                // rotate the stored (raw) K rows in place by R((ip0 + r) theta):
+                // R(ip0 theta) from the stage table times R(r theta), advanced
+                // from row to row by the step rotation.  Packed fp32 pairs; rows
+                // past nrows are rotated too (their scores are masked out).
+                const float4* rs4 = reinterpret_cast<const float4*>(rot + (s * NSUB + tg) * HALF);
+                float2 cc[4], ss[4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int i = cp * 8 + j;
-                        const float2 a = rs[i], bb = tab[r * HALF + i];
-                        const float cs = a.x * bb.x - a.y * bb.y;
-                        const float sn = a.y * bb.x + a.x * bb.y;
-                        yl[j] = xl[j] * cs - xh[j] * sn;
-                        yh[j] = xl[j] * sn + xh[j] * cs;
+                for (int q = 0; q < 4; ++q) {
+                    const float4 a = rs4[q * S::kCpr + rcp];
+                    const float2 ac = make_float2(a.x, a.z), as = make_float2(a.y, a.w);
+                    cc[q] = __ffma2_rn(ac, r0c[q], __fmul2_rn(as, make_float2(-r0s[q].x, -r0s[q].y)));
+                    ss[q] = __ffma2_rn(as, r0c[q], __fmul2_rn(ac, r0s[q]));
+                }
+                const int chi = rcp + S::kCpr;
+                const int lo_off = (rcp >> 3) * bstride, hi_off = (chi >> 3) * bstride;
+#pragma unroll
+                for (int k = 0; k < S::kRowsPerLane; ++k) {
+                    const int r = rrow0 + k * kRowStep;
+                    uint4* plo = reinterpret_cast<uint4*>(Ks + lo_off + r * 128 + ((((rcp & 7) ^ (r & 7))) << 4));
+                    uint4* phi = reinterpret_cast<uint4*>(Ks + hi_off + r * 128 + ((((chi & 7) ^ (r & 7))) << 4));
+                    const uint4 wl = *plo, wh = *phi;
+                    const uint32_t lw[4] = {wl.x, wl.y, wl.z, wl.w}, hw[4] = {wh.x, wh.y, wh.z, wh.w};
+                    uint32_t ol[4], oh[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 xl = make_float2(__uint_as_float(lw[q] << 16), __uint_as_float(lw[q] & 0xffff0000u));
+                        const float2 xh = make_float2(__uint_as_float(hw[q] << 16), __uint_as_float(hw[q] & 0xffff0000u));
+                        const float2 yl = __ffma2_rn(xl, cc[q], __fmul2_rn(xh, make_float2(-ss[q].x, -ss[q].y)));
+                        const float2 yh = __ffma2_rn(xl, ss[q], __fmul2_rn(xh, cc[q]));
+                        ol[q] = pack_bf16x2(yl.x, yl.y);
+                        oh[q] = pack_bf16x2(yh.x, yh.y);
                     }
-                    wl = make_uint4(pack_bf16x2(yl[0], yl[1]), pack_bf16x2(yl[2], yl[3]),
-                                    pack_bf16x2(yl[4], yl[5]), pack_bf16x2(yl[6], yl[7]));
-                    wh = make_uint4(pack_bf16x2(yh[0], yh[1]), pack_bf16x2(yh[2], yh[3]),
-                                    pack_bf16x2(yh[4], yh[5]), pack_bf16x2(yh[6], yh[7]));
-                    *reinterpret_cast<uint4*>(plo) = wl;
-                    *reinterpret_cast<uint4*>(phi) = wh;
+                    *plo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                    *phi = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                    if (k + 1 < S::kRowsPerLane) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 c0 = cc[q];
+                            cc[q] = __ffma2_rn(c0, stc[q], __fmul2_rn(ss[q], make_float2(-sts[q].x, -sts[q].y)));
+                            ss[q] = __ffma2_rn(ss[q], stc[q], __fmul2_rn(c0, sts[q]));
+                        }
+                    }
                 }
                 wrote = true;
                 if constexpr (S::kDsplit == 2) psync.sync(p.err); else __syncwarp();
@@ -782,7 +887,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                 for (int idx = lane; idx < per_box * BPW; idx += 32) {
                     const int bxl = idx / per_box, rem = idx % per_box;
                     const int r = nrows + rem / 8, ch = rem % 8;
-                    *reinterpret_cast<uint4*>(Vs + (hd * BPW + bxl) * S::kBoxBytes + r * 128 + ch * 16) =
+                    *reinterpret_cast<uint4*>(Vs + (hd * BPW + bxl) * bstride + r * 128 + ch * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 wrote = true;
@@ -799,7 +904,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                     const int bx = ks >> 2;
                     const int ch = ((ks & 3) << 1) + chs;
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(ku + bx * S::kBoxBytes + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+                    ldsm_x4(ku + bx * bstride + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
                     mma_bf16_16816(sa[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
                     mma_bf16_16816(sa[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
                 }
@@ -842,7 +947,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
                     const int bx = dt >> 3;
                     const int ch = (dt & 7) + chs;
                     uint32_t v0, v1, v2, v3;
-                    ldsm_x4_trans(vu + bx * S::kBoxBytes + tok * 128 + ((ch ^ (tok & 7)) << 4), v0, v1, v2, v3);
+                    ldsm_x4_trans(vu + bx * bstride + tok * 128 + ((ch ^ (tok & 7)) << 4), v0, v1, v2, v3);
                     mma_bf16_16816(o[j], pa0, 0u, pa2, 0u, v0, v1);
                     mma_bf16_16816(o[j + 1], pa0, 0u, pa2, 0u, v2, v3);
                 }
@@ -856,7 +961,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 128) ? 1 : 2)
 }
 
 template <int D, int GH, bool PAGED, bool READ>
-cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps, dim3 grid, cudaStream_t stream) {
     using SM = MmaSmem<D, GH, READ>;
     auto kern = decode_mma_kernel<D, GH, PAGED, READ>;
     auto comb = combine_streamk_kernel<D, GH, PAGED>;
@@ -882,7 +987,7 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, const void* tmap, dim3 gr
     cfg.stream = stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p, *static_cast<const CUtensorMap*>(tmap));
+    e = cudaLaunchKernelEx(&cfg, kern, p, maps);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t ccfg = {};
     ccfg.gridDim = dim3(p.B, p.Hkv * p.nsub, D / kCombineCols);

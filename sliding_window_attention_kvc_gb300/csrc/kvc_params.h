@@ -2,6 +2,7 @@
 // ABI (kvc_api.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -14,6 +15,7 @@ constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;  // + 1 copy-issuing w
 constexpr int kStages = 4;                       // bulk-copy pipeline depth
 constexpr int kTargetCtas = 608;                 // 152 SMs x 2 CTAs x 2 waves
 constexpr int kStreamCtas = 304;                 // stream-K grid: 152 SMs x 2 CTAs
+constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
 enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
@@ -54,12 +56,14 @@ struct DecodeParams {
     const int2* cta_items;      // PAGED plan: first item, item count of each CTA (stream-K kernel)
     long long layer_off;        // elements from cache base to this layer's K half
     long long kv_off;           // elements from the K half to the V half
+    int layer;
     int B, Hq, Hkv, G, nsub;
     int window, sinks, capacity;
     int bs, num_blocks, maxb;
     int nsplit;                 // fp32 window: splits per (sequence, kv head); bf16: stream-K CTAs
     int max_items;              // partial slots per q head (bound for every slot index)
     int rope;                   // kRopeNone / kRopeBaked / kRopeRead
+    int tma_whole;              // bf16: 1 = one tensor copy per run covers every column block
     float q_scale;              // softmax scale * log2(e)
     float theta_f[kMaxHalfDim];     // RoPE frequencies, fp32 (small in-tile angles)
     unsigned long long theta[kMaxHalfDim];   // RoPE frequencies as turns, fixed point: theta_i / (2 pi) * 2^64
@@ -105,13 +109,21 @@ struct TableParams {
     int n, B, maxb, num_blocks;
 };
 
+// bf16 caches: tensor maps over the cache for copies of a run of 16 r rows
+// (r = 1..kRunMaps), K and V of every column at once.  With tma_whole the map
+// is 5-D {64 columns, row, K|V, layer, column block} and one copy lands as
+// [column block][K|V][rows][128 bytes]; otherwise it is 4-D {column, row, K|V,
+// layer} and each 64-column block is its own copy, landing at the same place.
+struct KvTensorMaps {
+    CUtensorMap run[kRunMaps];
+};
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode(int dtype, int head_dim, int gh, bool paged, bool read_rope,
                           const DecodeParams& p, dim3 grid, cudaStream_t stream);
-// bf16 caches: tensor-core kernel fed by 2-D TMA copies through `tmap`
-// (a CUtensorMap over the cache viewed as [rows, head_dim]).
+// bf16 caches: tensor-core kernel fed by TMA tensor copies through `maps`.
 cudaError_t launch_decode_mma(int head_dim, int gh, bool paged, bool read_rope, const DecodeParams& p,
-                              const void* tmap, dim3 grid, cudaStream_t stream);
+                              const KvTensorMaps& maps, dim3 grid, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
