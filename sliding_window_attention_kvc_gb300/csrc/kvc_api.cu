@@ -69,10 +69,16 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     WorkspaceLayout w{};
     const int units = d->batch * d->kv_heads * g.nsub;
     const int groups = d->kv_heads * g.nsub;
-    // stream-K CTAs per (kv head, q-head group): bf16 kernels, and the paged plan
-    w.ctas = d->num_splits > 0 ? d->num_splits : (kStreamCtas + groups - 1) / groups;
+    // stream-K shares per (kv head, q-head group): bf16 kernels, and the paged
+    // plan.  bf16: a persistent grid of about two CTAs per SM claims them in turn.
+    const int persist = (kStreamCtas + groups - 1) / groups;
     if (d->layout == KVC_LAYOUT_PAGED || d->dtype == KVC_BF16) {
-        w.items = w.ctas + d->batch;       // slot x + b of segment (share x, sequence b)
+        const bool bf16 = d->dtype == KVC_BF16;
+        const int factor = (bf16 && d->layout == KVC_LAYOUT_PAGED && d->batch >= kPagedShareBatch)
+                               ? kPagedShareFactor : 1;
+        w.shares = d->num_splits > 0 ? d->num_splits : factor * persist;
+        w.ctas = bf16 ? (persist < w.shares ? persist : w.shares) : w.shares;
+        w.items = w.shares + d->batch;     // slot x + b of segment (share x, sequence b)
         w.nsplit = 0;
     } else {
         const int T = rows_per_stage(g.elt, d->head_dim);
@@ -88,21 +94,21 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     w.err = off;
     off += 256;
     w.counters = off;
-    off = align_up(off + (size_t)units * 4, 256);
+    off = align_up(off + (size_t)(units + 1) * 4, 256);
     w.part_ml = off;
     off = align_up(off + (size_t)w.items * d->q_heads * 8, 256);
     w.part_o = off;
     off = align_up(off + (size_t)w.items * d->q_heads * d->head_dim * 4, 256);
-    w.plan_rows = w.plan_seq = w.plan_items = w.plan_total = w.plan_cta = off;
+    w.plan_seq = w.plan_acc = w.plan_items = w.plan_total = w.plan_cta = off;
     if (d->layout == KVC_LAYOUT_PAGED) {
-        w.plan_rows = off;
-        off = align_up(off + (size_t)d->batch * d->max_blocks_per_seq * 4, 256);
         w.plan_seq = off;
         off = align_up(off + (size_t)d->batch * 8, 256);
+        w.plan_acc = off;
+        off = align_up(off + (size_t)d->batch * 12, 256);
         w.plan_items = off;
         off = align_up(off + (size_t)w.items * 16, 256);
         w.plan_cta = off;
-        off = align_up(off + (size_t)w.ctas * 8, 256);
+        off = align_up(off + (size_t)w.shares * 8, 256);
         w.plan_total = off;
         off += 256;
     }
@@ -327,7 +333,7 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     p.bs = d->block_size;
     p.num_blocks = d->num_blocks;
     p.maxb = d->max_blocks_per_seq;
-    p.nsplit = d->dtype == KVC_BF16 ? w.ctas : w.nsplit;   // bf16: stream-K CTAs per (kv head, group)
+    p.nsplit = d->dtype == KVC_BF16 ? w.shares : w.nsplit;   // bf16: stream-K shares per (kv head, group)
     p.max_items = w.items;
     p.rope = d->rope;
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
@@ -341,17 +347,31 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
         pp.table = block_table;
         pp.valid = valid_bits;
         pp.err = p.err;
-        pp.rows = reinterpret_cast<int32_t*>(ws + w.plan_rows);
+        pp.seq_off = reinterpret_cast<long long*>(ws + w.plan_acc);
+        pp.seq_rows = reinterpret_cast<int32_t*>(ws + w.plan_acc + (size_t)d->batch * 8);
+        pp.ticket = reinterpret_cast<uint32_t*>(ws + w.counters) + (size_t)d->batch * d->kv_heads * g.nsub;
         pp.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
         pp.items = reinterpret_cast<int4*>(ws + w.plan_items);
         pp.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
         pp.cta_items = reinterpret_cast<int2*>(ws + w.plan_cta);
-        pp.ctas = w.ctas;
+        pp.ctas = w.shares;
         pp.B = d->batch;
         pp.bs = d->block_size;
         pp.num_blocks = d->num_blocks;
         pp.maxb = d->max_blocks_per_seq;
         pp.max_items = w.items;
+        if (k_new) {             // kvc_decode_step: the plan kernel writes the new token first
+            pp.cache = const_cast<void*>(cache);
+            pp.k_new = k_new;
+            pp.v_new = v_new;
+            pp.layer_off = p.layer_off;
+            pp.kv_off = p.kv_off;
+            pp.Hkv = d->kv_heads;
+            pp.D = d->head_dim;
+            pp.rope = d->rope;
+            pp.elt = g.elt;
+            if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
+        }
         if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
         p.items = pp.items;
         p.seq_items = pp.seq_items;
@@ -452,8 +472,9 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
     if (rc) return rc;
     if (!k_new || !v_new) return KVC_ERR_NULL;
     if (!aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGN;
-    if (d->dtype == KVC_BF16 && d->layout != KVC_LAYOUT_PAGED) {
-        // one launch pair: the decode kernel writes the new token itself
+    if (d->dtype == KVC_BF16 || d->layout == KVC_LAYOUT_PAGED) {
+        // no separate append launch: the decode kernel (bf16 ring / sink+ring)
+        // or the paged plan kernel writes the new token itself
         return decode_impl(d, cache, layer, q, k_new, v_new, pos, block_table, valid_bits, out, workspace,
                            workspace_bytes, stream);
     }

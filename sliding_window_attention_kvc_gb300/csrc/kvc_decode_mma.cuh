@@ -163,10 +163,11 @@ __device__ __forceinline__ void window_partition(const DecodeParams& p, int b, l
 // Combine kernel for the stream-K decode: one CTA per (sequence, kv head,
 // q-head group, 32-column chunk).  out = sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)
 // over the sequence's partials, M = max m_i; an empty attended set gives 0.
-// Threads split the partials four ways and reduce through shared memory.
+// One warp per q head finds M and L; threads then split the partials into
+// groups (four loads in flight each) and reduce through shared memory.
 // ---------------------------------------------------------------------------
-constexpr int kCombineThreads = 128;
-constexpr int kCombineCols = 32;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineCols = 16;
 
 template <int D, int GH, bool PAGED>
 __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const __grid_constant__ DecodeParams p) {
@@ -209,6 +210,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
         nparts = s_fn[1];
         pdl_wait();                                 // the decode kernel's partials
     }
+    // the decode grid is done: ready its share counter for the next call
+    if (blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) p.counters[blockIdx.y] = 0u;
     if (first < 0 || nparts < 1 || first + nparts > p.max_items) {
         if (tid == 0) index_fault(p.err, 20, first);
         return;
@@ -222,16 +225,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
     auto ml_of = [&](int k, int h) -> float2 {
         return staged ? s_ml[k * GH + h] : __ldcg(&p.part_ml[(long long)(first + k) * p.Hq + qh0 + h]);
     };
-    if (tid < GH) {
+    // M and L of each q head: one warp per head
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < GH) {
         float M = -INFINITY;
-        for (int k = 0; k < nparts; ++k) M = fmaxf(M, ml_of(k, tid).x);
+        for (int k = lane; k < nparts; k += 32) M = fmaxf(M, ml_of(k, warp).x);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float L = 0.f;
-        for (int k = 0; k < nparts; ++k) {
-            const float2 ml = ml_of(k, tid);
+        for (int k = lane; k < nparts; k += 32) {
+            const float2 ml = ml_of(k, warp);
             L += (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
         }
-        s_M[tid] = M;
-        s_L[tid] = L;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (lane == 0) {
+            s_M[warp] = M;
+            s_L[warp] = L;
+        }
     }
     __syncthreads();
     const int pair = tid % PAIRS, grp = tid / PAIRS;
@@ -239,16 +250,29 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
     const int d0 = col0 + c4 * 4;
     const float M = s_M[h];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int k = grp; k < nparts; k += PG) {
-        const float2 ml = ml_of(k, h);
-        const float e = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-        const float4 v =
-            __ldcg(reinterpret_cast<const float4*>(p.part_o + ((long long)(first + k) * p.Hq + qh0 + h) * D + d0));
-        acc.x += v.x * e;
-        acc.y += v.y * e;
-        acc.z += v.z * e;
-        acc.w += v.w * e;
+    // four independent partial loads in flight per thread
+    for (int k0 = grp; k0 < nparts; k0 += 4 * PG) {
+        float4 v[4];
+        float e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u * PG;
+            e[u] = 0.f;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < nparts) {
+                const float2 ml = ml_of(k, h);
+                e[u] = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+                v[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((long long)(first + k) * p.Hq + qh0 + h) * D +
+                                                              d0));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            acc.x += v[u].x * e[u];
+            acc.y += v[u].y * e[u];
+            acc.z += v[u].z * e[u];
+            acc.w += v[u].w * e[u];
+        }
     }
     s_part[tid] = acc;
     __syncthreads();
@@ -269,7 +293,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
 }
 
 template <int D, int GH, bool PAGED, bool READ>
-__global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256) ? 255 : 200)
+// Two CTAs (ten warps) per SM: three warps share a sub-partition's 16K
+// registers, so a thread may hold at most 168.
+__global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ KvTensorMaps maps) {
     using S = MmaShape<D, READ>;
     using SM = MmaSmem<D, GH, READ>;
@@ -290,14 +316,11 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int x = blockIdx.x, kvh = blockIdx.y, z = blockIdx.z;
-    const int nctas = gridDim.x;
+    const int kvh = blockIdx.y, z = blockIdx.z;
+    const int group = kvh * gridDim.z + z;     // this (kv head, q-head group)'s share counter
 
-    int2 my_items = make_int2(0, 0);      // PAGED: first item, item count of this CTA
-    if constexpr (PAGED) {
-        my_items = p.cta_items[x];
-        if (my_items.y <= 0) return;
-    }
+    // inputs written by earlier kernels (append, plan) are read only after this
+    pdl_wait();
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -311,7 +334,6 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
 #pragma unroll
         for (int r = 0; r < kRunMaps; ++r) tma_prefetch_desc(&maps.run[r]);
     }
-    pdl_wait();                 // inputs written by earlier kernels (append, plan) are visible
     pdl_launch_dependents();    // the combine kernel may start launching
     __syncthreads();
 
@@ -343,15 +365,26 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
             open = false;
             ++it;
         };
-        // a segment starts on a fresh stage that carries its header
+        // a segment starts on a fresh stage that carries its header; its q rows
+        // are prefetched into L2 for the compute warps
         auto begin_segment = [&](const MmaSegment& hdr) -> bool {
             if (open) commit(0);
             if (!open_stage()) return false;
             if (lane == 0) {
                 meta[it % NST].flags = kSegBegin;
                 meta[it % NST].seg = hdr;
+                const __nv_bfloat16* qrow =
+                    static_cast<const __nv_bfloat16*>(p.q) + ((long long)hdr.b * p.Hq + kvh * p.G + z * GH) * D;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qrow), "r"((uint32_t)(GH * D * 2))
+                             : "memory");
             }
             return true;
+        };
+        // the next unclaimed share of this (kv head, q-head group)
+        auto claim = [&]() -> int {
+            int v = 0;
+            if (lane == 0) v = (int)atomicAdd(&p.counters[group], 1u);
+            return __shfl_sync(0xffffffffu, v, 0);
         };
         // A full stage is published only when the next run needs room, so the
         // last stage of a segment is still open here and carries kSegEnd.
@@ -427,6 +460,29 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
             fill += nsr;
             run_off += S::kBoxes * 2 * R * 128;
         };
+        // One sub-tile per calling lane, emitted by the lanes together: n rows
+        // (1..16) from K-half row urow, sub-tile `rank` after the stage's
+        // current fill (lanes of one call take distinct ranks below the room).
+        constexpr int kSubCopy = S::kBoxes * 2 * 16 * 128;
+        auto emit_sub_lane = [&](long long urow, int n, int rank) {
+            const int s = it % NST;
+            const int f = fill + rank;
+            meta[s].nrows[f] = n;
+            meta[s].ip0[f] = 0;
+            meta[s].newrow[f] = -1;
+            meta[s].base[f] = run_off + rank * kSubCopy;
+            meta[s].ld[f] = 16;
+            unsigned char* dst = stage_base + (size_t)s * S::kStageBytes + run_off + rank * kSubCopy;
+            mbar_expect_tx(&full[s], (uint32_t)kSubCopy);
+            if (p.tma_whole) {
+                tma_load_5d(dst, &maps.run[0], 0, (int)urow, 0, p.layer, 0, &full[s]);
+            } else {
+#pragma unroll
+                for (int bx = 0; bx < S::kBoxes; ++bx)
+                    tma_load_4d(dst + bx * 2 * 16 * 128, &maps.run[0], bx * S::kBoxCols, (int)urow, 0, p.layer,
+                                &full[s]);
+            }
+        };
 
         if constexpr (!PAGED) {
             // stream-K over the sequences: sequence b contributes
@@ -450,9 +506,10 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
             }
             // no more shares than units, so that every share is non-empty and a
             // sequence's partial count is exactly the shares it overlaps
-            const int G = (int)(total < nctas ? total : nctas);
-            const long long lo = x < G ? (long long)x * total / G : total;
-            const long long hi = x < G ? (long long)(x + 1) * total / G : total;
+            const int G = (int)(total < p.nsplit ? total : p.nsplit);
+            for (int xs = claim(); xs < G && ok; xs = claim()) {
+            const long long lo = (long long)xs * total / G;
+            const long long hi = (long long)(xs + 1) * total / G;
             long long run = 0;
             for (int base = 0; base < p.B && ok && run < hi; base += 32) {
                 int tb = 0, nl = 0;
@@ -477,7 +534,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
                     MmaSegment hdr;
                     hdr.b = b;
                     hdr.t = t_b;
-                    hdr.slot = x + b;
+                    hdr.slot = xs + b;
                     hdr.first_slot = fx + b;
                     hdr.nparts = lx - fx + 1;
                     if (!(ok = begin_segment(hdr))) break;
@@ -525,7 +582,11 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
                 }
                 run += __shfl_sync(0xffffffffu, incl, 31);
             }
+            }
         } else {
+            const int G = __ldcg(&p.n_items[1]);    // the plan's share count
+            for (int xs = claim(); xs < G && ok; xs = claim()) {
+            const int2 my_items = __ldcg(&p.cta_items[xs]);
             for (int k = 0; k < my_items.y && ok; ++k) {
                 const int item = my_items.x + k;
                 if (item < 0 || item >= p.max_items) {
@@ -551,6 +612,42 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
                 int lb = itv.y;
                 int rem = itv.w;
                 const int last_lb = tt < 0 ? -1 : tt / p.bs;
+                // blocks of at most 16 rows: one sub-tile each; the lanes take
+                // 32 blocks at once and emit them together
+                while (p.bs <= 16 && rem > 0 && lb <= last_lb && ok) {
+                    const int my_lb = lb + lane;
+                    int my_phys = -1, my_rows = 0;
+                    if (my_lb <= last_lb)
+                        my_rows = paged_block_rows(trow, p.valid, p.err, my_lb, tt, p.bs, p.num_blocks, &my_phys);
+                    const int row0 = (my_lb == itv.y) ? itv.z : 0;
+                    const int avail = my_rows > row0 ? my_rows - row0 : 0;
+                    int incl = avail;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += u;
+                    }
+                    const int take = max(0, min(avail, rem - (incl - avail)));
+                    rem -= min(rem, __shfl_sync(0xffffffffu, incl, 31));
+                    const long long urow = ((long long)my_phys * p.Hkv + kvh) * p.bs + row0;
+                    unsigned pending = __ballot_sync(0xffffffffu, take > 0);
+                    while (pending && ok) {
+                        const int room = ensure_room();
+                        if (!room) {
+                            ok = false;
+                            break;
+                        }
+                        const int rank = __popc(pending & ((1u << lane) - 1u));
+                        const bool mine = ((pending >> lane) & 1u) && rank < room;
+                        const unsigned emitted = __ballot_sync(0xffffffffu, mine);
+                        if (mine) emit_sub_lane(urow, take, rank);
+                        __syncwarp();
+                        fill += __popc(emitted);
+                        run_off += __popc(emitted) * kSubCopy;
+                        pending &= ~emitted;
+                    }
+                    lb += 32;
+                }
                 while (rem > 0 && lb <= last_lb && ok) {
                     const int my_lb = lb + lane;
                     int my_phys = -1, my_rows = 0;
@@ -581,6 +678,7 @@ __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__((READ && D >= 256)
                     lb += 32;
                 }
                 if (ok) end_segment();
+            }
             }
         }
         if (ok) {

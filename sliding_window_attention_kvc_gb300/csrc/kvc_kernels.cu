@@ -10,15 +10,49 @@ namespace kvc {
 // [sink] (S pinned sinks, then a ring), [share] 3.1 (block table).  RoPE is
 // baked into K only ([pool] "RoPE baked into K rows": V is never rotated).
 // ---------------------------------------------------------------------------
+// Write one token's K (RoPE baked at `pos` when rope == kRopeBaked) and V
+// rows for every kv head: K of head h at kc + h * head_stride, V kv_off
+// elements further; k_src / v_src are the token's [Hkv, D] rows.  Threads
+// first .. first + nthreads - 1 of the calling CTA (all by default) split the
+// (head, pair) work.
+template <typename Elt>
+__device__ __forceinline__ void write_token_rows(Elt* kc, long long kv_off, long long head_stride, const Elt* ks,
+                                                 const Elt* vs, int Hkv, int D, int rope, long long pos,
+                                                 const unsigned long long* theta, int first = 0, int nthreads = 0) {
+    using TR = EltTraits<Elt>;
+    const int half = D / 2;
+    Elt* vc = kc + kv_off;
+    if (nthreads <= 0) nthreads = blockDim.x;
+    for (int idx = (int)threadIdx.x - first; idx < Hkv * half; idx += nthreads) {
+        const int h = idx / half, i = idx % half;
+        const Elt* kr = ks + (long long)h * D;
+        const Elt* vr = vs + (long long)h * D;
+        Elt* kd = kc + h * head_stride;
+        Elt* vd = vc + h * head_stride;
+        const Elt k1 = kr[i], k2 = kr[i + half];
+        if (rope == kRopeBaked) {
+            float c, s;
+            rope_cos_sin(pos, theta[i], &c, &s);
+            const float x1 = TR::to_f32(k1), x2 = TR::to_f32(k2);
+            kd[i] = TR::from_f32(x1 * c - x2 * s);
+            kd[i + half] = TR::from_f32(x1 * s + x2 * c);
+        } else {
+            kd[i] = k1;
+            kd[i + half] = k2;
+        }
+        vd[i] = vr[i];
+        vd[i + half] = vr[i + half];
+    }
+}
+
 template <typename Elt>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
-    using TR = EltTraits<Elt>;
     const int i_tok = blockIdx.x, b = blockIdx.y;
     const int t0 = p.pos[b];
     const long long pos = (long long)t0 + i_tok;
     if (pos < 0) return;                       // left padding
     const long long last = (long long)t0 + p.n_new - 1;
-    const int D = p.D, half = D / 2;
+    const int D = p.D;
 
     long long row_base;                        // element offset of (row, kv head 0) in the K half
     long long head_stride;                     // elements between kv heads
@@ -43,30 +77,9 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
         head_stride = (long long)p.bs * D;
     }
     Elt* kc = static_cast<Elt*>(p.cache) + p.layer_off + row_base;
-    Elt* vc = kc + p.kv_off;
     const Elt* ks = static_cast<const Elt*>(p.k_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
     const Elt* vs = static_cast<const Elt*>(p.v_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
-
-    for (int idx = threadIdx.x; idx < p.Hkv * half; idx += blockDim.x) {
-        const int h = idx / half, i = idx % half;
-        const Elt* kr = ks + (long long)h * D;
-        const Elt* vr = vs + (long long)h * D;
-        Elt* kd = kc + h * head_stride;
-        Elt* vd = vc + h * head_stride;
-        const Elt k1 = kr[i], k2 = kr[i + half];
-        if (p.rope == kRopeBaked) {
-            float c, s;
-            rope_cos_sin((long long)pos, p.theta[i], &c, &s);
-            const float x1 = TR::to_f32(k1), x2 = TR::to_f32(k2);
-            kd[i] = TR::from_f32(x1 * c - x2 * s);
-            kd[i + half] = TR::from_f32(x1 * s + x2 * c);
-        } else {
-            kd[i] = k1;
-            kd[i + half] = k2;
-        }
-        vd[i] = vr[i];
-        vd[i + half] = vr[i + half];
-    }
+    write_token_rows<Elt>(kc, p.kv_off, head_stride, ks, vs, p.Hkv, D, p.rope, pos, p.theta);
 }
 
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream) {
@@ -80,140 +93,340 @@ cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream)
 
 // ---------------------------------------------------------------------------
 // Paged work plan (stream-K).  The attended rows of all sequences, laid end
-// to end, are cut into `ctas` nearly equal contiguous shares; the
-// intersection of share x with sequence b is work item x + b (items of one
-// sequence, and of one share, get consecutive indices; a share boundary that
-// falls exactly on a sequence boundary leaves one index unused, marked -1).
-//   1. rows[b][lb] = attended rows of logical block lb (0 if unmapped, not
-//      valid, or past t); a block-wide inclusive scan over the flattened
-//      [B][max_blocks] array turns it into P, so sequence b starts at
-//      O_b = P[b * maxb - 1] and holds R_b = P[(b + 1) * maxb - 1] - O_b rows;
-//   2. per sequence: the shares overlapping [O_b, O_b + R_b) (a sequence with
-//      no attended row still gets one empty item, for its zero output), each
-//      item's first block and row by binary search in P.
+// to end, are cut into G <= `ctas` nearly equal contiguous shares
+// [floor(x R / G), floor((x + 1) R / G)); the intersection of share x with
+// sequence b is work item x + b (items of one sequence, and of one share, get
+// consecutive indices; a share boundary that falls exactly on a sequence
+// boundary leaves one index unused, marked -1).  Two kernels, one CTA per
+// sequence each, chained by programmatic dependent launch:
+//   plan_count_kernel  R_b = attended rows of sequence b (blocks lb <= t_b / bs
+//                      that are mapped and valid; [pool] "kernel forgets
+//                      absent blocks").  With a new token to append
+//                      (kvc_decode_step) it first writes that token's K/V.
+//                      The last CTA to finish (an atomic ticket, no waiting)
+//                      takes O_b = sum of R before b, R, G, and each sequence's
+//                      first item and item count (a sequence with no attended
+//                      row gets one empty item, for its zero output).
+//   plan_items_kernel  the sequence-local prefix of rows per block; each item
+//                      of sequence b is written by the thread whose blocks hold
+//                      its first row.
 // ---------------------------------------------------------------------------
-constexpr int kPlanThreads = 1024;
-constexpr int kPlanPerThread = 8;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanPerThread = 16;
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
-    __shared__ int s_warp[32];
-    __shared__ int s_carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long n = (long long)p.B * p.maxb;
-
-    for (int i = tid; i < p.max_items; i += kPlanThreads) p.items[i] = make_int4(-1, 0, 0, 0);
-    for (int i = tid; i < p.ctas; i += kPlanThreads) p.cta_items[i] = make_int2(0x7fffffff, 0);
-    if (tid == 0) s_carry = 0;
-    __syncthreads();
-
-    // 1. rows per block and their block-wide inclusive scan, in chunks
-    for (long long base = 0; base < n; base += (long long)kPlanThreads * kPlanPerThread) {
-        int v[kPlanPerThread];
-        int tsum = 0;
+// Block-wide inclusive scan of one value per thread (kPlanThreads threads);
+// returns the thread's inclusive prefix and the block total in *total.
+template <typename T>
+__device__ __forceinline__ T plan_block_scan(T v, T* s_warp, T* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int NW = kPlanThreads / 32;
 #pragma unroll
-        for (int j = 0; j < kPlanPerThread; ++j) {
-            const long long idx = base + (long long)tid * kPlanPerThread + j;
-            int r = 0;
-            if (idx < n) {
-                const int b = (int)(idx / p.maxb), lb = (int)(idx % p.maxb);
-                const int t = clamp_paged_t(p.pos[b], p.maxb, p.bs);
-                int phys = -1;
-                r = paged_block_rows(p.table + (long long)b * p.maxb, p.valid, p.err, lb, t, p.bs, p.num_blocks,
-                                     &phys);
-            }
-            tsum += r;
-            v[j] = tsum;
-        }
-        int w = tsum;
+    for (int off = 1; off < 32; off <<= 1) {
+        const T u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+    }
+    if (lane == 31) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        T x = lane < NW ? s_warp[lane] : T(0);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off) w += u;
+            const T u = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += u;
         }
-        if (lane == 31) s_warp[warp] = w;
-        __syncthreads();
-        if (warp == 0) {
-            int x = s_warp[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, x, off);
-                if (lane >= off) x += u;
-            }
-            s_warp[lane] = x;
-        }
-        __syncthreads();
-        const int before = s_carry + (warp > 0 ? s_warp[warp - 1] : 0) + (w - tsum);
-#pragma unroll
-        for (int j = 0; j < kPlanPerThread; ++j) {
-            const long long idx = base + (long long)tid * kPlanPerThread + j;
-            if (idx < n) p.rows[idx] = before + v[j];
-        }
-        __syncthreads();
-        if (tid == 0) s_carry += s_warp[31];
-        __syncthreads();
-    }
-    const long long R = s_carry;
-    const int G = (int)(R < p.ctas ? (R > 0 ? R : 1) : p.ctas);   // no empty shares
-
-    // 2a. per sequence: offset, rows, first and last share
-    for (int b = tid; b < p.B; b += kPlanThreads) {
-        const int32_t* P = p.rows;
-        const long long Ob = b > 0 ? P[(long long)b * p.maxb - 1] : 0;
-        const long long Rb = P[(long long)(b + 1) * p.maxb - 1] - Ob;
-        int fx, lx;
-        if (Rb > 0) {
-            fx = streamk_share_of(Ob, R, G);
-            lx = streamk_share_of(Ob + Rb - 1, R, G);
-        } else {
-            fx = lx = R > 0 ? streamk_share_of(Ob < R ? Ob : R - 1, R, G) : 0;
-        }
-        p.seq_items[b] = make_int2(fx + b, lx - fx + 1);
+        if (lane < NW) s_warp[lane] = x;
     }
     __syncthreads();
-    // 2b. one thread per item index i = x + b: its sequence by binary search
-    // over the sequences' first items, then its first block and row
-    for (int i = tid; i < G + p.B && i < p.max_items; i += kPlanThreads) {
-        int lo_s = 0, hi_s = p.B - 1;
-        while (lo_s < hi_s) {                 // last sequence whose first item <= i
-            const int mid = (lo_s + hi_s + 1) >> 1;
-            if (p.seq_items[mid].x <= i) lo_s = mid; else hi_s = mid - 1;
+    const T r = v + (warp > 0 ? s_warp[warp - 1] : T(0));
+    *total = s_warp[NW - 1];
+    __syncthreads();
+    return r;
+}
+
+// Attended rows of kPlanPerThread logical blocks lb[j] of one sequence (as
+// paged_block_rows), with every table load issued before any valid-bit load,
+// so that the loads of all blocks are in flight together.
+__device__ __forceinline__ void plan_block_rows(const int32_t* trow, const uint32_t* valid, uint32_t* err,
+                                                const int* lb, int t, int nb, int bs, int num_blocks, int* rows) {
+    int phys[kPlanPerThread];
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) phys[j] = lb[j] < nb ? __ldg(trow + lb[j]) : -1;
+    uint32_t word[kPlanPerThread];
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) {
+        const bool in = phys[j] >= 0 && phys[j] < num_blocks;
+        word[j] = (in && valid) ? __ldg(valid + (phys[j] >> 5)) : 0xffffffffu;
+    }
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) {
+        int r = 0;
+        if (phys[j] >= num_blocks) {
+            set_error(err, 0x1u /* KVC_DEV_BAD_BLOCK */);
+        } else if (phys[j] >= 0 && ((word[j] >> (phys[j] & 31)) & 1u)) {
+            r = lb[j] == t / bs ? (t - lb[j] * bs + 1) : bs;
         }
-        const int b = lo_s;
-        const int2 si = p.seq_items[b];
-        if (i < si.x || i >= si.x + si.y) continue;      // unused index (stays -1)
-        const int x = i - b;
-        if (x < 0 || x >= p.ctas) {
-            index_fault(p.err, 6, i);
-            continue;
-        }
-        const int32_t* P = p.rows;
-        const long long Ob = b > 0 ? P[(long long)b * p.maxb - 1] : 0;
-        const long long Rb = P[(long long)(b + 1) * p.maxb - 1] - Ob;
+        rows[j] = r;
+    }
+}
+
+__device__ __forceinline__ void plan_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void plan_pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The step's new token (kvc_decode_step) of sequence b at position traw, to
+// row traw mod bs of logical block traw / bs.
+__device__ __forceinline__ void plan_append(const PlanParams& p, int b, int traw) {
+    if (!p.k_new || traw < 0) return;
+    const long long lb = traw / p.bs;
+    if (lb >= p.maxb) {
+        if (threadIdx.x == 0) set_error(p.err, 0x4u /* KVC_DEV_BAD_POSITION */);
+        return;
+    }
+    const int phys = p.table[(long long)b * p.maxb + lb];
+    if (phys < 0 || phys >= p.num_blocks) {
+        if (threadIdx.x == 0) set_error(p.err, phys < 0 ? 0x2u : 0x1u);
+        return;
+    }
+    const long long row_base = ((long long)phys * p.Hkv * p.bs + (traw % p.bs)) * p.D;
+    const long long tok = (long long)b * p.Hkv * p.D;
+    if (p.elt == 4)
+        write_token_rows<float>(static_cast<float*>(p.cache) + p.layer_off + row_base, p.kv_off,
+                                (long long)p.bs * p.D, static_cast<const float*>(p.k_new) + tok,
+                                static_cast<const float*>(p.v_new) + tok, p.Hkv, p.D, p.rope, traw, p.theta);
+    else
+        write_token_rows<__nv_bfloat16>(static_cast<__nv_bfloat16*>(p.cache) + p.layer_off + row_base, p.kv_off,
+                                        (long long)p.bs * p.D, static_cast<const __nv_bfloat16*>(p.k_new) + tok,
+                                        static_cast<const __nv_bfloat16*>(p.v_new) + tok, p.Hkv, p.D, p.rope, traw,
+                                        p.theta);
+}
+
+// First item and item count of a sequence with O_b rows before it and R_b rows.
+__device__ __forceinline__ int2 plan_seq_items(int b, long long Ob, long long Rb, long long R, int G) {
+    int fx, lx;
+    if (Rb > 0) {
+        fx = streamk_share_of(Ob, R, G);
+        lx = streamk_share_of(Ob + Rb - 1, R, G);
+    } else {
+        fx = lx = R > 0 ? streamk_share_of(Ob < R ? Ob : R - 1, R, G) : 0;
+    }
+    return make_int2(fx + b, lx - fx + 1);
+}
+
+// The items of sequence b (O_b, R_b; shares of R rows into G) whose first row
+// lies in this thread's blocks lb0 .. lb0 + kPlanPerThread - 1, which hold its
+// sequence-local rows [rs, re); v = their inclusive prefix from rs.  Share x
+// starts at floor(x R / G), inside [O_b + rs, O_b + re) iff
+// ceil((O_b + rs) G / R) <= x < ceil((O_b + re) G / R); the sequence's first
+// item starts at its row 0 when its share began in an earlier sequence.
+__device__ __forceinline__ void plan_write_items(const PlanParams& p, int b, long long Ob, long long Rb, long long R,
+                                                 int G, int2 si, int lb0, const int* v, long long rs, long long re) {
+    if (re <= rs) return;
+    const int fx = si.x - b, lx = fx + si.y - 1;
+    const long long A = Ob + rs, Bnd = Ob + re;
+    int x0 = (int)((A * G + R - 1) / R), x1 = (int)((Bnd * G + R - 1) / R);
+    if (x0 < fx) x0 = fx;
+    if (x1 > lx + 1) x1 = lx + 1;
+    if (rs == 0 && (long long)fx * R / G < Ob && x0 > fx) x0 = fx;
+    for (int x = x0; x < x1; ++x) {
         const long long lo = (long long)x * R / G, hi = (long long)(x + 1) * R / G;
         const long long s0 = (lo > Ob ? lo : Ob) - Ob;
         const long long s1 = (hi < Ob + Rb ? hi : Ob + Rb) - Ob;
-        int lb = 0, off = 0;
-        if (s1 > s0) {
-            // first block whose (sequence-local) inclusive prefix exceeds s0
-            int lo_b = 0, hi_b = p.maxb - 1;
-            const int32_t* Pb = P + (long long)b * p.maxb;
-            while (lo_b < hi_b) {
-                const int mid = (lo_b + hi_b) >> 1;
-                if (Pb[mid] - Ob > s0) hi_b = mid; else lo_b = mid + 1;
-            }
-            lb = lo_b;
-            off = (int)(s0 - ((lb > 0 ? Pb[lb - 1] : Ob) - Ob));
+        if (s1 <= s0 || s0 < rs || s0 >= re) continue;
+        int j = 0;
+        while (j < kPlanPerThread - 1 && rs + v[j] <= s0) ++j;
+        const int i = x + b;
+        if (x < 0 || x >= p.ctas || i >= p.max_items) {
+            index_fault(p.err, 6, i);
+            continue;
         }
-        p.items[i] = make_int4(b, lb, off, (int)(s1 > s0 ? s1 - s0 : 0));
+        const long long before = rs + (j > 0 ? v[j - 1] : 0);
+        p.items[i] = make_int4(b, lb0 + j, (int)(s0 - before), (int)(s1 - s0));
         atomicMin(&p.cta_items[x].x, i);
         atomicAdd(&p.cta_items[x].y, 1);
     }
-    if (tid == 0) *p.n_items = G + p.B;
+}
+
+__device__ __forceinline__ void plan_write_empty_item(const PlanParams& p, int b, int2 si) {
+    const int fx = si.x - b;
+    if (fx < 0 || fx >= p.ctas || si.x >= p.max_items) {
+        index_fault(p.err, 6, si.x);
+        return;
+    }
+    p.items[si.x] = make_int4(b, 0, 0, 0);
+    atomicMin(&p.cta_items[fx].x, si.x);
+    atomicAdd(&p.cta_items[fx].y, 1);
+}
+
+__device__ __forceinline__ void plan_init_items(const PlanParams& p) {
+    for (int i = threadIdx.x; i < p.max_items; i += kPlanThreads) p.items[i] = make_int4(-1, 0, 0, 0);
+    for (int i = threadIdx.x; i < p.ctas; i += kPlanThreads) p.cta_items[i] = make_int2(0x7fffffff, 0);
+}
+
+__device__ __forceinline__ void plan_write_header(const PlanParams& p, long long R, int G) {
+    p.n_items[0] = G + p.B;
+    p.n_items[1] = G;
+    *reinterpret_cast<long long*>(p.n_items + 2) = R;
+}
+
+// Shares of R rows: no more than the CTAs, and no empty share.
+__device__ __forceinline__ int plan_shares(long long R, int ctas) {
+    return (int)(R < ctas ? (R > 0 ? R : 1) : ctas);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const __grid_constant__ PlanParams p) {
+    __shared__ int s_wi[32];
+    __shared__ long long s_wl[32];
+    __shared__ int s_last;
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+    plan_pdl_wait();            // positions, table, valid bits may come from the previous kernel
+    const int traw = p.pos[b];
+    const int32_t* trow = p.table + (long long)b * p.maxb;
+    const int t = clamp_paged_t(traw, p.maxb, p.bs);
+    const int nb = t < 0 ? 0 : t / p.bs + 1;
+    constexpr int kChunk = kPlanThreads * kPlanPerThread;
+
+    if (gridDim.x == 1 && p.maxb <= kChunk) {
+        // one sequence whose blocks fit one pass: the whole plan here (the
+        // host launches no plan_items_kernel in this case; same test)
+        const int lb0 = tid * kPlanPerThread;
+        int lbs[kPlanPerThread], v[kPlanPerThread];
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = lb0 + j;
+        plan_block_rows(trow, p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, v);
+        int tsum = 0;
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) {
+            tsum += v[j];
+            v[j] = tsum;
+        }
+        int R32 = 0;
+        const int incl = plan_block_scan<int>(tsum, s_wi, &R32);
+        const long long R = R32;
+        const int G = plan_shares(R, p.ctas);
+        const int2 si = plan_seq_items(0, 0, R, R, G);
+        plan_init_items(p);
+        if (tid == 0) {
+            p.seq_rows[0] = R32;
+            p.seq_off[0] = 0;
+            p.seq_items[0] = si;
+            plan_write_header(p, R, G);
+        }
+        __syncthreads();
+        if (R > 0)
+            plan_write_items(p, 0, 0, R, R, G, si, lb0, v, incl - tsum, incl);
+        else if (tid == 0)
+            plan_write_empty_item(p, 0, si);
+        plan_append(p, b, traw);
+        return;
+    }
+
+    // R_b
+    int sum = 0;
+    for (int base = 0; base < nb; base += kChunk) {
+        int lbs[kPlanPerThread], v[kPlanPerThread];
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = base + j * kPlanThreads + tid;
+        plan_block_rows(trow, p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, v);
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) sum += v[j];
+    }
+    plan_append(p, b, traw);
+    int rb = 0;
+    plan_block_scan<int>(sum, s_wi, &rb);
+    if (tid == 0) p.seq_rows[b] = rb;
+
+    // the last CTA to get here: offsets, G, and each sequence's first item
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(p.ticket, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    plan_init_items(p);
+    long long run = 0;
+    for (int base = 0; base < p.B; base += kPlanThreads) {
+        const int bb = base + tid;
+        const long long r = bb < p.B ? (long long)__ldcg(&p.seq_rows[bb]) : 0;
+        long long chunk = 0;
+        const long long incl = plan_block_scan<long long>(r, s_wl, &chunk);
+        if (bb < p.B) p.seq_off[bb] = run + incl - r;
+        run += chunk;
+    }
+    const long long R = run;
+    const int G = plan_shares(R, p.ctas);
+    __syncthreads();
+    for (int bb = tid; bb < p.B; bb += kPlanThreads)
+        p.seq_items[bb] = plan_seq_items(bb, __ldcg(&p.seq_off[bb]), __ldcg(&p.seq_rows[bb]), R, G);
+    if (tid == 0) {
+        plan_write_header(p, R, G);
+        *p.ticket = 0u;                       // ready for the next plan
+    }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_items_kernel(const __grid_constant__ PlanParams p) {
+    __shared__ int s_wi[32];
+    const int tid = threadIdx.x;
+    const int b = blockIdx.x;
+    // Positions, table and valid bits were final when plan_count_kernel passed
+    // its own wait (this grid launches only after that): the rows of the first
+    // pass are loaded before waiting for plan_count_kernel's results.
+    const int32_t* trow = p.table + (long long)b * p.maxb;
+    const int t = clamp_paged_t(__ldg(p.pos + b), p.maxb, p.bs);
+    const int nb = t < 0 ? 0 : t / p.bs + 1;
+    constexpr int kChunk = kPlanThreads * kPlanPerThread;
+    int lbs[kPlanPerThread], v[kPlanPerThread];
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = tid * kPlanPerThread + j;
+    plan_block_rows(trow, p.valid, nullptr, lbs, t, nb, p.bs, p.num_blocks, v);
+    // No early trigger here: the decode grid fills every SM (two CTAs each)
+    // and must not launch while plan CTAs still hold registers, or its last
+    // CTAs start only when others finish.
+    plan_pdl_wait();
+    const int G = __ldcg(&p.n_items[1]);
+    const long long R = __ldcg(reinterpret_cast<const long long*>(p.n_items + 2));
+    const long long Ob = __ldcg(&p.seq_off[b]);
+    const long long Rb = __ldcg(&p.seq_rows[b]);
+    const int2 si = __ldcg(&p.seq_items[b]);
+    if (Rb <= 0) {              // one empty item
+        if (tid == 0) plan_write_empty_item(p, b, si);
+        return;
+    }
+    int carry = 0;
+    for (int base = 0; base < nb; base += kChunk) {
+        const int lb0 = base + tid * kPlanPerThread;
+        if (base > 0) {
+#pragma unroll
+            for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = lb0 + j;
+            plan_block_rows(trow, p.valid, nullptr, lbs, t, nb, p.bs, p.num_blocks, v);
+        }
+        int tsum = 0;
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) {
+            tsum += v[j];
+            v[j] = tsum;
+        }
+        int chunk = 0;
+        const int incl = plan_block_scan<int>(tsum, s_wi, &chunk);
+        plan_write_items(p, b, Ob, Rb, R, G, si, lb0, v, carry + incl - tsum, carry + incl);
+        carry += chunk;
+    }
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, plan_count_kernel, p);
+    if (e != cudaSuccess) return e;
+    // one sequence of at most kPlanThreads * kPlanPerThread blocks: planned in one kernel
+    if (p.B == 1 && (long long)p.maxb <= (long long)kPlanThreads * kPlanPerThread) return cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, plan_items_kernel, p);
 }
 
 // ---------------------------------------------------------------------------

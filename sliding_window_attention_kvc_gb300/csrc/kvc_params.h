@@ -15,6 +15,12 @@ constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;  // + 1 copy-issuing w
 constexpr int kStages = 4;                       // bulk-copy pipeline depth
 constexpr int kTargetCtas = 608;                 // 152 SMs x 2 CTAs x 2 waves
 constexpr int kStreamCtas = 304;                 // stream-K grid: 152 SMs x 2 CTAs
+// bf16 stream-K shares per persistent CTA (default).  Claiming several
+// shares in turn evens out CTAs that stream at different speeds (paged
+// batches: mixed lengths, shared-prefix blocks that hit in L2), at a fixed
+// cost per share (a segment start and a partial) that only long shares hide.
+constexpr int kPagedShareFactor = 3;             // paged caches with >= kPagedShareBatch sequences
+constexpr int kPagedShareBatch = 8;
 constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
@@ -23,18 +29,19 @@ enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
 // Workspace carve-up (byte offsets from the workspace base).
 struct WorkspaceLayout {
     size_t err;          // uint32 error word
-    size_t counters;     // uint32 [batch * kv_heads * nsub]
+    size_t counters;     // uint32 [batch * kv_heads * nsub + 1]: completion tickets (last: paged plan)
     size_t part_ml;      // float2 [items * q_heads]: running max (log2 units), sum of weights
     size_t part_o;       // float  [items * q_heads * head_dim]: unnormalised output
-    size_t plan_rows;    // PAGED: int32 [batch * max_blocks]: attended rows per block, then prefix
+    size_t plan_acc;     // PAGED: int64 [batch] rows before each sequence, then int32 [batch] its rows
     size_t plan_seq;     // PAGED: int2  [batch]: first item, item count
     size_t plan_items;   // PAGED: int4  [items]: (seq, first block, first row, rows)
-    size_t plan_total;   // PAGED: int32 number of items used
+    size_t plan_total;   // PAGED: int32 items used, int32 shares G, int64 attended rows R
     size_t plan_cta;     // PAGED: int2 [ctas]: first item, item count
     size_t total;
-    int items;           // partial slots per (q head): batch * nsplit, or paged items
+    int items;           // partial slots per (q head): batch * nsplit, or shares + batch
     int nsplit;          // RING / SINK_RING fp32: splits per (sequence, kv head)
-    int ctas;            // stream-K CTAs per (kv head, q-head group)
+    int shares;          // stream-K shares per (kv head, q-head group) (bf16, paged)
+    int ctas;            // persistent CTAs per (kv head, q-head group) that claim the shares
 };
 
 struct DecodeParams {
@@ -47,7 +54,7 @@ struct DecodeParams {
     const void* k_new;          // fused append (kvc_decode_step): [B, Hkv, D] pre-RoPE; null = none
     const void* v_new;
     uint32_t* err;
-    uint32_t* counters;
+    uint32_t* counters;         // bf16: [Hkv * nsub] share counters, zero between calls
     float2* part_ml;
     float* part_o;
     const int4* items;          // PAGED plan
@@ -60,7 +67,7 @@ struct DecodeParams {
     int B, Hq, Hkv, G, nsub;
     int window, sinks, capacity;
     int bs, num_blocks, maxb;
-    int nsplit;                 // fp32 window: splits per (sequence, kv head); bf16: stream-K CTAs
+    int nsplit;                 // fp32 window: splits per (sequence, kv head); bf16: stream-K shares
     int max_items;              // partial slots per q head (bound for every slot index)
     int rope;                   // kRopeNone / kRopeBaked / kRopeRead
     int tma_whole;              // bf16: 1 = one tensor copy per run covers every column block
@@ -74,12 +81,21 @@ struct PlanParams {
     const int32_t* table;
     const uint32_t* valid;
     uint32_t* err;
-    int32_t* rows;        // [B * maxb]
+    int32_t* seq_rows;    // [B]: attended rows of each sequence
+    long long* seq_off;   // [B]: attended rows of the sequences before it
+    uint32_t* ticket;     // zero between plans
     int2* seq_items;      // [B]: first item, item count
     int4* items;          // [max_items]: (seq, first block, first row, rows); seq -1 = unused
     int2* cta_items;      // [ctas]: first item, item count
-    int32_t* n_items;     // one past the last item used
+    int32_t* n_items;     // [0] one past the last item used, [1] G, [2..3] R (int64)
     int B, bs, num_blocks, maxb, max_items, ctas;
+    // the step's new token (kvc_decode_step); k_new == null: none
+    void* cache;
+    const void* k_new;    // [B, Hkv, D] pre-RoPE
+    const void* v_new;
+    long long layer_off, kv_off;
+    int Hkv, D, rope, elt;
+    unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
 };
 
 struct AppendParams {
