@@ -339,6 +339,34 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
+# DRAM bytes (read + write) per launch of decode_mma_kernel, from one ncu
+# capture per workload (summaries: profiles/decode_mma_<workload>.md), and the
+# digest of the kernel sources they were taken on: reported only while the
+# sources are unchanged.
+KERNEL_TRAFFIC = {"ring_bf16": 138464256, "sink_window_bf16": 544556288,
+                  "paged_shared_prefix_bf16": 894835456, "long_context_pool_bf16": 152987904}
+KERNEL_TRAFFIC_SOURCES = "00bd4bff9652560d92642479b4857f63f01448aeedb02ff359569be0a9ac922d"
+
+
+def _kernel_sources_digest():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "sliding_window_attention_kvc_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic(wl_name, override):
+    if override is not None:
+        return override
+    if wl_name in KERNEL_TRAFFIC and _kernel_sources_digest() == KERNEL_TRAFFIC_SOURCES:
+        return KERNEL_TRAFFIC[wl_name]
+    return None
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -552,7 +580,8 @@ def run_ours(args):
         "eager_ms_per_step": eager_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": args.traffic,
+                     "traffic": _traffic(wl.name, args.traffic),
+                     "traffic_kernel": "decode_mma_kernel, dram__bytes_read.sum + dram__bytes_write.sum per launch",
                      "kernel": "kvc_decode_step: " + ("decode_mma_kernel + combine_streamk_kernel"
                                                       if wl.dtype == "bf16" else "append + decode"),
                      "timer": "CUDA events around the timed region (K kvc_decode_step calls); per step",
