@@ -101,8 +101,9 @@ struct MmaSmem {
     static constexpr size_t kQcs = kRot + (READ ? (size_t)S::kStages * S::kNsub * S::kHalf * 8 : 0);  // [D/2] float2
     static constexpr size_t kMergeO = kQcs + (size_t)S::kHalf * 8;
     static constexpr size_t kMergeML = kMergeO + (size_t)S::kTokenGroups * GH * D * 4;
-    static constexpr size_t kFlag = kMergeML + (size_t)S::kTokenGroups * GH * 8;
-    static constexpr size_t kCbar = kFlag + 16;           // 3 mbarriers: all compute warps, 2 warp pairs
+    static constexpr size_t kHdr = kMergeML + (size_t)S::kTokenGroups * GH * 8;   // the CTA's first segment header
+    // 4 mbarriers: all compute warps, 2 warp pairs, first header published
+    static constexpr size_t kCbar = kHdr + sizeof(MmaSegment);
     static constexpr size_t kTotal = kCbar + 32 + 1024;   // + slack to align the base to 1024
 };
 
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
     float* merge_o = reinterpret_cast<float*>(smem + SM::kMergeO);
     float2* merge_ml = reinterpret_cast<float2*>(smem + SM::kMergeML);
     uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + SM::kCbar);
+    MmaSegment* first_hdr = reinterpret_cast<MmaSegment*>(smem + SM::kHdr);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -330,6 +332,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         mbar_init(&cbar[0], kConsumerWarps * 32);
         mbar_init(&cbar[1], 64);
         mbar_init(&cbar[2], 64);
+        mbar_init(&cbar[3], 1);
         mbar_fence_init();
 #pragma unroll
         for (int r = 0; r < kRunMaps; ++r) tma_prefetch_desc(&maps.run[r]);
@@ -340,8 +343,18 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
 
     if (warp == kConsumerWarps) {
         // =================== copy-issuing warp ==============================
-        int it = 0, fill = 0, run_off = 0;
-        bool ok = true, open = false;
+        int it = 0, fill = 0, run_off = 0, claims = 0;
+        bool ok = true, open = false, hdr_sent = false;
+        // the first segment's header goes to the compute warps at once, so that
+        // they load q while its first copy is in flight (b = -1: no segment)
+        auto publish_first = [&](const MmaSegment& hdr) {
+            if (hdr_sent) return;
+            hdr_sent = true;
+            if (lane == 0) {
+                *first_hdr = hdr;
+                mbar_arrive(&cbar[3]);
+            }
+        };
         auto open_stage = [&]() -> bool {
             const int s = it % NST;
             if (it >= NST && !mbar_wait(&empty[s], ((it / NST) - 1) & 1)) {
@@ -370,6 +383,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         auto begin_segment = [&](const MmaSegment& hdr) -> bool {
             if (open) commit(0);
             if (!open_stage()) return false;
+            publish_first(hdr);
             if (lane == 0) {
                 meta[it % NST].flags = kSegBegin;
                 meta[it % NST].seg = hdr;
@@ -380,11 +394,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             }
             return true;
         };
-        // the next unclaimed share of this (kv head, q-head group)
-        auto claim = [&]() -> int {
+        // the next share of this (kv head, q-head group) out of G: first share
+        // blockIdx.x, then gridDim.x, gridDim.x + 1, ... claimed through the counter
+        auto claim = [&](int G) -> int {
+            if (claims++ == 0 && (int)blockIdx.x < G) return blockIdx.x;
             int v = 0;
             if (lane == 0) v = (int)atomicAdd(&p.counters[group], 1u);
-            return __shfl_sync(0xffffffffu, v, 0);
+            return (int)gridDim.x + __shfl_sync(0xffffffffu, v, 0);
         };
         // A full stage is published only when the next run needs room, so the
         // last stage of a segment is still open here and carries kSegEnd.
@@ -507,7 +523,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             // no more shares than units, so that every share is non-empty and a
             // sequence's partial count is exactly the shares it overlaps
             const int G = (int)(total < p.nsplit ? total : p.nsplit);
-            for (int xs = claim(); xs < G && ok; xs = claim()) {
+            for (int xs = claim(G); xs < G && ok; xs = claim(G)) {
             const long long lo = (long long)xs * total / G;
             const long long hi = (long long)(xs + 1) * total / G;
             long long run = 0;
@@ -585,7 +601,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             }
         } else {
             const int G = __ldcg(&p.n_items[1]);    // the plan's share count
-            for (int xs = claim(); xs < G && ok; xs = claim()) {
+            for (int xs = claim(G); xs < G && ok; xs = claim(G)) {
             const int2 my_items = __ldcg(&p.cta_items[xs]);
             for (int k = 0; k < my_items.y && ok; ++k) {
                 const int item = my_items.x + k;
@@ -690,6 +706,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                     mbar_arrive(&full[it % NST]);
                 }
             }
+        }
+        if (!hdr_sent) {
+            MmaSegment none;
+            none.b = -1;
+            none.t = none.slot = none.first_slot = none.nparts = 0;
+            publish_first(none);
         }
         if (!ok && lane == 0) {
             // never leave with copies still landing in this CTA's shared memory;
@@ -854,6 +876,33 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         }
     };
 
+    // a segment header that fails its checks writes nothing
+    auto check_seg = [&](MmaSegment& sg) {
+        if (sg.b < 0 || sg.b >= p.B || sg.slot < 0 || sg.slot >= p.max_items || sg.first_slot < 0 ||
+            sg.nparts < 1 || sg.first_slot + sg.nparts > p.max_items || sg.slot < sg.first_slot ||
+            sg.slot >= sg.first_slot + sg.nparts) {
+            if (ctid == 0) index_fault(p.err, 3 + (sg.b < 0 || sg.b >= p.B ? 0 : 8), sg.slot);
+            sg.b = -1;
+        }
+    };
+    // q of the first segment, loaded while its first copy is in flight (not
+    // with read-time RoPE, whose in-place rotation needs the registers)
+    bool preloaded = false;
+    if (READ) {
+    } else if (mbar_wait(&cbar[3], 0)) {
+        MmaSegment first = *first_hdr;
+        if (first.b >= 0) {
+            check_seg(first);
+            if (first.b >= 0) {
+                seg = first;
+                load_q();
+                preloaded = true;
+            }
+        }
+    } else if (lane == 0) {
+        set_error(p.err, 0x8u /* KVC_DEV_TIMEOUT */);
+    }
+
     for (int it = 0;; ++it) {
         const int s = it % NST;
         if (!mbar_wait(&full[s], (it / NST) & 1)) {
@@ -869,13 +918,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         const int flags = meta[s].flags;
         if (flags & kSegBegin) {
             seg = meta[s].seg;
-            if (seg.b < 0 || seg.b >= p.B || seg.slot < 0 || seg.slot >= p.max_items || seg.first_slot < 0 ||
-                seg.nparts < 1 || seg.first_slot + seg.nparts > p.max_items || seg.slot < seg.first_slot ||
-                seg.slot >= seg.first_slot + seg.nparts) {
-                if (ctid == 0) index_fault(p.err, 3 + (seg.b < 0 || seg.b >= p.B ? 0 : 8), seg.slot);
-                seg.b = -1;                       // this segment writes nothing
+            check_seg(seg);
+            if (preloaded) {                      // the first segment: q is already in registers
+                preloaded = false;
+            } else {
+                if (seg.b >= 0) load_q(); else csync.sync(p.err), csync.sync(p.err);
             }
-            if (seg.b >= 0) load_q(); else csync.sync(p.err), csync.sync(p.err);
         }
         if (tg < nsub) {
             const int nrows = meta[s].nrows[tg];
