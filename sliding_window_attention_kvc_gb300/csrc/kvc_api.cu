@@ -99,13 +99,15 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     off = align_up(off + (size_t)w.items * d->q_heads * 8, 256);
     w.part_o = off;
     off = align_up(off + (size_t)w.items * d->q_heads * d->head_dim * 4, 256);
-    w.plan_seq = w.plan_acc = w.plan_items = w.plan_total = w.plan_cta = off;
+    w.plan_seq = w.plan_acc = w.plan_items = w.plan_info = w.plan_total = w.plan_cta = off;
     if (d->layout == KVC_LAYOUT_PAGED) {
         w.plan_seq = off;
         off = align_up(off + (size_t)d->batch * 8, 256);
         w.plan_acc = off;
         off = align_up(off + (size_t)d->batch * 12, 256);
         w.plan_items = off;
+        off = align_up(off + (size_t)w.items * 16, 256);
+        w.plan_info = off;
         off = align_up(off + (size_t)w.items * 16, 256);
         w.plan_cta = off;
         off = align_up(off + (size_t)w.shares * 8, 256);
@@ -352,6 +354,7 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
         pp.ticket = reinterpret_cast<uint32_t*>(ws + w.counters) + (size_t)d->batch * d->kv_heads * g.nsub;
         pp.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
         pp.items = reinterpret_cast<int4*>(ws + w.plan_items);
+        pp.item_info = reinterpret_cast<int4*>(ws + w.plan_info);
         pp.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
         pp.cta_items = reinterpret_cast<int2*>(ws + w.plan_cta);
         pp.ctas = w.shares;
@@ -374,6 +377,7 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
         }
         if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
         p.items = pp.items;
+        p.item_info = pp.item_info;
         p.seq_items = pp.seq_items;
         p.n_items = pp.n_items;
         p.cta_items = pp.cta_items;

@@ -180,6 +180,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
     __shared__ float s_M[GH], s_L[GH];
     __shared__ float4 s_part[kCombineThreads];
 
+    // the next kernel in the stream may begin launching; it waits for this
+    // grid to complete before it reads anything
+    pdl_launch_dependents();
     const int b = blockIdx.x;
     const int kvh = blockIdx.y / p.nsub, z = blockIdx.y % p.nsub;
     const int col0 = blockIdx.z * kCombineCols;
@@ -602,7 +605,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         } else {
             const int G = __ldcg(&p.n_items[1]);    // the plan's share count
             for (int xs = claim(G); xs < G && ok; xs = claim(G)) {
-            const int2 my_items = __ldcg(&p.cta_items[xs]);
+            // one sequence: share x holds exactly its item x
+            const int2 my_items = p.B == 1 ? make_int2(xs, 1) : __ldcg(&p.cta_items[xs]);
             for (int k = 0; k < my_items.y && ok; ++k) {
                 const int item = my_items.x + k;
                 if (item < 0 || item >= p.max_items) {
@@ -615,19 +619,55 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                     if (lane == 0) index_fault(p.err, 2, b);
                     break;
                 }
-                const int2 si = p.seq_items[b];
+                // (t, first slot, slot count, first physical block): read with the
+                // item for one sequence; a batch reads them per sequence
+                int4 inf;
+                if (p.B == 1) {
+                    inf = __ldcg(&p.item_info[item]);
+                } else {
+                    const int2 si = p.seq_items[b];
+                    inf = make_int4(p.pos[b], si.x, si.y, -1);
+                }
                 MmaSegment hdr;
                 hdr.b = b;
-                hdr.t = p.pos[b];
+                hdr.t = inf.x;
                 hdr.slot = item;
-                hdr.first_slot = si.x;
-                hdr.nparts = si.y;
+                hdr.first_slot = inf.y;
+                hdr.nparts = inf.z;
                 if (!(ok = begin_segment(hdr))) break;
                 const int tt = clamp_paged_t(hdr.t, p.maxb, p.bs);
                 const int32_t* trow = p.table + (long long)b * p.maxb;
                 int lb = itv.y;
                 int rem = itv.w;
                 const int last_lb = tt < 0 ? -1 : tt / p.bs;
+                // one sequence: the item's first block is attended by construction
+                // and its physical block comes with the item, so its copies need no
+                // table lookup
+                if (p.B == 1 && rem > 0 && lb <= last_lb && ok) {
+                    const int phys = inf.w;
+                    if (phys < 0 || phys >= p.num_blocks) {
+                        if (lane == 0) index_fault(p.err, 13, phys);
+                        ok = false;
+                        break;
+                    }
+                    const int brows = lb == last_lb ? tt - lb * p.bs + 1 : p.bs;
+                    const long long blk = ((long long)phys * p.Hkv + kvh) * p.bs;   // row in the K half
+                    int row = itv.z;
+                    int take = min(brows - row, rem);
+                    while (take > 0 && ok) {
+                        const int room = ensure_room();
+                        if (!room) {
+                            ok = false;
+                            break;
+                        }
+                        const int n = min(take, 16 * room);
+                        emit_run(blk + row, n, 0, -1, true);
+                        take -= n;
+                        rem -= n;
+                        row += n;
+                    }
+                    ++lb;
+                }
                 // blocks of at most 16 rows: one sub-tile each; the lanes take
                 // 32 blocks at once and emit them together
                 while (p.bs <= 16 && rem > 0 && lb <= last_lb && ok) {

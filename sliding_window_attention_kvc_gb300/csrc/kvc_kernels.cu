@@ -143,30 +143,36 @@ __device__ __forceinline__ T plan_block_scan(T v, T* s_warp, T* total) {
     return r;
 }
 
-// Attended rows of kPlanPerThread logical blocks lb[j] of one sequence (as
-// paged_block_rows), with every table load issued before any valid-bit load,
-// so that the loads of all blocks are in flight together.
-__device__ __forceinline__ void plan_block_rows(const int32_t* trow, const uint32_t* valid, uint32_t* err,
-                                                const int* lb, int t, int nb, int bs, int num_blocks, int* rows) {
-    int phys[kPlanPerThread];
-#pragma unroll
-    for (int j = 0; j < kPlanPerThread; ++j) phys[j] = lb[j] < nb ? __ldg(trow + lb[j]) : -1;
+// Attended rows of kPlanPerThread logical blocks lb[j] < nb of one sequence
+// (as paged_block_rows) whose table entries phys[j] are already loaded: every
+// valid-bit load is issued before any is used.
+__device__ __forceinline__ void plan_rows_of(const uint32_t* valid, uint32_t* err, const int* lb, int t, int nb,
+                                             int bs, int num_blocks, const int* phys, int* rows) {
     uint32_t word[kPlanPerThread];
 #pragma unroll
     for (int j = 0; j < kPlanPerThread; ++j) {
-        const bool in = phys[j] >= 0 && phys[j] < num_blocks;
+        const bool in = lb[j] < nb && phys[j] >= 0 && phys[j] < num_blocks;
         word[j] = (in && valid) ? __ldg(valid + (phys[j] >> 5)) : 0xffffffffu;
     }
 #pragma unroll
     for (int j = 0; j < kPlanPerThread; ++j) {
         int r = 0;
-        if (phys[j] >= num_blocks) {
+        if (lb[j] < nb && phys[j] >= num_blocks) {
             set_error(err, 0x1u /* KVC_DEV_BAD_BLOCK */);
-        } else if (phys[j] >= 0 && ((word[j] >> (phys[j] & 31)) & 1u)) {
+        } else if (lb[j] < nb && phys[j] >= 0 && ((word[j] >> (phys[j] & 31)) & 1u)) {
             r = lb[j] == t / bs ? (t - lb[j] * bs + 1) : bs;
         }
         rows[j] = r;
     }
+}
+
+// The same, loading the table entries first (all in flight together).
+__device__ __forceinline__ void plan_block_rows(const int32_t* trow, const uint32_t* valid, uint32_t* err,
+                                                const int* lb, int t, int nb, int bs, int num_blocks, int* rows,
+                                                int* phys) {
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) phys[j] = lb[j] < nb ? __ldg(trow + lb[j]) : -1;
+    plan_rows_of(valid, err, lb, t, nb, bs, num_blocks, phys, rows);
 }
 
 __device__ __forceinline__ void plan_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -174,14 +180,14 @@ __device__ __forceinline__ void plan_pdl_launch() { asm volatile("griddepcontrol
 
 // The step's new token (kvc_decode_step) of sequence b at position traw, to
 // row traw mod bs of logical block traw / bs.
-__device__ __forceinline__ void plan_append(const PlanParams& p, int b, int traw) {
+__device__ __forceinline__ void plan_append(const PlanParams& p, int b, int traw, int known_phys = -2) {
     if (!p.k_new || traw < 0) return;
     const long long lb = traw / p.bs;
     if (lb >= p.maxb) {
         if (threadIdx.x == 0) set_error(p.err, 0x4u /* KVC_DEV_BAD_POSITION */);
         return;
     }
-    const int phys = p.table[(long long)b * p.maxb + lb];
+    const int phys = known_phys >= -1 ? known_phys : p.table[(long long)b * p.maxb + lb];
     if (phys < 0 || phys >= p.num_blocks) {
         if (threadIdx.x == 0) set_error(p.err, phys < 0 ? 0x2u : 0x1u);
         return;
@@ -213,12 +219,16 @@ __device__ __forceinline__ int2 plan_seq_items(int b, long long Ob, long long Rb
 
 // The items of sequence b (O_b, R_b; shares of R rows into G) whose first row
 // lies in this thread's blocks lb0 .. lb0 + kPlanPerThread - 1, which hold its
-// sequence-local rows [rs, re); v = their inclusive prefix from rs.  Share x
+// sequence-local rows [rs, re); v = their inclusive prefix from rs, ph = their
+// physical blocks.  Each item gets its record (seq, first block, first row,
+// rows) and, for the decode's copy warp, (t_b, first slot and count of the
+// sequence's partials, physical block of its first block).  Share x
 // starts at floor(x R / G), inside [O_b + rs, O_b + re) iff
 // ceil((O_b + rs) G / R) <= x < ceil((O_b + re) G / R); the sequence's first
 // item starts at its row 0 when its share began in an earlier sequence.
-__device__ __forceinline__ void plan_write_items(const PlanParams& p, int b, long long Ob, long long Rb, long long R,
-                                                 int G, int2 si, int lb0, const int* v, long long rs, long long re) {
+__device__ __forceinline__ void plan_write_items(const PlanParams& p, int b, int tb, long long Ob, long long Rb,
+                                                 long long R, int G, int2 si, int lb0, const int* v, const int* ph,
+                                                 long long rs, long long re) {
     if (re <= rs) return;
     const int fx = si.x - b, lx = fx + si.y - 1;
     const long long A = Ob + rs, Bnd = Ob + re;
@@ -231,27 +241,37 @@ __device__ __forceinline__ void plan_write_items(const PlanParams& p, int b, lon
         const long long s0 = (lo > Ob ? lo : Ob) - Ob;
         const long long s1 = (hi < Ob + Rb ? hi : Ob + Rb) - Ob;
         if (s1 <= s0 || s0 < rs || s0 >= re) continue;
-        int j = 0;
-        while (j < kPlanPerThread - 1 && rs + v[j] <= s0) ++j;
+        // first block j whose prefix exceeds s0 (unrolled: v and ph stay in registers)
+        int j = 0, phj = ph[0];
+        long long before = rs;
+#pragma unroll
+        for (int jj = 0; jj < kPlanPerThread - 1; ++jj) {
+            if (rs + v[jj] <= s0) {
+                j = jj + 1;
+                before = rs + v[jj];
+                phj = ph[jj + 1];
+            }
+        }
         const int i = x + b;
         if (x < 0 || x >= p.ctas || i >= p.max_items) {
             index_fault(p.err, 6, i);
             continue;
         }
-        const long long before = rs + (j > 0 ? v[j - 1] : 0);
         p.items[i] = make_int4(b, lb0 + j, (int)(s0 - before), (int)(s1 - s0));
+        p.item_info[i] = make_int4(tb, si.x, si.y, phj);
         atomicMin(&p.cta_items[x].x, i);
         atomicAdd(&p.cta_items[x].y, 1);
     }
 }
 
-__device__ __forceinline__ void plan_write_empty_item(const PlanParams& p, int b, int2 si) {
+__device__ __forceinline__ void plan_write_empty_item(const PlanParams& p, int b, int tb, int2 si) {
     const int fx = si.x - b;
     if (fx < 0 || fx >= p.ctas || si.x >= p.max_items) {
         index_fault(p.err, 6, si.x);
         return;
     }
     p.items[si.x] = make_int4(b, 0, 0, 0);
+    p.item_info[si.x] = make_int4(tb, si.x, si.y, -1);
     atomicMin(&p.cta_items[fx].x, si.x);
     atomicAdd(&p.cta_items[fx].y, 1);
 }
@@ -279,20 +299,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const __grid_c
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
     plan_pdl_wait();            // positions, table, valid bits may come from the previous kernel
-    const int traw = p.pos[b];
     const int32_t* trow = p.table + (long long)b * p.maxb;
-    const int t = clamp_paged_t(traw, p.maxb, p.bs);
-    const int nb = t < 0 ? 0 : t / p.bs + 1;
     constexpr int kChunk = kPlanThreads * kPlanPerThread;
+    __shared__ int s_tok_phys;
 
     if (gridDim.x == 1 && p.maxb <= kChunk) {
         // one sequence whose blocks fit one pass: the whole plan here (the
-        // host launches no plan_items_kernel in this case; same test)
+        // host launches no plan_items_kernel in this case; same test).  The
+        // table is loaded in full without waiting for the position.
         const int lb0 = tid * kPlanPerThread;
-        int lbs[kPlanPerThread], v[kPlanPerThread];
+        int lbs[kPlanPerThread], v[kPlanPerThread], ph[kPlanPerThread];
 #pragma unroll
-        for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = lb0 + j;
-        plan_block_rows(trow, p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, v);
+        for (int j = 0; j < kPlanPerThread; ++j) {
+            lbs[j] = lb0 + j;
+            ph[j] = lb0 + j < p.maxb ? __ldg(trow + lb0 + j) : -1;
+        }
+        if (tid == 0) s_tok_phys = -2;
+        const int traw = __ldg(p.pos);
+        const int t = clamp_paged_t(traw, p.maxb, p.bs);
+        const int nb = t < 0 ? 0 : t / p.bs + 1;
+        plan_rows_of(p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, ph, v);
         int tsum = 0;
 #pragma unroll
         for (int j = 0; j < kPlanPerThread; ++j) {
@@ -300,7 +326,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const __grid_c
             v[j] = tsum;
         }
         int R32 = 0;
-        const int incl = plan_block_scan<int>(tsum, s_wi, &R32);
+        const int incl = plan_block_scan<int>(tsum, s_wi, &R32);   // (its barriers order the slot's reset)
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j)
+            if (traw >= 0 && lbs[j] == traw / p.bs) s_tok_phys = ph[j];
         const long long R = R32;
         const int G = plan_shares(R, p.ctas);
         const int2 si = plan_seq_items(0, 0, R, R, G);
@@ -313,20 +342,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const __grid_c
         }
         __syncthreads();
         if (R > 0)
-            plan_write_items(p, 0, 0, R, R, G, si, lb0, v, incl - tsum, incl);
+            plan_write_items(p, 0, traw, 0, R, R, G, si, lb0, v, ph, incl - tsum, incl);
         else if (tid == 0)
-            plan_write_empty_item(p, 0, si);
-        plan_append(p, b, traw);
+            plan_write_empty_item(p, 0, traw, si);
+        plan_append(p, b, traw, s_tok_phys);
         return;
     }
+
+    const int traw = p.pos[b];
+    const int t = clamp_paged_t(traw, p.maxb, p.bs);
+    const int nb = t < 0 ? 0 : t / p.bs + 1;
 
     // R_b
     int sum = 0;
     for (int base = 0; base < nb; base += kChunk) {
-        int lbs[kPlanPerThread], v[kPlanPerThread];
+        int lbs[kPlanPerThread], v[kPlanPerThread], ph[kPlanPerThread];
 #pragma unroll
         for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = base + j * kPlanThreads + tid;
-        plan_block_rows(trow, p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, v);
+        plan_block_rows(trow, p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, v, ph);
 #pragma unroll
         for (int j = 0; j < kPlanPerThread; ++j) sum += v[j];
     }
@@ -371,13 +404,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_items_kernel(const __grid_c
     // its own wait (this grid launches only after that): the rows of the first
     // pass are loaded before waiting for plan_count_kernel's results.
     const int32_t* trow = p.table + (long long)b * p.maxb;
-    const int t = clamp_paged_t(__ldg(p.pos + b), p.maxb, p.bs);
+    const int traw = __ldg(p.pos + b);
+    const int t = clamp_paged_t(traw, p.maxb, p.bs);
     const int nb = t < 0 ? 0 : t / p.bs + 1;
     constexpr int kChunk = kPlanThreads * kPlanPerThread;
-    int lbs[kPlanPerThread], v[kPlanPerThread];
+    int lbs[kPlanPerThread], v[kPlanPerThread], ph[kPlanPerThread];
 #pragma unroll
     for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = tid * kPlanPerThread + j;
-    plan_block_rows(trow, p.valid, nullptr, lbs, t, nb, p.bs, p.num_blocks, v);
+    plan_block_rows(trow, p.valid, nullptr, lbs, t, nb, p.bs, p.num_blocks, v, ph);
     // No early trigger here: the decode grid fills every SM (two CTAs each)
     // and must not launch while plan CTAs still hold registers, or its last
     // CTAs start only when others finish.
@@ -388,7 +422,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_items_kernel(const __grid_c
     const long long Rb = __ldcg(&p.seq_rows[b]);
     const int2 si = __ldcg(&p.seq_items[b]);
     if (Rb <= 0) {              // one empty item
-        if (tid == 0) plan_write_empty_item(p, b, si);
+        if (tid == 0) plan_write_empty_item(p, b, traw, si);
         return;
     }
     int carry = 0;
@@ -397,7 +431,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_items_kernel(const __grid_c
         if (base > 0) {
 #pragma unroll
             for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = lb0 + j;
-            plan_block_rows(trow, p.valid, nullptr, lbs, t, nb, p.bs, p.num_blocks, v);
+            plan_block_rows(trow, p.valid, nullptr, lbs, t, nb, p.bs, p.num_blocks, v, ph);
         }
         int tsum = 0;
 #pragma unroll
@@ -407,7 +441,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_items_kernel(const __grid_c
         }
         int chunk = 0;
         const int incl = plan_block_scan<int>(tsum, s_wi, &chunk);
-        plan_write_items(p, b, Ob, Rb, R, G, si, lb0, v, carry + incl - tsum, carry + incl);
+        plan_write_items(p, b, traw, Ob, Rb, R, G, si, lb0, v, ph, carry + incl - tsum, carry + incl);
         carry += chunk;
     }
 }

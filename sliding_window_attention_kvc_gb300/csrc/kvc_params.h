@@ -35,6 +35,7 @@ struct WorkspaceLayout {
     size_t plan_acc;     // PAGED: int64 [batch] rows before each sequence, then int32 [batch] its rows
     size_t plan_seq;     // PAGED: int2  [batch]: first item, item count
     size_t plan_items;   // PAGED: int4  [items]: (seq, first block, first row, rows)
+    size_t plan_info;    // PAGED: int4  [items]: (t of the sequence, its first slot, its slot count, first physical block)
     size_t plan_total;   // PAGED: int32 items used, int32 shares G, int64 attended rows R
     size_t plan_cta;     // PAGED: int2 [ctas]: first item, item count
     size_t total;
@@ -58,6 +59,7 @@ struct DecodeParams {
     float2* part_ml;
     float* part_o;
     const int4* items;          // PAGED plan
+    const int4* item_info;      // PAGED plan: (t, first slot, slot count, first physical block) per item
     const int2* seq_items;      // PAGED plan
     const int32_t* n_items;     // PAGED plan
     const int2* cta_items;      // PAGED plan: first item, item count of each CTA (stream-K kernel)
@@ -86,6 +88,7 @@ struct PlanParams {
     uint32_t* ticket;     // zero between plans
     int2* seq_items;      // [B]: first item, item count
     int4* items;          // [max_items]: (seq, first block, first row, rows); seq -1 = unused
+    int4* item_info;      // [max_items]: (t_b, first slot, slot count of b, physical block of the first block)
     int2* cta_items;      // [ctas]: first item, item count
     int32_t* n_items;     // [0] one past the last item used, [1] G, [2..3] R (int64)
     int B, bs, num_blocks, maxb, max_items, ctas;
