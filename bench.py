@@ -380,15 +380,19 @@ def _peaks():
 # the CPU oracle as a timed baseline
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, budget_s, max_rows=None):
+def oracle_sample(wl, budget_s, max_rows=None, part=(0, 1)):
     """Run the CPU oracle on (sequence, kv head) units of layer 0 until
-    `budget_s` seconds of oracle time are spent; returns (bytes, seconds, desc)."""
+    `budget_s` seconds of oracle time are spent; returns (bytes, seconds,
+    units).  part = (k, n): only the units u = b * kv_heads + h with u mod n == k."""
     import oracle
     spec = dict(rope=wl.rope, base=wl.rope_base, storage=wl.dtype, sinks=wl.sinks, window=wl.window)
     row_bytes = 2 * wl.head_dim * wl.elt_bytes
     g = wl.group_size
     done_bytes, spent, units = 0, 0.0, 0
     for b in range(wl.batch):
+        mine = [h for h in range(wl.kv_heads) if (b * wl.kv_heads + h) % part[1] == part[0]]
+        if not mine:
+            continue
         t = int(wl.positions[b])
         if wl.layout == "window":
             pos = oracle.window_attended(t, wl.sinks, wl.window)
@@ -398,7 +402,7 @@ def oracle_sample(wl, budget_s, max_rows=None):
             pos = pos[-max_rows:]
         k, v = wl.kv_history(0, b, pos)
         q = wl.query(0, b)
-        for h in range(wl.kv_heads):
+        for h in mine:
             qf = q[h * g:(h + 1) * g].double().numpy()
             kf, vf = k[:, h].double().numpy(), v[:, h].double().numpy()
             t0 = time.perf_counter()
@@ -411,11 +415,47 @@ def oracle_sample(wl, budget_s, max_rows=None):
     return done_bytes, spent, units
 
 
-def cpu_baseline(wl, budget_s=10.0):
-    nbytes, secs, units = oracle_sample(wl, budget_s)
-    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{units} (sequence, kv head) units of one layer-step of {wl.name}, "
-                      f"{nbytes / 1e6:.1f} MB of attended K/V, {secs:.1f} s single-threaded fp64"}
+def _oracle_worker(name, budget_s, k, n):
+    """One process of the all-core oracle timing (spawned: one BLAS thread)."""
+    wl = kvc_synth.make_workload(name)
+    return oracle_sample(wl, budget_s, part=(k, n))
+
+
+def cpu_baseline(wl, budget_s=10.0, cores=None):
+    """The fp64 oracle on the host cores: all cores (a spawn-started process
+    per core over disjoint sequences, for the same budget of wall time), and
+    one core, over bounded samples of the workload's units."""
+    nbytes1, secs1, units1 = oracle_sample(wl, budget_s)
+    single = nbytes1 / secs1 / 1e9
+    cores = cores or min(os.cpu_count() or 1, max(1, wl.batch * wl.kv_heads))
+    line = {"value": single, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{units1} (sequence, kv head) units of one layer-step of {wl.name}, "
+                      f"{nbytes1 / 1e6:.1f} MB of attended K/V, {secs1:.1f} s single-threaded fp64"}
+    if cores > 1:
+        import multiprocessing as mpr
+        env = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in env:
+            os.environ[k] = "1"
+        try:
+            with mpr.get_context("spawn").Pool(cores) as pool:
+                t0 = time.perf_counter()
+                res = pool.starmap(_oracle_worker, [(wl.name, budget_s, k, cores) for k in range(cores)])
+                wall = time.perf_counter() - t0
+        finally:
+            for k, v in env.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        nbytes = sum(r[0] for r in res)
+        busy = max(r[1] for r in res)
+        units = sum(r[2] for r in res)
+        line.update(value=nbytes / busy / 1e9, cores=cores,
+                    sample=f"{units} (sequence, kv head) units of one layer-step of {wl.name} over {cores} "
+                           f"processes (disjoint units), {nbytes / 1e6:.1f} MB of attended K/V, "
+                           f"{busy:.1f} s of oracle time per process (wall {wall:.1f} s incl. start-up)",
+                    single_core_value=single)
+    return line
 
 
 # ---------------------------------------------------------------------------
@@ -427,6 +467,48 @@ def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+# ---------------------------------------------------------------------------
+# replicas (N > 1): one process per GPU, no collective on the data path; the
+# ranks only meet for the barriers around the timed region and the max of
+# their times
+# ---------------------------------------------------------------------------
+
+def replica_init(world, backend="nccl", device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=device)
+        else:
+            dist.init_process_group(backend)
+
+
+def replica_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_max(value, world, device="cuda"):
+    """Largest `value` over the ranks (the slowest replica sets the job time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_done(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def job_throughput(bytes_per_step, world, ms_per_step):
+    """Whole-job GB/s: every rank streams bytes_per_step per step (weak scaling)."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
 def run_reference(args):
@@ -461,9 +543,7 @@ def run_ours(args):
     kvc = _kvc()
     rank, world, local = _dist()
     torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    replica_init(world, "nccl", torch.device("cuda", local))
     wl = kvc_synth.make_workload(args.workload)
     layers = args.layers or DEFAULT_LAYERS[args.workload]
     st = DecodeState(wl, layers, source="device", num_splits=args.num_splits)
@@ -471,9 +551,7 @@ def run_ours(args):
     nb = step_bytes(wl)
 
     def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+        replica_barrier(world)
 
     # warm-up
     for i in range(args.warmup):
@@ -526,13 +604,9 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replica_max(total_ms, world)
     ms_per_step = total_ms / K
-    value = world * nb["step_algorithmic"] / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(nb["step_algorithmic"], world, ms_per_step)
     # the step's kernels (decode + combine, fused append) take the whole step:
     # per launch of the step, algorithmic bytes / device time per step
     dec_mean = ms_per_step
@@ -593,9 +667,7 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    replica_done(world)
     return line if rank == 0 else None
 
 
