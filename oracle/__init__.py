@@ -14,6 +14,9 @@ What it computes, in fp64 numpy, slowly and plainly:
                 cache layouts, plus step-by-step layout models (a ring with a
                 head pointer, a compacting StreamingLLM cache, a physical
                 sink+ring, a block pool with a block table and valid bits).
+* `blocks`    – the paged cache's block manager: free list, prefix sharing
+                with reference counts, copy-on-write, release ([share] §3.2,
+                §5.1, §6.1).
 * `attention` – one decode step: scores q.k / sqrt(D), max-subtracted softmax,
                 weighted sum of V.  Every sum is exactly rounded (math.fsum),
                 so a result never depends on the order in which the attended
@@ -33,13 +36,14 @@ Pages cited (by title and section):
            baked into K rows".
 
 Pin status: every function here is pinned by `tests/test_oracle_pins.py`
+(the block manager by `tests/test_oracle_blocks.py`)
 against values the pages print, closed forms, a library routine
 (torch scaled_dot_product_attention in fp64) or brute force on tiny inputs.
 The numeric attention outputs of the full workloads have no worked example
 on the pages; they are pinned through those checks of the definition.
 """
 
-from . import attention, layouts, rope, storage
+from . import attention, blocks, layouts, rope, storage
 from .attention import attend, decode_masked_history, decode_reference, decode_sequence
 from .layouts import (
     PagedKV,
@@ -55,7 +59,7 @@ from .rope import inv_freq, rotate
 from .storage import round_bf16, round_storage
 
 __all__ = [
-    "attention", "layouts", "rope", "storage",
+    "attention", "blocks", "layouts", "rope", "storage",
     "attend", "decode_reference", "decode_masked_history", "decode_sequence",
     "PagedKV", "RingKV", "SinkRingKV", "StreamingKV",
     "incache_position", "paged_attended", "window_attended", "window_slot",
