@@ -117,6 +117,7 @@ typedef struct kvc_desc {
 #define KVC_DEV_BAD_ENTRY 0x10u      /* kvc_block_table_write / kvc_valid_write entry out of range */
 #define KVC_DEV_INTERNAL 0x20u       /* an index computed inside a kernel failed its bounds check
                                         (access skipped); a library bug, please report */
+#define KVC_DEV_NO_FREE_BLOCK 0x40u  /* kvc_block_prepare: the free list ran out (that sequence skipped) */
 
 /* Bytes of the cache tensor described by `d` (0 if `d` is invalid). */
 KVC_API size_t kvc_cache_bytes(const kvc_desc* d);
@@ -199,6 +200,47 @@ KVC_API int kvc_block_table_write(const kvc_desc* d, int32_t* block_table, uint3
 KVC_API int kvc_valid_write(const kvc_desc* d, uint32_t* valid_bits, int32_t n,
                             const int32_t* slot, const int32_t* value,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Block manager of a paged cache ([share] 3.1-3.2 block table and prefix
+ * sharing, 5.1 block manager, 6.1 reclaim on sequence end).  State, all
+ * caller-owned device memory: the block table and valid bits as above,
+ * refcount int32 [num_blocks] (table references of each block), free_list
+ * int32 [num_blocks] used as a stack (entries 0 .. *free_count - 1, top last)
+ * and free_count (one int32).  Start: table -1, refcount 0, free_list any
+ * permutation of the blocks, *free_count = num_blocks, valid bits 0.
+ * Within one call sequences are served in ascending order, exactly as one
+ * after the other, so the results are deterministic. */
+
+/* Before appending each sequence's next token (pos[b]; < 0: none), once per
+ * token for all layers: a token at a block's first row whose logical block
+ * is unmapped gets a new block from the top of the free list; a block
+ * referenced by more than one sequence (count > 1) is copied first: a new
+ * block receives its rows 0 .. pos mod block_size - 1 of every layer, K and
+ * V, every kv head, the sequence's entry points at it, the shared block's
+ * count drops by one (copy-on-write, [share] 3.2).  New blocks get count 1
+ * and their valid bit (valid_bits may be NULL).  Errors (device bits): an
+ * unmapped block entered mid-block (KVC_DEV_UNMAPPED_APPEND), a position past
+ * the table (KVC_DEV_BAD_POSITION), an exhausted free list
+ * (KVC_DEV_NO_FREE_BLOCK); the sequence is skipped. */
+KVC_API int kvc_block_prepare(const kvc_desc* d, void* cache, const int32_t* pos, int32_t* block_table,
+                              uint32_t* valid_bits, int32_t* refcount, int32_t* free_list, int32_t* free_count,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Prefix sharing ([share] 3.2, 5.1 share_prefix): for each i < n, logical
+ * blocks 0 .. nblocks[i] - 1 of sequence dst_seq[i] point at those of
+ * src_seq[i]; each shared block's count rises by one.  The destination's
+ * entries must be unmapped, else KVC_DEV_BAD_ENTRY and the entry is skipped. */
+KVC_API int kvc_block_share(const kvc_desc* d, int32_t* block_table, int32_t* refcount, int32_t n,
+                            const int32_t* src_seq, const int32_t* dst_seq, const int32_t* nblocks,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Sequences end ([share] 6.1): for each listed sequence every mapped block's
+ * count drops by one and its entry is unmapped; blocks whose count reaches
+ * zero return to the free list in ascending block id and lose their valid
+ * bit.  A sequence listed twice is released twice (caller error). */
+KVC_API int kvc_block_release(const kvc_desc* d, int32_t* block_table, uint32_t* valid_bits, int32_t* refcount,
+                              int32_t* free_list, int32_t* free_count, int32_t n, const int32_t* seq,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the library's own fixed scratch array used by
  * kvc_decode_attention_noalloc: 8 MiB of device memory, reserved on every GPU

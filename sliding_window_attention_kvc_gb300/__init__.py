@@ -29,11 +29,13 @@ KVC_ERR_TOO_LARGE = -8
 KVC_NOALLOC_SCRATCH_BYTES = 8 << 20
 KVC_DEV_BAD_BLOCK, KVC_DEV_UNMAPPED_APPEND, KVC_DEV_BAD_POSITION = 0x1, 0x2, 0x4
 KVC_DEV_TIMEOUT, KVC_DEV_BAD_ENTRY = 0x8, 0x10
+KVC_DEV_INTERNAL, KVC_DEV_NO_FREE_BLOCK = 0x20, 0x40
 
 ABI_FUNCTIONS = (
     "kvc_cache_bytes", "kvc_workspace_bytes", "kvc_workspace_init", "kvc_append",
     "kvc_decode_attention", "kvc_block_table_write", "kvc_valid_write", "kvc_get_error",
     "kvc_strerror", "kvc_decode_attention_noalloc", "kvc_decode_step",
+    "kvc_block_prepare", "kvc_block_share", "kvc_block_release",
 )
 
 
@@ -80,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.kvc_get_error.argtypes = [vp, vp]
         L.kvc_decode_attention_noalloc.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.kvc_decode_step.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.kvc_block_prepare.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.kvc_block_share.argtypes = [dp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.kvc_block_release.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
         L.kvc_strerror.argtypes = [ctypes.c_int]
         L.kvc_strerror.restype = ctypes.c_char_p
         for name in ABI_FUNCTIONS:
@@ -278,6 +283,50 @@ def valid_write(d: KvcDesc, valid_bits: torch.Tensor, slot: torch.Tensor, value:
     _check(lib().kvc_valid_write(ctypes.byref(d), _ptr(valid_bits), int(n), _ptr(slot), _ptr(value),
                                  _ptr(workspace), workspace.numel(), _stream(stream)),
            "kvc_valid_write")
+
+
+class BlockState:
+    """Device state of the paged cache's block manager (include/kvc.h): the
+    block table and valid bits, a reference count per block, and the free
+    list (a stack of block ids, `free_count` entries)."""
+
+    def __init__(self, d: KvcDesc, device="cuda", free_order=None):
+        self.table = torch.full((d.batch, d.max_blocks_per_seq), -1, dtype=torch.int32, device=device)
+        self.valid_bits = torch.zeros((d.num_blocks + 31) // 32, dtype=torch.int32, device=device)
+        self.refcount = torch.zeros(d.num_blocks, dtype=torch.int32, device=device)
+        order = list(range(d.num_blocks)) if free_order is None else list(free_order)
+        self.free_list = torch.tensor(order, dtype=torch.int32, device=device)
+        self.free_count = torch.tensor([len(order)], dtype=torch.int32, device=device)
+
+
+def block_prepare(d: KvcDesc, cache: torch.Tensor, pos: torch.Tensor, state: BlockState,
+                  workspace: torch.Tensor, stream=None):
+    _need(pos, "pos", torch.int32, d.batch)
+    _need(workspace, "workspace", torch.uint8)
+    _check(lib().kvc_block_prepare(ctypes.byref(d), _ptr(cache), _ptr(pos), _ptr(state.table),
+                                   _ptr(state.valid_bits), _ptr(state.refcount), _ptr(state.free_list),
+                                   _ptr(state.free_count), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvc_block_prepare")
+
+
+def block_share(d: KvcDesc, state: BlockState, src_seq: torch.Tensor, dst_seq: torch.Tensor,
+                nblocks: torch.Tensor, workspace: torch.Tensor, stream=None):
+    n = src_seq.numel()
+    for t, name in ((src_seq, "src_seq"), (dst_seq, "dst_seq"), (nblocks, "nblocks")):
+        _need(t, name, torch.int32, n)
+    _check(lib().kvc_block_share(ctypes.byref(d), _ptr(state.table), _ptr(state.refcount), int(n), _ptr(src_seq),
+                                 _ptr(dst_seq), _ptr(nblocks), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)),
+           "kvc_block_share")
+
+
+def block_release(d: KvcDesc, state: BlockState, seq: torch.Tensor, workspace: torch.Tensor, stream=None):
+    n = seq.numel()
+    _need(seq, "seq", torch.int32, n)
+    _check(lib().kvc_block_release(ctypes.byref(d), _ptr(state.table), _ptr(state.valid_bits),
+                                   _ptr(state.refcount), _ptr(state.free_list), _ptr(state.free_count), int(n),
+                                   _ptr(seq), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvc_block_release")
 
 
 def get_error(workspace: torch.Tensor, stream=None) -> int:

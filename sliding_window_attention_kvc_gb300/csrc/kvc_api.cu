@@ -99,7 +99,7 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     off = align_up(off + (size_t)w.items * d->q_heads * 8, 256);
     w.part_o = off;
     off = align_up(off + (size_t)w.items * d->q_heads * d->head_dim * 4, 256);
-    w.plan_seq = w.plan_acc = w.plan_items = w.plan_info = w.plan_total = w.plan_cta = off;
+    w.plan_seq = w.plan_acc = w.plan_items = w.plan_info = w.plan_total = w.plan_cta = w.blocks = off;
     if (d->layout == KVC_LAYOUT_PAGED) {
         w.plan_seq = off;
         off = align_up(off + (size_t)d->batch * 8, 256);
@@ -111,6 +111,9 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
         off = align_up(off + (size_t)w.items * 16, 256);
         w.plan_cta = off;
         off = align_up(off + (size_t)w.shares * 8, 256);
+        w.blocks = off;
+        off = align_up(off + align_up((size_t)d->batch * 5 * 4, 16) + (size_t)d->batch * 16 + 16 +
+                           (size_t)d->num_blocks * 4, 256);
         w.plan_total = off;
         off += 256;
     }
@@ -395,6 +398,38 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
 }
 
 
+namespace {
+// Block manager parameters over the workspace's block region.
+int block_params(const kvc_desc* d, const Geo& g, void* workspace, size_t workspace_bytes, kvc::BlockParams* p) {
+    if (d->layout != KVC_LAYOUT_PAGED) return KVC_ERR_DESC;
+    if (!workspace) return KVC_ERR_NULL;
+    if (!aligned16(workspace)) return KVC_ERR_ALIGN;
+    const WorkspaceLayout w = ws_layout(d, g);
+    if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    char* r = ws + w.blocks;
+    const size_t B = (size_t)d->batch;
+    *p = kvc::BlockParams{};
+    p->err = reinterpret_cast<uint32_t*>(ws + w.err);
+    p->tgt = reinterpret_cast<int32_t*>(r);
+    p->rcnt = p->tgt + B;
+    p->need = p->rcnt + B;
+    p->aidx = p->need + B;
+    p->prev = p->aidx + B;
+    p->copies = reinterpret_cast<int4*>(r + align_up(5 * 4 * B, 16));
+    p->ncopies = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(p->copies) + 16 * B);
+    p->flags = p->ncopies + 4;
+    p->B = d->batch;
+    p->bs = d->block_size;
+    p->num_blocks = d->num_blocks;
+    p->maxb = d->max_blocks_per_seq;
+    p->layers = d->layers;
+    p->Hkv = d->kv_heads;
+    p->D = d->head_dim;
+    return KVC_OK;
+}
+}  // namespace
+
 extern "C" {
 
 KVC_API size_t kvc_cache_bytes(const kvc_desc* d) {
@@ -539,6 +574,65 @@ KVC_API int kvc_valid_write(const kvc_desc* d, uint32_t* valid_bits, int32_t n, 
     return KVC_OK;
 }
 
+KVC_API int kvc_block_prepare(const kvc_desc* d, void* cache, const int32_t* pos, int32_t* block_table,
+                              uint32_t* valid_bits, int32_t* refcount, int32_t* free_list, int32_t* free_count,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (!cache || !pos || !block_table || !refcount || !free_list || !free_count) return KVC_ERR_NULL;
+    if (!aligned16(cache)) return KVC_ERR_ALIGN;
+    kvc::BlockParams p;
+    if ((rc = block_params(d, g, workspace, workspace_bytes, &p))) return rc;
+    p.cache = cache;
+    p.pos = pos;
+    p.table = block_table;
+    p.valid = valid_bits;
+    p.refcount = refcount;
+    p.free_list = free_list;
+    p.free_count = free_count;
+    return launch_block_prepare(g.elt, p, (cudaStream_t)stream) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+KVC_API int kvc_block_share(const kvc_desc* d, int32_t* block_table, int32_t* refcount, int32_t n,
+                            const int32_t* src_seq, const int32_t* dst_seq, const int32_t* nblocks, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (n < 0) return KVC_ERR_ARG;
+    if (n == 0) return KVC_OK;
+    if (!block_table || !refcount || !src_seq || !dst_seq || !nblocks) return KVC_ERR_NULL;
+    kvc::BlockParams p;
+    if ((rc = block_params(d, g, workspace, workspace_bytes, &p))) return rc;
+    p.table = block_table;
+    p.refcount = refcount;
+    p.src_seq = src_seq;
+    p.dst_seq = dst_seq;
+    p.nblocks = nblocks;
+    return launch_block_share(p, n, (cudaStream_t)stream) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+KVC_API int kvc_block_release(const kvc_desc* d, int32_t* block_table, uint32_t* valid_bits, int32_t* refcount,
+                              int32_t* free_list, int32_t* free_count, int32_t n, const int32_t* seq,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (n < 0) return KVC_ERR_ARG;
+    if (n == 0) return KVC_OK;
+    if (!block_table || !refcount || !free_list || !free_count || !seq) return KVC_ERR_NULL;
+    kvc::BlockParams p;
+    if ((rc = block_params(d, g, workspace, workspace_bytes, &p))) return rc;
+    p.table = block_table;
+    p.valid = valid_bits;
+    p.refcount = refcount;
+    p.free_list = free_list;
+    p.free_count = free_count;
+    p.src_seq = seq;
+    return launch_block_release(p, n, (cudaStream_t)stream) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
 KVC_API int kvc_get_error(void* workspace, void* stream) {
     if (!workspace) return KVC_ERR_NULL;
     cudaStream_t s = (cudaStream_t)stream;
@@ -567,6 +661,7 @@ KVC_API const char* kvc_strerror(int code) {
         case (int)KVC_DEV_TIMEOUT: return "device: a bounded wait timed out";
         case (int)KVC_DEV_BAD_ENTRY: return "device: table/valid update entry out of range";
         case (int)KVC_DEV_INTERNAL: return "device: an internal index check failed (access skipped)";
+        case (int)KVC_DEV_NO_FREE_BLOCK: return "device: no free block left for a new or copied block";
         default: return "unknown code";
     }
 }

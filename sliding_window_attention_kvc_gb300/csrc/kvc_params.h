@@ -38,6 +38,8 @@ struct WorkspaceLayout {
     size_t plan_info;    // PAGED: int4  [items]: (t of the sequence, its first slot, its slot count, first physical block)
     size_t plan_total;   // PAGED: int32 items used, int32 shares G, int64 attended rows R
     size_t plan_cta;     // PAGED: int2 [ctas]: first item, item count
+    size_t blocks;       // PAGED: block manager scratch: int32 [6 * batch], int4 [batch], int32 count,
+                         // int32 [num_blocks] reclaim flags
     size_t total;
     int items;           // partial slots per (q head): batch * nsplit, or shares + batch
     int nsplit;          // RING / SINK_RING fp32: splits per (sequence, kv head)
@@ -128,6 +130,32 @@ struct TableParams {
     int n, B, maxb, num_blocks;
 };
 
+// Block manager of a paged cache (kvc_block_prepare / _share / _release).
+struct BlockParams {
+    void* cache;
+    const int32_t* pos;        // [B]
+    int32_t* table;            // [B, maxb]
+    uint32_t* valid;           // may be null
+    int32_t* refcount;         // [num_blocks]
+    int32_t* free_list;        // [num_blocks]: stack, entries 0 .. *free_count - 1
+    int32_t* free_count;
+    uint32_t* err;
+    // workspace
+    int32_t* tgt;              // [B]: block of the next token, -2 new, -1 none
+    int32_t* rcnt;             // [B]: count of that block before the call
+    int32_t* need;             // [B]: takes a block
+    int32_t* aidx;             // [B]: allocation index
+    int32_t* prev;             // [B]: last earlier sequence writing the same block, or -1
+    int4* copies;              // [B]: (source, destination, rows, sequence)
+    int32_t* ncopies;
+    int32_t* flags;            // [num_blocks]: reclaimed by a release (zero between calls)
+    // share / release entries
+    const int32_t* src_seq;    // share: source; release: the sequences
+    const int32_t* dst_seq;
+    const int32_t* nblocks;
+    int B, bs, num_blocks, maxb, layers, Hkv, D;
+};
+
 // bf16 caches: tensor maps over the cache for copies of a run of 16 r rows
 // (r = 1..kRunMaps), K and V of every column at once.  With tma_whole the map
 // is 5-D {64 columns, row, K|V, layer, column block} and one copy lands as
@@ -147,5 +175,8 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
 cudaError_t launch_valid_write(const TableParams& p, cudaStream_t stream);
+cudaError_t launch_block_prepare(int elt, const BlockParams& p, cudaStream_t stream);
+cudaError_t launch_block_share(const BlockParams& p, int n, cudaStream_t stream);
+cudaError_t launch_block_release(const BlockParams& p, int n, cudaStream_t stream);
 
 }  // namespace kvc

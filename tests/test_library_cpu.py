@@ -108,6 +108,18 @@ def test_argument_errors_return_codes_without_launching(kvc):
     assert L.kvc_block_table_write(ctypes.byref(dpg), A, None, 0, None, None, None, None, 0, None) == kvc.KVC_OK
     assert L.kvc_get_error(None, None) == kvc.KVC_ERR_NULL
     assert kvc.strerror(kvc.KVC_ERR_ALIGN).startswith("pointer")
+    # block manager: paged descriptors only, pointers checked, nothing launched
+    dg = ctypes.byref(dpg)
+    assert L.kvc_block_prepare(dp, A, A, A, None, A, A, A, A, ws_n, None) == kvc.KVC_ERR_DESC
+    assert L.kvc_block_prepare(dg, A, A, None, None, A, A, A, A, nws, None) == kvc.KVC_ERR_NULL
+    assert L.kvc_block_prepare(dg, A + 8, A, A, None, A, A, A, A, nws, None) == kvc.KVC_ERR_ALIGN
+    assert L.kvc_block_prepare(dg, A, A, A, None, A, A, A, A, nws - 1, None) == kvc.KVC_ERR_WORKSPACE
+    assert L.kvc_block_share(dg, A, A, -1, A, A, A, A, nws, None) == kvc.KVC_ERR_ARG
+    assert L.kvc_block_share(dg, A, A, 0, None, None, None, None, 0, None) == kvc.KVC_OK
+    assert L.kvc_block_share(dg, A, A, 1, A, None, A, A, nws, None) == kvc.KVC_ERR_NULL
+    assert L.kvc_block_release(dg, A, None, A, A, A, -1, A, A, nws, None) == kvc.KVC_ERR_ARG
+    assert L.kvc_block_release(dg, A, None, A, A, None, 1, A, A, nws, None) == kvc.KVC_ERR_NULL
+    assert "free" in kvc.strerror(kvc.KVC_DEV_NO_FREE_BLOCK)
 
 
 def test_pack_valid_bits(kvc):
