@@ -709,6 +709,55 @@ def _e2e_step(st, fc, layer, hq, hk, hv, hp, hout):
     torch.cuda.current_stream().synchronize()
 
 
+def measure_block_prepare(args):
+    """One kvc_block_prepare call on a shared-prefix batch shaped like the
+    paged workload: 64 sequences in groups of 8 share a 2050-token prefix
+    (129 blocks of 16, the last holding 2 rows); every sequence then writes
+    token 2050, so in each group 7 copy the shared tail block and the last
+    writes in place.  The state is restored before each timed call; device
+    time per call from CUDA events, median over the repeats."""
+    kvc = _kvc()
+    B, G, prefix, bs, Hq, Hkv, D = 64, 8, 2050, 16, 32, 8, 128
+    layers = args.layers or 1
+    nb_seq = (prefix + bs - 1) // bs
+    num_blocks = (B // G) * nb_seq + B + 16
+    d = kvc.make_desc("paged", "baked", "bf16", layers, B, Hq, Hkv, D, block_size=bs, num_blocks=num_blocks,
+                      max_blocks_per_seq=nb_seq + 4)
+    cache = kvc.alloc_cache(d, fill=0.0)
+    ws = kvc.alloc_workspace(d)
+    st = kvc.BlockState(d)
+    leaders = list(range(0, B, G))
+    for t in range(0, prefix, bs):                 # leaders take their prefix blocks
+        pos = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+        pos[leaders] = t
+        kvc.block_prepare(d, cache, pos, st, ws)
+    src = torch.tensor([l for l in leaders for m in range(1, G)], dtype=torch.int32, device="cuda")
+    dst = torch.tensor([l + m for l in leaders for m in range(1, G)], dtype=torch.int32, device="cuda")
+    kvc.block_share(d, st, src, dst, torch.full_like(src, nb_seq), ws)
+    torch.cuda.synchronize()
+    snap = [x.clone() for x in (st.table, st.valid_bits, st.refcount, st.free_list, st.free_count)]
+    pos = torch.full((B,), prefix, dtype=torch.int32, device="cuda")
+    times = []
+    for i in range(args.warmup + args.steps):
+        for x, y in zip((st.table, st.valid_bits, st.refcount, st.free_list, st.free_count), snap):
+            x.copy_(y)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kvc.block_prepare(d, cache, pos, st, ws)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) * 1e3)
+    err = kvc.get_error(ws)
+    copies = int((st.table[:, nb_seq - 1] != snap[0][:, nb_seq - 1]).sum().item())
+    return {"measure": "kvc_block_prepare", "value": statistics.median(times), "unit": "us per call",
+            "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+            "config": {"sequences": B, "group": G, "prefix_tokens": prefix, "block_size": bs, "layers": layers,
+                       "kv_heads": Hkv, "head_dim": D, "copies": copies, "copied_bytes":
+                       copies * layers * 2 * Hkv * (prefix % bs) * D * 2},
+            "device_errors": err}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -722,12 +771,17 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--measure", choices=["block_prepare"], default=None,
+                    help="time a block-manager call instead of the decode step (separate JSON line)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode launch from an ncu capture of the current kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.measure == "block_prepare":
+        line = measure_block_prepare(args)
+    else:
+        line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line))
 
