@@ -758,6 +758,81 @@ def measure_block_prepare(args):
             "device_errors": err}
 
 
+def measure_pagein(args):
+    """Page-in overlapped with decode on the long-context pool's shape (one
+    sequence, 1024 slots of 64 tokens, 16 q / 4 kv heads, D 256): each step
+    brings `k` new blocks from pinned host memory into slots freed by the LRU
+    pager while the step's decode runs over the resident blocks.  Reports the
+    decode alone, the copies alone (copy stream), and the overlapped step,
+    each the median of device times from CUDA events."""
+    kvc = _kvc()
+    Hq, Hkv, D, bs, slots, nlog, k = 16, 4, 256, 64, 1024, 2048, 64
+    layers = args.layers or 1
+    d = kvc.make_desc("paged", "baked", "bf16", layers, 1, Hq, Hkv, D, block_size=bs, num_blocks=slots,
+                      max_blocks_per_seq=nlog)
+    g = torch.Generator().manual_seed(9)
+    host = torch.randn((nlog, layers, 2, Hkv, bs, D), generator=g).to(torch.bfloat16).pin_memory()
+    cache = kvc.alloc_cache(d, fill=0.0)
+    ws = kvc.alloc_workspace(d)
+    table = torch.full((1, nlog), -1, dtype=torch.int32, device="cuda")
+    valid = torch.zeros((slots + 31) // 32, dtype=torch.int32, device="cuda")
+    pager = kvc.Pager(slots)
+    cs = torch.cuda.Stream()
+    t = nlog * bs - 1
+    pos = torch.tensor([t], dtype=torch.int32, device="cuda")
+    q = torch.randn((1, Hq, D), device="cuda").to(torch.bfloat16)
+    window = list(range(nlog - 64, nlog))
+    rng = np.random.default_rng(9)
+    resident = list(rng.choice(nlog - 64, size=slots - 64, replace=False))
+    ins, outs = pager.plan(window + resident, [1] * 64 + [0] * (slots - 64))
+    pager.issue(d, cache, host, ins, cs)
+    pager.commit(d, 0, ins, table, valid)
+    torch.cuda.synchronize()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    dec, cop, both = [], [], []
+    for i in range(args.warmup + args.steps):
+        keep = [b for b in resident if rng.random() > k / len(resident)][: len(resident) - k]
+        new = [b for b in rng.permutation(nlog - 64).tolist() if b not in keep][:len(resident) - len(keep)]
+        resident = keep + new
+        ins, outs = pager.plan(window + resident, [1] * 64 + [0] * len(resident))
+        pager.evict(d, 0, outs, table, valid)
+        # decode alone
+        a0, a1 = ev(), ev()
+        a0.record()
+        kvc.decode_attention(d, cache, 0, q, pos, ws, block_table=table, valid_bits=valid)
+        a1.record()
+        # copies alone, then overlapped with a decode
+        c0, c1 = ev(), ev()
+        torch.cuda.synchronize()
+        c0.record(cs)
+        pager.issue(d, cache, host, ins, cs)
+        c1.record(cs)
+        torch.cuda.synchronize()
+        b0, b1 = ev(), ev()
+        b0.record()
+        pager.issue(d, cache, host, ins, cs)
+        kvc.decode_attention(d, cache, 0, q, pos, ws, block_table=table, valid_bits=valid)
+        pager.commit(d, 0, ins, table, valid)
+        b1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            dec.append(a0.elapsed_time(a1))
+            cop.append(c0.elapsed_time(c1))
+            both.append(b0.elapsed_time(b1))
+    nbytes = len(ins) * layers * 2 * Hkv * bs * D * 2
+    med = statistics.median
+    return {"measure": "page-in overlapped with decode", "unit": "ms",
+            "decode_ms": med(dec), "copy_ms": med(cop), "overlapped_step_ms": med(both),
+            "copy_GBps": nbytes / (med(cop) * 1e-3) / 1e9, "blocks_per_step": len(ins), "bytes_per_step": nbytes,
+            "steps": args.steps, "warmup": args.warmup,
+            "config": {"slots": slots, "logical_blocks": nlog, "block_size": bs, "q_heads": Hq, "kv_heads": Hkv,
+                       "head_dim": D, "layers": layers, "pinned_window_blocks": 64},
+            "device_errors": kvc.get_error(ws)}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -771,7 +846,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--measure", choices=["block_prepare"], default=None,
+    ap.add_argument("--measure", choices=["block_prepare", "pagein"], default=None,
                     help="time a block-manager call instead of the decode step (separate JSON line)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode launch from an ncu capture of the current kernel")
@@ -780,6 +855,8 @@ def main(argv=None):
         args.warmup = 3
     if args.measure == "block_prepare":
         line = measure_block_prepare(args)
+    elif args.measure == "pagein":
+        line = measure_pagein(args)
     else:
         line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:

@@ -242,6 +242,51 @@ KVC_API int kvc_block_release(const kvc_desc* d, int32_t* block_table, uint32_t*
                               int32_t* free_list, int32_t* free_count, int32_t n, const int32_t* seq,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Paging of a fixed pool of block slots between host memory and the device
+ * ([pool] "KV cache paging": a fixed pool of resident slots; blocks move on
+ * demand; the copy engine moves them while attention runs; LRU residency;
+ * blocks inside a sliding window stay resident).  A paged cache whose
+ * num_blocks slots hold logical blocks of sequence `seq`; the block table maps
+ * resident logical blocks to their slot, absent ones to -1 (valid bit off).
+ * The host copy of the K/V is pinned memory laid out
+ * [logical block][layer][K|V][kv head][row][head_dim] in the cache dtype. */
+typedef struct kvc_pager kvc_pager;
+
+/* Host object tracking num_slots slots; NULL if num_slots < 1. */
+KVC_API kvc_pager* kvc_pager_create(int32_t num_slots);
+KVC_API void kvc_pager_destroy(kvc_pager* pager);
+
+/* Host only.  The blocks one step needs (need[0 .. n-1], logical block ids;
+ * pinned[i] != 0 keeps block need[i] resident in later steps until a later
+ * call lists it with pinned 0; pinned may be NULL).  Missing blocks take, in
+ * list order, the lowest free slot, else the least recently used slot whose
+ * block is neither needed now nor pinned (ties: lowest slot).  Outputs (host
+ * arrays of n entries): the page-ins (in_block, in_slot; *n_in) and the
+ * victims (out_block, out_slot; *n_out).  KVC_ERR_ARG, nothing changed, if the
+ * needed and pinned blocks do not fit. */
+KVC_API int kvc_pager_plan(kvc_pager* pager, int32_t n, const int32_t* need, const uint8_t* pinned,
+                           int32_t* n_in, int32_t* in_block, int32_t* in_slot,
+                           int32_t* n_out, int32_t* out_block, int32_t* out_slot);
+
+/* Compute stream: the victims' table entries (sequence seq) become -1 and
+ * their slots' valid bits clear.  Host arrays; asynchronous. */
+KVC_API int kvc_pager_evict(const kvc_desc* d, int32_t seq, int32_t n, const int32_t* out_block,
+                            const int32_t* out_slot, int32_t* block_table, uint32_t* valid_bits, void* stream);
+
+/* Copy stream, after the compute stream's work enqueued so far: one 2-D copy
+ * per block (every layer, K and V) from host_kv into its slot, then an event
+ * kept by the pager.  Work enqueued on the compute stream after this call
+ * overlaps the copies. */
+KVC_API int kvc_pagein_issue(kvc_pager* pager, const kvc_desc* d, void* cache, const void* host_kv, int32_t n,
+                             const int32_t* in_block, const int32_t* in_slot, void* copy_stream,
+                             void* compute_stream);
+
+/* Compute stream waits for the last issue's copies, then the blocks' table
+ * entries point at their slots and the slots' valid bits are set. */
+KVC_API int kvc_pagein_commit(kvc_pager* pager, const kvc_desc* d, int32_t seq, int32_t n, const int32_t* in_block,
+                              const int32_t* in_slot, int32_t* block_table, uint32_t* valid_bits,
+                              void* compute_stream);
+
 /* Size of the library's own fixed scratch array used by
  * kvc_decode_attention_noalloc: 8 MiB of device memory, reserved on every GPU
  * that loads the library, from the first use until the process exits. */

@@ -36,6 +36,8 @@ ABI_FUNCTIONS = (
     "kvc_decode_attention", "kvc_block_table_write", "kvc_valid_write", "kvc_get_error",
     "kvc_strerror", "kvc_decode_attention_noalloc", "kvc_decode_step",
     "kvc_block_prepare", "kvc_block_share", "kvc_block_release",
+    "kvc_pager_create", "kvc_pager_destroy", "kvc_pager_plan", "kvc_pager_evict", "kvc_pagein_issue",
+    "kvc_pagein_commit",
 )
 
 
@@ -85,10 +87,19 @@ def lib() -> ctypes.CDLL:
         L.kvc_block_prepare.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.kvc_block_share.argtypes = [dp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.kvc_block_release.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
+        L.kvc_pager_create.argtypes = [i32]
+        L.kvc_pager_create.restype = vp
+        L.kvc_pager_destroy.argtypes = [vp]
+        L.kvc_pager_destroy.restype = None
+        L.kvc_pager_plan.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.kvc_pager_evict.argtypes = [dp, i32, i32, vp, vp, vp, vp, vp]
+        L.kvc_pagein_issue.argtypes = [vp, dp, vp, vp, i32, vp, vp, vp, vp]
+        L.kvc_pagein_commit.argtypes = [vp, dp, i32, i32, vp, vp, vp, vp, vp]
         L.kvc_strerror.argtypes = [ctypes.c_int]
         L.kvc_strerror.restype = ctypes.c_char_p
         for name in ABI_FUNCTIONS:
-            if name not in ("kvc_cache_bytes", "kvc_workspace_bytes", "kvc_strerror"):
+            if name not in ("kvc_cache_bytes", "kvc_workspace_bytes", "kvc_strerror", "kvc_pager_create",
+                            "kvc_pager_destroy"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -327,6 +338,64 @@ def block_release(d: KvcDesc, state: BlockState, seq: torch.Tensor, workspace: t
                                    _ptr(state.refcount), _ptr(state.free_list), _ptr(state.free_count), int(n),
                                    _ptr(seq), _ptr(workspace), workspace.numel(), _stream(stream)),
            "kvc_block_release")
+
+
+class Pager:
+    """kvc_pager: LRU residency of a fixed pool of slots (host object), with
+    page-in of blocks from pinned host memory on a copy stream."""
+
+    def __init__(self, num_slots: int):
+        self.num_slots = num_slots
+        self._p = lib().kvc_pager_create(int(num_slots))
+        if not self._p:
+            raise KvcError(KVC_ERR_ARG, "kvc_pager_create")
+
+    def close(self):
+        if self._p:
+            lib().kvc_pager_destroy(self._p)
+            self._p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def plan(self, need, pinned=None):
+        """need: logical block ids of this step -> (page-ins [(block, slot)], victims [(block, slot)])."""
+        n = len(need)
+        arr = (ctypes.c_int32 * max(1, n))
+        nd = arr(*need)
+        pn = (ctypes.c_uint8 * max(1, n))(*[1 if x else 0 for x in pinned]) if pinned is not None else None
+        ib, isl, ob, osl = arr(), arr(), arr(), arr()
+        ni, no = ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(lib().kvc_pager_plan(self._p, n, nd, pn, ctypes.byref(ni), ib, isl, ctypes.byref(no), ob, osl),
+               "kvc_pager_plan")
+        return ([(ib[i], isl[i]) for i in range(ni.value)], [(ob[i], osl[i]) for i in range(no.value)])
+
+    def evict(self, d: KvcDesc, seq: int, victims, block_table, valid_bits, stream=None):
+        n = len(victims)
+        arr = ctypes.c_int32 * max(1, n)
+        _check(lib().kvc_pager_evict(ctypes.byref(d), int(seq), n, arr(*[b for b, _ in victims]),
+                                     arr(*[s for _, s in victims]), _ptr(block_table),
+                                     _ptr(valid_bits) if valid_bits is not None else None, _stream(stream)),
+               "kvc_pager_evict")
+
+    def issue(self, d: KvcDesc, cache, host_kv, pageins, copy_stream, compute_stream=None):
+        n = len(pageins)
+        arr = ctypes.c_int32 * max(1, n)
+        _check(lib().kvc_pagein_issue(self._p, ctypes.byref(d), _ptr(cache), ctypes.c_void_p(host_kv.data_ptr()), n,
+                                      arr(*[b for b, _ in pageins]), arr(*[s for _, s in pageins]),
+                                      _stream(copy_stream), _stream(compute_stream)),
+               "kvc_pagein_issue")
+
+    def commit(self, d: KvcDesc, seq: int, pageins, block_table, valid_bits, stream=None):
+        n = len(pageins)
+        arr = ctypes.c_int32 * max(1, n)
+        _check(lib().kvc_pagein_commit(self._p, ctypes.byref(d), int(seq), n, arr(*[b for b, _ in pageins]),
+                                       arr(*[s for _, s in pageins]), _ptr(block_table),
+                                       _ptr(valid_bits) if valid_bits is not None else None, _stream(stream)),
+               "kvc_pagein_commit")
 
 
 def get_error(workspace: torch.Tensor, stream=None) -> int:
