@@ -168,11 +168,12 @@ __device__ __forceinline__ void window_partition(const DecodeParams& p, int b, l
 // groups (four loads in flight each) and reduce through shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kCombineThreads = 256;
-constexpr int kCombineCols = 16;
 
-template <int D, int GH, bool PAGED>
+// COLS columns per CTA: 16 when (sequence, kv head, group) units are few (more
+// CTAs per unit, shorter chains), 64 when they already fill a wave of CTAs.
+template <int D, int GH, bool PAGED, int COLS>
 __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const __grid_constant__ DecodeParams p) {
-    constexpr int C4 = kCombineCols / 4;           // float4 columns per chunk
+    constexpr int C4 = COLS / 4;                   // float4 columns per chunk
     constexpr int PAIRS = GH * C4;                 // (head, float4) outputs of the chunk
     constexpr int PG = kCombineThreads / PAIRS;    // partial groups
     constexpr int kMaxStaged = 1024;
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
     pdl_launch_dependents();
     const int b = blockIdx.x;
     const int kvh = blockIdx.y / p.nsub, z = blockIdx.y % p.nsub;
-    const int col0 = blockIdx.z * kCombineCols;
+    const int col0 = blockIdx.z * COLS;
     const int tid = threadIdx.x;
     const int qh0 = kvh * p.G + z * GH;
 
@@ -220,6 +221,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
         if (tid == 0) index_fault(p.err, 20, first);
         return;
     }
+    // this thread's first four partial outputs, loaded now: they do not depend
+    // on M, so their round trip overlaps the (m, l) staging below
+    const int pair = tid % PAIRS, grp = tid / PAIRS;
+    const int h = pair / C4, c4 = pair % C4;
+    const int d0 = col0 + c4 * 4;
+    float4 v0[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int k = grp + u * PG;
+        v0[u] = k < nparts ? __ldcg(reinterpret_cast<const float4*>(
+                                 p.part_o + ((long long)(first + k) * p.Hq + qh0 + h) * D + d0))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const int npl = nparts * GH;
     const bool staged = npl <= kMaxStaged;
     if (staged)
@@ -249,9 +263,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
         }
     }
     __syncthreads();
-    const int pair = tid % PAIRS, grp = tid / PAIRS;
-    const int h = pair / C4, c4 = pair % C4;
-    const int d0 = col0 + c4 * 4;
     const float M = s_M[h];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     // four independent partial loads in flight per thread
@@ -266,8 +277,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
             if (k < nparts) {
                 const float2 ml = ml_of(k, h);
                 e[u] = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
-                v[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((long long)(first + k) * p.Hq + qh0 + h) * D +
-                                                              d0));
+                v[u] = k0 == grp ? v0[u]
+                                 : __ldcg(reinterpret_cast<const float4*>(
+                                       p.part_o + ((long long)(first + k) * p.Hq + qh0 + h) * D + d0));
             }
         }
 #pragma unroll
@@ -1150,7 +1162,10 @@ template <int D, int GH, bool PAGED, bool READ>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps, dim3 grid, cudaStream_t stream) {
     using SM = MmaSmem<D, GH, READ>;
     auto kern = decode_mma_kernel<D, GH, PAGED, READ>;
-    auto comb = combine_streamk_kernel<D, GH, PAGED>;
+    // few (sequence, kv head, group) units: narrow column chunks, more CTAs each
+    const long long units = (long long)p.B * p.Hkv * p.nsub;
+    const bool narrow = units * (D / 16) <= 1216;
+    auto comb = narrow ? combine_streamk_kernel<D, GH, PAGED, 16> : combine_streamk_kernel<D, GH, PAGED, 64>;
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1176,7 +1191,7 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps,
     e = cudaLaunchKernelEx(&cfg, kern, p, maps);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t ccfg = {};
-    ccfg.gridDim = dim3(p.B, p.Hkv * p.nsub, D / kCombineCols);
+    ccfg.gridDim = dim3(p.B, p.Hkv * p.nsub, D / (narrow ? 16 : 64));
     ccfg.blockDim = dim3(kCombineThreads);
     ccfg.dynamicSmemBytes = 0;
     ccfg.stream = stream;
