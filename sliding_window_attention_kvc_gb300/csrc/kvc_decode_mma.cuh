@@ -141,7 +141,7 @@ __device__ __forceinline__ void window_partition(const DecodeParams& p, int b, l
         if (bb < p.B) {
             const int tb = p.pos[bb];
             const int nl = tb < 0 ? 0 : (tb + 1 < C ? tb + 1 : C);
-            st = nl > 0 ? (nl + 15) / 16 : 1;
+            st = (nl > 0 ? (nl + 15) / 16 : 1) + kSeqUnits;
         }
         long long pre = bb < b ? st : 0;
         long long me = bb == b ? st : 0;
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                 const int nl = tb < 0 ? 0 : (tb + 1 < C ? tb + 1 : C);
                 *t_out = tb;
                 *nl_out = nl;
-                return nl > 0 ? (nl + 15) / 16 : 1;
+                return (nl > 0 ? (nl + 15) / 16 : 1) + kSeqUnits;
             };
             long long total = 0;
             for (int base = 0; base < p.B; base += 32) {
@@ -569,8 +569,11 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                     hdr.first_slot = fx + b;
                     hdr.nparts = lx - fx + 1;
                     if (!(ok = begin_segment(hdr))) break;
-                    const int r0 = (int)((lo > Ob ? lo : Ob) - Ob) * 16;
-                    const int r1 = min((int)((hi < Ob + Sb ? hi : Ob + Sb) - Ob) * 16, nl_b);
+                    // units of the sequence: kSeqUnits charged for its segment
+                    // start, then one per 16 rows
+                    const int u0 = (int)((lo > Ob ? lo : Ob) - Ob), u1 = (int)((hi < Ob + Sb ? hi : Ob + Sb) - Ob);
+                    const int r0 = max(0, u0 - kSeqUnits) * 16;
+                    const int r1 = min(max(0, u1 - kSeqUnits) * 16, nl_b);
                     const long long base_row = ((long long)b * p.Hkv + kvh) * C;   // row in the K half
                     // slot of the token being decoded: the ring's wrap point, and
                     // (fused append) the row that receives the new K/V

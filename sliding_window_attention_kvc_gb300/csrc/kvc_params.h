@@ -21,6 +21,10 @@ constexpr int kStreamCtas = 304;                 // stream-K grid: 152 SMs x 2 C
 // cost per share (a segment start and a partial) that only long shares hide.
 constexpr int kPagedShareFactor = 3;             // paged caches with >= kPagedShareBatch sequences
 constexpr int kPagedShareBatch = 8;
+// bf16 ring / sink+ring stream-K partition: units charged to each sequence
+// for the start of its segment (a second segment costs a CTA a q load and a
+// partial write), besides one unit per 16 rows.
+constexpr int kSeqUnits = 4;
 constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
