@@ -343,9 +343,9 @@ class ClockSampler:
 # capture per workload (summaries: profiles/decode_mma_<workload>.md), and the
 # digest of the kernel sources they were taken on: reported only while the
 # sources are unchanged.
-KERNEL_TRAFFIC = {"ring_bf16": 138464256, "sink_window_bf16": 544556288,
-                  "paged_shared_prefix_bf16": 894835456, "long_context_pool_bf16": 152987904}
-KERNEL_TRAFFIC_SOURCES = "00bd4bff9652560d92642479b4857f63f01448aeedb02ff359569be0a9ac922d"
+KERNEL_TRAFFIC = {"ring_bf16": 137936896, "sink_window_bf16": 544711936,
+                  "paged_shared_prefix_bf16": 894593792, "long_context_pool_bf16": 153271552}
+KERNEL_TRAFFIC_SOURCES = "21fe28ed5882ab71be6cea79d7ff73dc146cbf27d6942ef5ccccb0a350772a4e"
 
 
 def _kernel_sources_digest():
