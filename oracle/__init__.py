@@ -9,6 +9,8 @@ method).
 What it computes, in fp64 numpy, slowly and plainly:
 
 * `storage`   – rounding of a value to the cache's storage type (bf16 / fp32).
+* `quant`     – per-row INT8 storage: fp32 scale max|x| / 127, codes rounded
+                to nearest-even ([primer] 5.1, quantised cache).
 * `rope`      – rotary position embedding, rotate-half pairing (i, i + D/2).
 * `layouts`   – slot maps, attended sets and in-cache positions of the three
                 cache layouts, plus step-by-step layout models (a ring with a
@@ -43,7 +45,7 @@ The numeric attention outputs of the full workloads have no worked example
 on the pages; they are pinned through those checks of the definition.
 """
 
-from . import attention, blocks, layouts, rope, storage
+from . import attention, blocks, layouts, quant, rope, storage
 from .attention import attend, decode_masked_history, decode_reference, decode_sequence
 from .layouts import (
     PagedKV,
@@ -59,7 +61,7 @@ from .rope import inv_freq, rotate
 from .storage import round_bf16, round_storage
 
 __all__ = [
-    "attention", "blocks", "layouts", "rope", "storage",
+    "attention", "blocks", "layouts", "quant", "rope", "storage",
     "attend", "decode_reference", "decode_masked_history", "decode_sequence",
     "PagedKV", "RingKV", "SinkRingKV", "StreamingKV",
     "incache_position", "paged_attended", "window_attended", "window_slot",

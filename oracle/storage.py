@@ -28,9 +28,13 @@ def round_f32(x):
 
 
 def round_storage(x, dtype: str):
-    """Round to the storage dtype "bf16" | "f32"."""
+    """The value read back after storing rows x [..., D] as "bf16" | "f32" |
+    "i8" (per-row INT8 codes and an fp32 scale, `oracle.quant`)."""
     if dtype == "bf16":
         return round_bf16(x)
     if dtype == "f32":
         return round_f32(x)
+    if dtype == "i8":
+        from .quant import store_i8
+        return store_i8(x)
     raise ValueError(dtype)

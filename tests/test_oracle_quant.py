@@ -1,0 +1,112 @@
+"""Pins of the oracle's per-row INT8 storage (oracle.quant) against closed
+forms, a brute-force search and exactness properties ([primer] 5.1,
+quantised cache: INT8 halves the memory; the per-row symmetric format is
+the reading taken)."""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention, quant
+
+
+def test_worked_row_closed_form():
+    # max |x| = 254 -> s = 2 exactly; the quotients are exact, so the codes
+    # are the plain ties-to-even roundings of x / 2
+    x = np.array([254.0, 1.0, -3.0, 5.0, -254.0, 0.0, 127.0, -0.5])
+    c, s = quant.quantize_rows(x)
+    assert s.dtype == np.float32 and float(s) == 2.0
+    assert c.dtype == np.int8
+    assert c.tolist() == [127, 0, -2, 2, -127, 0, 64, 0]
+    assert quant.dequantize_rows(c, s).tolist() == [254.0, 0.0, -4.0, 4.0, -254.0, 0.0, 128.0, 0.0]
+
+
+def test_zero_row_and_sign_of_the_maximum():
+    c, s = quant.quantize_rows(np.zeros((2, 8)))
+    assert s.tolist() == [0.0, 0.0] and not c.any()
+    assert not quant.dequantize_rows(c, s).any()
+    # the largest magnitude is negative: it still takes the full code range
+    c, s = quant.quantize_rows(np.array([-508.0, 4.0, 2.0]))
+    assert float(s) == 4.0 and c.tolist() == [-127, 1, 0]
+
+
+def _nearest_even_search(r):
+    """The integer k in [-127, 127] nearest to r, ties to the even one (search)."""
+    best = None
+    for k in range(-127, 128):
+        d = abs(r - k)
+        if best is None or d < best[0] or (d == best[0] and k % 2 == 0):
+            best = (d, k)
+    return best[1]
+
+
+def test_codes_against_brute_force_search():
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal((6, 16)) * np.array([1e-3, 1.0, 3.0, 50.0, 1e4, 0.25])[:, None]).astype(np.float32)
+    x[2, 5] = x[2, 5] * 0  # a zero entry in a nonzero row
+    c, s = quant.quantize_rows(x)
+    for i in range(x.shape[0]):
+        si = np.float32(np.max(np.abs(x[i])) / np.float32(127))
+        assert s[i] == si
+        for j in range(x.shape[1]):
+            r = float(np.float32(x[i, j] / si))
+            assert c[i, j] == _nearest_even_search(r), (i, j)
+
+
+def test_invariants_on_random_rows():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((200, 128)) * rng.uniform(1e-2, 1e2, size=(200, 1))
+    x32 = x.astype(np.float32).astype(np.float64)
+    c, s = quant.quantize_rows(x)
+    assert np.abs(c.astype(np.int32)).max() <= 127
+    # the largest magnitude of every row maps to +-127
+    assert (np.abs(c.astype(np.int32)).max(axis=1) == 127).all()
+    # read back within half a step (the fp32 quotient adds a relative 2^-24)
+    err = np.abs(x32 - quant.dequantize_rows(c, s))
+    assert (err <= s[:, None].astype(np.float64) * (0.5 + 1e-6)).all()
+    # scaling a row by a power of two scales s and keeps the codes
+    c2, s2 = quant.quantize_rows(x32 * 8.0)
+    assert (c2 == c).all() and (s2 == s * np.float32(8)).all()
+
+
+def test_integer_rows_are_stored_exactly_and_attention_is_unchanged():
+    # rows of integers in [-127, 127] holding +-127 have s = 1: lossless
+    rng = np.random.default_rng(9)
+    K = rng.integers(-127, 128, size=(12, 16)).astype(np.float64)
+    V = rng.integers(-127, 128, size=(12, 16)).astype(np.float64)
+    K[:, 3] = 127
+    V[:, 0] = -127
+    assert (quant.store_i8(K) == K).all() and (quant.store_i8(V) == V).all()
+    q = rng.standard_normal((4, 16)) * 0.05
+    ps = list(range(12))
+    want = attention.decode_reference(q, K, V, ps, 11)
+    got = attention.decode_reference(q, quant.store_i8(K), quant.store_i8(V), ps, 11, storage="i8")
+    assert (got == want).all()
+
+
+def test_baked_keys_are_quantised_after_rotation():
+    # with baked RoPE the stored key is the rotated row, quantised; at position
+    # 0 the rotation is the identity, so a lossless integer row stays exact
+    rng = np.random.default_rng(10)
+    K = rng.integers(-127, 128, size=(1, 8)).astype(np.float64)
+    K[0, 0] = 127
+    V = rng.standard_normal((1, 8))
+    q = rng.standard_normal((2, 8))
+    out = attention.decode_reference(q, K, V, [0], 0, rope="baked", storage="i8")
+    assert np.allclose(out, np.repeat(V, 2, axis=0), rtol=0, atol=0)
+    # at a later position the rows differ from the unrotated ones, but each
+    # still reads back within half a step of the rotated value
+    from oracle.rope import rotate
+    R = rotate(K, np.array([37]), 10000.0)
+    c, s = quant.quantize_rows(R)
+    assert np.abs(R - quant.dequantize_rows(c, s)).max() <= float(s[0]) * (0.5 + 1e-6) + 1e-6
+    assert math.isclose(float(s[0]), float(np.abs(R.astype(np.float32)).max()) / 127, rel_tol=1e-6)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_store_i8_matches_quantize_then_dequantize(D):
+    rng = np.random.default_rng(D)
+    x = rng.standard_normal((5, D))
+    c, s = quant.quantize_rows(x.astype(np.float32))
+    assert (quant.store_i8(x) == quant.dequantize_rows(c, s)).all()
