@@ -39,7 +39,8 @@ import kvc_synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "ring_bf16"
 DEFAULT_LAYERS = {"tiny_ring_sink_f32": 1, "ring_bf16": 8, "sink_window_bf16": 2,
-                  "paged_shared_prefix_bf16": 2, "long_context_pool_bf16": 4}
+                  "paged_shared_prefix_bf16": 2, "long_context_pool_bf16": 4,
+                  "ring_int8": 8, "paged_shared_prefix_int8": 2}
 
 
 def _kvc():
@@ -88,11 +89,13 @@ def attended_rows(wl):
 def step_bytes(wl):
     """Algorithmic bytes of one decode step (whole batch, one layer)."""
     rows, touched = attended_rows(wl)
-    row_bytes = wl.kv_heads * 2 * wl.head_dim * wl.elt_bytes     # K and V of one token
+    # K and V of one token (INT8: codes and row scales)
+    row_bytes = wl.kv_heads * 2 * (wl.head_dim * wl.elt_bytes + wl.row_scale_bytes)
     logical_kv = int(rows.sum()) * row_bytes
     unique_kv = logical_kv if touched is None else sum(touched.values()) * row_bytes
-    qo = 2 * wl.batch * wl.q_heads * wl.head_dim * wl.elt_bytes   # q in, out
-    appended = 2 * wl.batch * wl.kv_heads * 2 * wl.head_dim * wl.elt_bytes  # new K/V read + written
+    qo = 2 * wl.batch * wl.q_heads * wl.head_dim * wl.value_bytes   # q in, out
+    # new K/V read, and written to the cache
+    appended = wl.batch * wl.kv_heads * 2 * (wl.head_dim * (wl.value_bytes + wl.elt_bytes) + wl.row_scale_bytes)
     return {"kv_logical": logical_kv, "kv_unique": unique_kv, "qo": qo, "append": appended,
             "decode_algorithmic": unique_kv + qo, "step_algorithmic": unique_kv + qo + appended}
 
@@ -117,7 +120,7 @@ def _window_fill_inputs(wl, layer, source):
     parts.append(("window", wl.window, t - wl.window))
     for name, n, start in parts:
         if source == "cpu":
-            k = torch.zeros((wl.batch, n, wl.kv_heads, wl.head_dim), dtype=kvc_synth.to_dtype(wl.dtype))
+            k = torch.zeros((wl.batch, n, wl.kv_heads, wl.head_dim), dtype=kvc_synth.to_dtype(wl.value_dtype))
             v = torch.zeros_like(k)
             for b in range(wl.batch):
                 p = np.arange(start[b], start[b] + n)
@@ -127,9 +130,9 @@ def _window_fill_inputs(wl, layer, source):
                 v[b, keep] = vb
             k, v = k.cuda(), v.cuda()
         else:
-            k = _raw_rows_device((wl.batch, n, wl.kv_heads, wl.head_dim), wl.dtype,
+            k = _raw_rows_device((wl.batch, n, wl.kv_heads, wl.head_dim), wl.value_dtype,
                                  (wl.seed, layer, 101 if name == "sinks" else 102))
-            v = _raw_rows_device((wl.batch, n, wl.kv_heads, wl.head_dim), wl.dtype,
+            v = _raw_rows_device((wl.batch, n, wl.kv_heads, wl.head_dim), wl.value_dtype,
                                  (wl.seed, layer, 103 if name == "sinks" else 104))
         calls.append((k, v, torch.from_numpy(start.astype(np.int32)).cuda()))
     return calls
@@ -178,16 +181,19 @@ class DecodeState:
                 q = wl.queries(layer)
                 kn, vn = wl.new_kv(layer)
             else:
-                q = _raw_rows_device((wl.batch, wl.q_heads, wl.head_dim), wl.dtype, (wl.seed, layer, 105))
-                kn = _raw_rows_device((wl.batch, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, 106))
-                vn = _raw_rows_device((wl.batch, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, 107))
+                q = _raw_rows_device((wl.batch, wl.q_heads, wl.head_dim), wl.value_dtype, (wl.seed, layer, 105))
+                kn = _raw_rows_device((wl.batch, wl.kv_heads, wl.head_dim), wl.value_dtype, (wl.seed, layer, 106))
+                vn = _raw_rows_device((wl.batch, wl.kv_heads, wl.head_dim), wl.value_dtype, (wl.seed, layer, 107))
             self.q.append(q.contiguous().cuda())
             self.k_new.append(kn.contiguous().cuda())
             self.v_new.append(vn.contiguous().cuda())
         if wl.layout == "paged" and wl.valid is not None and poison:
             # non-resident slots hold no data: poison them, they must never be read
             bad = torch.from_numpy(~wl.valid).cuda()
-            self.cache[:, :, bad] = float("nan")
+            if wl.dtype == "i8":
+                kvc.int8_views(self.desc, self.cache)[1][:, :, bad] = float("nan")
+            else:
+                self.cache[:, :, bad] = float("nan")
         self.out = torch.empty((wl.batch, wl.q_heads, wl.head_dim), dtype=kvc.desc_dtype(self.desc),
                                device="cuda")
         torch.cuda.synchronize()
@@ -213,8 +219,8 @@ class DecodeState:
                     k, v = wl.kv_history(layer, b, np.arange(p0, p1))
                     k, v = k[None].cuda(), v[None].cuda()
                 else:
-                    k = _raw_rows_device((1, n, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, b, p0, 108))
-                    v = _raw_rows_device((1, n, wl.kv_heads, wl.head_dim), wl.dtype, (wl.seed, layer, b, p0, 109))
+                    k = _raw_rows_device((1, n, wl.kv_heads, wl.head_dim), wl.value_dtype, (wl.seed, layer, b, p0, 108))
+                    v = _raw_rows_device((1, n, wl.kv_heads, wl.head_dim), wl.value_dtype, (wl.seed, layer, b, p0, 109))
                 start = torch.tensor([p0], dtype=torch.int32, device="cuda")
                 rc = kvc.lib().kvc_append(ctypes.byref(d1), self.cache.data_ptr(), layer, k.data_ptr(),
                                           v.data_ptr(), n, start.data_ptr(), row_ptr, ws1.data_ptr(),
@@ -234,8 +240,8 @@ class DecodeState:
                                out=self.out if out is None else out)
 
     def launches_per_step(self):
-        """Kernels one kvc_decode_step launches (fused append for bf16 ring layouts)."""
-        bf16 = self.wl.dtype == "bf16"
+        """Kernels one kvc_decode_step launches (fused append for bf16 / INT8 ring layouts)."""
+        bf16 = self.wl.dtype in ("bf16", "i8")     # the tensor-core kernel
         paged = self.wl.layout == "paged"
         n = 1                              # decode kernel
         n += 1 if bf16 else 0              # combine kernel (bf16 stream-K)
@@ -386,7 +392,7 @@ def oracle_sample(wl, budget_s, max_rows=None, part=(0, 1)):
     units).  part = (k, n): only the units u = b * kv_heads + h with u mod n == k."""
     import oracle
     spec = dict(rope=wl.rope, base=wl.rope_base, storage=wl.dtype, sinks=wl.sinks, window=wl.window)
-    row_bytes = 2 * wl.head_dim * wl.elt_bytes
+    row_bytes = 2 * (wl.head_dim * wl.elt_bytes + wl.row_scale_bytes)
     g = wl.group_size
     done_bytes, spent, units = 0, 0.0, 0
     for b in range(wl.batch):
@@ -406,6 +412,10 @@ def oracle_sample(wl, budget_s, max_rows=None, part=(0, 1)):
             qf = q[h * g:(h + 1) * g].double().numpy()
             kf, vf = k[:, h].double().numpy(), v[:, h].double().numpy()
             t0 = time.perf_counter()
+            if wl.dtype == "i8":        # rows as an INT8 cache stores them (baked keys: after rotation)
+                vf = oracle.quant.store_i8(vf)
+                if wl.rope != "baked":
+                    kf = oracle.quant.store_i8(kf)
             oracle.decode_reference(qf, kf, vf, pos, t, **spec)
             spent += time.perf_counter() - t0
             done_bytes += len(pos) * row_bytes
@@ -657,7 +667,7 @@ def run_ours(args):
                      "traffic": _traffic(wl.name, args.traffic),
                      "traffic_kernel": "decode_mma_kernel, dram__bytes_read.sum + dram__bytes_write.sum per launch",
                      "kernel": "kvc_decode_step: " + ("decode_mma_kernel + combine_streamk_kernel"
-                                                      if wl.dtype == "bf16" else "append + decode"),
+                                                      if wl.dtype in ("bf16", "i8") else "append + decode"),
                      "timer": "CUDA events around the timed region (K kvc_decode_step calls); per step",
                      "algorithmic_bytes_per_launch": nb["step_algorithmic"]},
         "frac_of_8tbs": value / 8000.0,

@@ -25,7 +25,8 @@
  *     position) set bits in the workspace's error word; the kernel skips the
  *     offending access and carries on.  kvc_get_error() reads and clears them.
  *   - Element types: the cache, q, out, k_new and v_new share one element
- *     type (kvc_desc.dtype).  All arithmetic is fp32.
+ *     type (kvc_desc.dtype), except that an INT8 cache (KVC_I8) takes and
+ *     returns bf16 q, out, k_new and v_new.  All arithmetic is fp32.
  *   - Alignment: cache, q, out, k_new, v_new and workspace must be 16-byte
  *     aligned (KVC_ERR_ALIGN otherwise).
  */
@@ -69,18 +70,34 @@ typedef enum { KVC_LAYOUT_RING = 0, KVC_LAYOUT_SINK_RING = 1, KVC_LAYOUT_PAGED =
  *                C = S + W); q at min(t, C - 1).  RING and SINK_RING only. */
 typedef enum { KVC_ROPE_NONE = 0, KVC_ROPE_BAKED = 1, KVC_ROPE_READ_INCACHE = 2 } kvc_rope;
 
-typedef enum { KVC_F32 = 0, KVC_BF16 = 1 } kvc_dtype;
+/* Cache element types.
+ *  KVC_F32, KVC_BF16  rows stored as fp32 / bf16 (round to nearest even).
+ *  KVC_I8             [primer] 5.1 (quantised cache: INT8 halves the bytes):
+ *                     each stored row (one token's K or V of one kv head)
+ *                     keeps int8 codes and one fp32 scale s = max|x| / 127,
+ *                     codes rint(x / s) clamped to +-127 (IEEE fp32 quotient,
+ *                     ties to even), read back as code * s; a zero row has
+ *                     s = 0.  With baked RoPE the rotated key is quantised.
+ *                     q, out, k_new and v_new are bf16.  Requires head_dim
+ *                     128 or 256, RoPE NONE or BAKED, and rows per K (or V)
+ *                     half of a layer (batch * kv_heads * capacity, or
+ *                     num_blocks * kv_heads * block_size) a multiple of 4.
+ *                     Not accepted by the pool pager (kvc_pagein_issue). */
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_I8 = 2 } kvc_dtype;
 
 /* Cache geometry.  Cache memory layout ([primer] 3.1, K at index 0, V at 1):
  *   RING / SINK_RING: [layers, 2, batch, kv_heads, capacity, head_dim],
  *                     capacity = sinks + window;
  *   PAGED:            [layers, 2, num_blocks, kv_heads, block_size, head_dim].
+ * KVC_I8: that array holds the int8 codes and is followed directly by the
+ * fp32 row scales, [layers, 2, batch, kv_heads, capacity] (or [layers, 2,
+ * num_blocks, kv_heads, block_size]); kvc_cache_bytes counts both.
  * q_heads must be a multiple of kv_heads; q head h reads kv head
  * h / (q_heads / kv_heads) ([share] 2.2 and 4.1, grouped-query attention). */
 typedef struct kvc_desc {
     int32_t layout;             /* kvc_layout */
     int32_t rope;               /* kvc_rope */
-    int32_t dtype;              /* kvc_dtype */
+    int32_t dtype;              /* kvc_dtype (cache element type) */
     int32_t layers;
     int32_t batch;              /* sequences (rows of block_table for PAGED) */
     int32_t q_heads;

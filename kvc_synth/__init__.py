@@ -22,6 +22,9 @@ from .workloads import (
     sink_window_bf16,
     paged_shared_prefix_bf16,
     long_context_pool_bf16,
+    ring_int8,
+    paged_shared_prefix_int8,
+    as_int8,
 )
 
 __all__ = [
@@ -37,4 +40,7 @@ __all__ = [
     "sink_window_bf16",
     "paged_shared_prefix_bf16",
     "long_context_pool_bf16",
+    "ring_int8",
+    "paged_shared_prefix_int8",
+    "as_int8",
 ]

@@ -30,7 +30,7 @@ OWNER_SEQ, OWNER_GROUP = 0, 1
 class Workload:
     name: str
     layout: str                 # "window" (ring, or ring with pinned sinks) | "paged"
-    dtype: str                  # "f32" | "bf16"
+    dtype: str                  # cache storage: "f32" | "bf16" | "i8" (int8 codes + fp32 row scales, bf16 values)
     rope: str                   # "none" | "baked" | "read_time"
     batch: int
     q_heads: int
@@ -70,8 +70,23 @@ class Workload:
         return self.q_heads // self.kv_heads
 
     @property
+    def value_dtype(self) -> str:
+        """Type of the drawn values (q, K, V inputs): bf16 for an INT8 cache."""
+        return "bf16" if self.dtype == "i8" else self.dtype
+
+    @property
     def elt_bytes(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        """Bytes of one stored cache element (an INT8 code: 1)."""
+        return {"f32": 4, "bf16": 2, "i8": 1}[self.dtype]
+
+    @property
+    def row_scale_bytes(self) -> int:
+        """Bytes stored per cache row besides its elements (INT8: the fp32 scale)."""
+        return 4 if self.dtype == "i8" else 0
+
+    @property
+    def value_bytes(self) -> int:
+        return 4 if self.value_dtype == "f32" else 2
 
     def cache_shape(self, layers: int | None = None) -> tuple:
         """[layers, 2, batch, kv_heads, capacity, D] or [layers, 2, num_blocks, kv_heads, bs, D]."""
@@ -92,7 +107,7 @@ class Workload:
         p = np.asarray(positions, dtype=np.int64).reshape(-1)
         n = p.shape[0]
         H, D = self.kv_heads, self.head_dim
-        out_k = torch.empty((n, H, D), dtype=torch.float32).to(_td(self.dtype))
+        out_k = torch.empty((n, H, D), dtype=torch.float32).to(_td(self.value_dtype))
         out_v = torch.empty_like(out_k)
         if n == 0:
             return out_k.to(device), out_v.to(device)
@@ -105,8 +120,8 @@ class Workload:
         for u, (kd, idn, bk) in enumerate(uniq):
             sel = np.nonzero(inv == u)[0]
             base = (self.seed, layer, int(kd), int(idn), int(bk))
-            kb = randn(base + (STREAM_K,), (POSITION_BLOCK, H, D), self.dtype)
-            vb = randn(base + (STREAM_V,), (POSITION_BLOCK, H, D), self.dtype)
+            kb = randn(base + (STREAM_K,), (POSITION_BLOCK, H, D), self.value_dtype)
+            vb = randn(base + (STREAM_V,), (POSITION_BLOCK, H, D), self.value_dtype)
             idx = torch.from_numpy(off[sel])
             sel_t = torch.from_numpy(sel)
             out_k[sel_t] = kb[idx]
@@ -116,7 +131,7 @@ class Workload:
     def query(self, layer: int, b: int, t: int | None = None) -> torch.Tensor:
         """Pre-RoPE query of sequence b for the token at position t (default t_b): [q_heads, D]."""
         t = int(self.positions[b]) if t is None else int(t)
-        return randn((self.seed, layer, OWNER_SEQ, b, t, STREAM_Q), (self.q_heads, self.head_dim), self.dtype)
+        return randn((self.seed, layer, OWNER_SEQ, b, t, STREAM_Q), (self.q_heads, self.head_dim), self.value_dtype)
 
     def queries(self, layer: int, positions=None) -> torch.Tensor:
         pos = self.positions if positions is None else np.asarray(positions)
@@ -285,12 +300,32 @@ def long_context_pool_bf16(small: bool = False, layers: int = 1, density: float 
     )
 
 
+def as_int8(wl: Workload, name: str) -> Workload:
+    """The same workload (sizes, positions, seed, drawn values) over an INT8
+    cache; read-time RoPE becomes baked (INT8 rows hold rotated keys)."""
+    import dataclasses
+    return dataclasses.replace(wl, name=name, dtype="i8", rope="none" if wl.rope == "none" else "baked",
+                               notes=(wl.notes + "; " if wl.notes else "") + "INT8 cache, per-row fp32 scales")
+
+
+def ring_int8(small: bool = False, layers: int = 1) -> Workload:
+    """ring_bf16's sizes, positions and values over an INT8 cache."""
+    return as_int8(ring_bf16(small, layers), "ring_int8" + ("_small" if small else ""))
+
+
+def paged_shared_prefix_int8(small: bool = False, layers: int = 1) -> Workload:
+    """paged_shared_prefix_bf16's sizes, tables and values over an INT8 cache."""
+    return as_int8(paged_shared_prefix_bf16(small, layers), "paged_shared_prefix_int8" + ("_small" if small else ""))
+
+
 WORKLOAD_NAMES = {
     "tiny_ring_sink_f32": tiny_ring_sink_f32,
     "ring_bf16": ring_bf16,
     "sink_window_bf16": sink_window_bf16,
     "paged_shared_prefix_bf16": paged_shared_prefix_bf16,
     "long_context_pool_bf16": long_context_pool_bf16,
+    "ring_int8": ring_int8,
+    "paged_shared_prefix_int8": paged_shared_prefix_int8,
 }
 
 

@@ -19,8 +19,9 @@ LIB_PATH = os.path.join(_HERE, "libkvc.so")
 
 LAYOUTS = {"ring": 0, "sink_ring": 1, "paged": 2}
 ROPES = {"none": 0, "baked": 1, "read_time": 2}
-DTYPES = {torch.float32: 0, torch.bfloat16: 1}
-DTYPE_NAMES = {"f32": torch.float32, "bf16": torch.bfloat16}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.int8: 2}
+DTYPE_NAMES = {"f32": torch.float32, "bf16": torch.bfloat16, "i8": torch.int8}
+KVC_I8 = 2
 
 KVC_OK = 0
 KVC_ERR_NULL, KVC_ERR_DESC, KVC_ERR_UNSUPPORTED = -1, -2, -3
@@ -124,7 +125,14 @@ def make_desc(layout: str, rope: str, dtype, layers: int, batch: int, q_heads: i
 
 
 def desc_dtype(d: KvcDesc) -> torch.dtype:
+    """Element type of q, out, k_new and v_new (bf16 for an INT8 cache)."""
     return torch.float32 if d.dtype == 0 else torch.bfloat16
+
+
+def cache_dtype(d: KvcDesc) -> torch.dtype:
+    """Element type of the cache tensor: fp32, bf16, or bytes (uint8) for an
+    INT8 cache, whose buffer holds the codes followed by the fp32 row scales."""
+    return {0: torch.float32, 1: torch.bfloat16}.get(d.dtype, torch.uint8)
 
 
 def cache_shape(d: KvcDesc) -> tuple:
@@ -177,11 +185,33 @@ def _need(t: torch.Tensor, name: str, dtype=None, numel=None):
 
 
 def alloc_cache(d: KvcDesc, device="cuda", fill=None) -> torch.Tensor:
-    """Caller-owned cache tensor of the layout's shape (uninitialised unless `fill`)."""
+    """Caller-owned cache tensor of the layout's shape (uninitialised unless `fill`).
+
+    INT8 cache: a flat uint8 tensor of kvc_cache_bytes(d) bytes (`int8_views`
+    gives its codes and scales); `fill` sets every code and scale to
+    rint(fill) and fill, or NaN scales when fill is NaN."""
     shape = cache_shape(d)
+    if d.dtype == KVC_I8:
+        buf = torch.empty(cache_bytes(d), dtype=torch.uint8, device=device)
+        if fill is not None:
+            codes, scales = int8_views(d, buf)
+            codes.fill_(0 if fill != fill else int(round(fill)))
+            scales.fill_(fill)
+        return buf
     if fill is None:
         return torch.empty(shape, dtype=desc_dtype(d), device=device)
     return torch.full(shape, fill, dtype=desc_dtype(d), device=device)
+
+
+def int8_views(d: KvcDesc, cache: torch.Tensor):
+    """(codes int8 [cache_shape], scales fp32 [cache_shape[:-1]]) views of an INT8 cache buffer."""
+    shape = cache_shape(d)
+    n = 1
+    for x in shape:
+        n *= x
+    codes = cache[:n].view(torch.int8).view(shape)
+    scales = cache[n:n + 4 * (n // shape[-1])].view(torch.float32).view(shape[:-1])
+    return codes, scales
 
 
 def alloc_workspace(d: KvcDesc, device="cuda") -> torch.Tensor:
@@ -202,7 +232,7 @@ def append(d: KvcDesc, cache: torch.Tensor, layer: int, k_new: torch.Tensor, v_n
            pos: torch.Tensor, workspace: torch.Tensor, block_table: torch.Tensor | None = None, stream=None):
     """kvc_append: k_new / v_new [batch, n_new, kv_heads, D] (or [batch, kv_heads, D] for one token)."""
     dt = desc_dtype(d)
-    _need(cache, "cache", dt)
+    _need(cache, "cache", cache_dtype(d))
     _need(k_new, "k_new", dt)
     _need(v_new, "v_new", dt)
     _need(pos, "pos", torch.int32, d.batch)
@@ -224,7 +254,7 @@ def decode_attention(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tenso
                      stream=None) -> torch.Tensor:
     """kvc_decode_attention: q [batch, q_heads, D] -> out [batch, q_heads, D]."""
     dt = desc_dtype(d)
-    _need(cache, "cache", dt)
+    _need(cache, "cache", cache_dtype(d))
     _need(q, "q", dt, d.batch * d.q_heads * d.head_dim)
     _need(pos, "pos", torch.int32, d.batch)
     _need(workspace, "workspace", torch.uint8)
@@ -248,7 +278,7 @@ def decode_step(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, k_
                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """kvc_decode_step: append the token at pos (k_new / v_new [batch, kv_heads, D]) and attend."""
     dt = desc_dtype(d)
-    _need(cache, "cache", dt)
+    _need(cache, "cache", cache_dtype(d))
     _need(q, "q", dt, d.batch * d.q_heads * d.head_dim)
     _need(k_new, "k_new", dt, d.batch * d.kv_heads * d.head_dim)
     _need(v_new, "v_new", dt, d.batch * d.kv_heads * d.head_dim)

@@ -18,18 +18,28 @@
     KVC_INST(E, 256, 2, PG, RD)     \
     KVC_INST(E, 256, 4, PG, RD)
 
-// bf16 caches: tensor-core kernel (kvc_decode_mma.cuh)
-#define KVC_INST_MMA(D, GH, PG, RD)                                                                  \
-    template cudaError_t kvc::launch_decode_mma_t<D, GH, PG, RD>(const kvc::DecodeParams&,              \
-                                                                 const kvc::KvTensorMaps&, dim3, cudaStream_t);
+// bf16 and INT8 caches: tensor-core kernel (kvc_decode_mma.cuh)
+#define KVC_INST_MMA(D, GH, PG, RD, Q8)                                                               \
+    template cudaError_t kvc::launch_decode_mma_t<D, GH, PG, RD, Q8>(const kvc::DecodeParams&,          \
+                                                                     const kvc::KvTensorMaps&, dim3,     \
+                                                                     cudaStream_t);
 
-#define KVC_INST_MMA_ALL_D(PG, RD) \
-    KVC_INST_MMA(64, 1, PG, RD)    \
-    KVC_INST_MMA(64, 2, PG, RD)    \
-    KVC_INST_MMA(64, 4, PG, RD)    \
-    KVC_INST_MMA(128, 1, PG, RD)   \
-    KVC_INST_MMA(128, 2, PG, RD)   \
-    KVC_INST_MMA(128, 4, PG, RD)   \
-    KVC_INST_MMA(256, 1, PG, RD)   \
-    KVC_INST_MMA(256, 2, PG, RD)   \
-    KVC_INST_MMA(256, 4, PG, RD)
+#define KVC_INST_MMA_ALL_D(PG, RD)        \
+    KVC_INST_MMA(64, 1, PG, RD, false)    \
+    KVC_INST_MMA(64, 2, PG, RD, false)    \
+    KVC_INST_MMA(64, 4, PG, RD, false)    \
+    KVC_INST_MMA(128, 1, PG, RD, false)   \
+    KVC_INST_MMA(128, 2, PG, RD, false)   \
+    KVC_INST_MMA(128, 4, PG, RD, false)   \
+    KVC_INST_MMA(256, 1, PG, RD, false)   \
+    KVC_INST_MMA(256, 2, PG, RD, false)   \
+    KVC_INST_MMA(256, 4, PG, RD, false)
+
+// INT8: head_dim 128 and 256, no read-time RoPE
+#define KVC_INST_MMA_Q8(PG)               \
+    KVC_INST_MMA(128, 1, PG, false, true) \
+    KVC_INST_MMA(128, 2, PG, false, true) \
+    KVC_INST_MMA(128, 4, PG, false, true) \
+    KVC_INST_MMA(256, 1, PG, false, true) \
+    KVC_INST_MMA(256, 2, PG, false, true) \
+    KVC_INST_MMA(256, 4, PG, false, true)

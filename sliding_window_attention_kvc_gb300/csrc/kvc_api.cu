@@ -15,13 +15,14 @@ namespace kvc {
 
 template <typename Elt, int D, int GH, bool PAGED, bool READ>
 cudaError_t launch_decode_t(const DecodeParams& p, dim3 grid, cudaStream_t stream);
-template <int D, int GH, bool PAGED, bool READ>
+template <int D, int GH, bool PAGED, bool READ, bool Q8>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps, dim3 grid, cudaStream_t stream);
 
 namespace {
 
 struct Geo {
-    int elt;        // bytes per element
+    int elt;        // bytes per cache element (INT8: the codes)
+    int act_elt;    // bytes per element of q, out, k_new, v_new
     int C;          // window layouts: slots per (sequence, kv head)
     int G, GH, nsub;
     long long half_elems;   // elements of one K (or V) half of one layer
@@ -33,7 +34,7 @@ int rows_per_stage(int elt, int D) { return elt == 4 ? 8192 / (D * elt) : (D == 
 
 int check_desc(const kvc_desc* d, Geo* g) {
     if (!d) return KVC_ERR_NULL;
-    if (d->layout < 0 || d->layout > 2 || d->rope < 0 || d->rope > 2 || d->dtype < 0 || d->dtype > 1)
+    if (d->layout < 0 || d->layout > 2 || d->rope < 0 || d->rope > 2 || d->dtype < 0 || d->dtype > 2)
         return KVC_ERR_DESC;
     if (d->layers < 1 || d->batch < 1 || d->kv_heads < 1 || d->q_heads < 1 || d->q_heads % d->kv_heads)
         return KVC_ERR_DESC;
@@ -41,7 +42,9 @@ int check_desc(const kvc_desc* d, Geo* g) {
     if (d->num_splits < 0) return KVC_ERR_DESC;
     if (d->rope != KVC_ROPE_NONE && !(d->rope_base > 0.f)) return KVC_ERR_DESC;
     if (d->softmax_scale < 0.f) return KVC_ERR_DESC;
-    g->elt = d->dtype == KVC_F32 ? 4 : 2;
+    g->elt = d->dtype == KVC_F32 ? 4 : (d->dtype == KVC_BF16 ? 2 : 1);
+    g->act_elt = d->dtype == KVC_F32 ? 4 : 2;
+    if (d->dtype == KVC_I8 && (d->head_dim < 128 || d->rope == KVC_ROPE_READ_INCACHE)) return KVC_ERR_UNSUPPORTED;
     g->G = d->q_heads / d->kv_heads;
     g->GH = (g->G % 4 == 0) ? 4 : ((g->G % 2 == 0) ? 2 : 1);
     g->nsub = g->G / g->GH;
@@ -60,6 +63,8 @@ int check_desc(const kvc_desc* d, Geo* g) {
         g->C = d->window + d->sinks;
         g->half_elems = (long long)d->batch * d->kv_heads * g->C * d->head_dim;
     }
+    // INT8 scale tensor maps: rows of a half in multiples of 4 (16-byte strides)
+    if (d->dtype == KVC_I8 && (g->half_elems / d->head_dim) % 4) return KVC_ERR_UNSUPPORTED;
     return KVC_OK;
 }
 
@@ -71,9 +76,10 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     const int groups = d->kv_heads * g.nsub;
     // stream-K shares per (kv head, q-head group): bf16 kernels, and the paged
     // plan.  bf16: a persistent grid of about two CTAs per SM claims them in turn.
-    const int persist = (kStreamCtas + groups - 1) / groups;
-    if (d->layout == KVC_LAYOUT_PAGED || d->dtype == KVC_BF16) {
-        const bool bf16 = d->dtype == KVC_BF16;
+    const int stream_ctas = d->dtype == KVC_I8 ? kStreamCtasQ8 : kStreamCtas;
+    const int persist = (stream_ctas + groups - 1) / groups;
+    if (d->layout == KVC_LAYOUT_PAGED || d->dtype != KVC_F32) {
+        const bool bf16 = d->dtype != KVC_F32;     // tensor-core kernel (bf16 or INT8 cache)
         const int factor = (bf16 && d->layout == KVC_LAYOUT_PAGED && d->batch >= kPagedShareBatch)
                                ? kPagedShareFactor : 1;
         w.shares = d->num_splits > 0 ? d->num_splits : factor * persist;
@@ -155,17 +161,24 @@ cudaError_t launch_decode(int dtype, int D, int gh, bool paged, bool rd, const D
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_mma(int D, int gh, bool paged, bool rd, const DecodeParams& p, const KvTensorMaps& maps,
-                              dim3 grid, cudaStream_t s) {
-#define KVC_CASE(DD, GG, PG, RD) \
-    if (D == DD && gh == GG && paged == PG && rd == RD) return launch_decode_mma_t<DD, GG, PG, RD>(p, maps, grid, s);
-#define KVC_CASES(PG, RD)                                                   \
-    KVC_CASE(64, 1, PG, RD) KVC_CASE(64, 2, PG, RD) KVC_CASE(64, 4, PG, RD)    \
-    KVC_CASE(128, 1, PG, RD) KVC_CASE(128, 2, PG, RD) KVC_CASE(128, 4, PG, RD) \
-    KVC_CASE(256, 1, PG, RD) KVC_CASE(256, 2, PG, RD) KVC_CASE(256, 4, PG, RD)
+cudaError_t launch_decode_mma(int D, int gh, bool paged, bool rd, bool q8, const DecodeParams& p,
+                              const KvTensorMaps& maps, dim3 grid, cudaStream_t s) {
+#define KVC_CASE(DD, GG, PG, RD, Q)                                       \
+    if (D == DD && gh == GG && paged == PG && rd == RD && q8 == Q)        \
+        return launch_decode_mma_t<DD, GG, PG, RD, Q>(p, maps, grid, s);
+#define KVC_CASES(PG, RD)                                                                        \
+    KVC_CASE(64, 1, PG, RD, false) KVC_CASE(64, 2, PG, RD, false) KVC_CASE(64, 4, PG, RD, false)    \
+    KVC_CASE(128, 1, PG, RD, false) KVC_CASE(128, 2, PG, RD, false) KVC_CASE(128, 4, PG, RD, false) \
+    KVC_CASE(256, 1, PG, RD, false) KVC_CASE(256, 2, PG, RD, false) KVC_CASE(256, 4, PG, RD, false)
+#define KVC_CASES_Q8(PG)                                                                                 \
+    KVC_CASE(128, 1, PG, false, true) KVC_CASE(128, 2, PG, false, true) KVC_CASE(128, 4, PG, false, true) \
+    KVC_CASE(256, 1, PG, false, true) KVC_CASE(256, 2, PG, false, true) KVC_CASE(256, 4, PG, false, true)
     KVC_CASES(false, false)
     KVC_CASES(false, true)
     KVC_CASES(true, false)
+    KVC_CASES_Q8(false)
+    KVC_CASES_Q8(true)
+#undef KVC_CASES_Q8
 #undef KVC_CASES
 #undef KVC_CASE
     return cudaErrorInvalidValue;
@@ -206,8 +219,26 @@ int encode_kv_maps(const kvc_desc* d, const Geo& g, const void* cache, KvTensorM
     if (half_rows >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return KVC_ERR_CUDA;
-    const cuuint64_t row_bytes = (cuuint64_t)d->head_dim * 2, half_bytes = half_rows * row_bytes;
-    const cuuint32_t boxes = (cuuint32_t)(d->head_dim / 64);
+    const bool q8 = d->dtype == KVC_I8;
+    const CUtensorMapDataType type = q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t row_bytes = (cuuint64_t)d->head_dim * g.elt, half_bytes = half_rows * row_bytes;
+    const cuuint32_t bcols = 128u / (cuuint32_t)g.elt;                 // columns of a 128-byte box row
+    const cuuint32_t boxes = (cuuint32_t)(d->head_dim / bcols);
+    if (q8) {
+        // row scales: {row, K|V, layer} fp32 after the codes of every layer
+        void* scales = static_cast<char*>(const_cast<void*>(cache)) + (size_t)d->layers * 2 * half_bytes;
+        const cuuint64_t dims[3] = {half_rows, 2, (cuuint64_t)d->layers};
+        const cuuint64_t strides[2] = {half_rows * 4, 2 * half_rows * 4};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        const cuuint32_t box_run[3] = {(cuuint32_t)kScRunRows, 2, 1}, box_sub[3] = {(cuuint32_t)kScSubRows, 2, 1};
+        if (fn(&maps->sc_run, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scales, dims, strides, box_run, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            fn(&maps->sc_sub, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scales, dims, strides, box_sub, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return KVC_ERR_CUDA;
+    }
     for (int pass = boxes > 1 ? 0 : 1; pass < 2; ++pass) {
         const bool five = pass == 0;
         bool ok = true;
@@ -215,19 +246,19 @@ int encode_kv_maps(const kvc_desc* d, const Geo& g, const void* cache, KvTensorM
             const cuuint32_t R = 16u * (cuuint32_t)(r + 1);
             CUresult e;
             if (five) {
-                const cuuint64_t dims[5] = {64, half_rows, 2, (cuuint64_t)d->layers, boxes};
+                const cuuint64_t dims[5] = {bcols, half_rows, 2, (cuuint64_t)d->layers, boxes};
                 const cuuint64_t strides[4] = {row_bytes, half_bytes, 2 * half_bytes, 128};
-                const cuuint32_t box[5] = {64, R, 2, 1, boxes};
+                const cuuint32_t box[5] = {bcols, R, 2, 1, boxes};
                 const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-                e = fn(&maps->run[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(cache), dims, strides,
+                e = fn(&maps->run[r], type, 5, const_cast<void*>(cache), dims, strides,
                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             } else {
                 const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, half_rows, 2, (cuuint64_t)d->layers};
                 const cuuint64_t strides[3] = {row_bytes, half_bytes, 2 * half_bytes};
-                const cuuint32_t box[4] = {64, R, 2, 1};
+                const cuuint32_t box[4] = {bcols, R, 2, 1};
                 const cuuint32_t estr[4] = {1, 1, 1, 1};
-                e = fn(&maps->run[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides,
+                e = fn(&maps->run[r], type, 4, const_cast<void*>(cache), dims, strides,
                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             }
@@ -247,7 +278,7 @@ int kv_maps_for(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps
     struct Entry {
         const void* cache;
         long long half_elems;
-        int layers, head_dim, device, whole;
+        int layers, head_dim, dtype, device, whole;
         KvTensorMaps maps;
     };
     constexpr int kEntries = 8;
@@ -261,7 +292,7 @@ int kv_maps_for(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps
         for (int i = 0; i < used; ++i) {
             const Entry& e = entries[i];
             if (e.cache == cache && e.half_elems == g.half_elems && e.layers == d->layers &&
-                e.head_dim == d->head_dim && e.device == dev) {
+                e.head_dim == d->head_dim && e.dtype == d->dtype && e.device == dev) {
                 *maps = e.maps;
                 *whole = e.whole;
                 return KVC_OK;
@@ -276,6 +307,7 @@ int kv_maps_for(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps
     e.half_elems = g.half_elems;
     e.layers = d->layers;
     e.head_dim = d->head_dim;
+    e.dtype = d->dtype;
     e.device = dev;
     e.whole = *whole;
     e.maps = *maps;
@@ -327,6 +359,13 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     p.layer_off = (long long)layer * 2 * g.half_elems;
     p.layer = layer;
     p.kv_off = g.half_elems;
+    if (d->dtype == KVC_I8) {
+        const long long half_rows = g.half_elems / d->head_dim;
+        p.scales = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(cache)) +
+                                            (size_t)d->layers * 2 * (size_t)g.half_elems);
+        p.sc_layer_off = (long long)layer * 2 * half_rows;
+        p.sc_kv_off = half_rows;
+    }
     p.B = d->batch;
     p.Hq = d->q_heads;
     p.Hkv = d->kv_heads;
@@ -338,14 +377,14 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     p.bs = d->block_size;
     p.num_blocks = d->num_blocks;
     p.maxb = d->max_blocks_per_seq;
-    p.nsplit = d->dtype == KVC_BF16 ? w.shares : w.nsplit;   // bf16: stream-K shares per (kv head, group)
+    p.nsplit = d->dtype != KVC_F32 ? w.shares : w.nsplit;   // bf16 / INT8: stream-K shares per (kv head, group)
     p.max_items = w.items;
     p.rope = d->rope;
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
     p.q_scale = scale * 1.4426950408889634f;   // log2(e): softmax in base 2
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
 
-    dim3 grid(d->dtype == KVC_BF16 ? w.ctas : w.items, d->kv_heads, g.nsub);
+    dim3 grid(d->dtype != KVC_F32 ? w.ctas : w.items, d->kv_heads, g.nsub);
     if (paged) {
         PlanParams pp{};
         pp.pos = pos;
@@ -376,6 +415,9 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
             pp.D = d->head_dim;
             pp.rope = d->rope;
             pp.elt = g.elt;
+            pp.scales = p.scales;
+            pp.sc_layer_off = p.sc_layer_off;
+            pp.sc_kv_off = p.sc_kv_off;
             if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
         }
         if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
@@ -386,11 +428,12 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
         p.cta_items = pp.cta_items;
     }
     const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
-    if (d->dtype == KVC_BF16) {
+    if (d->dtype != KVC_F32) {
         KvTensorMaps maps;
         rc = kv_maps_for(d, g, cache, &maps, &p.tma_whole);
         if (rc) return rc;
-        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, p, maps, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
+        if (launch_decode_mma(d->head_dim, g.GH, paged, rd, d->dtype == KVC_I8, p, maps, grid, s) != cudaSuccess)
+            return KVC_ERR_CUDA;
         return KVC_OK;
     }
     if (launch_decode(d->dtype, d->head_dim, g.GH, paged, rd, p, grid, s) != cudaSuccess) return KVC_ERR_CUDA;
@@ -435,7 +478,9 @@ extern "C" {
 KVC_API size_t kvc_cache_bytes(const kvc_desc* d) {
     Geo g;
     if (check_desc(d, &g) != KVC_OK) return 0;
-    return (size_t)d->layers * 2 * (size_t)g.half_elems * g.elt;
+    const size_t rows = (size_t)d->layers * 2 * (size_t)(g.half_elems / d->head_dim);
+    // INT8: the codes, then one fp32 scale per row
+    return rows * d->head_dim * g.elt + (d->dtype == KVC_I8 ? rows * 4 : 0);
 }
 
 KVC_API size_t kvc_workspace_bytes(const kvc_desc* d) {
@@ -464,7 +509,7 @@ KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer, const void
     if (!cache || !k_new || !v_new || !pos || !workspace) return KVC_ERR_NULL;
     if (d->layout == KVC_LAYOUT_PAGED && !block_table) return KVC_ERR_NULL;
     if (!aligned16(cache) || !aligned16(workspace)) return KVC_ERR_ALIGN;
-    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & (uintptr_t)(g.elt - 1))
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & (uintptr_t)(g.act_elt - 1))
         return KVC_ERR_ALIGN;
     if (layer < 0 || layer >= d->layers || n_new < 1 || n_new > 0x7fffffff / 2) return KVC_ERR_ARG;
     const WorkspaceLayout w = ws_layout(d, g);
@@ -478,6 +523,12 @@ KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer, const void
     p.err = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + w.err);
     p.layer_off = (long long)layer * 2 * g.half_elems;
     p.kv_off = g.half_elems;
+    if (d->dtype == KVC_I8) {
+        const long long half_rows = g.half_elems / d->head_dim;
+        p.scales = reinterpret_cast<float*>(static_cast<char*>(cache) + (size_t)d->layers * 2 * (size_t)g.half_elems);
+        p.sc_layer_off = (long long)layer * 2 * half_rows;
+        p.sc_kv_off = half_rows;
+    }
     p.B = d->batch;
     p.Hkv = d->kv_heads;
     p.D = d->head_dim;
@@ -511,8 +562,8 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
     if (rc) return rc;
     if (!k_new || !v_new) return KVC_ERR_NULL;
     if (!aligned16(k_new) || !aligned16(v_new)) return KVC_ERR_ALIGN;
-    if (d->dtype == KVC_BF16 || d->layout == KVC_LAYOUT_PAGED) {
-        // no separate append launch: the decode kernel (bf16 ring / sink+ring)
+    if (d->dtype != KVC_F32 || d->layout == KVC_LAYOUT_PAGED) {
+        // no separate append launch: the decode kernel (bf16 / INT8 ring / sink+ring)
         // or the paged plan kernel writes the new token itself
         return decode_impl(d, cache, layer, q, k_new, v_new, pos, block_table, valid_bits, out, workspace,
                            workspace_bytes, stream);
@@ -585,6 +636,8 @@ KVC_API int kvc_block_prepare(const kvc_desc* d, void* cache, const int32_t* pos
     kvc::BlockParams p;
     if ((rc = block_params(d, g, workspace, workspace_bytes, &p))) return rc;
     p.cache = cache;
+    if (d->dtype == KVC_I8)
+        p.scales = reinterpret_cast<float*>(static_cast<char*>(cache) + (size_t)d->layers * 2 * (size_t)g.half_elems);
     p.pos = pos;
     p.table = block_table;
     p.valid = valid_bits;

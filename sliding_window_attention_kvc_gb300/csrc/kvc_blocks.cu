@@ -159,6 +159,12 @@ __global__ void __launch_bounds__(256) block_copy_kernel(const __grid_constant__
     const int n16 = c.z * p.D * (int)sizeof(Elt) / 16;   // 16-byte chunks of the rows to copy
     for (int k = threadIdx.x; k < n16; k += blockDim.x)
         reinterpret_cast<uint4*>(dst)[k] = reinterpret_cast<const uint4*>(src)[k];
+    if (p.scales) {                                      // INT8 cache: the rows' scales too
+        const long long rows_half = (long long)p.num_blocks * p.Hkv * p.bs;
+        const float* ss = p.scales + lk * rows_half + ((long long)c.x * p.Hkv + h) * p.bs;
+        float* sd = p.scales + lk * rows_half + ((long long)c.y * p.Hkv + h) * p.bs;
+        for (int k = threadIdx.x; k < c.z; k += blockDim.x) sd[k] = ss[k];
+    }
 }
 
 // One CTA per share entry: dst's logical blocks 0 .. nblocks-1 point at src's
@@ -253,8 +259,9 @@ cudaError_t launch_block_prepare(int elt, const BlockParams& p, cudaStream_t s) 
     e = cudaLaunchKernelEx(&cfg, block_prepare_kernel, p);
     if (e != cudaSuccess) return e;
     cfg = pdl_config(dim3(p.B, p.layers * 2 * p.Hkv), 256, s, &attr);
-    return elt == 4 ? cudaLaunchKernelEx(&cfg, block_copy_kernel<float>, p)
-                    : cudaLaunchKernelEx(&cfg, block_copy_kernel<__nv_bfloat16>, p);
+    return elt == 4   ? cudaLaunchKernelEx(&cfg, block_copy_kernel<float>, p)
+           : elt == 2 ? cudaLaunchKernelEx(&cfg, block_copy_kernel<__nv_bfloat16>, p)
+                      : cudaLaunchKernelEx(&cfg, block_copy_kernel<int8_t>, p);
 }
 
 cudaError_t launch_block_share(const BlockParams& p, int n, cudaStream_t s) {

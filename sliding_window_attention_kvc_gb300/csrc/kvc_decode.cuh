@@ -82,10 +82,16 @@ __device__ __forceinline__ int paged_block_rows(const int32_t* table_row, const 
     return lb == last ? (t - lb * bs + 1) : bs;
 }
 
+// n / d for n >= 0, d > 0: a 32-bit division when both fit.
+__device__ __forceinline__ long long div_nonneg(long long n, long long d) {
+    if (n >= 0 && n < 0x100000000LL && d > 0 && d < 0x100000000LL) return (long long)((unsigned)n / (unsigned)d);
+    return n / d;
+}
+
 // Share holding unit u of a stream-K partition of `total` units into
 // `shares` contiguous ranges [floor(x total / shares), floor((x + 1) total / shares)).
 __device__ __forceinline__ int streamk_share_of(long long u, long long total, int shares) {
-    return (int)(((u + 1) * shares - 1) / total);
+    return (int)div_nonneg((u + 1) * shares - 1, total);
 }
 
 __device__ __forceinline__ int clamp_paged_t(int t, int maxb, int bs) {

@@ -42,10 +42,10 @@
 
 namespace kvc {
 
-template <int D, bool READ>
+template <int D, bool READ, bool Q8 = false>
 struct MmaShape {
     static constexpr int kSub = 16;                           // rows per sub-tile
-    static constexpr int kBoxCols = 64;                       // bf16 columns per TMA box (128 bytes)
+    static constexpr int kBoxCols = Q8 ? 128 : 64;            // columns per TMA box row (128 bytes)
     static constexpr int kBoxes = D / kBoxCols;               // boxes per row of K (or V)
     static constexpr int kBoxBytes = kSub * 128;              // one 16-row box
     static constexpr int kSubBytes = kBoxes * kBoxBytes;      // K (or V) of one sub-tile
@@ -53,7 +53,12 @@ struct MmaShape {
     static constexpr int kTokenGroups = kConsumerWarps / kDsplit;
     static constexpr int kNsub = kTokenGroups;                // sub-tiles per stage (one per token group)
     static constexpr int kStageBytes = 2 * kNsub * kSubBytes; // K and V of kNsub sub-tiles
-    static constexpr int kStages = D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3);
+    static constexpr int kStages = Q8 ? (kQ8CtasPerSm >= 3 ? 3 : 5) : (D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3));
+    // INT8: row scales of each stage, one slot per sub-tile position (the
+    // first sub-tile of a copy holds that copy's K and V scales)
+    static constexpr int kScSlotBytes = Q8 ? 640 : 0;         // 2 x kScRunRows floats, 128-byte aligned
+    static constexpr int kScSlotFloats = kScSlotBytes / 4;
+    static constexpr int kScStageBytes = kNsub * kScSlotBytes;
     // READ_INCACHE rotation: a lane owns one 16-byte chunk pair (8 rotation
     // pairs) of kRowsPerLane rows of its warp's sub-tile
     static constexpr int kCpr = D / 16;                       // chunk pairs (i, i + D/2) per row
@@ -85,15 +90,18 @@ struct alignas(16) MmaStageMeta {
     int base[4];     // byte offset of each sub-tile's K rows (column block 0) in the stage
     int ld[4];       // rows of the copy the sub-tile belongs to: its K|V and column
                      // blocks lie 128 * ld bytes apart
+    int sbase[4];    // INT8: float index of the K scale of row 0 in the stage's scale area
+    int sld[4];      // INT8: floats from a K scale to the V scale of the same row
     MmaSegment seg;  // valid with kSegBegin
 };
 constexpr int kSegBegin = 1, kSegEnd = 2;
 
-template <int D, int GH, bool READ>
+template <int D, int GH, bool READ, bool Q8 = false>
 struct MmaSmem {
-    using S = MmaShape<D, READ>;
+    using S = MmaShape<D, READ, Q8>;
     static constexpr size_t kStage = 0;                                        // 1024-aligned stages
-    static constexpr size_t kBars = kStage + (size_t)S::kStages * S::kStageBytes;
+    static constexpr size_t kSc = kStage + (size_t)S::kStages * S::kStageBytes;  // INT8 row scales
+    static constexpr size_t kBars = kSc + (size_t)S::kStages * S::kScStageBytes;
     static constexpr size_t kMeta = kBars + 2 * S::kStages * sizeof(uint64_t);
     // READ_INCACHE: R(ip0 theta_i) of each sub-tile, [stage][sub][4][D/16][2] float2
     // (pair i = 8 cp + 2 jj + e at [jj][cp][e], so a lane's float4 loads are conflict-free)
@@ -308,19 +316,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
     }
 }
 
-template <int D, int GH, bool PAGED, bool READ>
+template <int D, int GH, bool PAGED, bool READ, bool Q8>
 // Two CTAs (ten warps) per SM: three warps share a sub-partition's 16K
 // registers, so a thread may hold at most 168.
-__global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
+__global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ? kQ8CtasPerSm : 2))
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ KvTensorMaps maps) {
-    using S = MmaShape<D, READ>;
-    using SM = MmaSmem<D, GH, READ>;
+    using S = MmaShape<D, READ, Q8>;
+    using SM = MmaSmem<D, GH, READ, Q8>;
+    static_assert(!(READ && Q8), "INT8 caches take no read-time RoPE");
+    static_assert(!Q8 || D >= 128, "INT8 rows are whole 128-byte column blocks");
     constexpr int NST = S::kStages, NSUB = S::kNsub, HALF = S::kHalf;
 
     extern __shared__ unsigned char smem_raw[];
     // the 128-byte swizzle pattern repeats every 1024 bytes: align the stages to it
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stage_base = smem + SM::kStage;
+    float* sc_base = reinterpret_cast<float*>(smem + SM::kSc);   // INT8: [stage][kScStageBytes / 4]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
     uint64_t* empty = full + NST;
     MmaStageMeta* meta = reinterpret_cast<MmaStageMeta*>(smem + SM::kMeta);
@@ -351,6 +362,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         mbar_fence_init();
 #pragma unroll
         for (int r = 0; r < kRunMaps; ++r) tma_prefetch_desc(&maps.run[r]);
+        if constexpr (Q8) {
+            tma_prefetch_desc(&maps.sc_run);
+            tma_prefetch_desc(&maps.sc_sub);
+        }
     }
     pdl_launch_dependents();    // the combine kernel may start launching
     __syncthreads();
@@ -475,10 +490,21 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                 meta[s].newrow[f] = (newrow >= lo && newrow < lo + 16) ? newrow - lo : -1;
                 meta[s].base[f] = run_off + lo * 128;
                 meta[s].ld[f] = R;
+                if constexpr (Q8) {
+                    // the run's scales land in the slot of its first sub-tile, from
+                    // row urow rounded down to a multiple of 4
+                    meta[s].sbase[f] = fill * S::kScSlotFloats + (int)(urow & 3) + lo;
+                    meta[s].sld[f] = kScRunRows;
+                }
             }
             if (lane == 0) {
                 unsigned char* dst = stage_base + (size_t)s * S::kStageBytes + run_off;
                 const CUtensorMap* map = &maps.run[nsr - 1];
+                if constexpr (Q8) {
+                    mbar_expect_tx(&full[s], (uint32_t)(2 * kScRunRows * 4));
+                    tma_load_3d(sc_base + (size_t)s * (S::kScStageBytes / 4) + fill * S::kScSlotFloats, &maps.sc_run,
+                                (int)(urow & ~3LL), 0, p.layer, &full[s]);
+                }
                 mbar_expect_tx(&full[s], (uint32_t)(S::kBoxes * 2 * R * 128));
                 if (p.tma_whole) {
                     tma_load_5d(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s]);
@@ -503,6 +529,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             meta[s].newrow[f] = -1;
             meta[s].base[f] = run_off + rank * kSubCopy;
             meta[s].ld[f] = 16;
+            if constexpr (Q8) {
+                meta[s].sbase[f] = f * S::kScSlotFloats + (int)(urow & 3);
+                meta[s].sld[f] = kScSubRows;
+                mbar_expect_tx(&full[s], (uint32_t)(2 * kScSubRows * 4));
+                tma_load_3d(sc_base + (size_t)s * (S::kScStageBytes / 4) + f * S::kScSlotFloats, &maps.sc_sub,
+                            (int)(urow & ~3LL), 0, p.layer, &full[s]);
+            }
             unsigned char* dst = stage_base + (size_t)s * S::kStageBytes + run_off + rank * kSubCopy;
             mbar_expect_tx(&full[s], (uint32_t)kSubCopy);
             if (p.tma_whole) {
@@ -528,9 +561,18 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                 return (nl > 0 ? (nl + 15) / 16 : 1) + kSeqUnits;
             };
             long long total = 0;
+            // up to 32 sequences: each lane keeps its own sequence's figures from
+            // this first pass (one read of the positions)
+            int c_tb = 0, c_nl = 0;
+            long long c_st = 0;
             for (int base = 0; base < p.B; base += 32) {
                 int tb = 0, nl = 0;
                 long long st = seq_tiles(base + lane, &tb, &nl);
+                if (base == 0) {
+                    c_tb = tb;
+                    c_nl = nl;
+                    c_st = st;
+                }
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) st += __shfl_xor_sync(0xffffffffu, st, off);
                 total += st;
@@ -539,12 +581,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             // sequence's partial count is exactly the shares it overlaps
             const int G = (int)(total < p.nsplit ? total : p.nsplit);
             for (int xs = claim(G); xs < G && ok; xs = claim(G)) {
-            const long long lo = (long long)xs * total / G;
-            const long long hi = (long long)(xs + 1) * total / G;
+            const long long lo = div_nonneg((long long)xs * total, G);
+            const long long hi = div_nonneg((long long)(xs + 1) * total, G);
             long long run = 0;
             for (int base = 0; base < p.B && ok && run < hi; base += 32) {
-                int tb = 0, nl = 0;
-                const long long st = seq_tiles(base + lane, &tb, &nl);
+                int tb = c_tb, nl = c_nl;
+                const long long st = p.B <= 32 ? c_st : seq_tiles(base + lane, &tb, &nl);
                 long long incl = st;
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
@@ -579,7 +621,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                     // (fused append) the row that receives the new K/V
                     int h_slot = 0;
                     if (t_b >= 0)
-                        h_slot = t_b < p.sinks ? t_b : p.sinks + (int)(((long long)t_b - p.sinks) % p.window);
+                        h_slot = t_b < p.sinks ? t_b : p.sinks + (int)((unsigned)(t_b - p.sinks) % (unsigned)p.window);
                     // READ_INCACHE: in-cache positions run on by one per slot between
                     // the sink/window boundary and the ring's wrap; they (and their
                     // angles) are computed afresh at those points and every 32 runs
@@ -786,6 +828,13 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
     const int hd = warp % S::kDsplit;     // which half of the output columns (D = 256)
     const int g = lane >> 2, c = lane & 3;
     constexpr int NCT = kConsumerWarps * 32;
+    // INT8 column order of Q K^T: k-step ks of lane c takes columns
+    // q8_col0(ks) .. + 3 (k-slots 2c, 2c + 1, 2c + 8, 2c + 9) -- any order of the
+    // summed columns will do, as long as q and K use the same one
+    auto q8_col0 = [&](int ks) {
+        const int k2 = ks >> 1;
+        return 128 * (k2 >> 2) + 16 * ((k2 & 3) + ((c >> 1) << 2)) + 8 * (c & 1) + 4 * (ks & 1);
+    };
     BoundedBarrier csync{&cbar[0], 0u};           // the four compute warps
     BoundedBarrier psync{&cbar[1 + (tg & 1)], 0u}; // the two warps sharing a sub-tile (head_dim 256)
 
@@ -819,6 +868,12 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
     uint32_t qa[S::kKsteps][2];
     float o[S::kNt][4];
     float m_run = -INFINITY, l_run = 0.f;
+    // INT8: fp16 tensor-core inputs.  q enters as q * q_scale * 2^-k (per head,
+    // k >= 0 keeping it below 2^14: qexp = 2^k returns in the scores); a row's
+    // weight enters as p * s_v / S_run, S_run the largest V scale of the segment
+    // so far (the accumulator is rescaled when it grows and multiplied back at
+    // the end), so weights stay in [0, 1]
+    float qexp = 1.f, S_run = 0.f;
 
     // q of sequence seg.b as mma A fragments: row g = q head (zero for g >= GH),
     // per k-step columns 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1); rotated,
@@ -834,6 +889,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                 set_error(p.err, 0x4u);
             if (READ) qpos = min(seg.t, p.capacity - 1);
         }
+        const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
+                                    ((long long)seg.b * p.Hq + kvh * p.G + z * GH + g) * D;
         csync.sync(p.err);                      // everyone is done with the previous qcs
         if (p.rope != kRopeNone) {
             for (int i = ctid; i < HALF; i += NCT) {
@@ -844,9 +901,30 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         }
         csync.sync(p.err);
         float qf[S::kKsteps][4];
-        if (g < GH) {
-            const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(p.q) +
-                                        ((long long)seg.b * p.Hq + kvh * p.G + z * GH + g) * D;
+        if (Q8 && g < GH) {
+            // INT8: k-step ks takes columns q8_col0(ks) .. + 3 (see the Q K^T
+            // product); each value is rotated with its pair column
+#pragma unroll
+            for (int ks = 0; ks < S::kKsteps; ++ks) {
+                const int d0 = q8_col0(ks);
+                const uint2 w = *reinterpret_cast<const uint2*>(qrow + d0);
+                float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                              __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u)};
+                if (p.rope != kRopeNone) {
+                    const uint2 wp = *reinterpret_cast<const uint2*>(qrow + (d0 < HALF ? d0 + HALF : d0 - HALF));
+                    const float y[4] = {__uint_as_float(wp.x << 16), __uint_as_float(wp.x & 0xffff0000u),
+                                        __uint_as_float(wp.y << 16), __uint_as_float(wp.y & 0xffff0000u)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 cs = qcs[(d0 + e) % HALF];
+                        // column i < D/2: x cos - x' sin; column i + D/2: x' sin + x cos
+                        x[e] = d0 < HALF ? x[e] * cs.x - y[e] * cs.y : y[e] * cs.y + x[e] * cs.x;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) qf[ks][e] = x[e];
+            }
+        } else if (g < GH) {
 #pragma unroll
             for (int ks = 0; ks < S::kKsteps; ++ks) {
                 const uint32_t lo = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c);
@@ -873,10 +951,31 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
 #pragma unroll
             for (int ks = 0; ks < S::kKsteps; ++ks) qf[ks][0] = qf[ks][1] = qf[ks][2] = qf[ks][3] = 0.f;
         }
+        if constexpr (Q8) {
+            float amax = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < S::kKsteps; ++ks) {
-            qa[ks][0] = pack_bf16x2(qf[ks][0] * p.q_scale, qf[ks][1] * p.q_scale);
-            qa[ks][1] = pack_bf16x2(qf[ks][2] * p.q_scale, qf[ks][3] * p.q_scale);
+            for (int ks = 0; ks < S::kKsteps; ++ks)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qf[ks][e] * p.q_scale));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            int ex = 0;
+            frexpf(amax, &ex);                        // amax < 2^ex
+            const int k = ex > 14 ? ex - 14 : 0;
+            qexp = ldexpf(1.f, k);
+            const float qs = ldexpf(p.q_scale, -k);
+#pragma unroll
+            for (int ks = 0; ks < S::kKsteps; ++ks) {
+                qa[ks][0] = pack_f16x2(qf[ks][0] * qs, qf[ks][1] * qs);
+                qa[ks][1] = pack_f16x2(qf[ks][2] * qs, qf[ks][3] * qs);
+            }
+            S_run = 0.f;
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < S::kKsteps; ++ks) {
+                qa[ks][0] = pack_bf16x2(qf[ks][0] * p.q_scale, qf[ks][1] * p.q_scale);
+                qa[ks][1] = pack_bf16x2(qf[ks][2] * p.q_scale, qf[ks][3] * p.q_scale);
+            }
         }
 #pragma unroll
         for (int j = 0; j < S::kNt; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -898,10 +997,19 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
         csync.sync(p.err);                     // merge buffers free (previous segment done with them)
         if (g < GH) {
             float* mo = merge_o + (tg * GH + g) * D;
+            if constexpr (Q8) {
+                // INT8: output tile j, column n of it is column hd * 128 + 16 n + j
 #pragma unroll
-            for (int j = 0; j < S::kNt; ++j) {
-                const int col = (hd * S::kNt + j) * 8 + 2 * c;
-                *reinterpret_cast<float2*>(mo + col) = make_float2(o[j][0], o[j][1]);
+                for (int j = 0; j < S::kNt; ++j) {
+                    mo[hd * S::kDl + 32 * c + j] = o[j][0] * S_run;
+                    mo[hd * S::kDl + 32 * c + 16 + j] = o[j][1] * S_run;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < S::kNt; ++j) {
+                    const int col = (hd * S::kNt + j) * 8 + 2 * c;
+                    *reinterpret_cast<float2*>(mo + col) = make_float2(o[j][0], o[j][1]);
+                }
             }
             if (c == 0 && hd == 0) merge_ml[tg * GH + g] = make_float2(m_run, lq);
         }
@@ -995,13 +1103,48 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                 // token being decoded.  Write its K (RoPE baked at t when BAKED) and V
                 // to the cache, and over the stale row just copied into shared memory.
                 const int nr = meta[s].newrow[tg];
-                if (nr >= 0) {
+                if (Q8 && nr >= 0) {
+                    if (hd == 0) {
+                        // INT8: quantise the new rows; codes and scales go to the cache
+                        // and over the stale copies in shared memory
+                        const long long unit = (long long)seg.b * p.Hkv + kvh;
+                        const int h_slot = seg.t < p.sinks ? seg.t
+                                                           : p.sinks + (int)((unsigned)(seg.t - p.sinks) % (unsigned)p.window);
+                        const long long row = unit * p.capacity + h_slot;
+                        int8_t* kg = const_cast<int8_t*>(static_cast<const int8_t*>(p.cache)) + p.layer_off + row * D;
+                        float* ksg = p.scales + p.sc_layer_off + row;
+                        int8_t kq[D / 32], vq[D / 32];
+                        float sk, sv;
+                        q8_store_token_warp<D / 64>(static_cast<const __nv_bfloat16*>(p.k_new) + unit * D,
+                                                    static_cast<const __nv_bfloat16*>(p.v_new) + unit * D, kg,
+                                                    kg + p.kv_off, ksg, ksg + p.sc_kv_off, p.rope, seg.t, p.theta,
+                                                    lane, kq, vq, &sk, &sv);
+#pragma unroll
+                        for (int m = 0; m < D / 64; ++m) {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int col = lane + 32 * m + e * HALF;
+                                const int off = (col >> 7) * bstride + nr * 128 +
+                                                ((((col & 127) >> 4) ^ (nr & 7)) << 4) + (col & 15);
+                                Ks[off] = (unsigned char)kq[2 * m + e];
+                                Vs[off] = (unsigned char)vq[2 * m + e];
+                            }
+                        }
+                        if (lane == 0) {
+                            float* scl = sc_base + (size_t)s * (S::kScStageBytes / 4) + meta[s].sbase[tg];
+                            scl[nr] = sk;
+                            scl[meta[s].sld[tg] + nr] = sv;
+                        }
+                    }
+                    wrote = true;
+                    if constexpr (S::kDsplit == 2) psync.sync(p.err); else __syncwarp();
+                } else if (nr >= 0) {
                     if (hd == 0) {
                         const long long unit = (long long)seg.b * p.Hkv + kvh;
                         const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(p.k_new) + unit * D;
                         const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(p.v_new) + unit * D;
                         const int h_slot = seg.t < p.sinks ? seg.t
-                                                           : p.sinks + (int)(((long long)seg.t - p.sinks) % p.window);
+                                                           : p.sinks + (int)((unsigned)(seg.t - p.sinks) % (unsigned)p.window);
                         __nv_bfloat16* kg = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(p.cache)) +
                                             p.layer_off + (unit * p.capacity + h_slot) * D;
                         __nv_bfloat16* vg = kg + p.kv_off;
@@ -1081,8 +1224,9 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
                 wrote = true;
                 if constexpr (S::kDsplit == 2) psync.sync(p.err); else __syncwarp();
             }
-            if (nrows < S::kSub) {
+            if (!Q8 && nrows < S::kSub) {
                 // rows past nrows may hold anything (NaN): zero this warp's V columns there
+                // (INT8 codes are always finite; their weights are zeroed instead)
                 constexpr int BPW = S::kBoxes / S::kDsplit;
                 const int per_box = (S::kSub - nrows) * 8;
                 for (int idx = lane; idx < per_box * BPW; idx += 32) {
@@ -1097,7 +1241,49 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
 
             // ---- S = Q K^T over the 16 rows: two 8-token n-tiles --------------
             float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
+            uint4 vw[2][2];          // INT8: V code chunks of tokens 2c, 2c + 1, 2c + 8, 2c + 9
+            if constexpr (Q8) {
+                // INT8: lane (g, c) reads 8 code bytes of rows g and g + 8 at columns
+                // q8_col0(2 k2) .. + 7 and turns them into the B fragments of k-steps
+                // 2 k2 and 2 k2 + 1 (the 16-byte chunks k2 mod 4 and k2 mod 4 + 4 of a
+                // 128-column block: a half-warp's reads fall on 8 distinct chunks)
+                uint2 kw[D / 32][2];
+#pragma unroll
+                for (int k2 = 0; k2 < D / 32; ++k2) {
+                    const int ch = (k2 & 3) + ((c >> 1) << 2);
+                    const int off = (k2 >> 2) * bstride + ((ch ^ (g & 7)) << 4) + ((c & 1) << 3);
+                    kw[k2][0] = *reinterpret_cast<const uint2*>(Ks + off + g * 128);
+                    kw[k2][1] = *reinterpret_cast<const uint2*>(Ks + off + (g + 8) * 128);
+                }
+                // the V chunks P V will need, loaded now so that their latency hides
+                // behind Q K^T and the softmax
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int ta = 2 * c + 8 * hlf;          // tokens ta, ta + 1 -> B register hlf
+                    vw[hlf][0] = *reinterpret_cast<const uint4*>(Vs + hd * bstride + ta * 128 + ((g ^ (ta & 7)) << 4));
+                    vw[hlf][1] = *reinterpret_cast<const uint4*>(Vs + hd * bstride + (ta + 1) * 128 +
+                                                                 ((g ^ ((ta + 1) & 7)) << 4));
+                }
+                float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int k2 = 0; k2 < D / 32; ++k2) {
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const uint32_t a = (s2 ? kw[k2][0].y : kw[k2][0].x) ^ 0x80808080u;
+                        const uint32_t e = (s2 ? kw[k2][1].y : kw[k2][1].x) ^ 0x80808080u;
+                        const int ks = 2 * k2 + s2;
+                        float (&acc)[2][4] = (kQ8SplitChains && s2) ? sb : sa;
+                        mma_f16_16816(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, q8_f16x2(a, 0x4140u), q8_f16x2(a, 0x4342u));
+                        mma_f16_16816(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, q8_f16x2(e, 0x4140u), q8_f16x2(e, 0x4342u));
+                    }
+                }
+                if constexpr (kQ8SplitChains) {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sa[i][e] += sb[i][e];
+                }
+            } else {
                 const int tok = ((lane >> 4) << 3) + (lane & 7);
                 const int chs = (lane >> 3) & 1;
 #pragma unroll
@@ -1114,6 +1300,19 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             // ---- online softmax on row g (this lane's q head) ----------------
             float sv[4] = {sa[0][0], sa[0][1], sa[1][0], sa[1][1]};
             const int tk0 = 2 * c;
+            float vsc[4] = {1.f, 1.f, 1.f, 1.f};
+            if constexpr (Q8) {
+                // scores of a row times its K scale; its V scale goes into the
+                // weight (zero past nrows, whose scales may be anything)
+                const float* scl = sc_base + (size_t)s * (S::kScStageBytes / 4) + meta[s].sbase[tg];
+                const float* vscl = scl + meta[s].sld[tg];
+                const int tk[4] = {tk0, tk0 + 1, tk0 + 8, tk0 + 9};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sv[e] *= scl[tk[e]] * qexp;
+                    vsc[e] = tk[e] < nrows ? vscl[tk[e]] : 0.f;
+                }
+            }
             if (tk0 >= nrows) sv[0] = -INFINITY;
             if (tk0 + 1 >= nrows) sv[1] = -INFINITY;
             if (tk0 + 8 >= nrows) sv[2] = -INFINITY;
@@ -1128,18 +1327,56 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
             for (int e = 0; e < 4; ++e) pe[e] = (sv[e] == -INFINITY || g >= GH) ? 0.f : exp2f(sv[e] - mn);
             l_run = l_run * alpha + ((pe[0] + pe[1]) + (pe[2] + pe[3]));
             m_run = mn;
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            float ofac = alpha;
+            uint32_t pa0, pa2;
+            if constexpr (Q8) {
+                // the 16 rows' largest V scale (lanes of one c share their rows)
+                float smax = fmaxf(fmaxf(vsc[0], vsc[1]), fmaxf(vsc[2], vsc[3]));
+                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
+                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
+                if (smax > S_run) {
+                    ofac *= S_run / smax;
+                    S_run = smax;
+                }
+                const float rS = S_run > 0.f ? __frcp_rn(S_run) : 0.f;
+                pa0 = pack_f16x2(pe[0] * vsc[0] * rS, pe[1] * vsc[1] * rS);
+                pa2 = pack_f16x2(pe[2] * vsc[2] * rS, pe[3] * vsc[3] * rS);
+            } else {
+                pa0 = pack_bf16x2(pe[0], pe[1]);
+                pa2 = pack_bf16x2(pe[2], pe[3]);
+            }
+            if (__any_sync(0xffffffffu, ofac != 1.f)) {
 #pragma unroll
                 for (int j = 0; j < S::kNt; ++j) {
-                    o[j][0] *= alpha;
-                    o[j][1] *= alpha;
+                    o[j][0] *= ofac;
+                    o[j][1] *= ofac;
                 }
             }
-            const uint32_t pa0 = pack_bf16x2(pe[0], pe[1]);
-            const uint32_t pa2 = pack_bf16x2(pe[2], pe[3]);
 
             // ---- O += P V over this warp's output columns ---------------------
-            {
+            if constexpr (Q8) {
+                // INT8: lane (g, c) reads 16 code bytes (columns hd * 128 + 16 g .. + 15)
+                // of tokens 2c, 2c + 1, 2c + 8, 2c + 9 (loaded with K, in vw); output
+                // tile j takes byte j.  Bytes of the two tokens of a register are
+                // interleaved first.
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const uint32_t a0 = (q4 == 0 ? vw[0][0].x : q4 == 1 ? vw[0][0].y : q4 == 2 ? vw[0][0].z : vw[0][0].w) ^ 0x80808080u;
+                    const uint32_t b0 = (q4 == 0 ? vw[0][1].x : q4 == 1 ? vw[0][1].y : q4 == 2 ? vw[0][1].z : vw[0][1].w) ^ 0x80808080u;
+                    const uint32_t a1 = (q4 == 0 ? vw[1][0].x : q4 == 1 ? vw[1][0].y : q4 == 2 ? vw[1][0].z : vw[1][0].w) ^ 0x80808080u;
+                    const uint32_t b1 = (q4 == 0 ? vw[1][1].x : q4 == 1 ? vw[1][1].y : q4 == 2 ? vw[1][1].z : vw[1][1].w) ^ 0x80808080u;
+                    // [a0 b0 a1 b1] and [a2 b2 a3 b3] of the two token rows
+                    const uint32_t lo0 = __byte_perm(a0, b0, 0x5140u), hi0 = __byte_perm(a0, b0, 0x7362u);
+                    const uint32_t lo1 = __byte_perm(a1, b1, 0x5140u), hi1 = __byte_perm(a1, b1, 0x7362u);
+#pragma unroll
+                    for (int jb = 0; jb < 4; ++jb) {
+                        const int j = 4 * q4 + jb;
+                        const uint32_t w0 = jb < 2 ? lo0 : hi0, w1 = jb < 2 ? lo1 : hi1;
+                        const uint32_t sel = (jb & 1) ? 0x4342u : 0x4140u;
+                        mma_f16_16816(o[j], pa0, 0u, pa2, 0u, q8_f16x2(w0, sel), q8_f16x2(w1, sel));
+                    }
+                }
+            } else {
                 const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
                 const int chs = lane >> 4;
 #pragma unroll
@@ -1161,10 +1398,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : 2)
     }
 }
 
-template <int D, int GH, bool PAGED, bool READ>
+template <int D, int GH, bool PAGED, bool READ, bool Q8>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps, dim3 grid, cudaStream_t stream) {
-    using SM = MmaSmem<D, GH, READ>;
-    auto kern = decode_mma_kernel<D, GH, PAGED, READ>;
+    using SM = MmaSmem<D, GH, READ, Q8>;
+    // the resident CTAs per SM that __launch_bounds__ plans for must fit in
+    // shared memory (228 KB per SM, 1 KB of it reserved per CTA)
+    constexpr int kCtasPerSm = (READ && D >= 256) ? 1 : (Q8 ? kQ8CtasPerSm : 2);
+    static_assert(kCtasPerSm * (SM::kTotal + 1024) <= 233472, "shared memory for the planned CTAs per SM");
+    auto kern = decode_mma_kernel<D, GH, PAGED, READ, Q8>;
     // few (sequence, kv head, group) units: narrow column chunks, more CTAs each
     const long long units = (long long)p.B * p.Hkv * p.nsub;
     const bool narrow = units * (D / 16) <= 1216;

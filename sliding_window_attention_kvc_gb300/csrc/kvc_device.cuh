@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -209,6 +210,126 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// INT8 cache rows ([primer] 5.1, quantised cache).  Each stored row (one
+// token's K or V for one kv head) keeps an fp32 scale s = max|x| / 127 and
+// codes c = rint(x / s) clamped to +-127 (IEEE fp32 quotients, nearest, ties
+// to even); it reads back as c * s.  A zero row keeps s = 0 and zero codes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int q8_code(float x, float s) {
+    if (!(s > 0.f)) return 0;
+    const float r = rintf(__fdiv_rn(x, s));
+    return (int)fminf(fmaxf(r, -127.f), 127.f);
+}
+
+// Warp-wide quantisation of one row whose N values per lane are x: returns
+// the row's scale (to every lane) and the lane's codes.
+template <int N>
+__device__ __forceinline__ float q8_quantize_lane(const float (&x)[N], int8_t (&c)[N]) {
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < N; ++k) a = fmaxf(a, fabsf(x[k]));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    const float s = __fdiv_rn(a, 127.f);
+#pragma unroll
+    for (int k = 0; k < N; ++k) c[k] = (int8_t)q8_code(x[k], s);
+    return s;
+}
+
+// One warp stores one token's K row (rotated at `pos` with baked RoPE) and V
+// row of one kv head: bf16 sources kr / vr [D], code rows kc / vc, scales
+// *ks / *vs.  Lane l handles the rotation pairs i = l + 32 m (columns i and
+// i + D/2, NP = D / 64 pairs); its codes come back in kq / vq as
+// [2m] = column i, [2m + 1] = column i + D/2, and the scales in sk / sv.
+template <int NP>
+__device__ __forceinline__ void q8_store_token_warp(const __nv_bfloat16* kr, const __nv_bfloat16* vr, int8_t* kc,
+                                                    int8_t* vc, float* ks, float* vs, int rope, long long pos,
+                                                    const unsigned long long* theta, int lane,
+                                                    int8_t (&kq)[2 * NP], int8_t (&vq)[2 * NP], float* sk,
+                                                    float* sv) {
+    constexpr int HALF = 32 * NP;
+    float kx[2 * NP], vx[2 * NP];
+#pragma unroll
+    for (int m = 0; m < NP; ++m) {
+        const int i = lane + 32 * m;
+        float x1 = __bfloat162float(kr[i]), x2 = __bfloat162float(kr[i + HALF]);
+        if (rope == 1 /* baked */) {
+            float c, s;
+            rope_cos_sin(pos, theta[i], &c, &s);
+            const float y1 = x1 * c - x2 * s, y2 = x1 * s + x2 * c;
+            x1 = y1;
+            x2 = y2;
+        }
+        kx[2 * m] = x1;
+        kx[2 * m + 1] = x2;
+        vx[2 * m] = __bfloat162float(vr[i]);
+        vx[2 * m + 1] = __bfloat162float(vr[i + HALF]);
+    }
+    *sk = q8_quantize_lane<2 * NP>(kx, kq);
+    *sv = q8_quantize_lane<2 * NP>(vx, vq);
+#pragma unroll
+    for (int m = 0; m < NP; ++m) {
+        const int i = lane + 32 * m;
+        kc[i] = kq[2 * m];
+        kc[i + HALF] = kq[2 * m + 1];
+        vc[i] = vq[2 * m];
+        vc[i + HALF] = vq[2 * m + 1];
+    }
+    if (lane == 0) {
+        *ks = *sk;
+        *vs = *sv;
+    }
+}
+
+// Two codes -> one register of two bf16 (lo: byte ka of a, hi: byte kb of
+// b), exact.  a and b are code words with 0x80 xor-ed into every byte, so a
+// byte holds c + 128; placed under the exponent of 2^23 it reads as the fp32
+// 2^23 + 128 + c, from which 2^23 + 128 is subtracted.
+__device__ __forceinline__ uint32_t q8_pair_bf16x2(uint32_t a, int ka, uint32_t b, int kb) {
+    const float fa = __int_as_float(__byte_perm(a, 0x4B000000u, 0x7540u | (uint32_t)ka));
+    const float fb = __int_as_float(__byte_perm(b, 0x4B000000u, 0x7540u | (uint32_t)kb));
+    const float2 f = __fadd2_rn(make_float2(fa, fb), make_float2(-8388736.f, -8388736.f));
+    return pack_bf16x2(f.x, f.y);
+}
+
+// D = A * B + D, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> one register of two fp16 (lo = first), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Two codes -> one register of two fp16, exact.  w holds codes with 0x80
+// xor-ed into every byte (a byte is c + 128); sel picks the bytes for the
+// low and high halves into byte positions 0 and 2 and 0x64 into 1 and 3
+// (0x4140: bytes 0 and 1 of w; 0x4342: bytes 2 and 3).  0x64uu is the fp16
+// 1024 + uu, from which 1024 + 128 is subtracted.
+__device__ __forceinline__ uint32_t q8_f16x2(uint32_t w, uint32_t sel) {
+    uint32_t x = __byte_perm(w, 0x64646464u, sel);
+    __half2 h = *reinterpret_cast<const __half2*>(&x);
+    h = __hsub2(h, __half2half2(__ushort_as_half((unsigned short)0x6480u)));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 3-D box load (TMA) at element coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];"
+        ::"r"(smem_u32(dst_smem)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
 }
 
 }  // namespace kvc

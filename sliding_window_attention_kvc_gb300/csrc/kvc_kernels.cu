@@ -45,6 +45,28 @@ __device__ __forceinline__ void write_token_rows(Elt* kc, long long kv_off, long
     }
 }
 
+// INT8 cache ([primer] 5.1, quantised cache): one warp per kv head stores
+// the token's K (RoPE baked at `pos`) and V rows as codes and row scales.
+// kc: K codes of kv head 0; ksc: its K scale; heads head_stride codes and
+// sc_head_stride scales apart; V kv_off codes and sc_kv_off scales further.
+template <int NP>
+__device__ __forceinline__ void q8_write_token_rows(int8_t* kc, long long kv_off, long long head_stride, float* ksc,
+                                                    long long sc_kv_off, long long sc_head_stride,
+                                                    const __nv_bfloat16* ks, const __nv_bfloat16* vs, int Hkv,
+                                                    int rope, long long pos, const unsigned long long* theta) {
+    constexpr int D = 64 * NP;
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int h = threadIdx.x >> 5; h < Hkv; h += nw) {
+        int8_t kq[2 * NP], vq[2 * NP];
+        float sk, sv;
+        int8_t* kd = kc + h * head_stride;
+        float* sd = ksc + h * sc_head_stride;
+        q8_store_token_warp<NP>(ks + (long long)h * D, vs + (long long)h * D, kd, kd + kv_off, sd, sd + sc_kv_off,
+                                rope, pos, theta, lane, kq, vq, &sk, &sv);
+    }
+}
+
+// Elt: the cache's element type; int8_t = INT8 cache, fed bf16 rows.
 template <typename Elt>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
     const int i_tok = blockIdx.x, b = blockIdx.y;
@@ -76,18 +98,33 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
         row_base = ((long long)phys * p.Hkv * p.bs + (pos % p.bs)) * D;
         head_stride = (long long)p.bs * D;
     }
-    Elt* kc = static_cast<Elt*>(p.cache) + p.layer_off + row_base;
-    const Elt* ks = static_cast<const Elt*>(p.k_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
-    const Elt* vs = static_cast<const Elt*>(p.v_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
-    write_token_rows<Elt>(kc, p.kv_off, head_stride, ks, vs, p.Hkv, D, p.rope, pos, p.theta);
+    if constexpr (sizeof(Elt) == 1) {
+        int8_t* kc = static_cast<int8_t*>(p.cache) + p.layer_off + row_base;
+        float* sc = p.scales + p.sc_layer_off + row_base / D;
+        const __nv_bfloat16* ks = static_cast<const __nv_bfloat16*>(p.k_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
+        const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(p.v_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
+        if (D == 128)
+            q8_write_token_rows<2>(kc, p.kv_off, head_stride, sc, p.sc_kv_off, head_stride / D, ks, vs, p.Hkv, p.rope,
+                                   pos, p.theta);
+        else
+            q8_write_token_rows<4>(kc, p.kv_off, head_stride, sc, p.sc_kv_off, head_stride / D, ks, vs, p.Hkv, p.rope,
+                                   pos, p.theta);
+    } else {
+        Elt* kc = static_cast<Elt*>(p.cache) + p.layer_off + row_base;
+        const Elt* ks = static_cast<const Elt*>(p.k_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
+        const Elt* vs = static_cast<const Elt*>(p.v_new) + ((long long)b * p.n_new + i_tok) * p.Hkv * D;
+        write_token_rows<Elt>(kc, p.kv_off, head_stride, ks, vs, p.Hkv, D, p.rope, pos, p.theta);
+    }
 }
 
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream) {
     dim3 grid(p.n_new, p.B);
     if (dtype == 0)
         append_kernel<float><<<grid, 256, 0, stream>>>(p);
-    else
+    else if (dtype == 1)
         append_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+    else
+        append_kernel<int8_t><<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -180,6 +217,20 @@ __device__ __forceinline__ void plan_pdl_launch() { asm volatile("griddepcontrol
 
 // The step's new token (kvc_decode_step) of sequence b at position traw, to
 // row traw mod bs of logical block traw / bs.
+// INT8 cache: the new token's rows at element row_base of the layer's K half.
+// Kept out of line: inlined, it slowed the bf16 plan kernel by several us.
+__device__ __noinline__ void plan_append_q8(const PlanParams& p, long long row_base, long long tok, int traw) {
+    int8_t* kc = static_cast<int8_t*>(p.cache) + p.layer_off + row_base;
+    float* sc = p.scales + p.sc_layer_off + row_base / p.D;
+    const __nv_bfloat16* ks = static_cast<const __nv_bfloat16*>(p.k_new) + tok;
+    const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(p.v_new) + tok;
+    const long long hs = (long long)p.bs * p.D;
+    if (p.D == 128)
+        q8_write_token_rows<2>(kc, p.kv_off, hs, sc, p.sc_kv_off, p.bs, ks, vs, p.Hkv, p.rope, traw, p.theta);
+    else
+        q8_write_token_rows<4>(kc, p.kv_off, hs, sc, p.sc_kv_off, p.bs, ks, vs, p.Hkv, p.rope, traw, p.theta);
+}
+
 __device__ __forceinline__ void plan_append(const PlanParams& p, int b, int traw, int known_phys = -2) {
     if (!p.k_new || traw < 0) return;
     const long long lb = traw / p.bs;
@@ -194,7 +245,9 @@ __device__ __forceinline__ void plan_append(const PlanParams& p, int b, int traw
     }
     const long long row_base = ((long long)phys * p.Hkv * p.bs + (traw % p.bs)) * p.D;
     const long long tok = (long long)b * p.Hkv * p.D;
-    if (p.elt == 4)
+    if (p.elt == 1)
+        plan_append_q8(p, row_base, tok, traw);
+    else if (p.elt == 4)
         write_token_rows<float>(static_cast<float*>(p.cache) + p.layer_off + row_base, p.kv_off,
                                 (long long)p.bs * p.D, static_cast<const float*>(p.k_new) + tok,
                                 static_cast<const float*>(p.v_new) + tok, p.Hkv, p.D, p.rope, traw, p.theta);

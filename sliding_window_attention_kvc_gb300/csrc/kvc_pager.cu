@@ -178,6 +178,7 @@ KVC_API int kvc_pagein_issue(kvc_pager* pg, const kvc_desc* d, void* cache, cons
                              void* compute_stream) {
     if (!pg || !d) return KVC_ERR_NULL;
     if (d->layout != KVC_LAYOUT_PAGED) return KVC_ERR_DESC;
+    if (d->dtype == KVC_I8) return KVC_ERR_UNSUPPORTED;   // host blocks hold no row scales
     if (n < 0) return KVC_ERR_ARG;
     if (n > 0 && (!cache || !host_kv || !in_block || !in_slot)) return KVC_ERR_NULL;
     int dev = 0;

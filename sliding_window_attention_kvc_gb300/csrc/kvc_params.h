@@ -26,6 +26,12 @@ constexpr int kPagedShareBatch = 8;
 // partial write), besides one unit per 16 rows.
 constexpr int kSeqUnits = 4;
 constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
+// INT8 caches: resident CTAs per SM of the decode kernel (its stages are half
+// the bytes of bf16 ones), and whether Q K^T accumulates even and odd k-steps
+// in separate registers (two shorter dependency chains)
+constexpr int kQ8CtasPerSm = 2;
+constexpr bool kQ8SplitChains = false;
+constexpr int kStreamCtasQ8 = 152 * kQ8CtasPerSm;
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
 enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
@@ -71,6 +77,9 @@ struct DecodeParams {
     const int2* cta_items;      // PAGED plan: first item, item count of each CTA (stream-K kernel)
     long long layer_off;        // elements from cache base to this layer's K half
     long long kv_off;           // elements from the K half to the V half
+    float* scales;              // INT8 cache: row scales [layers][K|V][rows of a half]; else null
+    long long sc_layer_off;     // INT8: scales from `scales` to this layer's K half
+    long long sc_kv_off;        // INT8: scales from the K half to the V half (rows of a half)
     int layer;
     int B, Hq, Hkv, G, nsub;
     int window, sinks, capacity;
@@ -103,6 +112,8 @@ struct PlanParams {
     const void* k_new;    // [B, Hkv, D] pre-RoPE
     const void* v_new;
     long long layer_off, kv_off;
+    float* scales;        // INT8 cache (elt 1): row scales; sc_layer_off / sc_kv_off as in DecodeParams
+    long long sc_layer_off, sc_kv_off;
     int Hkv, D, rope, elt;
     unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
 };
@@ -116,6 +127,8 @@ struct AppendParams {
     uint32_t* err;
     long long layer_off;
     long long kv_off;
+    float* scales;        // INT8 cache: row scales; sc_layer_off / sc_kv_off as in DecodeParams
+    long long sc_layer_off, sc_kv_off;
     int B, Hkv, D, n_new;
     int layout, window, sinks, capacity;
     int bs, num_blocks, maxb;
@@ -157,23 +170,31 @@ struct BlockParams {
     const int32_t* src_seq;    // share: source; release: the sequences
     const int32_t* dst_seq;
     const int32_t* nblocks;
+    float* scales;             // INT8 cache: row scales [layers][K|V][num_blocks * Hkv * bs]; else null
     int B, bs, num_blocks, maxb, layers, Hkv, D;
 };
 
-// bf16 caches: tensor maps over the cache for copies of a run of 16 r rows
-// (r = 1..kRunMaps), K and V of every column at once.  With tma_whole the map
-// is 5-D {64 columns, row, K|V, layer, column block} and one copy lands as
-// [column block][K|V][rows][128 bytes]; otherwise it is 4-D {column, row, K|V,
-// layer} and each 64-column block is its own copy, landing at the same place.
+// bf16 and INT8 caches: tensor maps over the cache for copies of a run of
+// 16 r rows (r = 1..kRunMaps), K and V of every column at once.  A column
+// block is 128 bytes of a row (64 bf16 or 128 INT8 columns).  With tma_whole
+// the map is 5-D {block columns, row, K|V, layer, column block} and one copy
+// lands as [column block][K|V][rows][128 bytes]; otherwise it is 4-D
+// {column, row, K|V, layer} and each column block is its own copy, landing
+// at the same place.  INT8 caches add 3-D maps {row, K|V, layer} over the row
+// scales: boxes of kScRunRows (runs) and kScSubRows (single sub-tiles) rows
+// from a row index rounded down to a multiple of 4 (16-byte TMA alignment).
+constexpr int kScRunRows = 68;                   // 64 + up to 3 rows of alignment, x 4 bytes = 272
+constexpr int kScSubRows = 20;                   // 16 + 3, rounded to 16 bytes
 struct KvTensorMaps {
     CUtensorMap run[kRunMaps];
+    CUtensorMap sc_run, sc_sub;
 };
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_decode(int dtype, int head_dim, int gh, bool paged, bool read_rope,
                           const DecodeParams& p, dim3 grid, cudaStream_t stream);
-// bf16 caches: tensor-core kernel fed by TMA tensor copies through `maps`.
-cudaError_t launch_decode_mma(int head_dim, int gh, bool paged, bool read_rope, const DecodeParams& p,
+// bf16 and INT8 (q8) caches: tensor-core kernel fed by TMA tensor copies through `maps`.
+cudaError_t launch_decode_mma(int head_dim, int gh, bool paged, bool read_rope, bool q8, const DecodeParams& p,
                               const KvTensorMaps& maps, dim3 grid, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);

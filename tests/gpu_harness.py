@@ -8,7 +8,7 @@ import torch
 
 import oracle
 
-TOL = {"f32": 2e-3, "bf16": 2e-2}
+TOL = {"f32": 2e-3, "bf16": 2e-2, "i8": 2e-2}   # max abs error of the outputs (INT8 cache: bf16 outputs)
 
 
 def attended(wl, b, t=None):
@@ -28,9 +28,15 @@ def oracle_outputs(wl, layer, seqs=None, positions=None):
         t = int(pos_all[b])
         p = attended(wl, b, t)
         k, v = wl.kv_history(layer, b, p)
+        kd, vd = k.double().numpy(), v.double().numpy()
+        if wl.dtype == "i8":
+            # rows as an INT8 cache stores them; baked keys are quantised after
+            # rotation, inside the oracle
+            vd = oracle.quant.store_i8(vd)
+            if wl.rope != "baked":
+                kd = oracle.quant.store_i8(kd)
         q = wl.query(layer, b, t)
-        outs.append(oracle.decode_sequence(q.double().numpy(), k.double().numpy(), v.double().numpy(),
-                                           p, t, **spec))
+        outs.append(oracle.decode_sequence(q.double().numpy(), kd, vd, p, t, **spec))
     return np.stack(outs)
 
 

@@ -61,8 +61,11 @@ def test_cache_and_workspace_sizes(kvc):
     for name in kvc_synth.WORKLOAD_NAMES:
         wl = kvc_synth.make_workload(name)
         d = bench.workload_desc(wl, layers=2)
-        elt = 4 if wl.dtype == "f32" else 2
-        assert kvc.cache_bytes(d) == int(np.prod(wl.cache_shape(2))) * elt
+        n = int(np.prod(wl.cache_shape(2)))
+        if wl.dtype == "i8":      # codes, then one fp32 scale per row
+            assert kvc.cache_bytes(d) == n + 4 * (n // wl.head_dim)
+        else:
+            assert kvc.cache_bytes(d) == n * (4 if wl.dtype == "f32" else 2)
         assert kvc.workspace_bytes(d) > 0
         assert tuple(kvc.cache_shape(d)) == wl.cache_shape(2)
 
@@ -76,6 +79,9 @@ def test_invalid_descriptors_are_rejected(kvc):
         dict(layout="ring", sinks=2),
         dict(layout="paged", block_size=0, num_blocks=4, max_blocks_per_seq=4),
         dict(layers=0),
+        dict(dtype="i8", head_dim=64),                       # INT8: whole 128-byte column blocks
+        dict(dtype="i8", layout="sink_ring", sinks=4, window=96, rope="read_time"),   # INT8: no read-time RoPE
+        dict(dtype="i8", batch=1, kv_heads=1, window=98),    # INT8: rows of a half not a multiple of 4
     ]
     for kw in bad:
         assert kvc.cache_bytes(_desc(kvc, **kw)) == 0, kw
@@ -120,6 +126,20 @@ def test_argument_errors_return_codes_without_launching(kvc):
     assert L.kvc_block_release(dg, A, None, A, A, A, -1, A, A, nws, None) == kvc.KVC_ERR_ARG
     assert L.kvc_block_release(dg, A, None, A, A, None, 1, A, A, nws, None) == kvc.KVC_ERR_NULL
     assert "free" in kvc.strerror(kvc.KVC_DEV_NO_FREE_BLOCK)
+
+
+def test_int8_views_cover_the_buffer(kvc):
+    d = _desc(kvc, dtype="i8", window=100)
+    buf = torch.zeros(kvc.cache_bytes(d), dtype=torch.uint8)
+    codes, scales = kvc.int8_views(d, buf)
+    assert codes.dtype == torch.int8 and tuple(codes.shape) == tuple(kvc.cache_shape(d))
+    assert scales.dtype == torch.float32 and tuple(scales.shape) == tuple(kvc.cache_shape(d))[:-1]
+    assert codes.numel() + 4 * scales.numel() == buf.numel()
+    scales.fill_(1.5)
+    codes.fill_(-3)
+    assert int(buf[:codes.numel()].view(torch.int8).min()) == -3
+    assert float(buf[codes.numel():].view(torch.float32).max()) == 1.5
+    assert kvc.desc_dtype(d) == torch.bfloat16 and kvc.cache_dtype(d) == torch.uint8
 
 
 def test_pack_valid_bits(kvc):
