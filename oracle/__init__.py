@@ -19,6 +19,9 @@ What it computes, in fp64 numpy, slowly and plainly:
 * `blocks`    – the paged cache's block manager: free list, prefix sharing
                 with reference counts, copy-on-write, release ([share] §3.2,
                 §5.1, §6.1).
+* `prefill`   – a chunk of T tokens: each token's output equals the decode
+                step at its position after the chunk's earlier tokens are
+                appended ([pool] chunked prefill, [ring] window as a mask).
 * `attention` – one decode step: scores q.k / sqrt(D), max-subtracted softmax,
                 weighted sum of V.  Every sum is exactly rounded (math.fsum),
                 so a result never depends on the order in which the attended
@@ -45,7 +48,7 @@ The numeric attention outputs of the full workloads have no worked example
 on the pages; they are pinned through those checks of the definition.
 """
 
-from . import attention, blocks, layouts, quant, rope, storage
+from . import attention, blocks, layouts, prefill, quant, rope, storage
 from .attention import attend, decode_masked_history, decode_reference, decode_sequence
 from .layouts import (
     PagedKV,
@@ -61,7 +64,7 @@ from .rope import inv_freq, rotate
 from .storage import round_bf16, round_storage
 
 __all__ = [
-    "attention", "blocks", "layouts", "quant", "rope", "storage",
+    "attention", "blocks", "layouts", "prefill", "quant", "rope", "storage",
     "attend", "decode_reference", "decode_masked_history", "decode_sequence",
     "PagedKV", "RingKV", "SinkRingKV", "StreamingKV",
     "incache_position", "paged_attended", "window_attended", "window_slot",
