@@ -843,6 +843,70 @@ def measure_pagein(args):
             "device_errors": kvc.get_error(ws)}
 
 
+def measure_prefill(args):
+    """Chunked prefill (kvc_prefill) of T = --chunk tokens per sequence on a
+    bf16 workload (default ring_bf16: 8 sequences, 32 q / 8 kv heads, D 128,
+    a full 4096-slot ring), each chunk ending at the workload's position t_b,
+    the cache holding every earlier position.  One call stages the chunk,
+    runs the attention and appends the chunk.  L2 is flushed (a 256 MiB write)
+    between timed calls; each call is timed with CUDA events.  Reports tokens/s
+    and the attention's algorithmic TFLOP/s (4 D flops per (token, q head,
+    attended key): q.k and p.v) against the measured bf16 tensor peak."""
+    kvc = _kvc()
+    name = args.workload if args.workload in ("ring_bf16", "paged_shared_prefix_bf16") else "ring_bf16"
+    wl = kvc_synth.make_workload(name)
+    T = args.chunk
+    pos0 = np.maximum(wl.positions - T + 1, 0)
+    import dataclasses
+    wl0 = dataclasses.replace(wl, positions=pos0)
+    st = DecodeState(wl0, 1, source="device")
+    B, Hq, Hkv, D = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
+    q = _raw_rows_device((B, T, Hq, D), "bf16", (wl.seed, 0, 201))
+    k = _raw_rows_device((B, T, Hkv, D), "bf16", (wl.seed, 0, 202))
+    v = _raw_rows_device((B, T, Hkv, D), "bf16", (wl.seed, 0, 203))
+    ws = kvc.alloc_prefill_workspace(st.desc, T)
+    out = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device="cuda")
+    pos_t = torch.from_numpy(pos0.astype(np.int32)).cuda()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    # algorithmic work: attended keys of every chunk token
+    import oracle
+    keys = 0
+    for b in range(B):
+        for i in range(T):
+            t = int(pos0[b]) + i
+            if wl.layout == "window":
+                keys += len(oracle.window_attended(t, wl.sinks, wl.window))
+            else:
+                keys += len(oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size))
+    flops = 4.0 * D * Hq * keys
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 255)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kvc.prefill(st.desc, st.cache, 0, q, k, v, pos_t, ws, block_table=st.table, valid_bits=st.valid_bits,
+                    out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peak = float(json.load(f)["bf16_tflops"])
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"measure": "chunked prefill", "metric": "prefill attention TFLOP/s", "value": achieved,
+            "unit": "TFLOP/s", "ms_per_call": ms, "tokens_per_s": B * T / (ms * 1e-3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_kind": "measured (cuBLAS bf16, burst)",
+                         "algorithmic_flops_per_call": flops,
+                         "kernel": "kvc_prefill: prefill_stage_kernel + prefill_kernel (mma.sync) + append_kernel",
+                         "timer": "CUDA events around each call, median, L2 flushed between calls"},
+            "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "chunk_tokens": T, "batch": B, "q_heads": Hq, "kv_heads": Hkv,
+                       "head_dim": D, "attended_keys": keys},
+            "device_errors": kvc.get_error(ws)}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -856,7 +920,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--measure", choices=["block_prepare", "pagein"], default=None,
+    ap.add_argument("--chunk", type=int, default=128, help="--measure prefill: tokens per chunk")
+    ap.add_argument("--measure", choices=["block_prepare", "pagein", "prefill"], default=None,
                     help="time a block-manager call instead of the decode step (separate JSON line)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode launch from an ncu capture of the current kernel")
@@ -867,6 +932,8 @@ def main(argv=None):
         line = measure_block_prepare(args)
     elif args.measure == "pagein":
         line = measure_pagein(args)
+    elif args.measure == "prefill":
+        line = measure_prefill(args)
     else:
         line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:

@@ -200,6 +200,32 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
                             const int32_t* block_table, const uint32_t* valid_bits,
                             void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Chunked prefill ([pool] "the real cost of long context": prefill in chunks
+ * of 128-256 tokens; [ring] 3.1 and 5.2: the window as a mask on the score
+ * matrix).  For each sequence b, T consecutive tokens at positions
+ * pos0[b] + i (i < T): token i gets the output the decode step at that
+ * position would give after the chunk's earlier tokens were appended --
+ * attention of its q over its attended set A(pos0[b] + i), keys before
+ * pos0[b] read from the cache as it stands (the state after position
+ * pos0[b] - 1), the chunk's keys from k_new / v_new -- and then the chunk is
+ * appended to the cache as kvc_append(n_new = T) would.  Positions below 0
+ * are left padding: zero output, nothing appended.
+ *   q          [batch, T, q_heads, head_dim] bf16, pre-RoPE.
+ *   k_new, v_new [batch, T, kv_heads, head_dim] bf16, pre-RoPE.
+ *   pos0       [batch] int32.
+ *   block_table, valid_bits  PAGED as in kvc_decode_attention; the chunk's
+ *              blocks must be mapped (the append reports unmapped ones).
+ *   out        [batch, T, q_heads, head_dim] bf16.
+ *   workspace  kvc_prefill_workspace_bytes(d, T) bytes: the decode workspace
+ *              followed by the chunk's staged rows.
+ * bf16 caches, head_dim 64 or 128, RoPE NONE or BAKED (KVC_ERR_UNSUPPORTED
+ * otherwise).  Calls on one workspace must not overlap on the GPU. */
+KVC_API size_t kvc_prefill_workspace_bytes(const kvc_desc* d, int32_t T);
+KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const void* q,
+                        const void* k_new, const void* v_new, int32_t T, const int32_t* pos0,
+                        const int32_t* block_table, const uint32_t* valid_bits,
+                        void* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Batched block-table update ([share] 3.1 block table, 5.1 block manager):
  * for each i < n, block_table[seq[i]][logical_block[i]] = physical_block[i];
  * -1 unmaps.  When valid_bits is not NULL, each mapped physical block gets its

@@ -38,7 +38,7 @@ ABI_FUNCTIONS = (
     "kvc_strerror", "kvc_decode_attention_noalloc", "kvc_decode_step",
     "kvc_block_prepare", "kvc_block_share", "kvc_block_release",
     "kvc_pager_create", "kvc_pager_destroy", "kvc_pager_plan", "kvc_pager_evict", "kvc_pagein_issue",
-    "kvc_pagein_commit",
+    "kvc_pagein_commit", "kvc_prefill_workspace_bytes", "kvc_prefill",
 )
 
 
@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
         L.kvc_get_error.argtypes = [vp, vp]
         L.kvc_decode_attention_noalloc.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.kvc_decode_step.argtypes = [dp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.kvc_prefill_workspace_bytes.argtypes = [dp, i32]
+        L.kvc_prefill_workspace_bytes.restype = sz
+        L.kvc_prefill.argtypes = [dp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp]
         L.kvc_block_prepare.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.kvc_block_share.argtypes = [dp, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.kvc_block_release.argtypes = [dp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp]
@@ -295,6 +298,47 @@ def decode_step(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, k_
                                  _ptr(pos), _ptr(block_table), _ptr(valid_bits), _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream)),
            "kvc_decode_step")
+    return out
+
+
+def prefill_workspace_bytes(d: KvcDesc, T: int) -> int:
+    return int(lib().kvc_prefill_workspace_bytes(ctypes.byref(d), int(T)))
+
+
+def alloc_prefill_workspace(d: KvcDesc, T: int, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace for kvc_prefill with chunks of up to T tokens (also a decode workspace)."""
+    n = prefill_workspace_bytes(d, T)
+    if n == 0:
+        raise KvcError(KVC_ERR_DESC, "kvc_prefill_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def prefill(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, k_new: torch.Tensor,
+            v_new: torch.Tensor, pos0: torch.Tensor, workspace: torch.Tensor,
+            block_table: torch.Tensor | None = None, valid_bits: torch.Tensor | None = None,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvc_prefill: q [batch, T, q_heads, D], k_new / v_new [batch, T, kv_heads, D] -> out [batch, T, q_heads, D]."""
+    dt = desc_dtype(d)
+    _need(cache, "cache", cache_dtype(d))
+    _need(q, "q", dt)
+    if q.numel() % (d.batch * d.q_heads * d.head_dim):
+        raise ValueError("q must be [batch, T, q_heads, head_dim]")
+    T = q.numel() // (d.batch * d.q_heads * d.head_dim)
+    _need(k_new, "k_new", dt, d.batch * T * d.kv_heads * d.head_dim)
+    _need(v_new, "v_new", dt, d.batch * T * d.kv_heads * d.head_dim)
+    _need(pos0, "pos0", torch.int32, d.batch)
+    _need(workspace, "workspace", torch.uint8)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, d.batch * d.max_blocks_per_seq)
+    if valid_bits is not None:
+        _need(valid_bits, "valid_bits", torch.int32, (d.num_blocks + 31) // 32)
+    if out is None:
+        out = torch.empty((d.batch, T, d.q_heads, d.head_dim), dtype=dt, device=q.device)
+    _need(out, "out", dt, d.batch * T * d.q_heads * d.head_dim)
+    _check(lib().kvc_prefill(ctypes.byref(d), _ptr(cache), int(layer), _ptr(q), _ptr(k_new), _ptr(v_new), int(T),
+                             _ptr(pos0), _ptr(block_table), _ptr(valid_bits), _ptr(out), _ptr(workspace),
+                             workspace.numel(), _stream(stream)),
+           "kvc_prefill")
     return out
 
 

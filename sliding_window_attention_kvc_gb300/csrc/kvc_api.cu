@@ -546,6 +546,104 @@ KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer, const void
     return KVC_OK;
 }
 
+namespace {
+// Staging area of kvc_prefill (the chunk's K and V rows, bf16), after the
+// decode workspace.
+size_t prefill_stage_offset(const kvc_desc* d, const Geo& g) { return align_up(ws_layout(d, g).total, 256); }
+size_t prefill_stage_bytes(const kvc_desc* d, long long T) {
+    return 2 * (size_t)d->batch * (size_t)T * (size_t)d->kv_heads * (size_t)d->head_dim * 2;
+}
+}  // namespace
+
+KVC_API size_t kvc_prefill_workspace_bytes(const kvc_desc* d, int32_t T) {
+    Geo g;
+    if (check_desc(d, &g) != KVC_OK || T < 1) return 0;
+    return prefill_stage_offset(d, g) + prefill_stage_bytes(d, T);
+}
+
+KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const void* q, const void* k_new,
+                        const void* v_new, int32_t T, const int32_t* pos0, const int32_t* block_table,
+                        const uint32_t* valid_bits, void* out, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    Geo g;
+    int rc = check_desc(d, &g);
+    if (rc) return rc;
+    if (d->dtype != KVC_BF16 || d->rope == KVC_ROPE_READ_INCACHE || (d->head_dim != 64 && d->head_dim != 128) ||
+        g.G > 64)
+        return KVC_ERR_UNSUPPORTED;
+    if (!cache || !q || !k_new || !v_new || !pos0 || !out || !workspace) return KVC_ERR_NULL;
+    const bool paged = d->layout == KVC_LAYOUT_PAGED;
+    if (paged && !block_table) return KVC_ERR_NULL;
+    if (!aligned16(cache) || !aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) ||
+        !aligned16(workspace))
+        return KVC_ERR_ALIGN;
+    if (layer < 0 || layer >= d->layers || T < 1 || T > 0x7fffffff / 2) return KVC_ERR_ARG;
+    if (workspace_bytes < kvc_prefill_workspace_bytes(d, T)) return KVC_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    const WorkspaceLayout w = ws_layout(d, g);
+    cudaStream_t s = (cudaStream_t)stream;
+    void* kst = ws + prefill_stage_offset(d, g);
+    void* vst = static_cast<char*>(kst) + prefill_stage_bytes(d, T) / 2;
+
+    AppendParams ap{};
+    ap.cache = cache;
+    ap.k_new = k_new;
+    ap.v_new = v_new;
+    ap.pos = pos0;
+    ap.table = block_table;
+    ap.err = reinterpret_cast<uint32_t*>(ws + w.err);
+    ap.layer_off = (long long)layer * 2 * g.half_elems;
+    ap.kv_off = g.half_elems;
+    ap.B = d->batch;
+    ap.Hkv = d->kv_heads;
+    ap.D = d->head_dim;
+    ap.n_new = T;
+    ap.layout = d->layout;
+    ap.window = d->window;
+    ap.sinks = d->layout == KVC_LAYOUT_SINK_RING ? d->sinks : 0;
+    ap.capacity = g.C;
+    ap.bs = d->block_size;
+    ap.num_blocks = d->num_blocks;
+    ap.maxb = d->max_blocks_per_seq;
+    ap.rope = d->rope;
+    if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, ap.theta, nullptr);
+    // 1. the chunk's rows as the cache will hold them
+    if (launch_prefill_stage(ap, kst, vst, s) != cudaSuccess) return KVC_ERR_CUDA;
+    // 2. attention: earlier keys from the cache as it stands, the chunk's from the stage
+    PrefillParams pp{};
+    pp.cache = cache;
+    pp.q = q;
+    pp.kst = kst;
+    pp.vst = vst;
+    pp.pos0 = pos0;
+    pp.table = block_table;
+    pp.valid = valid_bits;
+    pp.out = out;
+    pp.err = ap.err;
+    pp.layer_off = ap.layer_off;
+    pp.kv_off = ap.kv_off;
+    pp.B = d->batch;
+    pp.T = T;
+    pp.Hq = d->q_heads;
+    pp.Hkv = d->kv_heads;
+    pp.G = g.G;
+    pp.layout = d->layout;
+    pp.window = d->window;
+    pp.sinks = ap.sinks;
+    pp.capacity = g.C;
+    pp.bs = d->block_size;
+    pp.num_blocks = d->num_blocks;
+    pp.maxb = d->max_blocks_per_seq;
+    pp.rope = d->rope;
+    const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+    pp.q_scale = scale * 1.4426950408889634f;
+    if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
+    if (launch_prefill(d->head_dim, g.G, pp, s) != cudaSuccess) return KVC_ERR_CUDA;
+    // 3. the chunk appended
+    if (launch_append(d->dtype, ap, s) != cudaSuccess) return KVC_ERR_CUDA;
+    return KVC_OK;
+}
+
 KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t layer, const void* q,
                                  const int32_t* pos, const int32_t* block_table, const uint32_t* valid_bits,
                                  void* out, void* workspace, size_t workspace_bytes, void* stream) {

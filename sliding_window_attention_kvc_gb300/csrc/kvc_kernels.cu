@@ -117,6 +117,27 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ App
     }
 }
 
+// kvc_prefill: the chunk's K (RoPE baked at its position, as an append stores
+// it) and V rows of token blockIdx.x of sequence blockIdx.y, into the staging
+// buffers [B][T][Hkv][D] (bf16).  Left-padding positions stage nothing.
+__global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constant__ AppendParams p,
+                                                            __nv_bfloat16* kst, __nv_bfloat16* vst) {
+    const int i_tok = blockIdx.x, b = blockIdx.y;
+    const long long pos = (long long)p.pos[b] + i_tok;
+    if (pos < 0) return;
+    const long long row = ((long long)b * p.n_new + i_tok) * p.Hkv * p.D;
+    write_token_rows<__nv_bfloat16>(kst + row, (long long)(vst - kst), p.D,
+                                    static_cast<const __nv_bfloat16*>(p.k_new) + row,
+                                    static_cast<const __nv_bfloat16*>(p.v_new) + row, p.Hkv, p.D, p.rope, pos,
+                                    p.theta);
+}
+
+cudaError_t launch_prefill_stage(const AppendParams& p, void* kst, void* vst, cudaStream_t stream) {
+    prefill_stage_kernel<<<dim3(p.n_new, p.B), 256, 0, stream>>>(p, static_cast<__nv_bfloat16*>(kst),
+                                                                 static_cast<__nv_bfloat16*>(vst));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream) {
     dim3 grid(p.n_new, p.B);
     if (dtype == 0)

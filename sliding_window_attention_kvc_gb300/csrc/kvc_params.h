@@ -136,6 +136,25 @@ struct AppendParams {
     unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
 };
 
+// Chunked prefill (kvc_prefill): T tokens per sequence at pos0[b] + i.
+struct PrefillParams {
+    const void* cache;
+    const void* q;              // [B, T, Hq, D] pre-RoPE
+    const void* kst;            // staged chunk rows [B, T, Hkv, D], K as the cache stores it
+    const void* vst;
+    const int32_t* pos0;        // [B]
+    const int32_t* table;       // PAGED [B, maxb]
+    const uint32_t* valid;      // PAGED, may be null
+    void* out;                  // [B, T, Hq, D]
+    uint32_t* err;
+    long long layer_off, kv_off;
+    int B, T, Hq, Hkv, G;
+    int layout, window, sinks, capacity, bs, num_blocks, maxb;
+    int rope;
+    float q_scale;              // softmax scale * log2(e)
+    unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
+};
+
 struct TableParams {
     int32_t* table;
     uint32_t* valid;
@@ -199,6 +218,9 @@ cudaError_t launch_decode_mma(int head_dim, int gh, bool paged, bool read_rope, 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
+// kvc_prefill: the chunk's rows staged (K rotated as stored), then attention.
+cudaError_t launch_prefill_stage(const AppendParams& p, void* kst, void* vst, cudaStream_t stream);
+cudaError_t launch_prefill(int head_dim, int g, const PrefillParams& p, cudaStream_t stream);
 cudaError_t launch_valid_write(const TableParams& p, cudaStream_t stream);
 cudaError_t launch_block_prepare(int elt, const BlockParams& p, cudaStream_t stream);
 cudaError_t launch_block_share(const BlockParams& p, int n, cudaStream_t stream);

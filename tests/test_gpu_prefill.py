@@ -1,0 +1,127 @@
+"""Chunked prefill (kvc_prefill) on the GPU against oracle.prefill.
+
+The cache is first filled as it stands before the chunk (every position the
+decode step at pos0 would attend, except pos0 itself), then one call prefills
+T tokens per sequence.  Outputs are compared element by element with the
+oracle (tolerance 2e-2, bf16 outputs); the cache the call leaves must equal
+the cache after a plain kvc_append of the same chunk (so the ring slots the
+chunk overwrites were read before they were overwritten).  Cases: ring with a
+chunk across the first wrap and far past it, sink + ring, paged with shared
+prefix blocks, a chunk that starts at position 0, ragged chunk lengths (not a
+multiple of the 16 tokens a CTA takes), left padding, RoPE none and baked.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import kvc_synth
+import oracle
+from oracle.prefill import prefill_sequence
+from tests.gpu_harness import TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import sliding_window_attention_kvc_gb300 as m
+    return m
+
+
+def _attended_fn(wl, b):
+    if wl.layout == "window":
+        return lambda t: oracle.window_attended(t, wl.sinks, wl.window)
+    return lambda t: oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size)
+
+
+def _run(kvc, wl, pos0, T, layer=0):
+    """Prefill T tokens at pos0 [B]; returns (got [B, T, Hq, D], state, chunk q/k/v)."""
+    # the cache as it stands before the chunk (no history before position 0)
+    wl0 = dataclasses.replace(wl, positions=np.maximum(np.asarray(pos0, dtype=np.int64), 0))
+    st = bench.DecodeState(wl0, 1, source="cpu")
+    B, Hq, Hkv, D = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
+    q = torch.zeros((B, T, Hq, D), dtype=torch.bfloat16)
+    k = torch.zeros((B, T, Hkv, D), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    for b in range(B):
+        ps = np.arange(pos0[b], pos0[b] + T)
+        keep = ps >= 0
+        kb, vb = wl.kv_history(layer, b, ps[keep])
+        k[b, keep] = kb
+        v[b, keep] = vb
+        for i, t in enumerate(ps):
+            if t >= 0:
+                q[b, i] = wl.query(layer, b, int(t))
+    ws = kvc.alloc_prefill_workspace(st.desc, T)
+    ref_cache = st.cache.clone()
+    pos_t = torch.from_numpy(np.asarray(pos0, dtype=np.int32)).cuda()
+    out = kvc.prefill(st.desc, st.cache, layer, q.cuda(), k.cuda(), v.cuda(), pos_t, ws, block_table=st.table,
+                      valid_bits=st.valid_bits)
+    kvc.append(st.desc, ref_cache, layer, k.cuda(), v.cuda(), pos_t, ws, block_table=st.table)
+    torch.cuda.synchronize()
+    assert kvc.get_error(ws) == 0
+    return out.float().cpu().numpy(), st, ref_cache, q, k, v
+
+
+def _oracle(wl, b, pos0, T, q, layer=0):
+    N = max(pos0 + T, 1)
+    K, V = wl.kv_history(layer, b, np.arange(N))
+    spec = dict(rope=wl.rope, base=wl.rope_base, storage=wl.dtype, sinks=wl.sinks, window=wl.window)
+    return prefill_sequence(q[b].double().numpy(), K.double().numpy(), V.double().numpy(), pos0,
+                            _attended_fn(wl, b), **spec)
+
+
+CASES = {
+    # name: (workload, rope, pos0 per sequence, T)
+    "ring_wrap": ("ring_bf16", "baked", [150, 190, 4300], 37),
+    "ring_none_long": ("ring_bf16", "none", [0, 64, 1000], 70),
+    "sink_baked": ("sink_window_bf16", "baked", [3, 180, 987600], 45),
+    "sink_none": ("sink_window_bf16", "none", [100, 150, 50000], 33),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_prefill_window_layouts(kvc, case):
+    name, rope, pos0, T = CASES[case]
+    wl = dataclasses.replace(kvc_synth.make_workload(name, small=True), rope=rope)
+    got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
+    assert np.isfinite(got).all()
+    for b in range(wl.batch):
+        ref = _oracle(wl, b, pos0[b], T, q)
+        err = float(np.abs(got[b] - ref).max())
+        assert err <= TOL["bf16"], (case, b, err)
+    a, r = st.cache.float(), ref_cache.float()
+    same = (a == r) | (torch.isnan(a) & torch.isnan(r))
+    assert bool(same.all())
+
+
+def test_prefill_paged_shared_prefix(kvc):
+    wl = kvc_synth.make_workload("paged_shared_prefix_bf16", small=True)
+    T = 29
+    pos0 = [max(int(t) - T + 1, 0) for t in wl.positions]     # the chunk ends at each sequence's mapped tail
+    got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
+    assert np.isfinite(got).all()
+    for b in range(wl.batch):
+        Tb = min(T, int(wl.positions[b]) + 1 - pos0[b])         # rows past the mapped tail are not compared
+        ref = _oracle(wl, b, pos0[b], T, q)
+        err = float(np.abs(got[b, :Tb] - ref[:Tb]).max())
+        assert err <= TOL["bf16"], (b, err)
+
+
+def test_prefill_left_padding(kvc):
+    wl = kvc_synth.make_workload("ring_bf16", small=True)
+    pos0, T = [-5, 10, -1], 21
+    got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
+    for b in range(wl.batch):
+        pad = max(0, -pos0[b])
+        assert not got[b, :pad].any()
+        ref = _oracle(wl, b, pos0[b], T, q)
+        assert float(np.abs(got[b] - ref).max()) <= TOL["bf16"], b

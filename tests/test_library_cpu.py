@@ -126,6 +126,18 @@ def test_argument_errors_return_codes_without_launching(kvc):
     assert L.kvc_block_release(dg, A, None, A, A, A, -1, A, A, nws, None) == kvc.KVC_ERR_ARG
     assert L.kvc_block_release(dg, A, None, A, A, None, 1, A, A, nws, None) == kvc.KVC_ERR_NULL
     assert "free" in kvc.strerror(kvc.KVC_DEV_NO_FREE_BLOCK)
+    # chunked prefill: bf16 caches, head_dim 64 / 128, no read-time RoPE; sizes checked first
+    pw = kvc.prefill_workspace_bytes(d, 16)
+    assert pw > ws_n and kvc.prefill_workspace_bytes(d, 0) == 0
+    assert L.kvc_prefill(dp, A, 0, A, A, A, 0, A, None, None, A, A, pw, None) == kvc.KVC_ERR_ARG
+    assert L.kvc_prefill(dp, A, 0, A, A, A, 16, A, None, None, A, A, pw - 1, None) == kvc.KVC_ERR_WORKSPACE
+    assert L.kvc_prefill(dp, A, 0, None, A, A, 16, A, None, None, A, A, pw, None) == kvc.KVC_ERR_NULL
+    df = _desc(kvc, dtype="f32")
+    assert L.kvc_prefill(ctypes.byref(df), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
+        kvc.KVC_ERR_UNSUPPORTED
+    dr = _desc(kvc, layout="sink_ring", sinks=4, window=96, rope="read_time")
+    assert L.kvc_prefill(ctypes.byref(dr), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
+        kvc.KVC_ERR_UNSUPPORTED
 
 
 def test_int8_views_cover_the_buffer(kvc):
