@@ -76,7 +76,11 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     const int groups = d->kv_heads * g.nsub;
     // stream-K shares per (kv head, q-head group): bf16 kernels, and the paged
     // plan.  bf16: a persistent grid of about two CTAs per SM claims them in turn.
-    const int stream_ctas = d->dtype == KVC_I8 ? kStreamCtasQ8 : kStreamCtas;
+    // the persistent grid: 152 SMs times the decode kernel's resident CTAs
+    // (at least two: kernels held to one CTA per SM keep two shares per SM)
+    const int per_sm = decode_ctas_per_sm(d->dtype == KVC_I8, d->layout == KVC_LAYOUT_PAGED,
+                                          d->rope == KVC_ROPE_READ_INCACHE, d->head_dim);
+    const int stream_ctas = kStreamCtas / 2 * (per_sm > 2 ? per_sm : 2);
     const int persist = (stream_ctas + groups - 1) / groups;
     if (d->layout == KVC_LAYOUT_PAGED || d->dtype != KVC_F32) {
         const bool bf16 = d->dtype != KVC_F32;     // tensor-core kernel (bf16 or INT8 cache)

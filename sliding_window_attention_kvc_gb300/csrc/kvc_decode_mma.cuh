@@ -42,7 +42,7 @@
 
 namespace kvc {
 
-template <int D, bool READ, bool Q8 = false>
+template <int D, bool READ, bool Q8 = false, bool PAGED = false>
 struct MmaShape {
     static constexpr int kSub = 16;                           // rows per sub-tile
     static constexpr int kBoxCols = Q8 ? 128 : 64;            // columns per TMA box row (128 bytes)
@@ -53,7 +53,8 @@ struct MmaShape {
     static constexpr int kTokenGroups = kConsumerWarps / kDsplit;
     static constexpr int kNsub = kTokenGroups;                // sub-tiles per stage (one per token group)
     static constexpr int kStageBytes = 2 * kNsub * kSubBytes; // K and V of kNsub sub-tiles
-    static constexpr int kStages = Q8 ? (kQ8CtasPerSm >= 3 ? 3 : 5) : (D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3));
+    static constexpr int kCtasPerSm = decode_ctas_per_sm(Q8, PAGED, READ, D);
+    static constexpr int kStages = Q8 ? (kCtasPerSm >= 3 ? 3 : 5) : (D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3));
     // INT8: row scales of each stage, one slot per sub-tile position (the
     // first sub-tile of a copy holds that copy's K and V scales)
     static constexpr int kScSlotBytes = Q8 ? 640 : 0;         // 2 x kScRunRows floats, 128-byte aligned
@@ -96,9 +97,9 @@ struct alignas(16) MmaStageMeta {
 };
 constexpr int kSegBegin = 1, kSegEnd = 2;
 
-template <int D, int GH, bool READ, bool Q8 = false>
+template <int D, int GH, bool READ, bool Q8 = false, bool PAGED = false>
 struct MmaSmem {
-    using S = MmaShape<D, READ, Q8>;
+    using S = MmaShape<D, READ, Q8, PAGED>;
     static constexpr size_t kStage = 0;                                        // 1024-aligned stages
     static constexpr size_t kSc = kStage + (size_t)S::kStages * S::kStageBytes;  // INT8 row scales
     static constexpr size_t kBars = kSc + (size_t)S::kStages * S::kScStageBytes;
@@ -319,10 +320,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
 template <int D, int GH, bool PAGED, bool READ, bool Q8>
 // Two CTAs (ten warps) per SM: three warps share a sub-partition's 16K
 // registers, so a thread may hold at most 168.
-__global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ? kQ8CtasPerSm : 2))
+__global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, READ, D))
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ KvTensorMaps maps) {
-    using S = MmaShape<D, READ, Q8>;
-    using SM = MmaSmem<D, GH, READ, Q8>;
+    using S = MmaShape<D, READ, Q8, PAGED>;
+    using SM = MmaSmem<D, GH, READ, Q8, PAGED>;
     static_assert(!(READ && Q8), "INT8 caches take no read-time RoPE");
     static_assert(!Q8 || D >= 128, "INT8 rows are whole 128-byte column blocks");
     constexpr int NST = S::kStages, NSUB = S::kNsub, HALF = S::kHalf;
@@ -866,14 +867,18 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
     MmaSegment seg;
     seg.b = seg.t = seg.slot = seg.first_slot = seg.nparts = 0;
     uint32_t qa[S::kKsteps][2];
-    float o[S::kNt][4];
+    // output accumulators: bf16, O = P V in 8-column tiles; INT8, O^T = V^T P^T
+    // in 16-column tiles (rows: lane g's columns 16 g + mt and 16 g + 8 + mt,
+    // columns: q heads 2c, 2c + 1), half as many
+    constexpr int kOt = Q8 ? S::kNt / 2 : S::kNt;
+    float o[kOt][4];
     float m_run = -INFINITY, l_run = 0.f;
     // INT8: fp16 tensor-core inputs.  q enters as q * q_scale * 2^-k (per head,
     // k >= 0 keeping it below 2^14: qexp = 2^k returns in the scores); a row's
     // weight enters as p * s_v / S_run, S_run the largest V scale of the segment
     // so far (the accumulator is rescaled when it grows and multiplied back at
     // the end), so weights stay in [0, 1]
-    float qexp = 1.f, S_run = 0.f;
+    float qexp = 1.f, S_run = 0.f, rS = 0.f;   // rS = 1 / S_run
 
     // q of sequence seg.b as mma A fragments: row g = q head (zero for g >= GH),
     // per k-step columns 16 ks + 2c (+1) and 16 ks + 8 + 2c (+1); rotated,
@@ -970,6 +975,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
                 qa[ks][1] = pack_f16x2(qf[ks][2] * qs, qf[ks][3] * qs);
             }
             S_run = 0.f;
+            rS = 0.f;
         } else {
 #pragma unroll
             for (int ks = 0; ks < S::kKsteps; ++ks) {
@@ -978,7 +984,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
             }
         }
 #pragma unroll
-        for (int j = 0; j < S::kNt; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        for (int j = 0; j < kOt; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         m_run = -INFINITY;
         l_run = 0.f;
     };
@@ -995,15 +1001,24 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
         lq += __shfl_xor_sync(0xffffffffu, lq, 1);
         lq += __shfl_xor_sync(0xffffffffu, lq, 2);
         csync.sync(p.err);                     // merge buffers free (previous segment done with them)
+        if constexpr (Q8) {
+            // INT8: this lane holds q heads 2c, 2c + 1 at columns hd * 128 + 16 g + mt (+ 8)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int hh = 2 * c + e;
+                if (hh < GH) {
+                    float* mo = merge_o + (tg * GH + hh) * D + hd * S::kDl + 16 * g;
+#pragma unroll
+                    for (int mt = 0; mt < kOt; ++mt) {
+                        mo[mt] = o[mt][e] * S_run;
+                        mo[8 + mt] = o[mt][2 + e] * S_run;
+                    }
+                }
+            }
+        }
         if (g < GH) {
             float* mo = merge_o + (tg * GH + g) * D;
             if constexpr (Q8) {
-                // INT8: output tile j, column n of it is column hd * 128 + 16 n + j
-#pragma unroll
-                for (int j = 0; j < S::kNt; ++j) {
-                    mo[hd * S::kDl + 32 * c + j] = o[j][0] * S_run;
-                    mo[hd * S::kDl + 32 * c + 16 + j] = o[j][1] * S_run;
-                }
             } else {
 #pragma unroll
                 for (int j = 0; j < S::kNt; ++j) {
@@ -1330,15 +1345,16 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
             float ofac = alpha;
             uint32_t pa0, pa2;
             if constexpr (Q8) {
-                // the 16 rows' largest V scale (lanes of one c share their rows)
-                float smax = fmaxf(fmaxf(vsc[0], vsc[1]), fmaxf(vsc[2], vsc[3]));
-                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 1));
-                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
-                if (smax > S_run) {
+                // a V scale above S_run anywhere: the 16 rows' largest (lanes of one c
+                // share their rows) becomes S_run, the accumulator scaled down to it
+                const float lmax = fmaxf(fmaxf(vsc[0], vsc[1]), fmaxf(vsc[2], vsc[3]));
+                if (__any_sync(0xffffffffu, lmax > S_run)) {
+                    float smax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, 1));
+                    smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 2));
                     ofac *= S_run / smax;
                     S_run = smax;
+                    rS = __frcp_rn(S_run);
                 }
-                const float rS = S_run > 0.f ? __frcp_rn(S_run) : 0.f;
                 pa0 = pack_f16x2(pe[0] * vsc[0] * rS, pe[1] * vsc[1] * rS);
                 pa2 = pack_f16x2(pe[2] * vsc[2] * rS, pe[3] * vsc[3] * rS);
             } else {
@@ -1346,19 +1362,33 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
                 pa2 = pack_bf16x2(pe[2], pe[3]);
             }
             if (__any_sync(0xffffffffu, ofac != 1.f)) {
+                if constexpr (Q8) {
+                    // columns are q heads 2c and 2c + 1: their factors come from lanes 8c, 8c + 4
+                    const float f0 = __shfl_sync(0xffffffffu, ofac, 8 * c);
+                    const float f1 = __shfl_sync(0xffffffffu, ofac, 8 * c + 4);
 #pragma unroll
-                for (int j = 0; j < S::kNt; ++j) {
-                    o[j][0] *= ofac;
-                    o[j][1] *= ofac;
+                    for (int mt = 0; mt < kOt; ++mt) {
+                        o[mt][0] *= f0;
+                        o[mt][2] *= f0;
+                        o[mt][1] *= f1;
+                        o[mt][3] *= f1;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < S::kNt; ++j) {
+                        o[j][0] *= ofac;
+                        o[j][1] *= ofac;
+                    }
                 }
             }
 
             // ---- O += P V over this warp's output columns ---------------------
             if constexpr (Q8) {
-                // INT8: lane (g, c) reads 16 code bytes (columns hd * 128 + 16 g .. + 15)
-                // of tokens 2c, 2c + 1, 2c + 8, 2c + 9 (loaded with K, in vw); output
-                // tile j takes byte j.  Bytes of the two tokens of a register are
-                // interleaved first.
+                // INT8: O^T += V^T P^T.  Lane (g, c) holds 16 code bytes (columns
+                // hd * 128 + 16 g .. + 15) of tokens 2c, 2c + 1, 2c + 8, 2c + 9 (loaded with
+                // K, in vw); A rows g and g + 8 of m-tile mt are columns 16 g + mt and
+                // 16 g + 8 + mt, k = tokens; B = P^T is the softmax fragment as it is.
+                uint32_t x0[16], x1[16];        // byte j of tokens (2c, 2c + 1) and (2c + 8, 2c + 9)
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const uint32_t a0 = (q4 == 0 ? vw[0][0].x : q4 == 1 ? vw[0][0].y : q4 == 2 ? vw[0][0].z : vw[0][0].w) ^ 0x80808080u;
@@ -1370,12 +1400,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
                     const uint32_t lo1 = __byte_perm(a1, b1, 0x5140u), hi1 = __byte_perm(a1, b1, 0x7362u);
 #pragma unroll
                     for (int jb = 0; jb < 4; ++jb) {
-                        const int j = 4 * q4 + jb;
-                        const uint32_t w0 = jb < 2 ? lo0 : hi0, w1 = jb < 2 ? lo1 : hi1;
                         const uint32_t sel = (jb & 1) ? 0x4342u : 0x4140u;
-                        mma_f16_16816(o[j], pa0, 0u, pa2, 0u, q8_f16x2(w0, sel), q8_f16x2(w1, sel));
+                        x0[4 * q4 + jb] = q8_f16x2(jb < 2 ? lo0 : hi0, sel);
+                        x1[4 * q4 + jb] = q8_f16x2(jb < 2 ? lo1 : hi1, sel);
                     }
                 }
+#pragma unroll
+                for (int mt = 0; mt < kOt; ++mt)
+                    mma_f16_16816(o[mt], x0[mt], x0[8 + mt], x1[mt], x1[8 + mt], pa0, pa2);
             } else {
                 const int tok = (((lane >> 3) & 1) << 3) + (lane & 7);
                 const int chs = lane >> 4;
@@ -1400,10 +1432,10 @@ __global__ void __launch_bounds__(kDecodeThreads, (READ && D >= 256) ? 1 : (Q8 ?
 
 template <int D, int GH, bool PAGED, bool READ, bool Q8>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const KvTensorMaps& maps, dim3 grid, cudaStream_t stream) {
-    using SM = MmaSmem<D, GH, READ, Q8>;
+    using SM = MmaSmem<D, GH, READ, Q8, PAGED>;
     // the resident CTAs per SM that __launch_bounds__ plans for must fit in
     // shared memory (228 KB per SM, 1 KB of it reserved per CTA)
-    constexpr int kCtasPerSm = (READ && D >= 256) ? 1 : (Q8 ? kQ8CtasPerSm : 2);
+    constexpr int kCtasPerSm = decode_ctas_per_sm(Q8, PAGED, READ, D);
     static_assert(kCtasPerSm * (SM::kTotal + 1024) <= 233472, "shared memory for the planned CTAs per SM");
     auto kern = decode_mma_kernel<D, GH, PAGED, READ, Q8>;
     // few (sequence, kv head, group) units: narrow column chunks, more CTAs each

@@ -26,12 +26,16 @@ constexpr int kPagedShareBatch = 8;
 // partial write), besides one unit per 16 rows.
 constexpr int kSeqUnits = 4;
 constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
-// INT8 caches: resident CTAs per SM of the decode kernel (its stages are half
-// the bytes of bf16 ones), and whether Q K^T accumulates even and odd k-steps
-// in separate registers (two shorter dependency chains)
-constexpr int kQ8CtasPerSm = 2;
+// Resident CTAs per SM of the decode kernel.  INT8 stages are half the
+// bytes of bf16 ones; paged INT8 batches at head_dim <= 128 run three CTAs
+// per SM (the compute warps are the bound there; measured 164 -> 151 us on
+// the shared-prefix batch, while the ring lost 2% and head_dim 256 spills).
+// Q K^T of INT8 rows may accumulate even and odd k-steps in separate
+// registers (two shorter dependency chains): measured no gain, kept off.
+constexpr int decode_ctas_per_sm(bool q8, bool paged, bool read, int D) {
+    return (read && D >= 256) ? 1 : ((q8 && paged && D <= 128) ? 3 : 2);
+}
 constexpr bool kQ8SplitChains = false;
-constexpr int kStreamCtasQ8 = 152 * kQ8CtasPerSm;
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
 enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
