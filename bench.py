@@ -349,9 +349,10 @@ class ClockSampler:
 # capture per workload (summaries: profiles/decode_mma_<workload>.md), and the
 # digest of the kernel sources they were taken on: reported only while the
 # sources are unchanged.
-KERNEL_TRAFFIC = {"ring_bf16": 137936896, "sink_window_bf16": 544711936,
-                  "paged_shared_prefix_bf16": 894593792, "long_context_pool_bf16": 153271552}
-KERNEL_TRAFFIC_SOURCES = "21fe28ed5882ab71be6cea79d7ff73dc146cbf27d6942ef5ccccb0a350772a4e"
+KERNEL_TRAFFIC = {"ring_bf16": 138023936, "sink_window_bf16": 544682240,
+                  "paged_shared_prefix_bf16": 901444096, "long_context_pool_bf16": 153010688,
+                  "ring_int8": 69377113}
+KERNEL_TRAFFIC_SOURCES = "f2af116eff3de1b5245461d5a1c2c69f7955c13011e81e42c346c3e11ec8dff3"
 
 
 def _kernel_sources_digest():
