@@ -34,9 +34,10 @@ def kvc():
 
 
 class Scenario:
-    def __init__(self, kvc, num_blocks=NB, seed=11):
+    def __init__(self, kvc, num_blocks=NB, seed=11, dtype="bf16"):
         self.kvc = kvc
-        self.d = kvc.make_desc("paged", "none", "bf16", L, B, HQ, HKV, D, block_size=BS, num_blocks=num_blocks,
+        self.dtype = dtype
+        self.d = kvc.make_desc("paged", "none", dtype, L, B, HQ, HKV, D, block_size=BS, num_blocks=num_blocks,
                                max_blocks_per_seq=MAXB)
         self.cache = kvc.alloc_cache(self.d, fill=0.0)
         self.ws = kvc.alloc_workspace(self.d)
@@ -86,6 +87,19 @@ class Scenario:
         assert bm.check_invariants()
 
     def check_cache(self):
+        if self.dtype == "i8":
+            # INT8 rows: codes and scales equal the oracle's quantisation of what was appended
+            from oracle.quant import quantize_rows
+            codes, scales = (x.cpu() for x in self.kvc.int8_views(self.d, self.cache))
+            for b in range(B):
+                for p, (k, v) in self.hist[b].items():
+                    phys = self.bm.table[b, p // BS]
+                    assert phys >= 0
+                    for kv, x in ((0, k), (1, v)):
+                        cq, sq = quantize_rows(x.float().numpy())
+                        assert np.array_equal(codes[:, kv, phys, :, p % BS].numpy(), cq), (b, p, kv)
+                        assert np.array_equal(scales[:, kv, phys, :, p % BS].numpy(), sq), (b, p, kv)
+            return
         c = self.cache.cpu()
         for b in range(B):
             for p, (k, v) in self.hist[b].items():
@@ -109,13 +123,18 @@ class Scenario:
                 for h in range(HKV):
                     K = np.stack([self.hist[b][p][0][layer, h].double().numpy() for p in ps])
                     V = np.stack([self.hist[b][p][1][layer, h].double().numpy() for p in ps])
+                    if self.dtype == "i8":
+                        from oracle.quant import store_i8
+                        K, V = store_i8(K), store_i8(V)
                     ref = decode_reference(q[b, h * g:(h + 1) * g].double().numpy(), K, V, ps, t, rope="none",
-                                           storage="bf16")
+                                           storage=self.dtype)
                     assert np.abs(got[b, h * g:(h + 1) * g] - ref).max() <= TOL["bf16"], (layer, b, h)
 
 
-def test_block_manager_churn_matches_the_model(kvc):
-    sc = Scenario(kvc)
+@pytest.mark.parametrize("dtype", ["bf16", "i8"])
+def test_block_manager_churn_matches_the_model(kvc, dtype):
+    # INT8: copy-on-write copies carry the rows' scales with their codes
+    sc = Scenario(kvc, dtype=dtype)
     # sequences 0 and 3 write 21 and 6 tokens
     for t in range(21):
         sc.prepare_and_append([t, -1, -1, t if t < 6 else -1])
