@@ -347,21 +347,26 @@ class ClockSampler:
 
 # DRAM bytes (read + write) per launch of decode_mma_kernel, from one ncu
 # capture per workload (summaries: profiles/decode_mma_<workload>.md), and the
-# digest of the kernel sources they were taken on: reported only while the
-# sources are unchanged.
+# digest of the kernel's sources (KERNEL_TRAFFIC_FILES) they were taken on:
+# reported only while those sources are unchanged.
 KERNEL_TRAFFIC = {"ring_bf16": 138023936, "sink_window_bf16": 544682240,
                   "paged_shared_prefix_bf16": 901444096, "long_context_pool_bf16": 153010688,
                   "ring_int8": 69377113}
-KERNEL_TRAFFIC_SOURCES = "f2af116eff3de1b5245461d5a1c2c69f7955c13011e81e42c346c3e11ec8dff3"
+KERNEL_TRAFFIC_SOURCES = "89a889e7a237c9542d4df82fe52c77c6b9b05e6f711c0a07e8de63e93ff4b770"
+
+
+# the sources decode_mma_kernel and its launch are built from
+KERNEL_TRAFFIC_FILES = ("decode_inst.cuh", "decode_paged_bf16.cu", "decode_paged_i8.cu", "decode_window_bf16.cu",
+                        "decode_window_i8.cu", "kvc_api.cu", "kvc_decode.cuh", "kvc_decode_mma.cuh",
+                        "kvc_device.cuh", "kvc_params.h")
 
 
 def _kernel_sources_digest():
-    import glob
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "sliding_window_attention_kvc_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in KERNEL_TRAFFIC_FILES:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "sliding_window_attention_kvc_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
