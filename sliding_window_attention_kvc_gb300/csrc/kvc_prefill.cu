@@ -30,7 +30,7 @@ struct PfShape {
     static constexpr int kChunks = D / 8;                  // 16-byte chunks per row
     static constexpr int kTile = kPfKeys * D * 2;          // K (or V) of one tile
     static constexpr int kBuf = 2 * kTile;                 // K and V
-    static constexpr int kSmem = 2 * kBuf + 2 * kPfKeys * 4;   // two buffers + row flags
+    static constexpr int kSmem = 2 * kBuf + 2 * kPfKeys * 4 + 2 * kPfKeys * 8;   // two buffers, row flags, row sources
     static constexpr int kKsteps = D / 16;
     static constexpr int kNt = D / 8;                      // output 8-column tiles
 };
@@ -54,6 +54,9 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
     using S = PfShape<D>;
     extern __shared__ __align__(128) unsigned char pf_smem[];
     int* rowok = reinterpret_cast<int*>(pf_smem + 2 * S::kBuf);      // [2][kPfKeys]
+    // each key row's source, per buffer: element offset of its K row in the
+    // cache (>= 0), -(offset of its staged row) - 2, or -1 (no row)
+    long long* rowsrc = reinterpret_cast<long long*>(pf_smem + 2 * S::kBuf + 2 * kPfKeys * 4);   // [2][kPfKeys]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -151,50 +154,51 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
     const __nv_bfloat16* kst = static_cast<const __nv_bfloat16*>(p.kst);
     const __nv_bfloat16* vst = static_cast<const __nv_bfloat16*>(p.vst);
 
-    // gather tile k into buffer k & 1: thread tid copies chunk tid % kChunks of
-    // rows tid / kChunks + n * (128 / kChunks)
+    // gather tile k into buffer k & 1: first one thread per key row finds the
+    // row's source; then thread tid copies chunk tid % kChunks of rows
+    // tid / kChunks + n * (128 / kChunks)
     auto load_tile = [&](int k) {
         unsigned char* Kb = pf_smem + (k & 1) * S::kBuf;
         unsigned char* Vb = Kb + S::kTile;
         int* ok = rowok + (k & 1) * kPfKeys;
-        const int base = tile_base(k), end = tile_end(k);
-        constexpr int kRowsPerPass = kPfThreads / S::kChunks;
-        const int ch = tid % S::kChunks;
-        for (int r = tid / S::kChunks; r < kPfKeys; r += kRowsPerPass) {
-            const int pk = base + r;
-            const __nv_bfloat16* ks = nullptr;
-            const __nv_bfloat16* vs = nullptr;
-            bool good = pk < end && pk >= 0;
+        long long* src = rowsrc + (k & 1) * kPfKeys;
+        if (tid < kPfKeys) {
+            const int r = tid;
+            const int pk = tile_base(k) + r;
+            long long sv = -1;
+            bool good = pk < tile_end(k) && pk >= 0;
             if (good && paged) {
                 const int lb = pk / p.bs;
                 int phys = lb < p.maxb ? p.table[(long long)b * p.maxb + lb] : -1;
                 if (phys >= p.num_blocks) {
-                    if (ch == 0) set_error(p.err, 0x1u /* KVC_DEV_BAD_BLOCK */);
+                    set_error(p.err, 0x1u /* KVC_DEV_BAD_BLOCK */);
                     phys = -1;
                 }
                 good = phys >= 0 && (!p.valid || ((p.valid[phys >> 5] >> (phys & 31)) & 1u));
-                if (good && pk < pos0) {
-                    ks = cache + p.layer_off + (((long long)phys * p.Hkv + h) * p.bs + pk % p.bs) * D;
-                    vs = ks + p.kv_off;
-                }
+                if (good && pk < pos0) sv = p.layer_off + (((long long)phys * p.Hkv + h) * p.bs + pk % p.bs) * D;
             } else if (good && pk < pos0) {
                 const int slot = pk < p.sinks ? pk : p.sinks + (int)((unsigned)(pk - p.sinks) % (unsigned)p.window);
-                ks = cache + p.layer_off + (unit * C + slot) * D;
-                vs = ks + p.kv_off;
+                sv = p.layer_off + (unit * C + slot) * D;
             }
-            if (good && pk >= pos0) {                    // a row of the chunk itself
-                const long long row = (((long long)b * p.T + (pk - pos0)) * p.Hkv + h) * D;
-                ks = kst + row;
-                vs = vst + row;
-            }
-            if (good) {
-                cp_async16(Kb + pf_off<D>(r, ch), ks + ch * 8);
-                cp_async16(Vb + pf_off<D>(r, ch), vs + ch * 8);
-            } else {
+            if (good && pk >= pos0)                      // a row of the chunk itself
+                sv = -((((long long)b * p.T + (pk - pos0)) * p.Hkv + h) * D) - 2;
+            src[r] = good ? sv : -1;
+            ok[r] = good ? 1 : 0;
+        }
+        __syncthreads();
+        constexpr int kRowsPerPass = kPfThreads / S::kChunks;
+        const int ch = tid % S::kChunks;
+        for (int r = tid / S::kChunks; r < kPfKeys; r += kRowsPerPass) {
+            const long long sv = src[r];
+            if (sv == -1) {
                 *reinterpret_cast<uint4*>(Kb + pf_off<D>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(Vb + pf_off<D>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const __nv_bfloat16* ks = sv >= 0 ? cache + sv : kst + (-sv - 2);
+                const __nv_bfloat16* vs = sv >= 0 ? ks + p.kv_off : vst + (-sv - 2);
+                cp_async16(Kb + pf_off<D>(r, ch), ks + ch * 8);
+                cp_async16(Vb + pf_off<D>(r, ch), vs + ch * 8);
             }
-            if (ch == 0) ok[r] = good ? 1 : 0;
         }
     };
 
