@@ -49,8 +49,10 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Three CTAs per SM (168 registers a thread): measured 163 -> 169 TFLOP/s on
+// ring chunks, 185 -> 236 on the paged batch, against two at 173 registers.
 template <int D>
-__global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_constant__ PrefillParams p) {
     using S = PfShape<D>;
     extern __shared__ __align__(128) unsigned char pf_smem[];
     int* rowok = reinterpret_cast<int*>(pf_smem + 2 * S::kBuf);      // [2][kPfKeys]
