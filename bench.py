@@ -352,7 +352,7 @@ class ClockSampler:
 KERNEL_TRAFFIC = {"ring_bf16": 138023936, "sink_window_bf16": 544682240,
                   "paged_shared_prefix_bf16": 901444096, "long_context_pool_bf16": 153010688,
                   "ring_int8": 69377113}
-KERNEL_TRAFFIC_SOURCES = "89a889e7a237c9542d4df82fe52c77c6b9b05e6f711c0a07e8de63e93ff4b770"
+KERNEL_TRAFFIC_SOURCES = "b47253d875aa61897b0e36fb31dd83a3cf7c323aea62f9c76e321c0f83a346e0"
 
 
 # the sources decode_mma_kernel and its launch are built from

@@ -2,7 +2,9 @@
  * kvc.h - C ABI of the decode-step KV-cache attention library (libkvc.so).
  *
  * One new query per sequence attends over a fixed-capacity KV cache kept in
- * one of three layouts, and the new token's K/V is appended to that cache.
+ * one of three layouts, and the new token's K/V is appended to that cache;
+ * a chunk of new tokens can be prefilled the same way (kvc_prefill), and the
+ * cache can hold bf16, fp32 or per-row INT8 rows.
  * The operations follow these pages (cited by title and section):
  *
  *   [ring]   "Why sliding-window attention decodes with a ring KV cache"

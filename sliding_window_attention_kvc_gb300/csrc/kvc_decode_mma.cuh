@@ -1,4 +1,5 @@
-// Split-K decode attention for bf16 caches on the tensor cores, stream-K.
+// Split-K decode attention for bf16 and INT8 caches on the tensor cores,
+// stream-K.
 //
 // Work decomposition.  For each (kv head, q-head group) the attended rows of
 // all sequences, laid end to end, are cut into gridDim.x nearly equal
@@ -17,6 +18,9 @@
 //     O += P V    A = exp2(S - m) rounded to bf16, B = V rows, k = 16 tokens.
 // On a q head group of 4 the CUDA-core formulation spent ~97 warp
 // instructions per cached token (measured); these two products cost ~4.
+// INT8 rows (the Q8 variant) enter as fp16: codes are exact in fp16, q is
+// scaled by a power of two per head, and P V is computed as V^T P^T so that
+// a lane's V bytes form A fragments (see the Q8 branches below).
 //
 // Data movement.  Warp 4 walks the CTA's segments and cuts them into *runs*
 // of up to 64 consecutive cache rows (a paged block, or the slots of a ring
