@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const __grid_c
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
     plan_pdl_wait();            // positions, table, valid bits may come from the previous kernel
+    // the next kernel (the decode kernel, or plan_items_kernel) may launch now:
+    // it waits for this grid to complete before it reads anything
+    plan_pdl_launch();
     const int32_t* trow = p.table + (long long)b * p.maxb;
     constexpr int kChunk = kPlanThreads * kPlanPerThread;
     __shared__ int s_tok_phys;
