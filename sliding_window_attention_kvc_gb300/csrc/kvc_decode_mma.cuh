@@ -1283,7 +1283,6 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                     vw[hlf][1] = *reinterpret_cast<const uint4*>(Vs + hd * bstride + (ta + 1) * 128 +
                                                                  ((g ^ ((ta + 1) & 7)) << 4));
                 }
-                float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int k2 = 0; k2 < D / 32; ++k2) {
 #pragma unroll
@@ -1291,16 +1290,9 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                         const uint32_t a = (s2 ? kw[k2][0].y : kw[k2][0].x) ^ 0x80808080u;
                         const uint32_t e = (s2 ? kw[k2][1].y : kw[k2][1].x) ^ 0x80808080u;
                         const int ks = 2 * k2 + s2;
-                        float (&acc)[2][4] = (kQ8SplitChains && s2) ? sb : sa;
-                        mma_f16_16816(acc[0], qa[ks][0], 0u, qa[ks][1], 0u, q8_f16x2(a, 0x4140u), q8_f16x2(a, 0x4342u));
-                        mma_f16_16816(acc[1], qa[ks][0], 0u, qa[ks][1], 0u, q8_f16x2(e, 0x4140u), q8_f16x2(e, 0x4342u));
+                        mma_f16_16816(sa[0], qa[ks][0], 0u, qa[ks][1], 0u, q8_f16x2(a, 0x4140u), q8_f16x2(a, 0x4342u));
+                        mma_f16_16816(sa[1], qa[ks][0], 0u, qa[ks][1], 0u, q8_f16x2(e, 0x4140u), q8_f16x2(e, 0x4342u));
                     }
-                }
-                if constexpr (kQ8SplitChains) {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sa[i][e] += sb[i][e];
                 }
             } else {
                 const int tok = ((lane >> 4) << 3) + (lane & 7);

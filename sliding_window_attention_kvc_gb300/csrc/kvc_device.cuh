@@ -135,7 +135,6 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-__device__ __forceinline__ float exp2_approx(float x) { return exp2f(x); }
 
 }  // namespace kvc
 
@@ -144,15 +143,6 @@ namespace kvc {
 // ---------------------------------------------------------------------------
 // 2-D tensor copies (TMA) and tensor-core fragments for the bf16 kernel
 // ---------------------------------------------------------------------------
-
-// Box load of a 2-D tensor map at element coordinates (x, y) into shared
-// memory; completion counted on `bar` as transaction bytes.
-__device__ __forceinline__ void tma_load_2d(void* dst_smem, const void* tmap, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_u32(dst_smem)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
 
 // Box loads of a 4-D / 5-D tensor map at element coordinates (x, y, z, w[, v]).
 __device__ __forceinline__ void tma_load_4d(void* dst_smem, const void* tmap, int x, int y, int z, int w,

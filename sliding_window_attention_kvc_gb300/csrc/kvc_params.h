@@ -30,12 +30,9 @@ constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs 
 // bytes of bf16 ones; paged INT8 batches at head_dim <= 128 run three CTAs
 // per SM (the compute warps are the bound there; measured 164 -> 151 us on
 // the shared-prefix batch, while the ring lost 2% and head_dim 256 spills).
-// Q K^T of INT8 rows may accumulate even and odd k-steps in separate
-// registers (two shorter dependency chains): measured no gain, kept off.
 constexpr int decode_ctas_per_sm(bool q8, bool paged, bool read, int D) {
     return (read && D >= 256) ? 1 : ((q8 && paged && D <= 128) ? 3 : 2);
 }
-constexpr bool kQ8SplitChains = false;
 
 enum Layout : int { kRing = 0, kSinkRing = 1, kPaged = 2 };
 enum Rope : int { kRopeNone = 0, kRopeBaked = 1, kRopeRead = 2 };
