@@ -349,10 +349,10 @@ class ClockSampler:
 # capture per workload (summaries: profiles/decode_mma_<workload>.md), and the
 # digest of the kernel's sources (KERNEL_TRAFFIC_FILES) they were taken on:
 # reported only while those sources are unchanged.
-KERNEL_TRAFFIC = {"ring_bf16": 138023936, "sink_window_bf16": 544682240,
-                  "paged_shared_prefix_bf16": 901444096, "long_context_pool_bf16": 153010688,
-                  "ring_int8": 69377113}
-KERNEL_TRAFFIC_SOURCES = "b47253d875aa61897b0e36fb31dd83a3cf7c323aea62f9c76e321c0f83a346e0"
+KERNEL_TRAFFIC = {"ring_bf16": 137971712, "sink_window_bf16": 545077248,
+                  "paged_shared_prefix_bf16": 894324480, "long_context_pool_bf16": 153829120,
+                  "ring_int8": 69380806}
+KERNEL_TRAFFIC_SOURCES = "a38a479b073c576c6a3243a9b6697d2481bb30c00fc5adf641d0d0a62d752d26"
 
 
 # the sources decode_mma_kernel and its launch are built from
