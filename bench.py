@@ -352,7 +352,7 @@ class ClockSampler:
 KERNEL_TRAFFIC = {"ring_bf16": 137971712, "sink_window_bf16": 545077248,
                   "paged_shared_prefix_bf16": 894324480, "long_context_pool_bf16": 153829120,
                   "ring_int8": 69380806}
-KERNEL_TRAFFIC_SOURCES = "a38a479b073c576c6a3243a9b6697d2481bb30c00fc5adf641d0d0a62d752d26"
+KERNEL_TRAFFIC_SOURCES = "daec053141b84c75f772008f5c13b436bf8d40f257560ef093fe0589115af420"
 
 
 # the sources decode_mma_kernel and its launch are built from
@@ -852,14 +852,16 @@ def measure_pagein(args):
 def measure_prefill(args):
     """Chunked prefill (kvc_prefill) of T = --chunk tokens per sequence on a
     bf16 workload (default ring_bf16: 8 sequences, 32 q / 8 kv heads, D 128,
-    a full 4096-slot ring), each chunk ending at the workload's position t_b,
+    a full 4096-slot ring; also sink_window_bf16, whose RoPE is applied at
+    read time, and paged_shared_prefix_bf16), each chunk ending at the workload's position t_b,
     the cache holding every earlier position.  One call stages the chunk,
     runs the attention and appends the chunk.  L2 is flushed (a 256 MiB write)
     between timed calls; each call is timed with CUDA events.  Reports tokens/s
     and the attention's algorithmic TFLOP/s (4 D flops per (token, q head,
     attended key): q.k and p.v) against the measured bf16 tensor peak."""
     kvc = _kvc()
-    name = args.workload if args.workload in ("ring_bf16", "paged_shared_prefix_bf16") else "ring_bf16"
+    name = args.workload if args.workload in ("ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16") \
+        else "ring_bf16"
     wl = kvc_synth.make_workload(name)
     T = args.chunk
     pos0 = np.maximum(wl.positions - T + 1, 0)

@@ -220,8 +220,10 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
  *   out        [batch, T, q_heads, head_dim] bf16.
  *   workspace  kvc_prefill_workspace_bytes(d, T) bytes: the decode workspace
  *              followed by the chunk's staged rows.
- * bf16 caches, head_dim 64 or 128, RoPE NONE or BAKED (KVC_ERR_UNSUPPORTED
- * otherwise).  Calls on one workspace must not overlap on the GPU. */
+ * READ_INCACHE: each token's window keys at distance t - p and its sinks at
+ * min(t, C - 1) - p, as the decode step at t rotates them.
+ * bf16 caches, head_dim 64 or 128 (KVC_ERR_UNSUPPORTED otherwise).  Calls on
+ * one workspace must not overlap on the GPU. */
 KVC_API size_t kvc_prefill_workspace_bytes(const kvc_desc* d, int32_t T);
 KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const void* q,
                         const void* k_new, const void* v_new, int32_t T, const int32_t* pos0,

@@ -572,9 +572,7 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     Geo g;
     int rc = check_desc(d, &g);
     if (rc) return rc;
-    if (d->dtype != KVC_BF16 || d->rope == KVC_ROPE_READ_INCACHE || (d->head_dim != 64 && d->head_dim != 128) ||
-        g.G > 64)
-        return KVC_ERR_UNSUPPORTED;
+    if (d->dtype != KVC_BF16 || (d->head_dim != 64 && d->head_dim != 128) || g.G > 64) return KVC_ERR_UNSUPPORTED;
     if (!cache || !q || !k_new || !v_new || !pos0 || !out || !workspace) return KVC_ERR_NULL;
     const bool paged = d->layout == KVC_LAYOUT_PAGED;
     if (paged && !block_table) return KVC_ERR_NULL;
@@ -641,7 +639,7 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     pp.rope = d->rope;
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
     pp.q_scale = scale * 1.4426950408889634f;
-    if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
+    if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
     if (launch_prefill(d->head_dim, g.G, pp, s) != cudaSuccess) return KVC_ERR_CUDA;
     // 3. the chunk appended
     if (launch_append(d->dtype, ap, s) != cudaSuccess) return KVC_ERR_CUDA;

@@ -51,7 +51,9 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // Three CTAs per SM (168 registers a thread): measured 163 -> 169 TFLOP/s on
 // ring chunks, 185 -> 236 on the paged batch, against two at 173 registers.
-template <int D>
+// READ: read-time RoPE (a separate instance, so the none/baked kernel carries
+// none of its code or registers).
+template <int D, bool READ>
 __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_constant__ PrefillParams p) {
     using S = PfShape<D>;
     extern __shared__ __align__(128) unsigned char pf_smem[];
@@ -90,9 +92,11 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_con
     const bool all_rows = pos0 + i0 >= 0 && i0 + tq <= p.T;
 
     // q fragments (A of Q K^T): rows g, g + 8; columns 16 ks + 2c (+1), + 8;
-    // rotated at the token's position (baked RoPE), scaled by q_scale, bf16
+    // rotated (RoPE) at the token's position t, or at min(t, C - 1) for the
+    // sink keys of read-time RoPE (sinks_ip), scaled by q_scale, bf16
+    constexpr bool read_rope = READ;
     uint32_t qa[S::kKsteps][4];
-    {
+    auto load_q = [&](bool sinks_ip) {
         float qf[2][S::kKsteps][4];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -108,14 +112,15 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_con
                     qf[e][ks][2 * hf + 1] = __uint_as_float(w & 0xffff0000u);
                 }
             }
-            if (p.rope == kRopeBaked && row_ok[e] && row_t[e] >= 0) {
+            if (p.rope != kRopeNone && row_ok[e] && row_t[e] >= 0) {
+                const long long qpos = sinks_ip ? min(row_t[e], C - 1) : row_t[e];
 #pragma unroll
                 for (int ks = 0; ks < S::kKsteps / 2; ++ks) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int i = 16 * ks + 8 * (k >> 1) + 2 * c + (k & 1);
                         float cs, sn;
-                        rope_cos_sin((long long)row_t[e], p.theta[i], &cs, &sn);
+                        rope_cos_sin(qpos, p.theta[i], &cs, &sn);
                         const float x1 = qf[e][ks][k], x2 = qf[e][ks + S::kKsteps / 2][k];
                         qf[e][ks][k] = x1 * cs - x2 * sn;
                         qf[e][ks + S::kKsteps / 2][k] = x1 * sn + x2 * cs;
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_con
             qa[ks][2] = pack_bf16x2(qf[0][ks][2] * p.q_scale, qf[0][ks][3] * p.q_scale);
             qa[ks][3] = pack_bf16x2(qf[1][ks][2] * p.q_scale, qf[1][ks][3] * p.q_scale);
         }
-    }
+    };
 
     // key ranges: window layouts [0, min(S, t_hi + 1)) and [max(S, t_lo - W + 1), t_hi];
     // paged [0, t_hi]
@@ -147,6 +152,11 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_con
         }
     }
     const int n0 = (r0e - r0b + kPfKeys - 1) / kPfKeys;
+    // read-time RoPE: a window key at distance t - p from the query, a sink key
+    // at min(t, C - 1) - p ([sink] "RoPE cache position shifting"): keys are
+    // rotated at their own positions in shared memory, the query at t, or at
+    // min(t, C - 1) for the sink tiles, which come first
+    load_q(read_rope && n0 > 0);
     const int ntiles = n0 + (r1e > r1b ? (r1e - r1b + kPfKeys - 1) / kPfKeys : 0);
     auto tile_base = [&](int k) { return k < n0 ? r0b + k * kPfKeys : r1b + (k - n0) * kPfKeys; };
     auto tile_end = [&](int k) { return k < n0 ? r0e : r1e; };
@@ -220,6 +230,29 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_con
         const unsigned char* Vb = Kb + S::kTile;
         const int* ok = rowok + (k & 1) * kPfKeys;
         const int base = tile_base(k);
+        if constexpr (READ) {
+            if (k == n0 && n0 > 0) load_q(false);      // past the sink tiles: q at t
+            // rotate the raw K rows of the tile at their positions base + r: thread
+            // tid takes rotation pair i = tid % (D/2) of rows r0 .. r0 + kRun - 1,
+            // one exact angle, then the step R(theta_i) from row to row
+            constexpr int HALF = D / 2, kRun = kPfKeys * HALF / kPfThreads;
+            const int i = tid % HALF, r0 = (tid / HALF) * kRun;
+            float c0, s0, cst, sst;
+            rope_cos_sin((long long)(base + r0), p.theta[i], &c0, &s0);
+            rope_cos_sin(1, p.theta[i], &cst, &sst);
+            unsigned char* Kw = const_cast<unsigned char*>(Kb);
+            for (int r = r0; r < r0 + kRun; ++r) {
+                __nv_bfloat16* lo = reinterpret_cast<__nv_bfloat16*>(Kw + pf_off<D>(r, i >> 3) + (i & 7) * 2);
+                __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(Kw + pf_off<D>(r, (i + HALF) >> 3) + (i & 7) * 2);
+                const float x1 = __bfloat162float(*lo), x2 = __bfloat162float(*hi);
+                *lo = __float2bfloat16_rn(x1 * c0 - x2 * s0);
+                *hi = __float2bfloat16_rn(x1 * s0 + x2 * c0);
+                const float cn = c0 * cst - s0 * sst;
+                s0 = s0 * cst + c0 * sst;
+                c0 = cn;
+            }
+            __syncthreads();
+        }
 
         // ---- S = Q K^T: 16 rows x 64 keys (8 n-tiles) -----------------------
         float s[8][4];
@@ -338,7 +371,7 @@ __global__ void __launch_bounds__(kPfThreads, 3) prefill_kernel(const __grid_con
     }
 }
 
-template <int D>
+template <int D, bool READ>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
     using S = PfShape<D>;
     static std::atomic<unsigned long long> configured{0};
@@ -347,20 +380,21 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_relaxed) & bit)) {
-        e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+        e = cudaFuncSetAttribute(prefill_kernel<D, READ>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_relaxed);
     }
     const int tq = kPfRows / p.G;
     dim3 grid((p.T + tq - 1) / tq, p.Hkv, p.B);
-    prefill_kernel<D><<<grid, kPfThreads, S::kSmem, stream>>>(p);
+    prefill_kernel<D, READ><<<grid, kPfThreads, S::kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(int head_dim, int g, const PrefillParams& p, cudaStream_t stream) {
     if (g < 1 || g > kPfRows) return cudaErrorInvalidValue;
-    if (head_dim == 64) return launch_prefill_t<64>(p, stream);
-    if (head_dim == 128) return launch_prefill_t<128>(p, stream);
+    const bool read = p.rope == kRopeRead;
+    if (head_dim == 64) return read ? launch_prefill_t<64, true>(p, stream) : launch_prefill_t<64, false>(p, stream);
+    if (head_dim == 128) return read ? launch_prefill_t<128, true>(p, stream) : launch_prefill_t<128, false>(p, stream);
     return cudaErrorInvalidValue;
 }
 

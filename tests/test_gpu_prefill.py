@@ -8,7 +8,8 @@ the cache after a plain kvc_append of the same chunk (so the ring slots the
 chunk overwrites were read before they were overwritten).  Cases: ring with a
 chunk across the first wrap and far past it, sink + ring, paged with shared
 prefix blocks, a chunk that starts at position 0, ragged chunk lengths (not a
-multiple of the 16 tokens a CTA takes), left padding, RoPE none and baked.
+multiple of the 16 tokens a CTA takes), left padding, RoPE none, baked and read
+at in-cache positions.
 """
 
 import dataclasses
@@ -85,6 +86,10 @@ CASES = {
     "ring_none_long": ("ring_bf16", "none", [0, 64, 1000], 70),
     "sink_baked": ("sink_window_bf16", "baked", [3, 180, 987600], 45),
     "sink_none": ("sink_window_bf16", "none", [100, 150, 50000], 33),
+    # read-time RoPE (the sink workload's own mode): keys rotated at their
+    # in-cache positions relative to each chunk token
+    "sink_read": ("sink_window_bf16", "read_time", [3, 180, 987600], 45),
+    "ring_read": ("ring_bf16", "read_time", [150, 190, 4300], 37),
 }
 
 

@@ -135,8 +135,8 @@ def test_argument_errors_return_codes_without_launching(kvc):
     df = _desc(kvc, dtype="f32")
     assert L.kvc_prefill(ctypes.byref(df), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
         kvc.KVC_ERR_UNSUPPORTED
-    dr = _desc(kvc, layout="sink_ring", sinks=4, window=96, rope="read_time")
-    assert L.kvc_prefill(ctypes.byref(dr), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
+    d256 = _desc(kvc, head_dim=256)
+    assert L.kvc_prefill(ctypes.byref(d256), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
         kvc.KVC_ERR_UNSUPPORTED
 
 
