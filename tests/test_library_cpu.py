@@ -126,7 +126,7 @@ def test_argument_errors_return_codes_without_launching(kvc):
     assert L.kvc_block_release(dg, A, None, A, A, A, -1, A, A, nws, None) == kvc.KVC_ERR_ARG
     assert L.kvc_block_release(dg, A, None, A, A, None, 1, A, A, nws, None) == kvc.KVC_ERR_NULL
     assert "free" in kvc.strerror(kvc.KVC_DEV_NO_FREE_BLOCK)
-    # chunked prefill: bf16 caches, head_dim 64 / 128, no read-time RoPE; sizes checked first
+    # chunked prefill: bf16 caches, head_dim 64 / 128 (fp32 and D 256 refused); sizes checked first
     pw = kvc.prefill_workspace_bytes(d, 16)
     assert pw > ws_n and kvc.prefill_workspace_bytes(d, 0) == 0
     assert L.kvc_prefill(dp, A, 0, A, A, A, 0, A, None, None, A, A, pw, None) == kvc.KVC_ERR_ARG
