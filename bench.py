@@ -431,13 +431,24 @@ def oracle_sample(wl, budget_s, max_rows=None, part=(0, 1)):
     return done_bytes, spent, units
 
 
-def _oracle_worker(name, budget_s, k, n):
+def _oracle_worker(name, kw, budget_s, k, n):
     """One process of the all-core oracle timing (spawned: one BLAS thread)."""
-    wl = kvc_synth.make_workload(name)
+    wl = kvc_synth.make_workload(name, **kw)
     return oracle_sample(wl, budget_s, part=(k, n))
 
 
-def cpu_baseline(wl, budget_s=10.0, cores=None):
+def _workload_kw(args):
+    """Generator options taken from the command line (the pool's valid density)."""
+    if getattr(args, "density", None) is None:
+        return {}
+    if not args.workload.startswith("long_context_pool"):
+        raise SystemExit("--density applies to long_context_pool_bf16 only")
+    if not 0.0 <= args.density <= 1.0:
+        raise SystemExit("--density must be in [0, 1]")
+    return {"density": args.density}
+
+
+def cpu_baseline(wl, budget_s=10.0, cores=None, kw=None):
     """The fp64 oracle on the host cores: all cores (a spawn-started process
     per core over disjoint sequences, for the same budget of wall time), and
     one core, over bounded samples of the workload's units."""
@@ -455,7 +466,7 @@ def cpu_baseline(wl, budget_s=10.0, cores=None):
         try:
             with mpr.get_context("spawn").Pool(cores) as pool:
                 t0 = time.perf_counter()
-                res = pool.starmap(_oracle_worker, [(wl.name, budget_s, k, cores) for k in range(cores)])
+                res = pool.starmap(_oracle_worker, [(wl.name, kw or {}, budget_s, k, cores) for k in range(cores)])
                 wall = time.perf_counter() - t0
         finally:
             for k, v in env.items():
@@ -531,7 +542,8 @@ def run_reference(args):
     rank, world, _ = _dist()
     if rank != 0:
         return None
-    wl = kvc_synth.make_workload(args.workload)
+    kw = _workload_kw(args)
+    wl = kvc_synth.make_workload(args.workload, **kw)
     per_step = max(0.002, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
     # rows per step sized to the per-step budget (about 25k rows/s for D=128)
     rows = max(64, int(per_step * 25000 * 128 / wl.head_dim))
@@ -548,7 +560,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_s / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name},
+            "config": {"workload": wl.name, **kw},
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"each step: up to {rows} attended rows of (sequence, kv head) units, "
                                        f"~{per_step:.3f} s of fp64 oracle time; {tot_u} units, wall {wall:.1f} s"},
@@ -560,7 +572,8 @@ def run_ours(args):
     rank, world, local = _dist()
     torch.cuda.set_device(local)
     replica_init(world, "nccl", torch.device("cuda", local))
-    wl = kvc_synth.make_workload(args.workload)
+    kw = _workload_kw(args)
+    wl = kvc_synth.make_workload(args.workload, **kw)
     layers = args.layers or DEFAULT_LAYERS[args.workload]
     st = DecodeState(wl, layers, source="device", num_splits=args.num_splits)
     fc = FastCalls(st)
@@ -662,7 +675,7 @@ def run_ours(args):
                    "block_size": wl.block_size, "layers_cycled": layers, "rope": wl.rope,
                    "l2": f"inputs larger than L2: {layers} layers cycled, "
                          f"{layers * nb['kv_unique'] / 2**20:.0f} MiB of attended K/V",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", **kw},
         "steps_per_s": 1e3 / ms_per_step,
         "bytes_per_step": nb,
         "decode_kernel_ms": dec_mean,
@@ -670,7 +683,7 @@ def run_ours(args):
         "eager_ms_per_step": eager_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _traffic(wl.name, args.traffic),
+                     "traffic": _traffic(wl.name, args.traffic) if not kw else args.traffic,
                      "traffic_kernel": "decode_mma_kernel, dram__bytes_read.sum + dram__bytes_write.sum per launch",
                      "kernel": "kvc_decode_step: " + ("decode_mma_kernel + combine_streamk_kernel"
                                                       if wl.dtype in ("bf16", "i8") else "append + decode"),
@@ -682,7 +695,7 @@ def run_ours(args):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget, kw=kw)
     replica_done(world)
     return line if rank == 0 else None
 
@@ -927,6 +940,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(kvc_synth.WORKLOAD_NAMES), default=DEFAULT_WORKLOAD)
     ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--density", type=float, default=None,
+                    help="long_context_pool_bf16: valid-bit density of the pool's slots (default 0.5)")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

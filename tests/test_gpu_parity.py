@@ -196,15 +196,18 @@ def test_decode_small_elementwise(kvc, name, num_splits):
     assert kvc.get_error(st.ws) == 0
 
 
-@pytest.mark.parametrize("name,seqs", [
-    ("ring_bf16", [0, 5, 7]),
-    ("sink_window_bf16", [0, 13, 31]),
-    ("paged_shared_prefix_bf16", [0, 9, 40, 63]),
-    ("long_context_pool_bf16", [0]),
+@pytest.mark.parametrize("name,seqs,kw", [
+    ("ring_bf16", [0, 5, 7], {}),
+    ("sink_window_bf16", [0, 13, 31], {}),
+    ("paged_shared_prefix_bf16", [0, 9, 40, 63], {}),
+    ("long_context_pool_bf16", [0], {}),
+    # the pool's valid-density sweep (0.25 and every slot valid)
+    ("long_context_pool_bf16", [0], {"density": 0.25}),
+    ("long_context_pool_bf16", [0], {"density": 1.0}),
 ])
-def test_decode_full_size_sampled(kvc, name, seqs):
+def test_decode_full_size_sampled(kvc, name, seqs, kw):
     """Full workload sizes, bench.py's launch configuration, sampled sequences."""
-    wl = kvc_synth.make_workload(name)
+    wl = kvc_synth.make_workload(name, **kw)
     st = bench.DecodeState(wl, 1, source="cpu")
     got = st.step(0).float().cpu().numpy()
     assert np.isfinite(got).all()

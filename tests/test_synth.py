@@ -1,6 +1,7 @@
 """The seeded input generator: determinism, keying, workload structure."""
 
 import numpy as np
+import pytest
 import torch
 
 from kvc_synth import POSITION_BLOCK, make_workload, randn
@@ -61,6 +62,37 @@ def test_pool_workload_structure():
     assert sorted(mapped) == list(range(1024))
     assert (tb[-64:] >= 0).all() and wl.valid[tb[-64:]].all()
     assert 0.4 < wl.valid.mean() < 0.6
+
+
+@pytest.mark.parametrize("density", [0.25, 1.0])
+def test_pool_valid_density_sweep(density):
+    # the same resident blocks and slot order; only the valid bits follow the
+    # density, and the last 4096 tokens stay valid
+    base = long_context_pool_bf16(small=False)
+    wl = long_context_pool_bf16(small=False, density=density)
+    assert np.array_equal(wl.block_table, base.block_table)
+    tb = wl.block_table[0]
+    assert wl.valid[tb[-64:]].all()
+    # Bernoulli(density) over the 960 earlier slots, plus the 64 forced ones
+    assert abs(wl.valid.mean() - (density + (1 - density) * 64 / 1024)) < 0.03
+    if density == 1.0:
+        assert wl.valid.all()
+
+
+def test_bench_density_option_is_pool_only():
+    import argparse
+
+    import bench
+    ns = argparse.Namespace(workload="long_context_pool_bf16", density=0.25)
+    assert bench._workload_kw(ns) == {"density": 0.25}
+    assert bench._workload_kw(argparse.Namespace(workload="ring_bf16", density=None)) == {}
+    with pytest.raises(SystemExit):
+        bench._workload_kw(argparse.Namespace(workload="ring_bf16", density=0.25))
+    with pytest.raises(SystemExit):
+        bench._workload_kw(argparse.Namespace(workload="long_context_pool_bf16", density=1.5))
+    rows = [bench.step_bytes(make_workload("long_context_pool_bf16", density=x))["kv_unique"]
+            for x in (0.25, 0.5, 1.0)]
+    assert rows[0] < rows[1] < rows[2]
 
 
 def test_full_size_shapes():
