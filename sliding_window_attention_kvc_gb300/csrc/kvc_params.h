@@ -222,6 +222,7 @@ cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
 // kvc_prefill: the chunk's rows staged (K rotated as stored), then attention.
 cudaError_t launch_prefill_stage(const AppendParams& p, void* kst, void* vst, cudaStream_t stream);
 cudaError_t launch_prefill(int head_dim, int g, const PrefillParams& p, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);   // head_dim 128, tcgen05
 cudaError_t launch_valid_write(const TableParams& p, cudaStream_t stream);
 cudaError_t launch_block_prepare(int elt, const BlockParams& p, cudaStream_t stream);
 cudaError_t launch_block_share(const BlockParams& p, int n, cudaStream_t stream);

@@ -390,11 +390,12 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// head_dim 128 runs on the tcgen05 kernel (kvc_prefill_tc.cu), head_dim 64 here.
 cudaError_t launch_prefill(int head_dim, int g, const PrefillParams& p, cudaStream_t stream) {
     if (g < 1 || g > kPfRows) return cudaErrorInvalidValue;
     const bool read = p.rope == kRopeRead;
     if (head_dim == 64) return read ? launch_prefill_t<64, true>(p, stream) : launch_prefill_t<64, false>(p, stream);
-    if (head_dim == 128) return read ? launch_prefill_t<128, true>(p, stream) : launch_prefill_t<128, false>(p, stream);
+    if (head_dim == 128) return launch_prefill_tc(p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -90,13 +90,18 @@ CASES = {
     # in-cache positions relative to each chunk token
     "sink_read": ("sink_window_bf16", "read_time", [3, 180, 987600], 45),
     "ring_read": ("ring_bf16", "read_time", [150, 190, 4300], 37),
+    # head_dim 64 (the mma.sync kernel; 128 runs on tcgen05)
+    "ring_d64": ("ring_bf16", "baked", [150, 190, 4300], 37, {"head_dim": 64}),
+    "sink_read_d64": ("sink_window_bf16", "read_time", [3, 180, 987600], 45, {"head_dim": 64}),
+    # several CTAs per (sequence, kv head) along the chunk
+    "ring_long_chunk": ("ring_bf16", "baked", [150, 190, 4300], 130),
 }
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_prefill_window_layouts(kvc, case):
-    name, rope, pos0, T = CASES[case]
-    wl = dataclasses.replace(kvc_synth.make_workload(name, small=True), rope=rope)
+    name, rope, pos0, T, *extra = CASES[case]
+    wl = dataclasses.replace(kvc_synth.make_workload(name, small=True), rope=rope, **(extra[0] if extra else {}))
     got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
     assert np.isfinite(got).all()
     for b in range(wl.batch):
