@@ -924,7 +924,7 @@ def measure_prefill(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "algorithmic_flops_per_call": flops,
-                         "kernel": "kvc_prefill: prefill_stage_kernel + prefill_kernel (mma.sync) + append_kernel",
+                         "kernel": "kvc_prefill: prefill_stage_kernel + prefill_tc_kernel (tcgen05, head_dim 128) + append_kernel",
                          "timer": "CUDA events around each call, median, L2 flushed between calls"},
             "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "chunk_tokens": T, "batch": B, "q_heads": Hq, "kv_heads": Hkv,

@@ -16,8 +16,9 @@
 //                    updates its running max and sum (base 2) and writes its
 //                    bf16 probabilities over the K tile, which S no longer needs
 //   O  = O a + P V   O lives in TMEM columns 0..127; a row is rescaled in place
-//                    (tcgen05.ld / st) only when its running max rose; P V is
-//                    tcgen05.mma M=128 N=128 K=64, V as an N-major operand
+//                    (tcgen05.ld / st) only when its reference max moved (by
+//                    more than 8 in base 2); P V is tcgen05.mma M=128 N=128
+//                    K=64, V as an N-major operand
 // Completion of each product is tracked by an mbarrier (tcgen05.commit); every
 // wait is bounded and the decision to stop is taken by the whole CTA.
 #include "kvc_decode.cuh"
@@ -43,6 +44,7 @@ constexpr int kTcSmem = kTcOffMeta + kTcMeta + 1024;   // + room to align the ba
 constexpr int kTcOCol = 0;                          // O: TMEM columns [0, 128)
 constexpr int kTcSCol = 128;                        // S: TMEM columns [128, 192)
 constexpr int kTcTmemCols = 256;
+constexpr float kTcLazy = 8.f;                      // lazy rescale threshold (log2 units)
 // two CTAs fit an SM by shared memory (228 KiB, 1 KiB reserved per CTA) and
 // three do not, so the CTAs of one SM never ask for more than its 512 columns
 static_assert(2 * (kTcSmem + 1024) <= 228 * 1024 && 3 * (kTcSmem + 1024) > 228 * 1024, "occupancy");
@@ -352,6 +354,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const __grid_
             tc_commit(bar_s);
         }
         issued_s = k;
+        // P V of tile k - 1 (queued before S) completes first: O may be rescaled
+        // below, and buffer (k + 1) & 1 (tile k - 1's K/P and V) takes tile k + 1
+        // now, while S, the softmax and P V of tile k run
+        if (k > 0) {
+            if (__syncthreads_or(!mbar_wait(bar_o, (k - 1) & 1))) {
+                dead = true;
+                break;
+            }
+            tc_fence_after();
+            if (k + 1 < ntiles) load_tile(k + 1);
+            tc_cp_async_commit();
+        }
         if (__syncthreads_or(!mbar_wait(bar_s, k & 1))) {
             dead = true;
             break;
@@ -384,8 +398,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const __grid_
                 mx = fmaxf(mx, s[j]);
             }
         }
-        const float mn = fmaxf(m_run, mx);
-        const float alpha = (mn == -INFINITY || mn == m_run) ? 1.f : exp2f(m_run - mn);
+        // the row's reference max moves only when the tile's max exceeds it by
+        // more than kTcLazy (base 2): probabilities stay below 2^kTcLazy, and O
+        // and l share the reference, so the result is unchanged while most
+        // tiles skip the rescale of O
+        float mn = m_run, alpha = 1.f;
+        if (mx > m_run + kTcLazy) {
+            mn = mx;
+            alpha = m_run == -INFINITY ? 1.f : exp2f(m_run - mn);   // no attended key yet: O's row is zero
+        }
         float ls = 0.f;
 #pragma unroll
         for (int j = 0; j < kTcKeys; ++j) {
@@ -395,16 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) prefill_tc_kernel(const __grid_
         l_run = l_run * alpha + ls;
         m_run = mn;
 
-        // P V of tile k - 1 must be complete: O is rescaled below, and buffer
-        // (k + 1) & 1 (tile k - 1's K/P and V) is refilled with tile k + 1
         if (k > 0) {
-            if (__syncthreads_or(!mbar_wait(bar_o, (k - 1) & 1))) {
-                dead = true;
-                break;
-            }
-            tc_fence_after();
-            if (k + 1 < ntiles) load_tile(k + 1);
-            tc_cp_async_commit();
             // tcgen05.ld / st are warp-wide: a warp rescales when any of its rows
             // needs it (alpha is 1 for the others)
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
