@@ -1,4 +1,5 @@
-// Chunked prefill attention for bf16 caches ([pool] "the real cost of long
+// Chunked prefill attention for bf16 caches at head_dim 64 (head_dim 128 runs
+// on the tcgen05 kernel of kvc_prefill_tc.cu) ([pool] "the real cost of long
 // context": prefill in chunks of 128-256 tokens, one mechanism with the paged
 // pool; [ring] 3.1 and 5.2: during prefill the window is a mask on the score
 // matrix).
