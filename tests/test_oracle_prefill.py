@@ -122,3 +122,61 @@ def test_left_padding_rows_are_zero():
     assert not got[:2].any()
     want = prefill.prefill_sequence(q[2:], K, V, 0, lambda t: layouts.window_attended(t, 0, 4))
     assert np.array_equal(got[2:], want)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes (in copies of the prefill oracle, on the CPU): each fails
+# the masked-SDPA pin for some layout and RoPE mode
+# ---------------------------------------------------------------------------
+
+def _check_prefill(pfn) -> bool:
+    """test_prefill_matches_masked_sdpa for a prefill function pfn; False on the first failure."""
+    for layout in ("ring", "sink", "paged"):
+        for rope_mode in ("none", "baked"):
+            rng = np.random.default_rng(30)
+            T, Hq, Hkv, D, S, W, pos0, q, K, V, att = _case(layout, rng)
+            got = pfn(q, K, V, pos0, att, rope=rope_mode, sinks=S, window=W)
+            N, g = K.shape[0], Hq // Hkv
+            mask = np.zeros((T, N), dtype=bool)
+            for i in range(T):
+                mask[i, att(pos0 + i)] = True
+            t_rows = pos0 + np.arange(T)
+            for h in range(Hq):
+                qh, Kh = q[:, h], K[:, h // g]
+                if rope_mode == "baked":
+                    qh = rope.rotate(qh, t_rows)
+                    Kh = storage.round_storage(rope.rotate(Kh, np.arange(N)), "f32")
+                if not np.allclose(got[:, h], _sdpa_masked(qh, Kh, V[:, h // g], mask), rtol=0, atol=1e-12):
+                    return False
+    return True
+
+
+def _planted_prefill(mistake):
+    """A copy of the prefill oracle with one mistake planted ("none": a faithful copy)."""
+    def pfn(q_chunk, K_hist, V_hist, pos0, attended, **spec):
+        T = q_chunk.shape[0]
+        out = np.zeros_like(q_chunk, dtype=np.float64)
+        for i in range(T):
+            t = pos0 + i
+            ps = np.asarray(attended(t), dtype=np.int64)
+            qi = q_chunk[i]
+            if mistake == "causal_off_by_one":           # the next token is visible too
+                nxt = np.asarray(attended(t + 1), dtype=np.int64)
+                ps = nxt[nxt <= min(t + 1, K_hist.shape[0] - 1)]
+            elif mistake == "rope_at_pos0" and spec.get("rope") == "baked":
+                qi = rope.rotate(qi, pos0 - t)            # with the rotation at t: q rotated at pos0
+            elif mistake == "no_chunk_keys":              # the chunk's own rows left out (self kept)
+                ps = ps[(ps < pos0) | (ps == t)]
+            elif mistake == "one_window_per_chunk":       # the last token's set for every token
+                last = np.asarray(attended(pos0 + T - 1), dtype=np.int64)
+                ps = last[last <= t]
+            out[i] = attention.decode_sequence(qi, K_hist[ps], V_hist[ps], ps, t, **spec)
+        return out
+    return pfn
+
+
+@pytest.mark.parametrize("mistake", ["causal_off_by_one", "rope_at_pos0", "no_chunk_keys", "one_window_per_chunk"])
+def test_planted_prefill_mistakes_fail_the_pin(mistake):
+    assert _check_prefill(prefill.prefill_sequence)
+    assert _check_prefill(_planted_prefill("none"))
+    assert not _check_prefill(_planted_prefill(mistake))

@@ -110,3 +110,51 @@ def test_store_i8_matches_quantize_then_dequantize(D):
     x = rng.standard_normal((5, D))
     c, s = quant.quantize_rows(x.astype(np.float32))
     assert (quant.store_i8(x) == quant.dequantize_rows(c, s)).all()
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes (in copies of the quantiser, on the CPU): each fails a pin
+# ---------------------------------------------------------------------------
+
+def _check_quantizer(qfn) -> bool:
+    """The pins above, for a quantiser qfn(x) -> (codes, scales); False on the first failure."""
+    try:
+        c, s = qfn(np.array([254.0, 1.0, -3.0, 5.0, -254.0, 0.0, 127.0, -0.5]))
+        assert float(s) == 2.0 and np.asarray(c).tolist() == [127, 0, -2, 2, -127, 0, 64, 0]
+        c, s = qfn(np.array([-508.0, 4.0, 2.0]))
+        assert float(s) == 4.0 and np.asarray(c).tolist() == [-127, 1, 0]
+        rng = np.random.default_rng(7)
+        x = (rng.standard_normal((6, 16)) * np.array([1e-3, 1.0, 3.0, 50.0, 1e4, 0.25])[:, None]).astype(np.float32)
+        c, s = qfn(x)
+        for i in range(x.shape[0]):
+            si = np.float32(np.max(np.abs(x[i])) / np.float32(127))
+            assert np.asarray(s)[i] == si
+            for j in range(x.shape[1]):
+                assert np.asarray(c)[i, j] == _nearest_even_search(float(np.float32(x[i, j] / si)))
+        return True
+    except AssertionError:
+        return False
+
+
+def _planted(scale_div=127.0, rounding=np.rint, per_tensor=False, signed_max=False):
+    def qfn(x):
+        x32 = np.asarray(x, dtype=np.float32)
+        a = np.max(x32, axis=-1) if signed_max else np.max(np.abs(x32), axis=-1)
+        if per_tensor:
+            a = np.full_like(a, np.max(np.abs(x32)))
+        s = (np.abs(a) / np.float32(scale_div)).astype(np.float32)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            r = (x32 / s[..., None]).astype(np.float32)
+        c = np.where(s[..., None] > 0, np.clip(rounding(r), -127, 127), 0)
+        return c.astype(np.int8), s
+    return qfn
+
+
+def test_planted_quantizer_mistakes_fail_a_pin():
+    assert _check_quantizer(quant.quantize_rows)
+    assert _check_quantizer(_planted())                       # the planted form with no mistake passes
+    assert not _check_quantizer(_planted(scale_div=128.0))    # scale from the wrong code maximum
+    assert not _check_quantizer(_planted(rounding=np.trunc))  # truncation instead of rounding
+    assert not _check_quantizer(_planted(rounding=lambda r: np.floor(r + 0.5)))   # ties away from the even code
+    assert not _check_quantizer(_planted(per_tensor=True))    # one scale for the whole tensor, not per row
+    assert not _check_quantizer(_planted(signed_max=True))    # scale from the signed maximum
