@@ -179,3 +179,27 @@ def test_step_bytes_formula():
     wl = kvc_synth.make_workload("paged_shared_prefix_bf16")
     nb = bench.step_bytes(wl)
     assert nb["kv_unique"] < nb["kv_logical"]
+
+
+@pytest.mark.parametrize("name", ["tiny_ring_sink_f32", "ring_bf16", "sink_window_bf16", "paged_shared_prefix_bf16",
+                                  "long_context_pool_bf16", "ring_int8"])
+def test_step_bytes_match_the_oracle_attended_sets(name):
+    # the roofline's algorithmic bytes, recounted from the oracle's attended
+    # sets: logical = every (sequence, attended position); unique (paged) =
+    # the distinct (physical block, row) pairs those positions read
+    import oracle
+    wl = kvc_synth.make_workload(name)
+    row = wl.kv_heads * 2 * (wl.head_dim * wl.elt_bytes + wl.row_scale_bytes)
+    logical, cells = 0, set()
+    for b in range(wl.batch):
+        t = int(wl.positions[b])
+        if wl.layout == "window":
+            ps = oracle.window_attended(t, wl.sinks, wl.window)
+        else:
+            ps = oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size)
+            phys = wl.block_table[b][ps // wl.block_size]
+            cells.update(zip(phys.tolist(), (ps % wl.block_size).tolist()))
+        logical += len(ps)
+    nb = bench.step_bytes(wl)
+    assert nb["kv_logical"] == logical * row
+    assert nb["kv_unique"] == (logical if wl.layout == "window" else len(cells)) * row
