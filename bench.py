@@ -352,7 +352,7 @@ class ClockSampler:
 KERNEL_TRAFFIC = {"ring_bf16": 137971712, "sink_window_bf16": 545077248,
                   "paged_shared_prefix_bf16": 894324480, "long_context_pool_bf16": 153829120,
                   "ring_int8": 69380806}
-KERNEL_TRAFFIC_SOURCES = "daec053141b84c75f772008f5c13b436bf8d40f257560ef093fe0589115af420"
+KERNEL_TRAFFIC_SOURCES = "a96d8dd46101b49c8cb03c78c55fef8c1d8857ccaebfd4669a5519fa3fac06bc"
 
 
 # the sources decode_mma_kernel and its launch are built from

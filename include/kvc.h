@@ -223,7 +223,10 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
  * READ_INCACHE: each token's window keys at distance t - p and its sinks at
  * min(t, C - 1) - p, as the decode step at t rotates them.
  * bf16 caches, head_dim 64 or 128 (KVC_ERR_UNSUPPORTED otherwise).  Calls on
- * one workspace must not overlap on the GPU. */
+ * one workspace must not overlap on the GPU.  At head_dim 128 the attention
+ * runs on the tcgen05 tensor cores: each of its CTAs (at most two per SM)
+ * holds 256 tensor-memory columns while it runs, so a kernel of another
+ * library that holds an SM's tensor memory at the same time delays it. */
 KVC_API size_t kvc_prefill_workspace_bytes(const kvc_desc* d, int32_t T);
 KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const void* q,
                         const void* k_new, const void* v_new, int32_t T, const int32_t* pos0,
