@@ -90,6 +90,60 @@ def test_invalid_descriptors_are_rejected(kvc):
     assert L.kvc_cache_bytes(None) == 0
 
 
+def _documented_cache_bytes(f):
+    """The cache size include/kvc.h documents for descriptor fields f, or 0
+    where the documented constraints reject it."""
+    layout, rope, dtype = f["layout"], f["rope"], f["dtype"]
+    if min(f["layers"], f["batch"], f["q_heads"], f["kv_heads"]) < 1 or f["q_heads"] % f["kv_heads"]:
+        return 0
+    if f["head_dim"] not in (64, 128, 256) or f["num_splits"] < 0 or f["softmax_scale"] < 0:
+        return 0
+    if rope != 0 and not f["rope_base"] > 0:
+        return 0
+    if layout == 2:                                   # PAGED
+        if min(f["block_size"], f["num_blocks"], f["max_blocks_per_seq"]) < 1 or rope == 2:
+            return 0
+        rows = f["num_blocks"] * f["kv_heads"] * f["block_size"]
+    else:
+        if f["window"] < 1 or (layout == 0 and f["sinks"] != 0) or (layout == 1 and f["sinks"] < 1):
+            return 0
+        rows = f["batch"] * f["kv_heads"] * (f["sinks"] + f["window"])
+    if dtype == 2 and (f["head_dim"] < 128 or rope == 2 or rows % 4):
+        return 0
+    elems = f["layers"] * 2 * rows * f["head_dim"]
+    if dtype == 2:
+        return elems + 4 * f["layers"] * 2 * rows     # codes, then one fp32 scale per row
+    return elems * (4 if dtype == 0 else 2)
+
+
+def test_random_descriptors_follow_the_documented_rules(kvc):
+    # seeded random descriptors around the boundaries of every documented rule
+    rng = np.random.default_rng(2024)
+    L = kvc.lib()
+    pick = lambda *v: v[int(rng.integers(len(v)))]
+
+    def field(good, bad):                             # a valid value 85% of the time
+        return pick(*good) if rng.random() < 0.85 else pick(*bad)
+
+    accepted = 0
+    for _ in range(3000):
+        f = dict(layout=pick(0, 1, 2), rope=pick(0, 1, 2), dtype=pick(0, 1, 2), layers=field((1, 2, 3), (0,)),
+                 batch=field((1, 2, 5), (0,)), kv_heads=field((1, 2, 3), (0,)),
+                 head_dim=field((64, 128, 256), (32, 96)), window=field((1, 7, 64, 100), (-1, 0)),
+                 sinks=pick(-1, 0, 0, 1, 4), block_size=field((1, 16, 64), (0,)), num_blocks=field((1, 3, 8), (0,)),
+                 max_blocks_per_seq=field((1, 4), (0,)), num_splits=field((0, 3), (-1,)),
+                 rope_base=field((10000.0, 500.0), (-1.0, 0.0)), softmax_scale=field((0.0, 0.125), (-0.5,)))
+        f["q_heads"] = max(f["kv_heads"], 1) * pick(1, 2, 4) + (1 if rng.random() < 0.1 else 0)
+        d = kvc.KvcDesc(f["layout"], f["rope"], f["dtype"], f["layers"], f["batch"], f["q_heads"], f["kv_heads"],
+                        f["head_dim"], f["window"], f["sinks"], f["block_size"], f["num_blocks"],
+                        f["max_blocks_per_seq"], f["num_splits"], f["rope_base"], f["softmax_scale"])
+        want = _documented_cache_bytes(f)
+        assert L.kvc_cache_bytes(ctypes.byref(d)) == want, f
+        assert (L.kvc_workspace_bytes(ctypes.byref(d)) > 0) == (want > 0), f
+        accepted += want > 0
+    assert 100 < accepted < 2900                      # both sides of the rules were exercised
+
+
 def test_argument_errors_return_codes_without_launching(kvc):
     L = kvc.lib()
     d = _desc(kvc)
