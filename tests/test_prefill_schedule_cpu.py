@@ -52,7 +52,7 @@ def test_tile_schedule_keeps_exactly_the_attended_set(rows_per_cta):
     for _ in range(60):
         S = int(rng.choice([0, 1, 4]))
         W = int(rng.choice([1, 7, 60, 64, 100, 200]))
-        G = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 3, 4, 6, 8]))
         T = int(rng.integers(1, 140))
         pos0 = int(rng.choice([-20, -1, 0, 3, 63, 64, 150, 4300]))
         tq = rows_per_cta // G
