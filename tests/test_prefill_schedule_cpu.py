@@ -62,3 +62,51 @@ def test_tile_schedule_keeps_exactly_the_attended_set(rows_per_cta):
                 t = pos0 + i
                 want = set(oracle.window_attended(t, S, W).tolist()) if t >= 0 else set()
                 assert keys == want, (S, W, G, T, pos0, i0, i)
+
+
+def _cta_keys_paged(i0, tq, T, pos0, table, valid, bs):
+    """{row -> kept keys} for one CTA on a paged cache: keys [0, t_hi] in
+    64-key tiles, a key kept when its block is mapped and valid (the row
+    source) and, outside interior tiles, when p <= t."""
+    i_last = min(i0 + tq, T) - 1
+    t_hi, t_lo = pos0 + i_last, max(pos0 + i0, 0)
+    all_rows = pos0 + i0 >= 0 and i0 + tq <= T
+    r1e = t_hi + 1 if (i_last >= i0 and t_hi >= 0) else 0
+    ntiles = (r1e + KEYS - 1) // KEYS
+    rows = [(i0 + tl, pos0 + i0 + tl) for tl in range(tq) if i0 + tl < T]
+    kept = {i: set() for i, _ in rows}
+    for k in range(ntiles):
+        base = k * KEYS
+        interior = all_rows and base + KEYS <= r1e and base + KEYS - 1 <= t_lo
+        for pk in range(base, base + KEYS):
+            lb = pk // bs
+            phys = table[lb] if (pk < r1e and lb < len(table)) else -1
+            ok = phys >= 0 and bool(valid[phys])
+            for i, t in rows:
+                if interior:
+                    assert not ok or pk <= t
+                if ok and (interior or pk <= t):
+                    kept[i].add(pk)
+    return kept
+
+
+@pytest.mark.parametrize("rows_per_cta", [128, 64])
+def test_paged_tile_schedule_keeps_exactly_the_attended_set(rows_per_cta):
+    rng = np.random.default_rng(78)
+    for _ in range(40):
+        bs = int(rng.choice([1, 16, 64]))
+        nlog, nphys = 40, 48
+        table = rng.permutation(nphys)[:nlog].astype(np.int64)
+        table[rng.random(nlog) < 0.2] = -1                      # unmapped blocks
+        valid = rng.random(nphys) < 0.7
+        G = int(rng.choice([1, 2, 3, 4, 8]))
+        T = int(rng.integers(1, 100))
+        pos0 = int(rng.choice([-5, 0, 7, 64, 300]))
+        pos0 = min(pos0, nlog * bs - T)                         # the chunk stays inside the table
+        tq = rows_per_cta // G
+        for i0 in range(0, T, tq):
+            kept = _cta_keys_paged(i0, tq, T, pos0, table, valid, bs)
+            for i, keys in kept.items():
+                t = pos0 + i
+                want = set(oracle.paged_attended(t, table, valid, bs).tolist()) if t >= 0 else set()
+                assert keys == want, (bs, G, T, pos0, i0, i)
