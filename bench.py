@@ -8,11 +8,14 @@ over `layers` cache layers so the working set (>= 1 GiB) is far larger than
 the 126 MiB L2: every step reads its KV from HBM.
 
 Prints one JSON line.  `value` = algorithmic bytes per step (attended K/V
-rows + q + out + the appended row) / device time per step, in GB/s;
-`roofline` relates the decode kernel's own time to the measured HBM copy peak;
-`e2e` repeats the metric with host-resident inputs copied in and the output
-copied out every step; `cpu_baseline` times the CPU oracle on a bounded
-sample.  `--impl reference` times the CPU oracle as the reference arm.
+rows + q + out + the appended row) / device time per step, in GB/s, from the
+median of five timed loops of exactly K steps (CUDA graphs, replayed once
+untimed first); `roofline` relates the step's time to the measured HBM copy
+peak; `per_workload` times the other workloads the same way in the same
+process; `e2e` repeats the metric with host-resident inputs copied in (one
+packed copy) and the output copied out every step; `cpu_baseline` times the
+CPU oracle on a bounded sample.  `--impl reference` times the CPU oracle as
+the reference arm, with the same metric and config.
 """
 
 from __future__ import annotations
@@ -37,7 +40,7 @@ if ROOT not in sys.path:
 
 import kvc_synth  # noqa: E402
 
-DEFAULT_WORKLOAD = "ring_bf16"
+DEFAULT_WORKLOAD = "paged_shared_prefix_bf16"
 DEFAULT_LAYERS = {"tiny_ring_sink_f32": 1, "ring_bf16": 8, "sink_window_bf16": 2,
                   "paged_shared_prefix_bf16": 2, "long_context_pool_bf16": 4,
                   "ring_int8": 8, "paged_shared_prefix_int8": 2}
@@ -346,9 +349,9 @@ class ClockSampler:
 
 
 # DRAM bytes (read + write) per launch of decode_mma_kernel, from one ncu
-# capture per workload (summaries: profiles/decode_mma_<workload>.md), and the
-# digest of the kernel's sources (KERNEL_TRAFFIC_FILES) they were taken on:
-# reported only while those sources are unchanged.
+# capture per workload, and the digest of the kernel's sources
+# (KERNEL_TRAFFIC_FILES) they were taken on: reported only while those
+# sources are unchanged.
 KERNEL_TRAFFIC = {"ring_bf16": 137971712, "sink_window_bf16": 545077248,
                   "paged_shared_prefix_bf16": 894324480, "long_context_pool_bf16": 153829120,
                   "ring_int8": 69380806}
@@ -538,12 +541,35 @@ def job_throughput(bytes_per_step, world, ms_per_step):
     return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
 
 
+METRIC = "decode-attention KV HBM GB/s"
+TIMED_LOOPS = 5           # timed loops of K steps; the median loop sets ms_per_step
+PER_WORKLOAD_STEPS = 200  # steps per timed loop of each per_workload entry
+# configurations timed beside the headline in the same process: the other
+# workloads of the statement, the pool's valid-density sweep, the INT8 caches
+PER_WORKLOAD = [("tiny_ring_sink_f32", {}), ("ring_bf16", {}), ("sink_window_bf16", {}),
+                ("paged_shared_prefix_bf16", {}), ("long_context_pool_bf16", {}),
+                ("long_context_pool_bf16", {"density": 0.25}), ("long_context_pool_bf16", {"density": 1.0}),
+                ("ring_int8", {}), ("paged_shared_prefix_int8", {})]
+
+
+def workload_config(wl, layers, world, kw):
+    """The `config` object of both arms' JSON lines: the workload by name and shape."""
+    nb = step_bytes(wl)
+    return {"workload": wl.name, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
+            "head_dim": wl.head_dim, "window": wl.window, "sinks": wl.sinks,
+            "block_size": wl.block_size, "layers_cycled": layers, "rope": wl.rope, "cache_dtype": wl.dtype,
+            "l2": f"inputs larger than L2: {layers} layers cycled, "
+                  f"{layers * nb['kv_unique'] / 2**20:.0f} MiB of attended K/V",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU", **kw}
+
+
 def run_reference(args):
     rank, world, _ = _dist()
     if rank != 0:
         return None
     kw = _workload_kw(args)
     wl = kvc_synth.make_workload(args.workload, **kw)
+    layers = getattr(args, "layers", 0) or DEFAULT_LAYERS[args.workload]
     per_step = max(0.002, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
     # rows per step sized to the per-step budget (about 25k rows/s for D=128)
     rows = max(64, int(per_step * 25000 * 128 / wl.head_dim))
@@ -556,15 +582,115 @@ def run_reference(args):
         tot_b, tot_s, tot_u = tot_b + b, tot_s + s, tot_u + u
     wall = time.perf_counter() - t0
     val = tot_b / tot_s / 1e9
-    return {"impl": "reference", "metric": "decode-attention KV GB/s", "value": val, "unit": "GB/s",
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_s / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, **kw},
+            "config": workload_config(wl, layers, world, kw),
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"each step: up to {rows} attended rows of (sequence, kv head) units, "
                                        f"~{per_step:.3f} s of fp64 oracle time; {tot_u} units, wall {wall:.1f} s"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def capture_graphs(st, K):
+    """CUDA graphs of K consecutive steps (layers cycled): graph A holds n steps
+    (a whole number of layer cycles) and is replayed K // n times, graph B the
+    remaining K mod n steps.  Returns [(graph, replays)], or [] if capture fails."""
+    layers = st.layers
+    n = min(K, max(layers, (512 // layers) * layers))
+    reps, rest = divmod(K, n)
+    graphs = []
+    for count in (n, rest):
+        if count == 0 or (count == n and reps == 0):
+            continue
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fcg = FastCalls(st)           # binds the capture stream
+            for i in range(count):
+                fcg.step(i % layers)
+        graphs.append((g, reps if count == n else 1))
+    return graphs
+
+
+def timed_loops(st, fc, K, loops, graphs, barrier=lambda: None):
+    """`loops` timed loops of exactly K steps each, every loop bracketed by a
+    barrier and a device synchronize on both sides and timed with CUDA events
+    on the launching stream.  Graphs are replayed once, untimed, first (their
+    upload and first launch stay out of the timed region); before each loop
+    the GPU is held ~10 ms so that the host's launches queue ahead of it.
+    Returns the loop times in ms."""
+    layers = st.layers
+    if graphs:
+        for g, _ in graphs:
+            g.replay()
+    else:
+        for i in range(min(K, 3 * layers)):
+            fc.step(i % layers)
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(loops):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        start.record()
+        if graphs:
+            for g, r in graphs:
+                for _ in range(r):
+                    g.replay()
+        else:
+            for i in range(K):
+                fc.step(i % layers)
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+        out.append(start.elapsed_time(end))
+    return out
+
+
+def _roofline(wl, nb, ms_per_step, kw, traffic_override):
+    peak, peak_kind = _peaks()
+    achieved = nb["step_algorithmic"] / (ms_per_step * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_kind": peak_kind,
+            "traffic": _traffic(wl.name, traffic_override) if not kw else traffic_override,
+            "traffic_kernel": "decode_mma_kernel, dram__bytes_read.sum + dram__bytes_write.sum per launch",
+            "kernel": "kvc_decode_step: " + ("decode_mma_kernel + combine_streamk_kernel"
+                                             if wl.dtype in ("bf16", "i8") else "append + decode"),
+            "timer": "CUDA events around each timed loop of K kvc_decode_step calls; median loop, per step",
+            "algorithmic_bytes_per_launch": nb["step_algorithmic"]}
+
+
+def measure_workload(name, kw, steps, loops):
+    """One per_workload entry: the workload's own state, graph-replayed loops
+    of `steps` steps, median loop."""
+    wl = kvc_synth.make_workload(name, **kw)
+    layers = DEFAULT_LAYERS[name]
+    st = DecodeState(wl, layers, source="device")
+    fc = FastCalls(st)
+    for i in range(3 * layers):
+        fc.step(i % layers)
+    torch.cuda.synchronize()
+    graphs = capture_graphs(st, steps)
+    times = timed_loops(st, fc, steps, loops, graphs)
+    kvc = _kvc()
+    err = kvc.get_error(st.ws)
+    ms = statistics.median(times) / steps
+    nb = step_bytes(wl)
+    entry = {"workload": name, **kw, "ms_per_step": ms, "us_per_step": ms * 1e3, "steps_per_s": 1e3 / ms,
+             "value": nb["step_algorithmic"] / (ms * 1e-3) / 1e9, "unit": "GB/s",
+             "bytes_per_step": nb, "loop_ms": times, "steps_per_loop": steps, "layers_cycled": layers,
+             "gpu_launches_per_step": st.launches_per_step(), "device_errors": err}
+    if wl.dtype != "f32":
+        entry["roofline_frac"] = entry["value"] / _peaks()[0]
+        entry["frac_of_8tbs"] = entry["value"] / 8000.0
+    else:
+        entry["note"] = "latency-bound (32 KiB of K/V per step): steps/s is the figure"
+    del st, fc, graphs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
 
 
 def run_ours(args):
@@ -588,111 +714,69 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    # The timed region replays CUDA graphs of the K steps (the launches keep
+    # The timed loops replay CUDA graphs of the K steps (the launches keep
     # their programmatic-dependency edges); without --eager the host's launch
-    # cost stays out of the device timeline.  Graph A holds n steps (a whole
-    # number of layer cycles), graph B the remaining K mod n steps.
-    graphs = []
-    timing = "eager"
+    # cost stays out of the device timeline.
+    graphs, timing = [], "eager"
     if not args.eager:
         try:
-            n = min(K, max(layers, (512 // layers) * layers))
-            reps, rest = divmod(K, n)
-            for count in (n, rest):
-                if count == 0 or (count == n and reps == 0):
-                    continue
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    fcg = FastCalls(st)           # binds the capture stream
-                    for i in range(count):
-                        fcg.step(i % layers)
-                graphs.append((g, reps if count == n else 1))
-            timing = "cuda_graph"
+            graphs = capture_graphs(st, K)
+            timing = "cuda_graph (one untimed replay first)"
         except Exception as exc:                  # capture unsupported: time eagerly
             graphs = []
             timing = f"eager (graph capture failed: {type(exc).__name__})"
         torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
-    if not graphs:
-        torch.cuda._sleep(20_000_000)      # ~10 ms head start: the host enqueues ahead of the GPU
-    start.record()
-    if graphs:
-        for g, r in graphs:
-            for _ in range(r):
-                g.replay()
-    else:
-        for i in range(K):
-            fc.step(i % layers)
-    end.record()
-    torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    total_ms = replica_max(total_ms, world)
+    loops = timed_loops(st, fc, K, args.loops, graphs, barrier)
+    med = statistics.median(loops)
+    total_ms = replica_max(med, world)
     ms_per_step = total_ms / K
     value = job_throughput(nb["step_algorithmic"], world, ms_per_step)
-    # the step's kernels (decode + combine, fused append) take the whole step:
-    # per launch of the step, algorithmic bytes / device time per step
-    dec_mean = ms_per_step
-    achieved = nb["step_algorithmic"] / (dec_mean * 1e-3) / 1e9
-    peak, peak_kind = _peaks()
     err = kvc.get_error(st.ws)
     if err:
         raise RuntimeError(f"device error bits {err:#x} during the timed region")
 
-    # the same steps launched one by one (untimed for the headline): what a
-    # caller without graphs sees per step
+    # the same steps launched one by one: what a caller without graphs sees
     eager_ms = None
     if graphs:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ne = min(K, 2000)
-        torch.cuda.synchronize()
-        torch.cuda._sleep(20_000_000)
-        e0.record()
-        for i in range(ne):
-            fc.step(i % layers)
-        e1.record()
-        torch.cuda.synchronize()
-        eager_ms = e0.elapsed_time(e1) / ne
+        ne = min(max(K, 200), 2000)
+        eager_ms = statistics.median(timed_loops(st, fc, ne, 3, [])) / ne
+
+    per_workload = None
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        per_workload = []
+        for name, pkw in PER_WORKLOAD:
+            if name == wl.name and pkw == kw:
+                continue
+            per_workload.append(measure_workload(name, pkw, PER_WORKLOAD_STEPS, args.loops))
+    clk = clocks.stop()
 
     # end to end: host inputs copied in, host output copied out, every step
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(st, fc, args, nb)
+        e2e = run_e2e(st, args, nb)
 
     line = {
-        "metric": "decode-attention KV HBM GB/s",
+        "metric": METRIC,
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.q_heads, "kv_heads": wl.kv_heads,
-                   "head_dim": wl.head_dim, "window": wl.window, "sinks": wl.sinks,
-                   "block_size": wl.block_size, "layers_cycled": layers, "rope": wl.rope,
-                   "l2": f"inputs larger than L2: {layers} layers cycled, "
-                         f"{layers * nb['kv_unique'] / 2**20:.0f} MiB of attended K/V",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU", **kw},
+        "config": workload_config(wl, layers, world, kw),
         "steps_per_s": 1e3 / ms_per_step,
         "bytes_per_step": nb,
-        "decode_kernel_ms": dec_mean,
         "timing": timing,
+        "timed_loops": len(loops),
+        "loop_ms": loops,
         "eager_ms_per_step": eager_ms,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _traffic(wl.name, args.traffic) if not kw else args.traffic,
-                     "traffic_kernel": "decode_mma_kernel, dram__bytes_read.sum + dram__bytes_write.sum per launch",
-                     "kernel": "kvc_decode_step: " + ("decode_mma_kernel + combine_streamk_kernel"
-                                                      if wl.dtype in ("bf16", "i8") else "append + decode"),
-                     "timer": "CUDA events around the timed region (K kvc_decode_step calls); per step",
-                     "algorithmic_bytes_per_launch": nb["step_algorithmic"]},
+        "roofline": _roofline(wl, nb, ms_per_step, kw, args.traffic),
         "frac_of_8tbs": value / 8000.0,
         "clocks": clk,
         "gpu_launches": st.launches_per_step() * K,
+        "gpu_launches_note": "kernels launched in one timed loop of K steps",
         "e2e": e2e,
+        "per_workload": per_workload,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget, kw=kw)
@@ -700,42 +784,77 @@ def run_ours(args):
     return line if rank == 0 else None
 
 
-def run_e2e(st, fc, args, nb):
-    wl = st.wl
+class PackedInputs:
+    """A step's inputs packed into one buffer, q | k_new | v_new | pos, each
+    part at a 256-byte offset: one pinned host buffer per layer and one device
+    staging buffer whose views the step reads, so that a step copies its
+    inputs in with one host-to-device copy."""
+
+    def __init__(self, st):
+        parts0 = [st.q[0], st.k_new[0], st.v_new[0], st.pos]
+        self.offs, off = [], 0
+        for t in parts0:
+            self.offs.append(off)
+            off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+        self.nbytes = off
+        self.dev = torch.zeros(off, dtype=torch.uint8, device="cuda")
+        self.host = []
+        for layer in range(st.layers):
+            h = torch.zeros(off, dtype=torch.uint8)
+            for t, o in zip([st.q[layer], st.k_new[layer], st.v_new[layer], st.pos], self.offs):
+                raw = t.contiguous().view(-1).view(torch.uint8).cpu()
+                h[o:o + raw.numel()] = raw
+            self.host.append(h.pin_memory())
+
+    def ptr(self, i):
+        return self.dev.data_ptr() + self.offs[i]
+
+
+def run_e2e(st, args, nb):
+    """The metric end to end through the C ABI: every step copies its packed
+    inputs from pinned host memory (one copy), runs kvc_decode_step on the
+    staged views, copies the output back to pinned host memory and waits."""
+    kvc = _kvc()
+    L = kvc.lib()
     layers = st.layers
     K = max(10, min(args.steps, 2000))
-    hq = [st.q[l].cpu().pin_memory() for l in range(layers)]
-    hk = [st.k_new[l].cpu().pin_memory() for l in range(layers)]
-    hv = [st.v_new[l].cpu().pin_memory() for l in range(layers)]
-    hp = st.pos.cpu().pin_memory()
+    pk = PackedInputs(st)
     hout = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = hq[0].numel() * hq[0].element_size() + 2 * hk[0].numel() * hk[0].element_size() + \
-        hp.numel() * hp.element_size()
-    d2h = hout.numel() * hout.element_size()
+    s = torch.cuda.current_stream()
+    d = ctypes.byref(st.desc)
+    tb = st.table.data_ptr() if st.table is not None else None
+    vb = st.valid_bits.data_ptr() if st.valid_bits is not None else None
+    args_of = [(d, st.cache.data_ptr(), l, pk.ptr(0), pk.ptr(1), pk.ptr(2), pk.ptr(3), tb, vb,
+                st.out.data_ptr(), st.ws.data_ptr(), st.ws.numel(), s.cuda_stream) for l in range(layers)]
+
+    def step(i):
+        layer = i % layers
+        pk.dev.copy_(pk.host[layer], non_blocking=True)
+        rc = L.kvc_decode_step(*args_of[layer])
+        if rc:
+            raise RuntimeError(f"kvc_decode_step: {rc}")
+        hout.copy_(st.out, non_blocking=True)
+        s.synchronize()
+
     for i in range(3):
-        _e2e_step(st, fc, i % layers, hq, hk, hv, hp, hout)
+        step(i)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for i in range(K):
-        _e2e_step(st, fc, i % layers, hq, hk, hv, hp, hout)
-    e.record()
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / K
+    times = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(K):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times) / K
     return {"value": nb["step_algorithmic"] / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "note": "per step: pinned host q/k/v/pos -> device, append + attention, out -> pinned host, "
-                    "host waits for the result"}
-
-
-def _e2e_step(st, fc, layer, hq, hk, hv, hp, hout):
-    st.q[layer].copy_(hq[layer], non_blocking=True)
-    st.k_new[layer].copy_(hk[layer], non_blocking=True)
-    st.v_new[layer].copy_(hv[layer], non_blocking=True)
-    st.pos.copy_(hp, non_blocking=True)
-    fc.step(layer)
-    hout.copy_(st.out, non_blocking=True)
-    torch.cuda.current_stream().synchronize()
+            "h2d_bytes_per_step": pk.nbytes, "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+            "steps": K, "loops": len(times),
+            "note": "per step: one copy of the packed inputs (q, k_new, v_new, pos) from pinned host memory, "
+                    "kvc_decode_step on the staged views, out -> pinned host, host waits for the result; "
+                    "median of 3 loops"}
 
 
 def measure_block_prepare(args):
@@ -945,6 +1064,9 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only the headline workload (no per_workload entries)")
+    ap.add_argument("--loops", type=int, default=TIMED_LOOPS, help="timed loops of K steps (median reported)")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one by one (no CUDA graph)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--chunk", type=int, default=128, help="--measure prefill: tokens per chunk")

@@ -17,10 +17,18 @@
  *
  * Conventions shared by every entry point
  *   - Every buffer argument is a DEVICE pointer owned by the caller (cache,
- *     queries, outputs, tables, workspace); the library allocates nothing and
- *     keeps no state between calls.  `stream` is a cudaStream_t (NULL = the
- *     legacy default stream); every call except kvc_get_error only enqueues
- *     work on it and returns.
+ *     queries, outputs, tables, workspace); the library allocates no device
+ *     memory.  `stream` is a cudaStream_t (NULL = the legacy default stream);
+ *     every call except kvc_get_error only enqueues work on it and returns.
+ *   - State the library keeps across calls (host side, thread-safe):
+ *     (1) the TMA tensor maps of the last 8 bf16 / INT8 caches it decoded,
+ *     keyed by (cache address, layers, rows per K half, head_dim, dtype,
+ *     device): a cache freed and a different one allocated at the same
+ *     address with the same shape reuses the maps, which are still correct,
+ *     since they depend on nothing else;  (2) kvc_pager objects, which the
+ *     caller creates and destroys;  (3) the fixed device scratch of
+ *     kvc_decode_attention_noalloc (see there).  Everything else a call
+ *     needs lives in the caller's workspace.
  *   - Return value: KVC_OK (0) or a negative KVC_ERR_* code.  On a negative
  *     code nothing was launched.  Errors that only the device can see (a
  *     block id out of range, an append into an unmapped block, a bad
@@ -159,8 +167,10 @@ KVC_API int kvc_workspace_init(const kvc_desc* d, void* workspace, size_t worksp
  *                 i is at pos[b] + i.  Tokens at negative positions are
  *                 skipped (left padding).
  *   block_table   PAGED: [batch, max_blocks_per_seq] int32; else NULL.
- * BAKED rotates K at its absolute position (angle reduced in fp64, rotated in
- * fp32, stored rounded to nearest-even); V is never rotated ([pool]).  For
+ * BAKED rotates K at its absolute position (the angle p * theta_i reduced
+ * exactly as a 64-bit fixed-point fraction of a turn, its sine and cosine
+ * and the rotation in fp32, stored rounded to nearest-even); V is never
+ * rotated ([pool]).  For
  * RING / SINK_RING the cache ends as if the tokens were appended one at a
  * time in order: a token that a later token of the same call overwrites is
  * not written.  Ring appends must come in position order, one call per step,
@@ -174,8 +184,11 @@ KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer,
 
 /* Decode attention for one layer ([primer] 2.2 and 4.2, [sink] softmax
  * equations): out = softmax(q . K^T * scale) . V over the attended set of
- * each sequence, fp32 online softmax, split over the KV length and combined
- * in the same launch.
+ * each sequence, fp32 online softmax, split over the KV length into partial
+ * results (m, l, o) in the workspace.  fp32 caches combine the partials in
+ * the same kernel (the last CTA of a sequence); bf16 and INT8 caches launch
+ * a separate combine kernel right behind the attention kernel (programmatic
+ * dependent launch), and PAGED caches run a work-plan kernel before it.
  *   q       [batch, q_heads, head_dim], pre-RoPE.
  *   pos     [batch] int32: position t of the token being decoded (already
  *           appended, so t attends to itself; [ring] 4.3).
@@ -357,7 +370,10 @@ KVC_API int kvc_pagein_commit(kvc_pager* pager, const kvc_desc* d, int32_t seq, 
  *     call.  Inputs and outputs are still the caller's device buffers.
  *   - The first call on a device (with that device current) looks up the
  *     scratch array's device address; make that first call before any stream
- *     capture.  Later calls only enqueue work on `stream`.
+ *     capture.  The address is kept per device and context: after the
+ *     device's context was destroyed and created again (cudaDeviceReset),
+ *     the next call looks it up again, so make that call outside capture
+ *     too.  Later calls only enqueue work on `stream`.
  *   - Every call on a device shares the one scratch array and finds it as the
  *     previous call left it; the call clears the parts that must start at
  *     zero (error word, completion counters) on `stream` before its kernels.

@@ -832,22 +832,59 @@ namespace {
 static __device__ __align__(256) unsigned char kvc_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;   // unique id of the context the address belongs to
+    void* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
+
+// Unique id of the calling thread's current context (0 when none is current
+// yet), through the runtime's driver entry points.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrentFn>(a);
+            get_id = reinterpret_cast<GetIdFn>(b);
+        }
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device with that device current.
+// with that device current, once per device and context: a context that was
+// torn down and created again (cudaDeviceReset) may hold the array at another
+// address, and is looked up afresh.
 int scratch_on_current_device(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVC_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& a = g_scratch_addr[dev];
+    unsigned long long id = current_context_id();
+    if (!a.ptr || id == 0 || id != a.ctx_id) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, kvc_noalloc_scratch) != cudaSuccess || !ptr) return KVC_ERR_CUDA;
-        g_scratch_addr[dev] = ptr;
+        if (id == 0) id = current_context_id();   // the lookup made the context current
+        a.ptr = ptr;
+        a.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = a.ptr;
     return KVC_OK;
 }
 

@@ -4,10 +4,12 @@ The no-allocation entry point serves callers that cannot call cudaMalloc once
 they are running (a serving loop with device memory fixed at start-up, a
 plugin inside a framework that owns all device memory): it keeps its split-K
 partials, counters and work plan in the library's own fixed scratch array
-instead of a caller workspace.  This test calls it through the C ABI twice in
-a row (the second call finds the scratch as the first left it) and checks
-both outputs against the ordinary entry point on the same inputs, within the
-tolerances of the other GPU tests.  It sits in its own file, collected last,
+instead of a caller workspace.  These tests call it through the C ABI twice in
+a row (the second call finds the scratch as the first left it), and in an
+interleaved order of workloads with different layouts, batches and split
+counts, and check every output against the ordinary entry point on the same
+inputs: within the tolerances of the other GPU tests, and bit for bit, since
+both run the same kernels.  It sits in its own file, collected last,
 and passes both alone in a fresh process and after the other tests.
 """
 
@@ -44,21 +46,50 @@ def _noalloc(kvc, st, out):
     assert rc == 0, kvc.strerror(rc)
 
 
-@pytest.mark.parametrize("name", ["ring_bf16", "sink_window_bf16", "paged_shared_prefix_bf16",
-                                  "long_context_pool_bf16"])
+NAMES = ["ring_bf16", "sink_window_bf16", "paged_shared_prefix_bf16", "long_context_pool_bf16"]
+
+
+def _workspace_reference(kvc, st):
+    """The ordinary entry point (caller workspace) on the same inputs, after
+    the step's token was appended."""
+    st.step(0)
+    return kvc.decode_attention(st.desc, st.cache, 0, st.q[0], st.pos, st.ws, block_table=st.table,
+                                valid_bits=st.valid_bits).clone()
+
+
+def _check(kvc, st, ref, name):
+    out = torch.full_like(st.out, float("nan"))
+    _noalloc(kvc, st, out)
+    torch.cuda.synchronize()
+    got = out.float()
+    assert torch.isfinite(got).all(), name
+    err = float((got - ref.float()).abs().max())
+    assert err <= TOL[st.wl.dtype], (name, err)
+    # the same kernels on the same inputs: nothing may leak through the scratch
+    assert torch.equal(out, ref), name
+
+
+@pytest.mark.parametrize("name", NAMES)
 def test_noalloc_matches_workspace_entry_point_twice(kvc, name):
     wl = kvc_synth.make_workload(name, small=True)
     st = bench.DecodeState(wl, 1, source="cpu")
-    # append the step's token, then the ordinary call with a caller workspace
-    ref = st.step(0).float().clone()
+    ref = _workspace_reference(kvc, st)
     for _ in range(2):
-        out = torch.full_like(st.out, float("nan"))
-        _noalloc(kvc, st, out)
-        torch.cuda.synchronize()
-        got = out.float()
-        assert torch.isfinite(got).all()
-        err = float((got - ref).abs().max())
-        assert err <= TOL[wl.dtype], (name, err)
+        _check(kvc, st, ref, name)
+
+
+def test_noalloc_calls_of_different_layouts_interleaved(kvc):
+    """Each call finds the scratch as a call of another layout, batch and split
+    count left it (partials, plan and counters at other offsets)."""
+    states = {}
+    for name in NAMES:
+        st = bench.DecodeState(kvc_synth.make_workload(name, small=True), 1, source="cpu")
+        states[name] = (st, _workspace_reference(kvc, st))
+    order = ["paged_shared_prefix_bf16", "ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16",
+             "long_context_pool_bf16", "ring_bf16", "long_context_pool_bf16", "paged_shared_prefix_bf16"]
+    for name in order:
+        st, ref = states[name]
+        _check(kvc, st, ref, name)
 
 
 def test_noalloc_rejects_problems_larger_than_the_scratch(kvc):
