@@ -389,7 +389,19 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
 
     dim3 grid(d->dtype != KVC_F32 ? w.ctas : w.items, d->kv_heads, g.nsub);
-    if (paged) {
+    // one paged sequence on the tensor-core kernel: its CTAs plan their own
+    // shares from the block table and write the step's token themselves
+    // (the CTAs bulk-copy the table and the valid words: 16-byte aligned buffers)
+    p.self_plan = (paged && d->dtype != KVC_F32 && d->batch == 1 && d->max_blocks_per_seq <= kSelfPlanMax &&
+                   (d->num_blocks + 31) / 32 <= kSelfPlanValidWords && aligned16(block_table) &&
+                   (!valid_bits || aligned16(valid_bits))) ? 1 : 0;
+    if (p.self_plan) {
+        p.seq_items = reinterpret_cast<int2*>(ws + w.plan_seq);
+        p.n_items = reinterpret_cast<int32_t*>(ws + w.plan_total);
+        p.items = reinterpret_cast<int4*>(ws + w.plan_items);
+        p.item_info = reinterpret_cast<int4*>(ws + w.plan_info);
+        p.cta_items = reinterpret_cast<int2*>(ws + w.plan_cta);
+    } else if (paged) {
         PlanParams pp{};
         pp.pos = pos;
         pp.table = block_table;

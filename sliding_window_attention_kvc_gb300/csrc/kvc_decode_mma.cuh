@@ -82,8 +82,164 @@ struct MmaSegment {
     int slot;        // partial slot of this segment
     int first_slot;  // first partial slot of the sequence
     int nparts;      // partials of the sequence
-    int pad[3];
+    int new_row;     // self-planned paged step: K-half row that receives the new token, else -1
+    int pad[2];
 };
+
+// A single paged sequence's plan, made by each decode CTA for itself.
+struct SelfPlan {
+    int G;           // shares of the attended rows
+    int lb, row;     // share blockIdx.x: first logical block, and first row in it
+    int rows;        // rows of the share
+    int phys;        // physical block of lb
+    int traw;        // the sequence's position
+    int tphys;       // physical block of the logical block holding traw (-1: unmapped or none)
+    int tattended;   // that block is attended (mapped and valid)
+};
+
+// Plan of a one-sequence paged cache, by all threads of the CTA ([pool]
+// "kernel forgets absent blocks": logical blocks <= t / bs that are mapped and
+// valid; the last one up to row t mod bs).  The table and the valid words are
+// staged in shared memory with coalesced loads (s_tab, s_val: the pipeline
+// stages, not yet in use).  Warp w looks at logical blocks [1024 w, 1024 (w + 1)),
+// 32 at a time; a ballot per 32 gives the attended blocks, and a scan of the
+// warps' counts their ranks.  Every attended block but the sequence's last
+// holds bs rows, so row r of the attended rows lies in the attended block of
+// rank r / bs, at row r mod bs.  Shares: [floor(x R / G), floor((x + 1) R / G))
+// with G = min(R, shares) (1 when R = 0), as the plan kernel cuts them.
+// The parameters arrive by value: read through a reference to the kernel's
+// parameter block, every field access would be a generic load.
+struct SelfPlanArgs {
+    const int32_t* table;
+    const uint32_t* valid;
+    const int32_t* pos;
+    uint32_t* err;
+    int2* seq_items;
+    int maxb, num_blocks, bs, nsplit;
+};
+
+static __device__ __noinline__ void self_plan_single(const SelfPlanArgs p, SelfPlan* sp, int* s_red,
+                                                     int32_t* s_tab, uint32_t* s_val, uint64_t* bar) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = kDecodeThreads / 32;
+    constexpr int PER = kSelfPlanMax / kDecodeThreads;          // table entries per thread
+    static_assert(NW * 1024 >= kSelfPlanMax, "the warps' ranges cover the table");
+    const int maxb = p.maxb, nvw = (p.num_blocks + 31) >> 5;
+    // the table and the valid words land in shared memory by bulk copies of
+    // their whole 16-byte multiples (the host takes this path only for 16-byte
+    // aligned buffers), completing on `bar`; the last 1-3 entries of each are
+    // loaded by threads
+    const int tab4 = maxb & ~3, val4 = p.valid ? (nvw & ~3) : 0;
+    if (tid == 0) {
+        mbar_expect_tx(bar, (uint32_t)((tab4 + val4) * 4));
+        if (tab4) bulk_load(s_tab, p.table, (uint32_t)(tab4 * 4), bar);
+        if (val4) bulk_load(s_val, p.valid, (uint32_t)(val4 * 4), bar);
+        mbar_arrive(bar);
+    }
+    if (tid < maxb - tab4) s_tab[tab4 + tid] = __ldcg(p.table + tab4 + tid);
+    if (p.valid) {
+        if (tid < nvw - val4) s_val[val4 + tid] = __ldcg(p.valid + val4 + tid);
+    } else {
+        for (int i = tid; i < nvw; i += kDecodeThreads) s_val[i] = 0xffffffffu;
+    }
+    const int traw = __ldcg(p.pos);
+    if (!mbar_wait(bar, 0)) {
+        // the copies never landed: plan nothing (every share empty)
+        if (tid == 0) set_error(p.err, 0x8u /* KVC_DEV_TIMEOUT */);
+        for (int i = tid; i < maxb; i += kDecodeThreads) s_tab[i] = -1;
+    }
+    if (tid == 0) {
+        sp->tphys = -1;
+        sp->tattended = 0;
+        sp->lb = sp->row = sp->rows = 0;
+        sp->phys = -1;
+    }
+    __syncthreads();
+    const int t = clamp_paged_t(traw, maxb, p.bs);
+    const int nb = t < 0 ? 0 : t / p.bs + 1;
+    const int last_rows = t < 0 ? 0 : t - (nb - 1) * p.bs + 1;
+    const bool reporter = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    bool bad = false;
+    auto attended = [&](int e) -> bool {
+        if (e >= nb) return false;
+        const int q = s_tab[e];
+        if (q < 0) return false;
+        if (q >= p.num_blocks) {
+            bad = true;
+            return false;
+        }
+        return (s_val[q >> 5] >> (q & 31)) & 1u;
+    };
+    // lane k keeps the ballot of the warp's k-th group of 32 blocks (a short
+    // loop: this runs once per launch, from a cold instruction cache)
+    uint32_t my_m = 0;
+    int cnt = 0;
+    const int nbk = p.num_blocks;
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) {
+        // branch-free: both shared-memory reads issued unconditionally
+        const int e = warp * 1024 + k * 32 + lane;
+        const int q = s_tab[e < nb ? e : 0];
+        const bool in = e < nb && q >= 0 && q < nbk;
+        const uint32_t w = s_val[in ? (q >> 5) : 0];
+        bad |= e < nb && q >= nbk;
+        const uint32_t mk = __ballot_sync(0xffffffffu, in && ((w >> (q & 31)) & 1u));
+        if (lane == k) my_m = mk;
+        cnt += __popc(mk);
+    }
+    if (bad && reporter) set_error(p.err, 0x1u /* KVC_DEV_BAD_BLOCK */);
+    if (lane == 0) s_red[warp] = cnt;
+    __syncthreads();
+    int before = 0, nblk = 0;
+#pragma unroll 1
+    for (int k = 0; k < NW; ++k) {
+        const int c = s_red[k];
+        before += k < warp ? c : 0;
+        nblk += c;
+    }
+    const bool last_att = nb > 0 && attended(nb - 1);
+    const int R = nblk * p.bs - (last_att ? p.bs - last_rows : 0);
+    const int G = R < p.nsplit ? (R > 0 ? R : 1) : p.nsplit;
+    const int x = blockIdx.x;
+    if (x < G && R > 0) {
+        const int lo = (int)((long long)x * R / G), hi = (int)((long long)(x + 1) * R / G);
+        const int kb = lo / p.bs;                       // rank of the share's first block
+        if (kb >= before && kb < before + cnt) {        // in this warp's blocks (warp-uniform)
+            const int c = __popc(my_m);
+            int incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            const int j = kb - before - (incl - c);     // its rank among this lane's 32 blocks
+            if (j >= 0 && j < c) {
+                uint32_t mm = my_m;
+#pragma unroll 1
+                for (int q = 0; q < j; ++q) mm &= mm - 1u;
+                const int e = warp * 1024 + lane * 32 + (__ffs(mm) - 1);
+                sp->lb = e;
+                sp->row = lo - kb * p.bs;
+                sp->rows = hi - lo;
+                sp->phys = s_tab[e];
+            }
+        }
+    }
+    // the block that receives the step's new token (kvc_decode_step)
+    if (tid == 0 && traw >= 0 && traw == t) {
+        const int tlb = traw / p.bs;
+        sp->tphys = s_tab[tlb];
+        sp->tattended = attended(tlb);
+    }
+    if (tid == 0) {
+        sp->G = G;
+        sp->traw = traw;
+        if (reporter) p.seq_items[0] = make_int2(0, G);   // the combine's view of the partials
+    }
+    // the staged table leaves the stages to the tensor copies
+    fence_proxy_async_smem();
+    __syncthreads();
+}
 
 struct alignas(16) MmaStageMeta {
     int nsub;        // sub-tiles in the stage (0 allowed); -1 = end of the stream
@@ -321,6 +477,42 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
     }
 }
 
+// One warp writes token t of kv head kvh of sequence 0 (k_new / v_new) to
+// K-half row `row` of the layer: K rotated at t when BAKED, V as it is; an
+// INT8 cache stores codes and row scales.
+template <int D, bool Q8>
+__device__ __noinline__ void append_token_warp(const DecodeParams& p, long long row, int kvh, int t, int lane) {
+    const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(p.k_new) + (long long)kvh * D;
+    const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(p.v_new) + (long long)kvh * D;
+    if constexpr (Q8) {
+        int8_t* kg = const_cast<int8_t*>(static_cast<const int8_t*>(p.cache)) + p.layer_off + row * D;
+        float* ksg = p.scales + p.sc_layer_off + row;
+        int8_t kq[D / 32], vq[D / 32];
+        float sk, sv;
+        q8_store_token_warp<D / 64>(kn, vn, kg, kg + p.kv_off, ksg, ksg + p.sc_kv_off, p.rope, t, p.theta, lane, kq,
+                                    vq, &sk, &sv);
+    } else {
+        constexpr int HALF = D / 2;
+        __nv_bfloat16* kg = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(p.cache)) + p.layer_off +
+                            row * D;
+        __nv_bfloat16* vg = kg + p.kv_off;
+        for (int i = lane; i < HALF; i += 32) {
+            __nv_bfloat16 k1 = kn[i], k2 = kn[i + HALF];
+            if (p.rope == kRopeBaked) {
+                float cs, sn;
+                rope_cos_sin((long long)t, p.theta[i], &cs, &sn);
+                const float x1 = __bfloat162float(k1), x2 = __bfloat162float(k2);
+                k1 = __float2bfloat16_rn(x1 * cs - x2 * sn);
+                k2 = __float2bfloat16_rn(x1 * sn + x2 * cs);
+            }
+            kg[i] = k1;
+            kg[i + HALF] = k2;
+            vg[i] = vn[i];
+            vg[i + HALF] = vn[i + HALF];
+        }
+    }
+}
+
 template <int D, int GH, bool PAGED, bool READ, bool Q8>
 // Two CTAs (ten warps) per SM: three warps share a sub-partition's 16K
 // registers, so a thread may hold at most 168.
@@ -352,10 +544,11 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
     const int kvh = blockIdx.y, z = blockIdx.z;
     const int group = kvh * gridDim.z + z;     // this (kv head, q-head group)'s share counter
 
-    // inputs written by earlier kernels (append, plan) are read only after this
-    pdl_wait();
-
+    // shared-memory barriers and the tensor maps depend on the launch only:
+    // set up before waiting for the previous kernel in the stream
+    __shared__ uint64_t s_plan_bar;      // one paged sequence: the staged table landed
     if (tid == 0) {
+        mbar_init(&s_plan_bar, 1);
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
@@ -372,12 +565,31 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             tma_prefetch_desc(&maps.sc_sub);
         }
     }
+    // inputs written by earlier kernels (append, plan) are read only after this
+    pdl_wait();
     pdl_launch_dependents();    // the combine kernel may start launching
     __syncthreads();
+    // one paged sequence: this CTA's share, planned here (no plan kernel)
+    __shared__ SelfPlan s_plan;
+    __shared__ int s_red[kDecodeThreads / 32];
+    if constexpr (PAGED) {
+        static_assert((size_t)NST * S::kStageBytes >= (size_t)(kSelfPlanMax + kSelfPlanValidWords) * 4,
+                      "the stages hold the staged table and valid words");
+        if (p.self_plan) {
+            const SelfPlanArgs a{p.table, p.valid, p.pos, p.err, const_cast<int2*>(p.seq_items),
+                                 p.maxb, p.num_blocks, p.bs, p.nsplit};
+            self_plan_single(a, &s_plan, s_red, reinterpret_cast<int32_t*>(stage_base),
+                             reinterpret_cast<uint32_t*>(stage_base + kSelfPlanMax * 4), &s_plan_bar);
+        }
+    }
 
 
     if (warp == kConsumerWarps) {
         // =================== copy-issuing warp ==============================
+        // K/V rows read once per call stream through L2 as evict-first, except
+        // paged batches, whose shared blocks are read by several sequences
+        const bool evict_first = !(PAGED && p.B > 1);
+        const uint64_t pol = l2_policy_evict_first();
         int it = 0, fill = 0, run_off = 0, claims = 0;
         bool ok = true, open = false, hdr_sent = false;
         // the first segment's header goes to the compute warps at once, so that
@@ -512,11 +724,20 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 }
                 mbar_expect_tx(&full[s], (uint32_t)(S::kBoxes * 2 * R * 128));
                 if (p.tma_whole) {
-                    tma_load_5d(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s]);
+                    if (evict_first)
+                        tma_load_5d_hint(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s], pol);
+                    else
+                        tma_load_5d(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s]);
                 } else {
 #pragma unroll
-                    for (int bx = 0; bx < S::kBoxes; ++bx)
-                        tma_load_4d(dst + bx * 2 * R * 128, map, bx * S::kBoxCols, (int)urow, 0, p.layer, &full[s]);
+                    for (int bx = 0; bx < S::kBoxes; ++bx) {
+                        if (evict_first)
+                            tma_load_4d_hint(dst + bx * 2 * R * 128, map, bx * S::kBoxCols, (int)urow, 0, p.layer,
+                                             &full[s], pol);
+                        else
+                            tma_load_4d(dst + bx * 2 * R * 128, map, bx * S::kBoxCols, (int)urow, 0, p.layer,
+                                        &full[s]);
+                    }
                 }
             }
             fill += nsr;
@@ -526,12 +747,12 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
         // (1..16) from K-half row urow, sub-tile `rank` after the stage's
         // current fill (lanes of one call take distinct ranks below the room).
         constexpr int kSubCopy = S::kBoxes * 2 * 16 * 128;
-        auto emit_sub_lane = [&](long long urow, int n, int rank) {
+        auto emit_sub_lane = [&](long long urow, int n, int rank, int newrow) {
             const int s = it % NST;
             const int f = fill + rank;
             meta[s].nrows[f] = n;
             meta[s].ip0[f] = 0;
-            meta[s].newrow[f] = -1;
+            meta[s].newrow[f] = newrow;
             meta[s].base[f] = run_off + rank * kSubCopy;
             meta[s].ld[f] = 16;
             if constexpr (Q8) {
@@ -615,6 +836,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                     hdr.slot = xs + b;
                     hdr.first_slot = fx + b;
                     hdr.nparts = lx - fx + 1;
+                    hdr.new_row = -1;   // the window path marks the new token's run instead
                     if (!(ok = begin_segment(hdr))) break;
                     // units of the sequence: kSeqUnits charged for its segment
                     // start, then one per 16 rows
@@ -665,17 +887,37 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             }
             }
         } else {
-            const int G = __ldcg(&p.n_items[1]);    // the plan's share count
-            for (int xs = claim(G); xs < G && ok; xs = claim(G)) {
+            const bool self = p.self_plan != 0;
+            const int G = self ? s_plan.G : __ldcg(&p.n_items[1]);    // the plan's share count
+            // self-planned step: the new token's K-half row, when this CTA's
+            // share holds it (it is the sequence's last attended row)
+            int new_lb = -1, new_r = 0, new_row = -1;
+            if (self && p.k_new && s_plan.traw >= 0 && s_plan.tphys >= 0 && s_plan.tphys < p.num_blocks) {
+                new_lb = s_plan.traw / p.bs;
+                new_r = s_plan.traw % p.bs;
+                new_row = (s_plan.tphys * p.Hkv + kvh) * p.bs + new_r;
+                if (!s_plan.tattended) {
+                    // mapped but not resident: written here, never read by this step
+                    if ((int)blockIdx.x == 0 && z == 0) append_token_warp<D, Q8>(p, new_row, kvh, s_plan.traw, lane);
+                    new_lb = -1;
+                }
+            } else if (self && p.k_new && s_plan.traw >= 0 && (int)blockIdx.x == 0 && kvh == 0 && z == 0 &&
+                       lane == 0) {
+                set_error(p.err, (s_plan.traw / p.bs >= p.maxb) ? 0x4u : (s_plan.tphys < 0 ? 0x2u : 0x1u));
+            }
+            auto newrow_of = [&](int lbk, int row0, int n) -> int {
+                return (lbk == new_lb && new_r >= row0 && new_r < row0 + n) ? new_r - row0 : -1;
+            };
+            for (int xs = claim(G); xs < G && ok; xs = self ? G : claim(G)) {
             // one sequence: share x holds exactly its item x
-            const int2 my_items = p.B == 1 ? make_int2(xs, 1) : __ldcg(&p.cta_items[xs]);
+            const int2 my_items = (self || p.B == 1) ? make_int2(xs, 1) : __ldcg(&p.cta_items[xs]);
             for (int k = 0; k < my_items.y && ok; ++k) {
                 const int item = my_items.x + k;
                 if (item < 0 || item >= p.max_items) {
                     if (lane == 0) index_fault(p.err, 1, item);
                     break;
                 }
-                const int4 itv = p.items[item];
+                const int4 itv = self ? make_int4(0, s_plan.lb, s_plan.row, s_plan.rows) : p.items[item];
                 const int b = itv.x;
                 if (b < 0 || b >= p.B) {
                     if (lane == 0) index_fault(p.err, 2, b);
@@ -684,7 +926,9 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 // (t, first slot, slot count, first physical block): read with the
                 // item for one sequence; a batch reads them per sequence
                 int4 inf;
-                if (p.B == 1) {
+                if (self) {
+                    inf = make_int4(s_plan.traw, 0, G, s_plan.phys);
+                } else if (p.B == 1) {
                     inf = __ldcg(&p.item_info[item]);
                 } else {
                     const int2 si = p.seq_items[b];
@@ -696,6 +940,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 hdr.slot = item;
                 hdr.first_slot = inf.y;
                 hdr.nparts = inf.z;
+                hdr.new_row = new_row;
                 if (!(ok = begin_segment(hdr))) break;
                 const int tt = clamp_paged_t(hdr.t, p.maxb, p.bs);
                 const int32_t* trow = p.table + (long long)b * p.maxb;
@@ -723,7 +968,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                             break;
                         }
                         const int n = min(take, 16 * room);
-                        emit_run(blk + row, n, 0, -1, true);
+                        emit_run(blk + row, n, 0, newrow_of(lb, row, n), true);
                         take -= n;
                         rem -= n;
                         row += n;
@@ -758,7 +1003,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                         const int rank = __popc(pending & ((1u << lane) - 1u));
                         const bool mine = ((pending >> lane) & 1u) && rank < room;
                         const unsigned emitted = __ballot_sync(0xffffffffu, mine);
-                        if (mine) emit_sub_lane(urow, take, rank);
+                        if (mine) emit_sub_lane(urow, take, rank, newrow_of(my_lb, row0, take));
                         __syncwarp();
                         fill += __popc(emitted);
                         run_off += __popc(emitted) * kSubCopy;
@@ -787,7 +1032,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                                 break;
                             }
                             const int n = min(take, 16 * room);
-                            emit_run(blk + row, n, 0, -1, true);
+                            emit_run(blk + row, n, 0, newrow_of(lb + src, row, n), true);
                             take -= n;
                             rem -= n;
                             row += n;
@@ -813,6 +1058,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             MmaSegment none;
             none.b = -1;
             none.t = none.slot = none.first_slot = none.nparts = 0;
+            none.new_row = -1;
             publish_first(none);
         }
         if (!ok && lane == 0) {
@@ -1117,19 +1363,29 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             const uint32_t ku = smem_u32(Ks), vu = smem_u32(Vs);
             bool wrote = false;
 
-            if constexpr (!PAGED) {
+            {
                 // fused append (kvc_decode_step): this sub-tile holds the slot of the
                 // token being decoded.  Write its K (RoPE baked at t when BAKED) and V
                 // to the cache, and over the stale row just copied into shared memory.
+                // Window layouts: the token's slot; a self-planned paged sequence:
+                // the row the header names.
                 const int nr = meta[s].newrow[tg];
+                long long new_row = 0;
+                if (nr >= 0) {
+                    if constexpr (PAGED) {
+                        new_row = seg.new_row;
+                    } else {
+                        const int h_slot = seg.t < p.sinks ? seg.t
+                                                           : p.sinks + (int)((unsigned)(seg.t - p.sinks) % (unsigned)p.window);
+                        new_row = ((long long)seg.b * p.Hkv + kvh) * p.capacity + h_slot;
+                    }
+                }
                 if (Q8 && nr >= 0) {
                     if (hd == 0) {
                         // INT8: quantise the new rows; codes and scales go to the cache
                         // and over the stale copies in shared memory
                         const long long unit = (long long)seg.b * p.Hkv + kvh;
-                        const int h_slot = seg.t < p.sinks ? seg.t
-                                                           : p.sinks + (int)((unsigned)(seg.t - p.sinks) % (unsigned)p.window);
-                        const long long row = unit * p.capacity + h_slot;
+                        const long long row = new_row;
                         int8_t* kg = const_cast<int8_t*>(static_cast<const int8_t*>(p.cache)) + p.layer_off + row * D;
                         float* ksg = p.scales + p.sc_layer_off + row;
                         int8_t kq[D / 32], vq[D / 32];
@@ -1162,10 +1418,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                         const long long unit = (long long)seg.b * p.Hkv + kvh;
                         const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(p.k_new) + unit * D;
                         const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(p.v_new) + unit * D;
-                        const int h_slot = seg.t < p.sinks ? seg.t
-                                                           : p.sinks + (int)((unsigned)(seg.t - p.sinks) % (unsigned)p.window);
                         __nv_bfloat16* kg = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(p.cache)) +
-                                            p.layer_off + (unit * p.capacity + h_slot) * D;
+                                            p.layer_off + new_row * D;
                         __nv_bfloat16* vg = kg + p.kv_off;
                         for (int i = lane; i < HALF; i += 32) {
                             __nv_bfloat16 k1 = kn[i], k2 = kn[i + HALF];

@@ -26,6 +26,12 @@ constexpr int kPagedShareBatch = 8;
 // partial write), besides one unit per 16 rows.
 constexpr int kSeqUnits = 4;
 constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
+// Paged caches of one sequence: the decode CTAs plan their own stream-K share
+// from the block table and valid bits, staged in their (still empty) pipeline
+// stages, without a plan kernel, when the table has at most kSelfPlanMax
+// entries and the valid bits at most kSelfPlanValidWords words.
+constexpr int kSelfPlanMax = 5120;
+constexpr int kSelfPlanValidWords = 4096;
 // Resident CTAs per SM of the decode kernel.  INT8 stages are half the
 // bytes of bf16 ones; paged INT8 batches at head_dim <= 128 run three CTAs
 // per SM (the compute warps are the bound there; measured 164 -> 151 us on
@@ -89,6 +95,7 @@ struct DecodeParams {
     int max_items;              // partial slots per q head (bound for every slot index)
     int rope;                   // kRopeNone / kRopeBaked / kRopeRead
     int tma_whole;              // bf16: 1 = one tensor copy per run covers every column block
+    int self_plan;              // PAGED, one sequence: the decode CTAs plan their shares (no plan kernel)
     float q_scale;              // softmax scale * log2(e)
     float theta_f[kMaxHalfDim];     // RoPE frequencies, fp32 (small in-tile angles)
     unsigned long long theta[kMaxHalfDim];   // RoPE frequencies as turns, fixed point: theta_i / (2 pi) * 2^64
