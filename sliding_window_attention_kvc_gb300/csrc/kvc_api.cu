@@ -320,6 +320,43 @@ int kv_maps_for(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps
     return KVC_OK;
 }
 
+// Paged caches, for the warp-specialised prefill: {column, row, K|V, layer}
+// with boxes of one block (bs rows) of K or of V, 64 columns.
+int encode_block_map(const kvc_desc* d, const Geo& g, const void* cache, CUtensorMap* map) {
+    const unsigned long long half_rows = (unsigned long long)g.half_elems / d->head_dim;
+    if (half_rows >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return KVC_ERR_CUDA;
+    const cuuint64_t row_bytes = (cuuint64_t)d->head_dim * 2, half_bytes = half_rows * row_bytes;
+    const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, half_rows, 2, (cuuint64_t)d->layers};
+    const cuuint64_t strides[3] = {row_bytes, half_bytes, 2 * half_bytes};
+    const cuuint32_t box[4] = {64, (cuuint32_t)d->block_size, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? KVC_OK
+               : KVC_ERR_CUDA;
+}
+
+// The chunk's staged rows, K [batch][T][kv head][D] then V at kv_bytes past
+// it: {64 columns, kv head, batch * T, K|V, column block}, boxes of 64 tokens
+// of one kv head, K and V, every column.
+int encode_stage_map(const kvc_desc* d, const void* kst, long long T, size_t kv_bytes, CUtensorMap* map) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return KVC_ERR_CUDA;
+    const cuuint64_t D = (cuuint64_t)d->head_dim;
+    const cuuint64_t dims[5] = {64, (cuuint64_t)d->kv_heads, (cuuint64_t)(d->batch * T), 2, D / 64};
+    const cuuint64_t strides[4] = {D * 2, (cuuint64_t)d->kv_heads * D * 2, (cuuint64_t)kv_bytes, 128};
+    const cuuint32_t box[5] = {64, 1, 64, 2, (cuuint32_t)(D / 64)};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(kst), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? KVC_OK
+               : KVC_ERR_CUDA;
+}
+
 }  // namespace
 
 }  // namespace kvc
@@ -584,7 +621,13 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     Geo g;
     int rc = check_desc(d, &g);
     if (rc) return rc;
-    if (d->dtype != KVC_BF16 || (d->head_dim != 64 && d->head_dim != 128) || g.G > 64) return KVC_ERR_UNSUPPORTED;
+    if (d->dtype != KVC_BF16) return KVC_ERR_UNSUPPORTED;
+    const bool paged_l = d->layout == KVC_LAYOUT_PAGED;
+    // the warp-specialised kernel: 128-row Q tiles of whole GQA groups, paged
+    // blocks that pack a 64-key tile, chunks no longer than the window
+    const bool ws_kernel = 128 % g.G == 0 &&
+                           (paged_l ? (d->block_size % 8 == 0 && 64 % d->block_size == 0) : T <= d->window);
+    if (!ws_kernel && ((d->head_dim != 64 && d->head_dim != 128) || g.G > 64)) return KVC_ERR_UNSUPPORTED;
     if (!cache || !q || !k_new || !v_new || !pos0 || !out || !workspace) return KVC_ERR_NULL;
     const bool paged = d->layout == KVC_LAYOUT_PAGED;
     if (paged && !block_table) return KVC_ERR_NULL;
@@ -649,10 +692,25 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     pp.num_blocks = d->num_blocks;
     pp.maxb = d->max_blocks_per_seq;
     pp.rope = d->rope;
+    pp.layer = layer;
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
     pp.q_scale = scale * 1.4426950408889634f;
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
-    if (launch_prefill(d->head_dim, g.G, pp, s) != cudaSuccess) return KVC_ERR_CUDA;
+    if (ws_kernel) {
+        PrefillMaps pm;
+        std::memset(&pm, 0, sizeof(pm));
+        if (paged_l) {
+            if ((rc = encode_block_map(d, g, cache, &pm.block))) return rc;
+        } else {
+            KvTensorMaps km;
+            if ((rc = kv_maps_for(d, g, cache, &km, &pm.slot_whole))) return rc;
+            pm.slot = km.run[kRunMaps - 1];                 // 64-row runs
+        }
+        if ((rc = encode_stage_map(d, kst, T, prefill_stage_bytes(d, T) / 2, &pm.stage))) return rc;
+        if (launch_prefill_ws(d->head_dim, pp, pm, s) != cudaSuccess) return KVC_ERR_CUDA;
+    } else if (launch_prefill(d->head_dim, g.G, pp, s) != cudaSuccess) {
+        return KVC_ERR_CUDA;
+    }
     // 3. the chunk appended
     if (launch_append(d->dtype, ap, s) != cudaSuccess) return KVC_ERR_CUDA;
     return KVC_OK;

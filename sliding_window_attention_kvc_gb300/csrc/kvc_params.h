@@ -159,8 +159,23 @@ struct PrefillParams {
     int B, T, Hq, Hkv, G;
     int layout, window, sinks, capacity, bs, num_blocks, maxb;
     int rope;
+    int layer;
     float q_scale;              // softmax scale * log2(e)
     unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
+};
+
+// Tensor maps of the warp-specialised prefill (kvc_prefill_ws.cu), bf16 rows,
+// 64-column boxes, 128-byte swizzle:
+//   slot   window caches: 64 consecutive rows of a K half with their V rows,
+//          5-D {64 columns, row, K|V, layer, column block} (slot_whole) or
+//          4-D {column, row, K|V, layer} one column block at a time;
+//   block  paged caches: {column, row, K|V, layer}, boxes of one block (bs
+//          rows) of K or of V, one column block;
+//   stage  the chunk's staged rows [batch][T][kv head][D] (K, then V):
+//          {64 columns, kv head, batch * T, K|V, column block}, 64 tokens.
+struct PrefillMaps {
+    CUtensorMap slot, block, stage;
+    int slot_whole;
 };
 
 struct TableParams {
@@ -230,6 +245,8 @@ cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
 cudaError_t launch_prefill_stage(const AppendParams& p, void* kst, void* vst, cudaStream_t stream);
 cudaError_t launch_prefill(int head_dim, int g, const PrefillParams& p, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);   // head_dim 128, tcgen05
+// head_dim 64 / 128 / 256, warp-specialised tcgen05 with TMA tiles
+cudaError_t launch_prefill_ws(int head_dim, const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream);
 cudaError_t launch_valid_write(const TableParams& p, cudaStream_t stream);
 cudaError_t launch_block_prepare(int elt, const BlockParams& p, cudaStream_t stream);
 cudaError_t launch_block_share(const BlockParams& p, int n, cudaStream_t stream);

@@ -215,7 +215,7 @@ def _run_prefill(kvc, p, pos0, T, table=None, valid_bits=None):
 
 
 @pytest.mark.parametrize("D,rope,sinks", [(128, "baked", 0), (128, "read_time", 4), (64, "none", 0),
-                                          (64, "read_time", 4)])
+                                          (64, "read_time", 4), (256, "baked", 0), (256, "read_time", 4)])
 def test_prefill_window_sets_exact(kvc, D, rope, sinks):
     """Ring and sink+ring chunks before, across and far past the first wrap,
     with left padding; ids: sinks keep their position, window positions count
@@ -254,13 +254,13 @@ def test_prefill_window_sets_exact(kvc, D, rope, sinks):
     _run_prefill(kvc, p, pos0, T)
 
 
-@pytest.mark.parametrize("D", [128, 64])
-def test_prefill_paged_sets_exact(kvc, D):
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 16), (256, 64), (128, 32)])
+def test_prefill_paged_sets_exact(kvc, D, bs):
     """Paged chunks over a table with a shared prefix, holes and invalid
     blocks; the chunk's own blocks mapped and resident; ids = positions."""
-    rng = np.random.default_rng(21 + D)
+    rng = np.random.default_rng(21 + D + bs)
     Hq, Hkv, _ = GEOM[D]
-    B, bs, maxb, T = 6, 16, 24, 96
+    B, maxb, T = 6, 24 * 16 // bs, 96
     nb = 3 + B * maxb + B * (T // bs + 2)   # room for private blocks under the chunks
     table, valid, _ = _random_paged(rng, B, bs, maxb, nb, share=True, empty=False)
     pos0 = np.array([-7, 0, 5, 40, 150, bs * maxb - T], dtype=np.int64)

@@ -95,6 +95,11 @@ CASES = {
     "sink_read_d64": ("sink_window_bf16", "read_time", [3, 180, 987600], 45, {"head_dim": 64}),
     # several CTAs per (sequence, kv head) along the chunk
     "ring_long_chunk": ("ring_bf16", "baked", [150, 190, 4300], 130),
+    # head_dim 256 (the long-context pool's head size)
+    "ring_d256": ("ring_bf16", "baked", [150, 190, 4300], 37, {"head_dim": 256}),
+    "sink_read_d256": ("sink_window_bf16", "read_time", [3, 180, 987600], 45, {"head_dim": 256}),
+    # a chunk longer than the window: the pre-tile kernels take it
+    "ring_chunk_past_window": ("ring_bf16", "baked", [150, 190, 4300], 230),
 }
 
 
@@ -135,3 +140,15 @@ def test_prefill_left_padding(kvc):
         assert not got[b, :pad].any()
         ref = _oracle(wl, b, pos0[b], T, q)
         assert float(np.abs(got[b] - ref).max()) <= TOL["bf16"], b
+
+
+def test_prefill_long_context_pool_d256(kvc):
+    """The pool's shape (head_dim 256, 64-token blocks, valid mask): a chunk of
+    96 tokens ending at the sequence's position, in its always-resident tail."""
+    wl = kvc_synth.make_workload("long_context_pool_bf16", small=True)
+    T = 96
+    pos0 = [int(wl.positions[0]) - T + 1]
+    got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
+    assert np.isfinite(got).all()
+    ref = _oracle(wl, 0, pos0[0], T, q)
+    assert float(np.abs(got[0] - ref).max()) <= TOL["bf16"]
