@@ -36,7 +36,6 @@ namespace {
 
 constexpr int kWsKeys = 64;                 // keys per tile
 constexpr int kWsRows = 128;                // rows per Q tile (TMEM lanes)
-constexpr int kWsThreads = 384;             // 12 warps
 constexpr int kWsSoftmax0 = 4;              // first softmax warp
 constexpr float kWsLazy = 8.f;
 
@@ -58,6 +57,8 @@ struct WsShape {
     static constexpr int TmemCols = 512;
     static constexpr int SCol0 = NQ * D;                       // S buffers after the O tiles
     static_assert(NQ * D + NQ * 2 * kWsKeys <= TmemCols, "TMEM columns");
+    // 4 control warps, then 4 softmax warps per Q tile (one thread per row)
+    static constexpr int Threads = 32 * (kWsSoftmax0 + 4 * NQ);
 };
 
 // How the softmax masks a tile's keys: every key seen by every row of the
@@ -153,11 +154,43 @@ __device__ __forceinline__ void ws_st32(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void ws_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void ws_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 2^a and 2^b in one special-function op: the arguments rounded to fp16
+// (ex2.approx.f16x2) and the results widened to fp32.  Softmax arguments here
+// are <= 8 (the lazy reference max), so fp16 keeps them to 2^-8 or better --
+// finer than the bf16 rounding P gets for P V; a masked key's -inf gives 0.
+__device__ __forceinline__ float2 ws_ex2_pair(float a, float b) {
+    float2 r;
+    asm("{\n\t.reg .b32 h;\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.f16x2.f32 h, %3, %2;\n\t"
+        "ex2.approx.f16x2 h, h;\n\t"
+        "mov.b32 {lo, hi}, h;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t"
+        "cvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a), "f"(b));
+    return r;
+}
+
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes (or the hint, 0.1 ms, runs out) instead of coming
+// back to re-issue the test, which would take issue slots from the softmax warps
+__device__ __forceinline__ bool ws_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 100000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // A bounded wait that also gives up once another role has given up.
 __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (ws_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!ws_try_wait(bar, parity)) {
         if (*abort || clock64() - t0 > kWaitCycles) return false;
     }
     return true;
@@ -166,7 +199,7 @@ __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile
 }  // namespace
 
 template <int D, bool READ>
-__global__ void __launch_bounds__(kWsThreads, 1)
+__global__ void __launch_bounds__(WsShape<D>::Threads, 1)
     prefill_ws_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ PrefillMaps maps) {
     using S = WsShape<D>;
     constexpr int NQ = S::NQ, NST = S::STAGES, CB = S::CB;
@@ -508,7 +541,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             constexpr uint32_t kIdescS = ws_idesc(kWsRows, kWsKeys, 0);
             constexpr uint32_t kIdescO = ws_idesc(kWsRows, D, 1);
             bool ok = true;
-            int nt = 0;
+            int nt = 0x7fffffff;
             auto stage_u = [&](int j) { return sm_u + S::OffStage + (j % NST) * S::StageBytes; };
             // S_i(j) = Q_i K_j^T
             auto issue_s = [&](int j) {
@@ -530,31 +563,34 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     ws_commit(&bars->s_full[i][j & 1]);
                 }
             };
-            auto wait_ready = [&](int j) -> bool {
-                if (!ws_wait(&bars->ready[j % NST], (j / NST) & 1, abort)) return false;
-                return meta[j % NST].kind != kTileEnd;
-            };
-            bool have = wait_ready(0);
-            if (*abort) ok = false;
-            if (ok && have) {
-                for (int i = 0; i < NQ && ok; ++i)
-                    if (!ws_wait(&bars->q_ready[i], 0, abort)) ok = false;
-                if (ok) issue_s(0);
-            }
-            int j = 0;
-            while (ok && have) {
-                // S of the next tile first: it runs while the softmax of tile j does
-                bool next = wait_ready(j + 1);
-                if (*abort) {
+            // S of tile t for every Q tile, once its keys are in place; false at
+            // the end marker (nt = t) or when a wait gave up
+            auto try_issue = [&](int t) -> bool {
+                if (!ok || t >= nt) return false;
+                if (!ws_wait(&bars->ready[t % NST], (t / NST) & 1, abort)) {
                     ok = false;
-                    break;
+                    return false;
                 }
-                if (next) {
-                    if (READ && sink_tile && j + 1 == 1)         // q re-rotated past the sink tile
-                        for (int i = 0; i < NQ && ok; ++i)
-                            if (!ws_wait(&bars->q_ready[i], 1, abort)) ok = false;
-                    if (ok) issue_s(j + 1);
+                if (meta[t % NST].kind == kTileEnd) {
+                    nt = t;
+                    return false;
                 }
+                for (int i = 0; i < NQ && ok; ++i) {
+                    // q at position 0, and (read-time RoPE) again past the sink tile
+                    if (t == 0 && !ws_wait(&bars->q_ready[i], 0, abort)) ok = false;
+                    if (READ && sink_tile && t == 1 && !ws_wait(&bars->q_ready[i], 1, abort)) ok = false;
+                }
+                if (ok) issue_s(t);
+                return ok;
+            };
+            // S runs LA tiles ahead of P V: each Q tile's next scores are queued
+            // on the tensor cores while its softmax works on the current ones.
+            // LA + 1 tiles are in flight, so the stages must hold them.
+            constexpr int LA = NST >= 3 ? 2 : 1;
+            int issued = 0;
+            while (issued < LA && try_issue(issued)) ++issued;
+            int j = 0;
+            for (; ok && j < issued; ++j) {
                 // O_i += P_i V_j
                 for (int i = 0; i < NQ && ok; ++i) {
                     if (!ws_wait(&bars->p_full[i], j & 1, abort)) {
@@ -572,13 +608,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
                 if (!ok) break;
                 ws_commit(&bars->empty[j % NST]);       // K and V of tile j are done with
-                ++j;
-                have = next;
+                if (issued == j + LA && try_issue(issued)) ++issued;
             }
+            if (*abort) ok = false;
             nt = j;
             if (ok) {
                 // the end: the softmax warps learn the tile count at the S slot
-                // they wait on next
+                // they wait on next (every S before it has been consumed)
                 bars->ntiles = nt;
                 for (int i = 0; i < NQ; ++i) mbar_arrive(&bars->s_full[i][nt & 1]);
             } else {
@@ -691,9 +727,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     sv[k] = allowed ? sv[k] : -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            // four independent chains (latency, not issue slots, is what the
+            // softmax warps wait on)
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int k = 0; k < kWsKeys; k += 2) mx = fmaxf(mx, fmaxf(sv[k], sv[k + 1]));
+            for (int k = 0; k < kWsKeys; k += 4)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) mq[u] = fmaxf(mq[u], sv[k + u]);
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             float mn = m_run, alpha = 1.f;
             if (mx > m_run + kWsLazy) {
                 mn = mx;
@@ -701,16 +742,18 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
             // p = 2^(s - m) (exactly 0 for a masked key: 2^-inf), summed in pairs
             const float nmn = mn == -INFINITY ? 0.f : -mn;
-            float2 ls2 = make_float2(0.f, 0.f);
+            float2 ls2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
             for (int k = 0; k < kWsKeys; k += 2) {
                 const float2 d2 = __fadd2_rn(make_float2(sv[k], sv[k + 1]), make_float2(nmn, nmn));
-                sv[k] = exp2f(d2.x);
-                sv[k + 1] = exp2f(d2.y);
-                ls2 = __fadd2_rn(ls2, make_float2(sv[k], sv[k + 1]));
+                const float2 e2 = ws_ex2_pair(d2.x, d2.y);
+                sv[k] = e2.x;
+                sv[k + 1] = e2.y;
+                ls2[(k >> 1) & 3] = __fadd2_rn(ls2[(k >> 1) & 3], e2);
             }
-            const float ls = ls2.x + ls2.y;
-            l_run = l_run * alpha + ls;
+            const float2 lsa = __fadd2_rn(__fadd2_rn(ls2[0], ls2[1]), __fadd2_rn(ls2[2], ls2[3]));
+            l_run = l_run * alpha + (lsa.x + lsa.y);
             m_run = mn;
             // P V of the previous tile is done: P's buffer and O are free
             if (j > 0 && !ws_wait(&bars->o_done[qi], (j - 1) & 1, abort)) {
@@ -804,7 +847,7 @@ static cudaError_t launch_prefill_ws_t(const PrefillParams& p, const PrefillMaps
     }
     const int tok = kWsRows / p.G * WsShape<D>::NQ;
     dim3 grid((p.T + tok - 1) / tok, p.Hkv, p.B);
-    prefill_ws_kernel<D, READ><<<grid, kWsThreads, kSmem, stream>>>(p, maps);
+    prefill_ws_kernel<D, READ><<<grid, WsShape<D>::Threads, kSmem, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
