@@ -89,6 +89,26 @@ def attended_rows(wl):
     return rows, touched
 
 
+def attended_count(wl, b, t):
+    """Keys the token at position t of sequence b attends: the sinks below S
+    and the window's last W positions (window layouts), or the rows up to t of
+    mapped and valid blocks (paged)."""
+    if t < 0:
+        return 0
+    if wl.layout == "window":
+        sinks = min(wl.sinks, t + 1)
+        lo = max(wl.sinks, t - wl.window + 1)
+        return sinks + max(0, t - lo + 1)
+    bs = wl.block_size
+    n = 0
+    for lb in range(t // bs + 1):
+        phys = int(wl.block_table[b, lb])
+        if phys < 0 or (wl.valid is not None and not wl.valid[phys]):
+            continue
+        n += bs if lb < t // bs else t - lb * bs + 1
+    return n
+
+
 def step_bytes(wl):
     """Algorithmic bytes of one decode step (whole batch, one layer)."""
     rows, touched = attended_rows(wl)
@@ -745,12 +765,25 @@ def run_ours(args):
         eager_ms = statistics.median(timed_loops(st, fc, ne, 3, [])) / ne
 
     per_workload = None
+    prefill = None
     if rank == 0 and world == 1 and not args.no_per_workload:
         per_workload = []
         for name, pkw in PER_WORKLOAD:
             if name == wl.name and pkw == kw:
                 continue
             per_workload.append(measure_workload(name, pkw, PER_WORKLOAD_STEPS, args.loops))
+        # chunked prefill (kvc_prefill), 128-token chunks ending at each
+        # sequence's position, on the three bf16 layouts
+        prefill = []
+        for name in ("ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16"):
+            pa = argparse.Namespace(workload=name, chunk=128, steps=20, warmup=3)
+            r = measure_prefill(pa)
+            prefill.append({"workload": name, "chunk_tokens": 128, "ms_per_call": r["ms_per_call"],
+                            "tokens_per_s": r["tokens_per_s"], "tflops": r["value"],
+                            "roofline_frac": r["roofline"]["frac"], "peak_kind": r["roofline"]["peak_kind"],
+                            "rope": "read_time" if name == "sink_window_bf16" else "baked",
+                            "device_errors": r["device_errors"]})
+            torch.cuda.empty_cache()
     clk = clocks.stop()
 
     # end to end: host inputs copied in, host output copied out, every step
@@ -777,6 +810,7 @@ def run_ours(args):
         "gpu_launches_note": "kernels launched in one timed loop of K steps",
         "e2e": e2e,
         "per_workload": per_workload,
+        "prefill": prefill,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget, kw=kw)
@@ -1009,15 +1043,7 @@ def measure_prefill(args):
     pos_t = torch.from_numpy(pos0.astype(np.int32)).cuda()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     # algorithmic work: attended keys of every chunk token
-    import oracle
-    keys = 0
-    for b in range(B):
-        for i in range(T):
-            t = int(pos0[b]) + i
-            if wl.layout == "window":
-                keys += len(oracle.window_attended(t, wl.sinks, wl.window))
-            else:
-                keys += len(oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size))
+    keys = sum(attended_count(wl, b, int(pos0[b]) + i) for b in range(B) for i in range(T))
     flops = 4.0 * D * Hq * keys
     times = []
     for i in range(args.warmup + args.steps):
@@ -1043,7 +1069,7 @@ def measure_prefill(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "algorithmic_flops_per_call": flops,
-                         "kernel": "kvc_prefill: prefill_stage_kernel + prefill_tc_kernel (tcgen05, head_dim 128) + append_kernel",
+                         "kernel": "kvc_prefill: prefill_stage_kernel + prefill_ws_kernel (tcgen05, warp-specialised) + append_kernel",
                          "timer": "CUDA events around each call, median, L2 flushed between calls"},
             "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "chunk_tokens": T, "batch": B, "q_heads": Hq, "kv_heads": Hkv,

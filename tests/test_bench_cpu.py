@@ -30,3 +30,23 @@ def test_reference_arm_takes_the_pool_density():
     args = argparse.Namespace(workload="long_context_pool_bf16", density=0.25, steps=1, warmup=3)
     line = bench.run_reference(args)
     assert line["config"]["workload"] == "long_context_pool_bf16" and line["config"]["density"] == 0.25
+
+
+def test_attended_count_matches_the_oracle_sets():
+    """The bench's closed-form key counts (its FLOP and byte figures) equal the
+    sizes of the oracle's attended sets ([ring] 2.2, [sink] cache-set
+    equation, [pool] mapped and valid blocks)."""
+    import oracle
+    for name in ("ring_bf16", "sink_window_bf16", "paged_shared_prefix_bf16", "long_context_pool_bf16"):
+        for small in (True, False):
+            wl = bench.kvc_synth.make_workload(name, small=small)
+            for b in range(min(wl.batch, 3)):
+                tb = int(wl.positions[b])
+                for t in (tb, tb - 5, 0, 3, tb - 200):
+                    if t < 0:
+                        continue
+                    if wl.layout == "window":
+                        ref = len(oracle.window_attended(t, wl.sinks, wl.window))
+                    else:
+                        ref = len(oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size))
+                    assert bench.attended_count(wl, b, t) == ref, (name, b, t)
