@@ -372,10 +372,10 @@ class ClockSampler:
 # capture per workload, and the digest of the kernel's sources
 # (KERNEL_TRAFFIC_FILES) they were taken on: reported only while those
 # sources are unchanged.
-KERNEL_TRAFFIC = {"ring_bf16": 137971712, "sink_window_bf16": 545077248,
-                  "paged_shared_prefix_bf16": 894324480, "long_context_pool_bf16": 153829120,
-                  "ring_int8": 69380806}
-KERNEL_TRAFFIC_SOURCES = "a96d8dd46101b49c8cb03c78c55fef8c1d8857ccaebfd4669a5519fa3fac06bc"
+KERNEL_TRAFFIC = {"ring_bf16": 137521664, "sink_window_bf16": 543171072,
+                  "paged_shared_prefix_bf16": 900302336, "long_context_pool_bf16": 153094144,
+                  "ring_int8": 69873408}
+KERNEL_TRAFFIC_SOURCES = "69ad45ef89365701209951fcb7e826d478c32492662b3cebbb062dced218d4b0"
 
 
 # the sources decode_mma_kernel and its launch are built from

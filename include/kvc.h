@@ -235,11 +235,17 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
  *              followed by the chunk's staged rows.
  * READ_INCACHE: each token's window keys at distance t - p and its sinks at
  * min(t, C - 1) - p, as the decode step at t rotates them.
- * bf16 caches, head_dim 64 or 128 (KVC_ERR_UNSUPPORTED otherwise).  Calls on
- * one workspace must not overlap on the GPU.  At head_dim 128 the attention
- * runs on the tcgen05 tensor cores: each of its CTAs (at most two per SM)
- * holds 256 tensor-memory columns while it runs, so a kernel of another
- * library that holds an SM's tensor memory at the same time delays it. */
+ * bf16 caches, head_dim 64, 128 or 256.  KVC_ERR_UNSUPPORTED: another cache
+ * dtype; at head_dim 256, a ring or sink+ring chunk longer than the window,
+ * paged blocks whose size is not a multiple of 8 dividing 64, or a GQA group
+ * that does not divide 128.  Calls on one workspace must not overlap on the
+ * GPU.  The attention runs on the tcgen05 tensor cores: a CTA of the
+ * warp-specialised kernel (one per SM) holds all 512 tensor-memory columns
+ * of its SM while it runs (the kernel for chunks longer than the window: 256
+ * columns, two CTAs per SM), so a kernel of another library that holds an
+ * SM's tensor memory at the same time delays it.  A wait that does not end
+ * within its bound sets KVC_DEV_TIMEOUT in the device error word and the
+ * CTA returns, leaving that chunk's output undefined. */
 KVC_API size_t kvc_prefill_workspace_bytes(const kvc_desc* d, int32_t T);
 KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const void* q,
                         const void* k_new, const void* v_new, int32_t T, const int32_t* pos0,
