@@ -188,7 +188,10 @@ KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer,
  * results (m, l, o) in the workspace.  fp32 caches combine the partials in
  * the same kernel (the last CTA of a sequence); bf16 and INT8 caches launch
  * a separate combine kernel right behind the attention kernel (programmatic
- * dependent launch), and PAGED caches run a work-plan kernel before it.
+ * dependent launch).  PAGED batches run a planning kernel before the
+ * attention kernel (per sequence: attended rows, attended-block directory,
+ * the readers of each block); a single paged sequence on a bf16 or INT8
+ * cache is planned inside the attention kernel.
  *   q       [batch, q_heads, head_dim], pre-RoPE.
  *   pos     [batch] int32: position t of the token being decoded (already
  *           appended, so t attends to itself; [ring] 4.3).

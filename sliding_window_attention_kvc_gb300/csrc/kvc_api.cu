@@ -109,7 +109,7 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
     off = align_up(off + (size_t)w.items * d->q_heads * 8, 256);
     w.part_o = off;
     off = align_up(off + (size_t)w.items * d->q_heads * d->head_dim * 4, 256);
-    w.plan_seq = w.plan_acc = w.plan_items = w.plan_info = w.plan_total = w.plan_cta = w.blocks = off;
+    w.plan_seq = w.plan_acc = w.plan_items = w.plan_info = w.plan_total = w.plan_cta = w.plan_dir = w.plan_refs = w.blocks = off;
     if (d->layout == KVC_LAYOUT_PAGED) {
         w.plan_seq = off;
         off = align_up(off + (size_t)d->batch * 8, 256);
@@ -121,6 +121,10 @@ WorkspaceLayout ws_layout(const kvc_desc* d, const Geo& g) {
         off = align_up(off + (size_t)w.items * 16, 256);
         w.plan_cta = off;
         off = align_up(off + (size_t)w.shares * 8, 256);
+        w.plan_dir = off;
+        off = align_up(off + (size_t)d->batch * ((d->max_blocks_per_seq + 31) / 32) * 8, 256);
+        w.plan_refs = off;
+        off = align_up(off + (size_t)d->num_blocks * 4, 256);
         w.blocks = off;
         off = align_up(off + align_up((size_t)d->batch * 5 * 4, 16) + (size_t)d->batch * 16 + 16 +
                            (size_t)d->num_blocks * 4, 256);
@@ -473,7 +477,20 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
             pp.sc_kv_off = p.sc_kv_off;
             if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
         }
-        if (launch_plan(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
+        if (d->dtype != KVC_F32) {
+            // the tensor-core kernel cuts its own shares from the rows and the
+            // directory of each sequence
+            pp.dir = reinterpret_cast<int2*>(ws + w.plan_dir);
+            pp.dir_groups = (d->max_blocks_per_seq + 31) / 32;
+            pp.refs = reinterpret_cast<uint32_t*>(ws + w.plan_refs);
+            if (launch_plan_rows(pp, s) != cudaSuccess) return KVC_ERR_CUDA;
+            p.seq_rows = pp.seq_rows;
+            p.dir = pp.dir;
+            p.dir_groups = pp.dir_groups;
+            p.refs = pp.refs;
+        } else if (launch_plan(pp, s) != cudaSuccess) {
+            return KVC_ERR_CUDA;
+        }
         p.items = pp.items;
         p.item_info = pp.item_info;
         p.seq_items = pp.seq_items;

@@ -82,6 +82,27 @@ __device__ __forceinline__ int paged_block_rows(const int32_t* table_row, const 
     return lb == last ? (t - lb * bs + 1) : bs;
 }
 
+// The same, with the block's reader count of this step (refs, null: 1)
+// loaded beside its valid word.
+__device__ __forceinline__ int paged_block_rows_refs(const int32_t* table_row, const uint32_t* valid,
+                                                     const uint32_t* refs, uint32_t* err, int lb, int t, int bs,
+                                                     int num_blocks, int* phys_out, uint32_t* refs_out) {
+    const int last = t / bs;
+    *refs_out = 1u;
+    if (t < 0 || lb > last) return 0;
+    const int phys = table_row[lb];
+    *phys_out = phys;
+    if (phys < 0) return 0;
+    if (phys >= num_blocks) {
+        set_error(err, 0x1u /* KVC_DEV_BAD_BLOCK */);
+        return 0;
+    }
+    const uint32_t w = valid ? valid[phys >> 5] : 0xffffffffu;
+    *refs_out = refs ? __ldcg(refs + phys) : 1u;
+    if (!((w >> (phys & 31)) & 1u)) return 0;
+    return lb == last ? (t - lb * bs + 1) : bs;
+}
+
 // n / d for n >= 0, d > 0: a 32-bit division when both fit.
 __device__ __forceinline__ long long div_nonneg(long long n, long long d) {
     if (n >= 0 && n < 0x100000000LL && d > 0 && d < 0x100000000LL) return (long long)((unsigned)n / (unsigned)d);
@@ -92,6 +113,20 @@ __device__ __forceinline__ long long div_nonneg(long long n, long long d) {
 // `shares` contiguous ranges [floor(x total / shares), floor((x + 1) total / shares)).
 __device__ __forceinline__ int streamk_share_of(long long u, long long total, int shares) {
     return (int)div_nonneg((u + 1) * shares - 1, total);
+}
+
+// Paged stream-K plan: G shares of the R attended rows of the batch laid end to
+// end (no more shares than rows, at least one).  Sequence b, with O_b rows
+// before it and R_b rows, meets shares first .. last; a sequence with no
+// attended row gets the share that holds row O_b (row R - 1 past the end) for
+// its empty segment.  Its segment with share x writes partial slot x + b.
+__device__ __forceinline__ int paged_share_count(long long R, int shares) {
+    return (int)(R < shares ? (R > 0 ? R : 1) : shares);
+}
+__device__ __forceinline__ int2 paged_seq_shares(long long Ob, long long Rb, long long R, int G) {
+    if (Rb > 0) return make_int2(streamk_share_of(Ob, R, G), streamk_share_of(Ob + Rb - 1, R, G));
+    const int x = R > 0 ? streamk_share_of(Ob < R ? Ob : R - 1, R, G) : 0;
+    return make_int2(x, x);
 }
 
 __device__ __forceinline__ int clamp_paged_t(int t, int maxb, int bs) {

@@ -329,6 +329,32 @@ __device__ __forceinline__ void window_partition(const DecodeParams& p, int b, l
     *Sb = sb;
 }
 
+// The same for a paged batch: its attended rows (plan_rows_kernel's seq_rows),
+// and those of the sequences before b.
+__device__ __forceinline__ void paged_partition(const DecodeParams& p, int b, long long* total, long long* Ob,
+                                                long long* Rb) {
+    const int lane = threadIdx.x & 31;
+    long long tot = 0, before = 0, rb = 0;
+    for (int base = 0; base < p.B; base += 32) {
+        const int bb = base + lane;
+        long long st = bb < p.B ? (long long)__ldcg(p.seq_rows + bb) : 0;
+        long long pre = bb < b ? st : 0;
+        long long me = bb == b ? st : 0;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            st += __shfl_xor_sync(0xffffffffu, st, off);
+            pre += __shfl_xor_sync(0xffffffffu, pre, off);
+            me += __shfl_xor_sync(0xffffffffu, me, off);
+        }
+        tot += st;
+        before += pre;
+        rb += me;
+    }
+    *total = tot;
+    *Ob = before;
+    *Rb = rb;
+}
+
 // ---------------------------------------------------------------------------
 // Combine kernel for the stream-K decode: one CTA per (sequence, kv head,
 // q-head group, 32-column chunk).  out = sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)
@@ -361,13 +387,29 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
 
     // which partial slots belong to sequence b (inputs that the decode kernel does not write)
     int first = 0, nparts = 0;
-    if constexpr (PAGED) {
-        pdl_wait();                                 // the plan is written by an earlier kernel
+    __shared__ int s_fn[2];
+    if (PAGED && !p.seq_rows) {
+        pdl_wait();                                 // one self-planned sequence: the decode kernel's count
         const int2 si = p.seq_items[b];
         first = si.x;
         nparts = si.y;
+    } else if (PAGED) {
+        // a batch: the shares that meet b, from the plan's rows (written before
+        // the decode kernel started, so before this grid launched)
+        if (tid < 32) {
+            long long R, Ob, Rb;
+            paged_partition(p, b, &R, &Ob, &Rb);
+            const int2 fl = paged_seq_shares(Ob, Rb, R, paged_share_count(R, p.nsplit));
+            if (tid == 0) {
+                s_fn[0] = fl.x + b;
+                s_fn[1] = fl.y - fl.x + 1;
+            }
+        }
+        __syncthreads();
+        first = s_fn[0];
+        nparts = s_fn[1];
+        pdl_wait();                                 // the decode kernel's partials
     } else {
-        __shared__ int s_fn[2];
         if (tid < 32) {
             long long total, Ob, Sb;
             window_partition(p, b, &total, &Ob, &Sb);
@@ -384,8 +426,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_streamk_kernel(const 
         nparts = s_fn[1];
         pdl_wait();                                 // the decode kernel's partials
     }
-    // the decode grid is done: ready its share counter for the next call
+    // the decode grid is done: ready its share counter, and a paged batch's
+    // block reader counts, for the next call
     if (blockIdx.x == 0 && blockIdx.z == 0 && tid == 0) p.counters[blockIdx.y] = 0u;
+    if (PAGED && p.refs) {
+        const long long ncta = (long long)gridDim.x * gridDim.y * gridDim.z;
+        const long long cta = ((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        for (long long i = cta * kCombineThreads + tid; i < p.num_blocks; i += ncta * kCombineThreads) p.refs[i] = 0u;
+    }
     if (first < 0 || nparts < 1 || first + nparts > p.max_items) {
         if (tid == 0) index_fault(p.err, 20, first);
         return;
@@ -586,8 +634,8 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
 
     if (warp == kConsumerWarps) {
         // =================== copy-issuing warp ==============================
-        // K/V rows read once per call stream through L2 as evict-first, except
-        // paged batches, whose shared blocks are read by several sequences
+        // K/V rows read once per call stream through L2 as evict-first; in a
+        // paged batch, the blocks that one sequence alone attends (refs)
         const bool evict_first = !(PAGED && p.B > 1);
         const uint64_t pol = l2_policy_evict_first();
         int it = 0, fill = 0, run_off = 0, claims = 0;
@@ -677,7 +725,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
         // many sub-tiles.  ip0: in-cache position of the first row (READ_INCACHE);
         // exact: its angles computed afresh rather than advanced by 16 from the
         // previous sub-tile's; newrow: run row of the token being appended or -1.
-        auto emit_run = [&](long long urow, int n, int ip0, int newrow, bool exact) {
+        auto emit_run = [&](long long urow, int n, int ip0, int newrow, bool exact, bool ef) {
             const int s = it % NST;
             const int nsr = (n + 15) >> 4;
             const int R = nsr * 16;
@@ -724,14 +772,14 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 }
                 mbar_expect_tx(&full[s], (uint32_t)(S::kBoxes * 2 * R * 128));
                 if (p.tma_whole) {
-                    if (evict_first)
+                    if (ef)
                         tma_load_5d_hint(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s], pol);
                     else
                         tma_load_5d(dst, map, 0, (int)urow, 0, p.layer, 0, &full[s]);
                 } else {
 #pragma unroll
                     for (int bx = 0; bx < S::kBoxes; ++bx) {
-                        if (evict_first)
+                        if (ef)
                             tma_load_4d_hint(dst + bx * 2 * R * 128, map, bx * S::kBoxCols, (int)urow, 0, p.layer,
                                              &full[s], pol);
                         else
@@ -747,7 +795,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
         // (1..16) from K-half row urow, sub-tile `rank` after the stage's
         // current fill (lanes of one call take distinct ranks below the room).
         constexpr int kSubCopy = S::kBoxes * 2 * 16 * 128;
-        auto emit_sub_lane = [&](long long urow, int n, int rank, int newrow) {
+        auto emit_sub_lane = [&](long long urow, int n, int rank, int newrow, bool ef) {
             const int s = it % NST;
             const int f = fill + rank;
             meta[s].nrows[f] = n;
@@ -765,12 +813,20 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             unsigned char* dst = stage_base + (size_t)s * S::kStageBytes + run_off + rank * kSubCopy;
             mbar_expect_tx(&full[s], (uint32_t)kSubCopy);
             if (p.tma_whole) {
-                tma_load_5d(dst, &maps.run[0], 0, (int)urow, 0, p.layer, 0, &full[s]);
+                if (ef)
+                    tma_load_5d_hint(dst, &maps.run[0], 0, (int)urow, 0, p.layer, 0, &full[s], pol);
+                else
+                    tma_load_5d(dst, &maps.run[0], 0, (int)urow, 0, p.layer, 0, &full[s]);
             } else {
 #pragma unroll
-                for (int bx = 0; bx < S::kBoxes; ++bx)
-                    tma_load_4d(dst + bx * 2 * 16 * 128, &maps.run[0], bx * S::kBoxCols, (int)urow, 0, p.layer,
-                                &full[s]);
+                for (int bx = 0; bx < S::kBoxes; ++bx) {
+                    if (ef)
+                        tma_load_4d_hint(dst + bx * 2 * 16 * 128, &maps.run[0], bx * S::kBoxCols, (int)urow, 0,
+                                         p.layer, &full[s], pol);
+                    else
+                        tma_load_4d(dst + bx * 2 * 16 * 128, &maps.run[0], bx * S::kBoxCols, (int)urow, 0, p.layer,
+                                    &full[s]);
+                }
             }
         };
 
@@ -878,7 +934,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                             prev_n = n;
                         }
                         const int newrow = (p.k_new && t_b >= 0 && h_slot >= r && h_slot < r + n) ? h_slot - r : -1;
-                        emit_run(base_row + r, n, ip0, newrow, exact);
+                        emit_run(base_row + r, n, ip0, newrow, exact, evict_first);
                         r += n;
                     }
                     if (ok) end_segment();
@@ -888,7 +944,21 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             }
         } else {
             const bool self = p.self_plan != 0;
-            const int G = self ? s_plan.G : __ldcg(&p.n_items[1]);    // the plan's share count
+            // batch: the shares are cut here from each sequence's attended rows
+            // (seq_rows, plan_rows_kernel) laid end to end, as the plan defines
+            // them; rows of the first 64 sequences stay in registers
+            long long Rt = 0;
+            int rows0 = 0, rows1 = 0;
+            if (!self) {
+                rows0 = lane < p.B ? __ldcg(p.seq_rows + lane) : 0;
+                rows1 = 32 + lane < p.B ? __ldcg(p.seq_rows + 32 + lane) : 0;
+                long long r = (long long)rows0 + rows1;
+                for (int base = 64; base < p.B; base += 32) r += base + lane < p.B ? __ldcg(p.seq_rows + base + lane) : 0;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+                Rt = r;
+            }
+            const int G = self ? s_plan.G : paged_share_count(Rt, p.nsplit);
             // self-planned step: the new token's K-half row, when this CTA's
             // share holds it (it is the sequence's last attended row)
             int new_lb = -1, new_r = 0, new_row = -1;
@@ -908,32 +978,12 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             auto newrow_of = [&](int lbk, int row0, int n) -> int {
                 return (lbk == new_lb && new_r >= row0 && new_r < row0 + n) ? new_r - row0 : -1;
             };
-            for (int xs = claim(G); xs < G && ok; xs = self ? G : claim(G)) {
-            // one sequence: share x holds exactly its item x
-            const int2 my_items = (self || p.B == 1) ? make_int2(xs, 1) : __ldcg(&p.cta_items[xs]);
-            for (int k = 0; k < my_items.y && ok; ++k) {
-                const int item = my_items.x + k;
-                if (item < 0 || item >= p.max_items) {
-                    if (lane == 0) index_fault(p.err, 1, item);
-                    break;
-                }
-                const int4 itv = self ? make_int4(0, s_plan.lb, s_plan.row, s_plan.rows) : p.items[item];
+            // One segment: sequence itv.x from logical block itv.y, row itv.z, for
+            // itv.w attended rows; inf = (t, first partial slot and slot count of
+            // the sequence, physical block of itv.y or -2 when not known), `item`
+            // its partial slot.
+            auto walk_item = [&](const int4 itv, const int4 inf, int item) {
                 const int b = itv.x;
-                if (b < 0 || b >= p.B) {
-                    if (lane == 0) index_fault(p.err, 2, b);
-                    break;
-                }
-                // (t, first slot, slot count, first physical block): read with the
-                // item for one sequence; a batch reads them per sequence
-                int4 inf;
-                if (self) {
-                    inf = make_int4(s_plan.traw, 0, G, s_plan.phys);
-                } else if (p.B == 1) {
-                    inf = __ldcg(&p.item_info[item]);
-                } else {
-                    const int2 si = p.seq_items[b];
-                    inf = make_int4(p.pos[b], si.x, si.y, -1);
-                }
                 MmaSegment hdr;
                 hdr.b = b;
                 hdr.t = inf.x;
@@ -941,21 +991,21 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 hdr.first_slot = inf.y;
                 hdr.nparts = inf.z;
                 hdr.new_row = new_row;
-                if (!(ok = begin_segment(hdr))) break;
+                if (!(ok = begin_segment(hdr))) return;
                 const int tt = clamp_paged_t(hdr.t, p.maxb, p.bs);
                 const int32_t* trow = p.table + (long long)b * p.maxb;
                 int lb = itv.y;
                 int rem = itv.w;
                 const int last_lb = tt < 0 ? -1 : tt / p.bs;
-                // one sequence: the item's first block is attended by construction
-                // and its physical block comes with the item, so its copies need no
-                // table lookup
-                if (p.B == 1 && rem > 0 && lb <= last_lb && ok) {
+                // self-planned sequence: the item's first block is attended by
+                // construction and its physical block comes with the item, so its
+                // copies need no table lookup
+                if (inf.w != -2 && rem > 0 && lb <= last_lb && ok) {
                     const int phys = inf.w;
                     if (phys < 0 || phys >= p.num_blocks) {
                         if (lane == 0) index_fault(p.err, 13, phys);
                         ok = false;
-                        break;
+                        return;
                     }
                     const int brows = lb == last_lb ? tt - lb * p.bs + 1 : p.bs;
                     const long long blk = ((long long)phys * p.Hkv + kvh) * p.bs;   // row in the K half
@@ -968,7 +1018,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                             break;
                         }
                         const int n = min(take, 16 * room);
-                        emit_run(blk + row, n, 0, newrow_of(lb, row, n), true);
+                        emit_run(blk + row, n, 0, newrow_of(lb, row, n), true, evict_first);
                         take -= n;
                         rem -= n;
                         row += n;
@@ -980,8 +1030,11 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 while (p.bs <= 16 && rem > 0 && lb <= last_lb && ok) {
                     const int my_lb = lb + lane;
                     int my_phys = -1, my_rows = 0;
+                    uint32_t my_refs = 1u;
                     if (my_lb <= last_lb)
-                        my_rows = paged_block_rows(trow, p.valid, p.err, my_lb, tt, p.bs, p.num_blocks, &my_phys);
+                        my_rows = paged_block_rows_refs(trow, p.valid, p.refs, p.err, my_lb, tt, p.bs, p.num_blocks,
+                                                        &my_phys, &my_refs);
+                    const bool my_ef = p.refs ? my_refs <= 1u : evict_first;
                     const int row0 = (my_lb == itv.y) ? itv.z : 0;
                     const int avail = my_rows > row0 ? my_rows - row0 : 0;
                     int incl = avail;
@@ -1003,7 +1056,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                         const int rank = __popc(pending & ((1u << lane) - 1u));
                         const bool mine = ((pending >> lane) & 1u) && rank < room;
                         const unsigned emitted = __ballot_sync(0xffffffffu, mine);
-                        if (mine) emit_sub_lane(urow, take, rank, newrow_of(my_lb, row0, take));
+                        if (mine) emit_sub_lane(urow, take, rank, newrow_of(my_lb, row0, take), my_ef);
                         __syncwarp();
                         fill += __popc(emitted);
                         run_off += __popc(emitted) * kSubCopy;
@@ -1014,14 +1067,18 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 while (rem > 0 && lb <= last_lb && ok) {
                     const int my_lb = lb + lane;
                     int my_phys = -1, my_rows = 0;
+                    uint32_t my_refs = 1u;
                     if (my_lb <= last_lb)
-                        my_rows = paged_block_rows(trow, p.valid, p.err, my_lb, tt, p.bs, p.num_blocks, &my_phys);
+                        my_rows = paged_block_rows_refs(trow, p.valid, p.refs, p.err, my_lb, tt, p.bs, p.num_blocks,
+                                                        &my_phys, &my_refs);
+                    const bool my_ef = p.refs ? my_refs <= 1u : evict_first;
                     unsigned mask = __ballot_sync(0xffffffffu, my_rows > 0);
                     while (mask && rem > 0 && ok) {
                         const int src = __ffs(mask) - 1;
                         mask &= mask - 1;
                         const int phys = __shfl_sync(0xffffffffu, my_phys, src);
                         const int brows = __shfl_sync(0xffffffffu, my_rows, src);
+                        const bool bef = __shfl_sync(0xffffffffu, (int)my_ef, src) != 0;
                         int row = (lb + src == itv.y) ? itv.z : 0;
                         int take = min(brows - row, rem);
                         const long long blk = ((long long)phys * p.Hkv + kvh) * p.bs;   // row in the K half
@@ -1032,7 +1089,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                                 break;
                             }
                             const int n = min(take, 16 * room);
-                            emit_run(blk + row, n, 0, newrow_of(lb + src, row, n), true);
+                            emit_run(blk + row, n, 0, newrow_of(lb + src, row, n), true, bef);
                             take -= n;
                             rem -= n;
                             row += n;
@@ -1041,7 +1098,94 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                     lb += 32;
                 }
                 if (ok) end_segment();
-            }
+            };
+            // The first attended block of row s0 of sequence b (position tb):
+            // the block of rank s0 / bs, by the directory: the last 32-block
+            // group with fewer attended blocks before it than that rank holds it.
+            auto first_block = [&](int b, int tb, long long s0, int* lb_out, int* row_out) -> bool {
+                const int kb = (int)(s0 / p.bs);
+                const int tt = clamp_paged_t(tb, p.maxb, p.bs);
+                const int ng = tt < 0 ? 0 : (tt / p.bs) / 32 + 1;
+                const int2* drow = p.dir + (long long)b * p.dir_groups;
+                int gsel = -1;
+                int2 esel = make_int2(0, 0);
+                for (int g0 = 0; g0 < ng; g0 += 32) {
+                    const int g = g0 + lane;
+                    const int2 e = g < ng ? __ldcg(drow + g) : make_int2(0, 0);
+                    const unsigned le = __ballot_sync(0xffffffffu, g < ng && e.y <= kb);
+                    if (le) {
+                        const int src = 31 - __clz(le);
+                        gsel = g0 + src;
+                        esel.x = __shfl_sync(0xffffffffu, e.x, src);
+                        esel.y = __shfl_sync(0xffffffffu, e.y, src);
+                    }
+                    if (le != 0xffffffffu) break;
+                }
+                uint32_t mm = (uint32_t)esel.x;
+                const int k = kb - esel.y;
+                if (gsel < 0 || k < 0 || k >= __popc(mm)) {
+                    if (lane == 0) index_fault(p.err, 14, kb);
+                    return false;
+                }
+#pragma unroll 1
+                for (int q = 0; q < k; ++q) mm &= mm - 1u;
+                *lb_out = gsel * 32 + (__ffs(mm) - 1);
+                *row_out = (int)(s0 - (long long)kb * p.bs);
+                return true;
+            };
+            for (int xs = claim(G); xs < G && ok; xs = self ? G : claim(G)) {
+                if (self) {
+                    // one sequence: share x holds exactly its item x
+                    walk_item(make_int4(0, s_plan.lb, s_plan.row, s_plan.rows), make_int4(s_plan.traw, 0, G, s_plan.phys),
+                              xs);
+                    continue;
+                }
+                // the sequences that meet share xs, in order (b meets shares
+                // paged_seq_shares(...).x .. .y; its segment is slot xs + b): one
+                // lane per sequence tests its own, a ballot gathers them
+                const long long lo = div_nonneg((long long)xs * Rt, G), hi = div_nonneg((long long)(xs + 1) * Rt, G);
+                long long run = 0;
+                for (int base = 0; base < p.B && ok; base += 32) {
+                    // past share xs: only the empty sequences after the last row
+                    // belong to the last share
+                    if (run >= hi && hi < Rt) break;
+                    const int bb = base + lane;
+                    const int r = base == 0 ? rows0 : base == 32 ? rows1
+                                : (bb < p.B ? __ldcg(p.seq_rows + bb) : 0);
+                    long long incl = r;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const long long u = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += u;
+                    }
+                    const long long Ob = run + incl - r;
+                    bool meet;
+                    if (r > 0) {
+                        meet = Ob < hi && Ob + r > lo;
+                    } else {
+                        const long long u = Ob < Rt ? Ob : Rt - 1;     // its empty segment's row
+                        meet = Rt > 0 ? (u >= lo && u < hi) : xs == 0;
+                    }
+                    unsigned mset = __ballot_sync(0xffffffffu, bb < p.B && meet);
+                    while (mset && ok) {
+                        const int j = __ffs(mset) - 1;
+                        mset &= mset - 1u;
+                        const int b = base + j;
+                        const long long Rb = __shfl_sync(0xffffffffu, r, j);
+                        const long long Obj = __shfl_sync(0xffffffffu, Ob, j);
+                        const int2 fl = paged_seq_shares(Obj, Rb, Rt, G);
+                        const int tb = p.pos[b];
+                        int lb = 0, row = 0, rows = 0;
+                        if (Rb > 0) {
+                            const long long s0 = (lo > Obj ? lo : Obj) - Obj;
+                            const long long s1 = (hi < Obj + Rb ? hi : Obj + Rb) - Obj;
+                            rows = (int)(s1 - s0);
+                            if (!first_block(b, tb, s0, &lb, &row)) rows = 0;
+                        }
+                        walk_item(make_int4(b, lb, row, rows), make_int4(tb, fl.x + b, fl.y - fl.x + 1, -2), xs + b);
+                    }
+                    run += __shfl_sync(0xffffffffu, incl, 31);
+                }
             }
         }
         if (ok) {

@@ -155,8 +155,10 @@ cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream)
 // [floor(x R / G), floor((x + 1) R / G)); the intersection of share x with
 // sequence b is work item x + b (items of one sequence, and of one share, get
 // consecutive indices; a share boundary that falls exactly on a sequence
-// boundary leaves one index unused, marked -1).  Two kernels, one CTA per
-// sequence each, chained by programmatic dependent launch:
+// boundary leaves one index unused, marked -1).  The tensor-core decode of a
+// batch cuts these shares itself from plan_rows_kernel's per-sequence rows
+// (below); the fp32 decode, one CTA per item, takes them from two kernels,
+// one CTA per sequence each, chained by programmatic dependent launch:
 //   plan_count_kernel  R_b = attended rows of sequence b (blocks lb <= t_b / bs
 //                      that are mapped and valid; [pool] "kernel forgets
 //                      absent blocks").  With a new token to append
@@ -281,14 +283,8 @@ __device__ __forceinline__ void plan_append(const PlanParams& p, int b, int traw
 
 // First item and item count of a sequence with O_b rows before it and R_b rows.
 __device__ __forceinline__ int2 plan_seq_items(int b, long long Ob, long long Rb, long long R, int G) {
-    int fx, lx;
-    if (Rb > 0) {
-        fx = streamk_share_of(Ob, R, G);
-        lx = streamk_share_of(Ob + Rb - 1, R, G);
-    } else {
-        fx = lx = R > 0 ? streamk_share_of(Ob < R ? Ob : R - 1, R, G) : 0;
-    }
-    return make_int2(fx + b, lx - fx + 1);
+    const int2 fl = paged_seq_shares(Ob, Rb, R, G);
+    return make_int2(fl.x + b, fl.y - fl.x + 1);
 }
 
 // The items of sequence b (O_b, R_b; shares of R rows into G) whose first row
@@ -362,9 +358,7 @@ __device__ __forceinline__ void plan_write_header(const PlanParams& p, long long
 }
 
 // Shares of R rows: no more than the CTAs, and no empty share.
-__device__ __forceinline__ int plan_shares(long long R, int ctas) {
-    return (int)(R < ctas ? (R > 0 ? R : 1) : ctas);
-}
+__device__ __forceinline__ int plan_shares(long long R, int ctas) { return paged_share_count(R, ctas); }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_count_kernel(const __grid_constant__ PlanParams p) {
     __shared__ int s_wi[32];
@@ -521,6 +515,177 @@ __global__ void __launch_bounds__(kPlanThreads) plan_items_kernel(const __grid_c
         plan_write_items(p, b, traw, Ob, Rb, R, G, si, lb0, v, ph, carry + incl - tsum, carry + incl);
         carry += chunk;
     }
+}
+
+// Rows and attended-block directory of each sequence, for the tensor-core
+// decode, whose CTAs cut their own shares from them (one CTA per sequence):
+//   seq_rows[b]      R_b, as plan_count_kernel counts it;
+//   dir[b][g]        (bits i: logical block 32 g + i is attended, attended
+//                    blocks of b before block 32 g), for g <= t_b / bs / 32.
+//   refs[q]          += 1 for each sequence that attends physical block q:
+//                    blocks read by one sequence stream through L2 as
+//                    evict-first, shared ones (prefixes) stay for their
+//                    other readers.
+// Every attended block but a sequence's last holds bs rows, so its row r lies
+// in the attended block of rank r / bs, which the directory finds with one
+// search over g and one bit select.  With a new token to append
+// (kvc_decode_step) the CTA writes it first, as plan_count_kernel does.
+__global__ void __launch_bounds__(kPlanThreads) plan_rows_kernel(const __grid_constant__ PlanParams p) {
+    constexpr int NW = kPlanThreads / 32;
+    constexpr int kGroups = NW * kPlanPerThread;      // 32-block groups of one pass
+    constexpr int kChunk = kPlanThreads * kPlanPerThread;
+    constexpr int kAppPairs = 4;                      // bf16 append: (kv head, pair) units per thread
+    __shared__ int s_grp[kGroups];
+    __shared__ int s_wi[32];
+    __shared__ int s_pass;
+    __shared__ int s_tok_phys;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    plan_pdl_wait();            // positions, table, valid bits may come from the previous kernel
+    // the decode kernel may launch now: it waits for this grid to complete
+    // before it reads anything
+    plan_pdl_launch();
+    const int32_t* trow = p.table + (long long)b * p.maxb;
+    // Issued together, before any is used: the position, the table entries of
+    // the first pass (all of them, not only those the position reaches) and,
+    // on a bf16 cache, the step's new token.
+    const int traw = p.pos[b];
+    int ph0[kPlanPerThread];
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) {
+        const int lb = j * kPlanThreads + tid;
+        ph0[j] = lb < p.maxb ? __ldg(trow + lb) : -1;
+    }
+    const int half = p.D / 2;
+    const bool app16 = p.k_new && p.elt == 2 && p.Hkv * half <= kAppPairs * kPlanThreads;
+    __nv_bfloat162 kx[kAppPairs], vx[kAppPairs];      // (x_i, x_{i + D/2}) of unit tid + u kPlanThreads
+    if (app16) {
+        const __nv_bfloat16* ks = static_cast<const __nv_bfloat16*>(p.k_new) + (long long)b * p.Hkv * p.D;
+        const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(p.v_new) + (long long)b * p.Hkv * p.D;
+#pragma unroll
+        for (int u = 0; u < kAppPairs; ++u) {
+            const int idx = tid + u * kPlanThreads;
+            if (idx < p.Hkv * half) {
+                const int off = (idx / half) * p.D + idx % half;
+                kx[u] = __halves2bfloat162(ks[off], ks[off + half]);
+                vx[u] = __halves2bfloat162(vs[off], vs[off + half]);
+            }
+        }
+    }
+    if (tid == 0) s_tok_phys = -2;
+    __syncthreads();
+    const int t = clamp_paged_t(traw, p.maxb, p.bs);
+    const int nb = t < 0 ? 0 : t / p.bs + 1;
+    const int tok_lb = traw >= 0 ? traw / p.bs : -1;
+    int2* drow = p.dir + (long long)b * p.dir_groups;
+    int sum = 0, before = 0;
+    for (int base = 0; base < nb; base += kChunk) {
+        // thread tid takes blocks base + j kPlanThreads + tid: warp w's lanes
+        // cover the 32 blocks of group (base + j kPlanThreads) / 32 + w
+        int lbs[kPlanPerThread], v[kPlanPerThread], ph[kPlanPerThread];
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) lbs[j] = base + j * kPlanThreads + tid;
+        if (base == 0) {
+#pragma unroll
+            for (int j = 0; j < kPlanPerThread; ++j) ph[j] = lbs[j] < nb ? ph0[j] : -1;
+            plan_rows_of(p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, ph, v);
+        } else {
+            plan_block_rows(trow, p.valid, p.err, lbs, t, nb, p.bs, p.num_blocks, v, ph);
+        }
+        uint32_t m[kPlanPerThread];
+#pragma unroll
+        for (int j = 0; j < kPlanPerThread; ++j) {
+            if (lbs[j] == tok_lb) s_tok_phys = ph[j];        // the new token's block
+            if (v[j] > 0) atomicAdd(p.refs + ph[j], 1u);
+            sum += v[j];
+            m[j] = __ballot_sync(0xffffffffu, v[j] > 0);
+            if (lane == 0) s_grp[j * NW + warp] = __popc(m[j]);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive prefix of the pass's groups in block order (4 per lane)
+            int c[kGroups / 32], tot = 0;
+#pragma unroll
+            for (int k = 0; k < kGroups / 32; ++k) {
+                c[k] = s_grp[lane * (kGroups / 32) + k];
+                tot += c[k];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            int ex = before + incl - tot;
+#pragma unroll
+            for (int k = 0; k < kGroups / 32; ++k) {
+                s_grp[lane * (kGroups / 32) + k] = ex;
+                ex += c[k];
+            }
+            if (lane == 31) s_pass = incl;
+        }
+        __syncthreads();
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < kPlanPerThread; ++j) {
+                const int lb0 = base + j * kPlanThreads + warp * 32;
+                if (lb0 < nb) drow[lb0 >> 5] = make_int2((int)m[j], s_grp[j * NW + warp]);
+            }
+        }
+        before += s_pass;
+        __syncthreads();
+    }
+    const int tok_phys = s_tok_phys;
+    if (!app16) {
+        plan_append(p, b, traw, tok_phys);
+    } else if (traw >= 0) {
+        // the new token's rows from the registers loaded above (as plan_append)
+        const int phys = tok_lb < p.maxb ? (tok_phys >= -1 ? tok_phys : __ldg(trow + tok_lb)) : -1;
+        if (tok_lb >= p.maxb || phys < 0 || phys >= p.num_blocks) {
+            if (tid == 0) set_error(p.err, tok_lb >= p.maxb ? 0x4u : (phys < 0 ? 0x2u : 0x1u));
+        } else {
+            __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(p.cache) + p.layer_off +
+                                ((long long)phys * p.Hkv * p.bs + traw % p.bs) * p.D;
+            const long long hs = (long long)p.bs * p.D;
+#pragma unroll
+            for (int u = 0; u < kAppPairs; ++u) {
+                const int idx = tid + u * kPlanThreads;
+                if (idx < p.Hkv * half) {
+                    const int h = idx / half, i = idx % half;
+                    __nv_bfloat16* kd = kc + h * hs;
+                    __nv_bfloat16* vd = kd + p.kv_off;
+                    __nv_bfloat16 k1 = kx[u].x, k2 = kx[u].y;
+                    if (p.rope == kRopeBaked) {
+                        float c, sn;
+                        rope_cos_sin((long long)traw, p.theta[i], &c, &sn);
+                        const float x1 = __bfloat162float(k1), x2 = __bfloat162float(k2);
+                        k1 = __float2bfloat16_rn(x1 * c - x2 * sn);
+                        k2 = __float2bfloat16_rn(x1 * sn + x2 * c);
+                    }
+                    kd[i] = k1;
+                    kd[i + half] = k2;
+                    vd[i] = vx[u].x;
+                    vd[i + half] = vx[u].y;
+                }
+            }
+        }
+    }
+    int rb = 0;
+    plan_block_scan<int>(sum, s_wi, &rb);
+    if (tid == 0) p.seq_rows[b] = rb;
+}
+
+cudaError_t launch_plan_rows(const PlanParams& p, cudaStream_t stream) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_rows_kernel, p);
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {

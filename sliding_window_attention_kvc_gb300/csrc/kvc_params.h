@@ -18,8 +18,10 @@ constexpr int kStreamCtas = 304;                 // stream-K grid: 152 SMs x 2 C
 // bf16 stream-K shares per persistent CTA (default).  Claiming several
 // shares in turn evens out CTAs that stream at different speeds (paged
 // batches: mixed lengths, shared-prefix blocks that hit in L2), at a fixed
-// cost per share (a segment start and a partial) that only long shares hide.
-constexpr int kPagedShareFactor = 3;             // paged caches with >= kPagedShareBatch sequences
+// cost per share (a segment start and a partial) that only long shares hide:
+// on the 64-sequence shared-prefix batch 2 shares per CTA measured 158.4 us,
+// 3 160.6, 4 166.6, 6 172.2.
+constexpr int kPagedShareFactor = 2;             // paged caches with >= kPagedShareBatch sequences
 constexpr int kPagedShareBatch = 8;
 // bf16 ring / sink+ring stream-K partition: units charged to each sequence
 // for the start of its segment (a second segment costs a CTA a q load and a
@@ -55,6 +57,8 @@ struct WorkspaceLayout {
     size_t plan_info;    // PAGED: int4  [items]: (t of the sequence, its first slot, its slot count, first physical block)
     size_t plan_total;   // PAGED: int32 items used, int32 shares G, int64 attended rows R
     size_t plan_cta;     // PAGED: int2 [ctas]: first item, item count
+    size_t plan_dir;     // PAGED: int2 [batch][ceil(maxb / 32)]: attended-block directory (mask, blocks before)
+    size_t plan_refs;    // PAGED: uint32 [num_blocks]: sequences attending each block this step (zero between calls)
     size_t blocks;       // PAGED: block manager scratch: int32 [6 * batch], int4 [batch], int32 count,
                          // int32 [num_blocks] reclaim flags
     size_t total;
@@ -82,6 +86,11 @@ struct DecodeParams {
     const int2* seq_items;      // PAGED plan
     const int32_t* n_items;     // PAGED plan
     const int2* cta_items;      // PAGED plan: first item, item count of each CTA (stream-K kernel)
+    const int32_t* seq_rows;    // PAGED batch on the tensor-core kernel: attended rows of each sequence
+    const int2* dir;            // ... and each sequence's attended-block directory (plan_rows_kernel)
+    int dir_groups;             // directory entries per sequence: ceil(maxb / 32)
+    uint32_t* refs;             // ... and the sequences attending each physical block (the combine
+                                // kernel zeroes it for the next call)
     long long layer_off;        // elements from cache base to this layer's K half
     long long kv_off;           // elements from the K half to the V half
     float* scales;              // INT8 cache: row scales [layers][K|V][rows of a half]; else null
@@ -114,6 +123,10 @@ struct PlanParams {
     int4* item_info;      // [max_items]: (t_b, first slot, slot count of b, physical block of the first block)
     int2* cta_items;      // [ctas]: first item, item count
     int32_t* n_items;     // [0] one past the last item used, [1] G, [2..3] R (int64)
+    int2* dir;            // plan_rows_kernel: [B][dir_groups] (mask of attended blocks 32 g .. 32 g + 31,
+                          // attended blocks of the sequence before block 32 g)
+    int dir_groups;
+    uint32_t* refs;       // plan_rows_kernel: [num_blocks] += 1 per sequence attending the block
     int B, bs, num_blocks, maxb, max_items, ctas;
     // the step's new token (kvc_decode_step); k_new == null: none
     void* cache;
@@ -239,6 +252,7 @@ cudaError_t launch_decode(int dtype, int head_dim, int gh, bool paged, bool read
 cudaError_t launch_decode_mma(int head_dim, int gh, bool paged, bool read_rope, bool q8, const DecodeParams& p,
                               const KvTensorMaps& maps, dim3 grid, cudaStream_t stream);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+cudaError_t launch_plan_rows(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_table_write(const TableParams& p, cudaStream_t stream);
 // kvc_prefill: the chunk's rows staged (K rotated as stored), then attention.
