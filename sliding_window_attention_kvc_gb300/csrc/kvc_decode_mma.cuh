@@ -613,6 +613,138 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             tma_prefetch_desc(&maps.sc_sub);
         }
     }
+    if constexpr (!PAGED && !Q8) {
+        // While the previous kernel in the stream finishes, the copy warp guesses
+        // its first share from the positions as they stand and prefetches its
+        // first kSpecRows K and V rows into L2.  A guess may be stale (the
+        // previous kernel may still write positions or rows): it only steers
+        // prefetch hints, clamped inside the layer, and nothing read from it is
+        // used after the wait.
+        if (warp == kConsumerWarps) {
+            const int C = p.capacity;
+            long long total = 0;
+            for (int base = 0; base < p.B; base += 32) {
+                const int bb = base + lane;
+                long long st = 0;
+                if (bb < p.B) {
+                    const int tb = *(volatile const int*)(p.pos + bb);
+                    const int nl = tb < 0 ? 0 : (tb + 1 < C ? tb + 1 : C);
+                    st = (nl > 0 ? (nl + 15) / 16 : 1) + kSeqUnits;
+                }
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) st += __shfl_xor_sync(0xffffffffu, st, off);
+                total += st;
+            }
+            const int G = (int)(total < p.nsplit ? total : p.nsplit);
+            if ((int)blockIdx.x < G && total > 0) {
+                const long long lo = div_nonneg((long long)blockIdx.x * total, G);
+                long long run = 0;
+                for (int base = 0; base < p.B; base += 32) {
+                    const int bb = base + lane;
+                    int nl = 0;
+                    long long st = 0;
+                    if (bb < p.B) {
+                        const int tb = *(volatile const int*)(p.pos + bb);
+                        nl = tb < 0 ? 0 : (tb + 1 < C ? tb + 1 : C);
+                        st = (nl > 0 ? (nl + 15) / 16 : 1) + kSeqUnits;
+                    }
+                    long long incl = st;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const long long u = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += u;
+                    }
+                    const long long Ob = run + incl - st;
+                    const unsigned hit = __ballot_sync(0xffffffffu, bb < p.B && Ob <= lo && lo < Ob + st);
+                    if (hit) {
+                        if (lane == __ffs(hit) - 1) {
+                            const int r0 = (int)max(0LL, lo - Ob - kSeqUnits) * 16;
+                            const int n = min(nl - r0, kSpecRows);
+                            if (n > 0) {
+                                const int elt = Q8 ? 1 : 2;
+                                const long long row = ((long long)bb * p.Hkv + kvh) * C + r0;
+                                const char* k0 = static_cast<const char*>(p.cache) +
+                                                 (p.layer_off + row * D) * elt;
+                                bulk_prefetch_l2(k0, (uint32_t)(n * D * elt));
+                                bulk_prefetch_l2(k0 + p.kv_off * elt, (uint32_t)(n * D * elt));
+                            }
+                        }
+                        break;
+                    }
+                    run += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+        }
+    }
+    if constexpr (PAGED && !Q8) {
+        // A paged batch: the same guess from the plan's per-sequence rows and
+        // block directory as they stand (the plan kernel may be rewriting them,
+        // for this call or the last), and the block table; every index is
+        // clamped, and only prefetch hints depend on it.
+        if (warp == kConsumerWarps && !p.self_plan && p.seq_rows) {
+            long long Rt = 0;
+            for (int base = 0; base < p.B; base += 32)
+                Rt += base + lane < p.B ? (long long)max(0, *(volatile const int*)(p.seq_rows + base + lane)) : 0;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) Rt += __shfl_xor_sync(0xffffffffu, Rt, off);
+            const int G = paged_share_count(Rt, p.nsplit);
+            if ((int)blockIdx.x < G && Rt > 0) {
+                const long long lo = div_nonneg((long long)blockIdx.x * Rt, G);
+                long long run = 0;
+                for (int base = 0; base < p.B; base += 32) {
+                    const int bb = base + lane;
+                    const long long r =
+                        bb < p.B ? (long long)max(0, *(volatile const int*)(p.seq_rows + bb)) : 0;
+                    long long incl = r;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const long long u = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += u;
+                    }
+                    const long long Ob = run + incl - r;
+                    const unsigned hit = __ballot_sync(0xffffffffu, r > 0 && Ob <= lo && lo < Ob + r);
+                    if (hit) {
+                        const int src = __ffs(hit) - 1;
+                        const int b = base + src;
+                        const long long s0 = __shfl_sync(0xffffffffu, lo - Ob, src);
+                        // the block of rank s0 / bs, by the directory's group counts
+                        const int kb = (int)(s0 / p.bs);
+                        const int2* drow = p.dir + (long long)b * p.dir_groups;
+                        const int ng = min(p.dir_groups, 32);
+                        int2 e = make_int2(0, 0x7fffffff);
+                        if (lane < ng) {
+                            e.x = *(volatile const int*)(&drow[lane].x);
+                            e.y = *(volatile const int*)(&drow[lane].y);
+                        }
+                        const unsigned le = __ballot_sync(0xffffffffu, lane < ng && e.y <= kb);
+                        if (le) {
+                            const int gs = 31 - __clz(le);
+                            uint32_t mm = (uint32_t)__shfl_sync(0xffffffffu, e.x, gs);
+                            const int k = kb - __shfl_sync(0xffffffffu, e.y, gs);
+                            if (k >= 0 && k < __popc(mm)) {
+#pragma unroll 1
+                                for (int q = 0; q < k; ++q) mm &= mm - 1u;
+                                const int lb0 = gs * 32 + (__ffs(mm) - 1);
+                                // the next blocks of the sequence from lb0, one per lane
+                                const int lbl = lb0 + lane;
+                                if (lane < kSpecRows / p.bs && lbl < p.maxb) {
+                                    const int phys = *(volatile const int*)(p.table + (long long)b * p.maxb + lbl);
+                                    if (phys >= 0 && phys < p.num_blocks) {
+                                        const long long row = ((long long)phys * p.Hkv + kvh) * p.bs;
+                                        const char* k0 = static_cast<const char*>(p.cache) + (p.layer_off + row * D) * 2;
+                                        bulk_prefetch_l2(k0, (uint32_t)(p.bs * D * 2));
+                                        bulk_prefetch_l2(k0 + p.kv_off * 2, (uint32_t)(p.bs * D * 2));
+                                    }
+                                }
+                            }
+                        }
+                        break;
+                    }
+                    run += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+        }
+    }
     // inputs written by earlier kernels (append, plan) are read only after this
     pdl_wait();
     pdl_launch_dependents();    // the combine kernel may start launching

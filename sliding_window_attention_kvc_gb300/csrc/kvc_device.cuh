@@ -194,6 +194,12 @@ __device__ __forceinline__ void tma_load_5d_hint(void* dst_smem, const void* tma
         : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2: a
+// hint, with no effect on what any load returns.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

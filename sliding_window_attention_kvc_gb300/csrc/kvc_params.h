@@ -28,6 +28,10 @@ constexpr int kPagedShareBatch = 8;
 // partial write), besides one unit per 16 rows.
 constexpr int kSeqUnits = 4;
 constexpr int kRunMaps = 4;                      // bf16 kernel: copies of runs of 16, 32, 48, 64 rows
+// bf16 caches: K/V rows of its first share that a decode CTA prefetches into
+// L2 while it waits for the previous kernel in the stream (window caches:
+// rows; paged batches: whole blocks, at most kSpecRows rows of them).
+constexpr int kSpecRows = 128;
 // Paged caches of one sequence: the decode CTAs plan their own stream-K share
 // from the block table and valid bits, staged in their (still empty) pipeline
 // stages, without a plan kernel, when the table has at most kSelfPlanMax
