@@ -43,7 +43,7 @@ import kvc_synth  # noqa: E402
 DEFAULT_WORKLOAD = "paged_shared_prefix_bf16"
 DEFAULT_LAYERS = {"tiny_ring_sink_f32": 1, "ring_bf16": 8, "sink_window_bf16": 2,
                   "paged_shared_prefix_bf16": 2, "long_context_pool_bf16": 4,
-                  "ring_int8": 8, "paged_shared_prefix_int8": 2}
+                  "ring_int8": 8, "sink_window_int8": 2, "paged_shared_prefix_int8": 2}
 
 
 def _kvc():
@@ -569,7 +569,7 @@ PER_WORKLOAD_STEPS = 200  # steps per timed loop of each per_workload entry
 PER_WORKLOAD = [("tiny_ring_sink_f32", {}), ("ring_bf16", {}), ("sink_window_bf16", {}),
                 ("paged_shared_prefix_bf16", {}), ("long_context_pool_bf16", {}),
                 ("long_context_pool_bf16", {"density": 0.25}), ("long_context_pool_bf16", {"density": 1.0}),
-                ("ring_int8", {}), ("paged_shared_prefix_int8", {})]
+                ("ring_int8", {}), ("sink_window_int8", {}), ("paged_shared_prefix_int8", {})]
 
 
 def workload_config(wl, layers, world, kw):

@@ -87,11 +87,13 @@ typedef enum { KVC_ROPE_NONE = 0, KVC_ROPE_BAKED = 1, KVC_ROPE_READ_INCACHE = 2 
  *                     keeps int8 codes and one fp32 scale s = max|x| / 127,
  *                     codes rint(x / s) clamped to +-127 (IEEE fp32 quotient,
  *                     ties to even), read back as code * s; a zero row has
- *                     s = 0.  With baked RoPE the rotated key is quantised.
- *                     q, out, k_new and v_new are bf16.  Requires head_dim
- *                     128 or 256, RoPE NONE or BAKED, and rows per K (or V)
- *                     half of a layer (batch * kv_heads * capacity, or
- *                     num_blocks * kv_heads * block_size) a multiple of 4.
+ *                     s = 0.  With baked RoPE the rotated key is quantised;
+ *                     with READ_INCACHE the raw key is, and the decode
+ *                     rotates code * s at the in-cache position.  q, out,
+ *                     k_new and v_new are bf16.  Requires head_dim 128 or
+ *                     256, and rows per K (or V) half of a layer (batch *
+ *                     kv_heads * capacity, or num_blocks * kv_heads *
+ *                     block_size) a multiple of 4.
  *                     Not accepted by the pool pager (kvc_pagein_issue). */
 typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_I8 = 2 } kvc_dtype;
 

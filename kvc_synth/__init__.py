@@ -23,6 +23,7 @@ from .workloads import (
     paged_shared_prefix_bf16,
     long_context_pool_bf16,
     ring_int8,
+    sink_window_int8,
     paged_shared_prefix_int8,
     as_int8,
 )
@@ -41,6 +42,7 @@ __all__ = [
     "paged_shared_prefix_bf16",
     "long_context_pool_bf16",
     "ring_int8",
+    "sink_window_int8",
     "paged_shared_prefix_int8",
     "as_int8",
 ]

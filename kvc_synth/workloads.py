@@ -313,6 +313,15 @@ def ring_int8(small: bool = False, layers: int = 1) -> Workload:
     return as_int8(ring_bf16(small, layers), "ring_int8" + ("_small" if small else ""))
 
 
+def sink_window_int8(small: bool = False, layers: int = 1) -> Workload:
+    """sink_window_bf16's sizes, positions and values over an INT8 cache that
+    keeps its keys raw and rotates them at read time (in-cache positions)."""
+    import dataclasses
+    wl = as_int8(sink_window_bf16(small, layers), "sink_window_int8" + ("_small" if small else ""))
+    return dataclasses.replace(wl, rope="read_time",
+                               notes=wl.notes.replace("INT8 cache", "INT8 cache, raw keys rotated at read time"))
+
+
 def paged_shared_prefix_int8(small: bool = False, layers: int = 1) -> Workload:
     """paged_shared_prefix_bf16's sizes, tables and values over an INT8 cache."""
     return as_int8(paged_shared_prefix_bf16(small, layers), "paged_shared_prefix_int8" + ("_small" if small else ""))
@@ -325,6 +334,7 @@ WORKLOAD_NAMES = {
     "paged_shared_prefix_bf16": paged_shared_prefix_bf16,
     "long_context_pool_bf16": long_context_pool_bf16,
     "ring_int8": ring_int8,
+    "sink_window_int8": sink_window_int8,
     "paged_shared_prefix_int8": paged_shared_prefix_int8,
 }
 

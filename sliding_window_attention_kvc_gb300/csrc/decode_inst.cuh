@@ -35,11 +35,11 @@
     KVC_INST_MMA(256, 2, PG, RD, false)   \
     KVC_INST_MMA(256, 4, PG, RD, false)
 
-// INT8: head_dim 128 and 256, no read-time RoPE
-#define KVC_INST_MMA_Q8(PG)               \
-    KVC_INST_MMA(128, 1, PG, false, true) \
-    KVC_INST_MMA(128, 2, PG, false, true) \
-    KVC_INST_MMA(128, 4, PG, false, true) \
-    KVC_INST_MMA(256, 1, PG, false, true) \
-    KVC_INST_MMA(256, 2, PG, false, true) \
-    KVC_INST_MMA(256, 4, PG, false, true)
+// INT8: head_dim 128 and 256; read-time RoPE on window caches only
+#define KVC_INST_MMA_Q8(PG, RD)        \
+    KVC_INST_MMA(128, 1, PG, RD, true) \
+    KVC_INST_MMA(128, 2, PG, RD, true) \
+    KVC_INST_MMA(128, 4, PG, RD, true) \
+    KVC_INST_MMA(256, 1, PG, RD, true) \
+    KVC_INST_MMA(256, 2, PG, RD, true) \
+    KVC_INST_MMA(256, 4, PG, RD, true)

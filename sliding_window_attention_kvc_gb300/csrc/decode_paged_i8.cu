@@ -1,3 +1,3 @@
 // Decode kernels: PAGED layout, INT8 cache (tensor cores).
 #include "decode_inst.cuh"
-KVC_INST_MMA_Q8(true)
+KVC_INST_MMA_Q8(true, false)

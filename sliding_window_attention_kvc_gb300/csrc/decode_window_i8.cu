@@ -1,3 +1,3 @@
 // Decode kernels: RING / SINK_RING layouts, INT8 cache (tensor cores).
 #include "decode_inst.cuh"
-KVC_INST_MMA_Q8(false)
+KVC_INST_MMA_Q8(false, false)

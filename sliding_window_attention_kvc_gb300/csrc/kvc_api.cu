@@ -44,7 +44,7 @@ int check_desc(const kvc_desc* d, Geo* g) {
     if (d->softmax_scale < 0.f) return KVC_ERR_DESC;
     g->elt = d->dtype == KVC_F32 ? 4 : (d->dtype == KVC_BF16 ? 2 : 1);
     g->act_elt = d->dtype == KVC_F32 ? 4 : 2;
-    if (d->dtype == KVC_I8 && (d->head_dim < 128 || d->rope == KVC_ROPE_READ_INCACHE)) return KVC_ERR_UNSUPPORTED;
+    if (d->dtype == KVC_I8 && d->head_dim < 128) return KVC_ERR_UNSUPPORTED;
     g->G = d->q_heads / d->kv_heads;
     g->GH = (g->G % 4 == 0) ? 4 : ((g->G % 2 == 0) ? 2 : 1);
     g->nsub = g->G / g->GH;
@@ -178,14 +178,15 @@ cudaError_t launch_decode_mma(int D, int gh, bool paged, bool rd, bool q8, const
     KVC_CASE(64, 1, PG, RD, false) KVC_CASE(64, 2, PG, RD, false) KVC_CASE(64, 4, PG, RD, false)    \
     KVC_CASE(128, 1, PG, RD, false) KVC_CASE(128, 2, PG, RD, false) KVC_CASE(128, 4, PG, RD, false) \
     KVC_CASE(256, 1, PG, RD, false) KVC_CASE(256, 2, PG, RD, false) KVC_CASE(256, 4, PG, RD, false)
-#define KVC_CASES_Q8(PG)                                                                                 \
-    KVC_CASE(128, 1, PG, false, true) KVC_CASE(128, 2, PG, false, true) KVC_CASE(128, 4, PG, false, true) \
-    KVC_CASE(256, 1, PG, false, true) KVC_CASE(256, 2, PG, false, true) KVC_CASE(256, 4, PG, false, true)
+#define KVC_CASES_Q8(PG, RD)                                                                    \
+    KVC_CASE(128, 1, PG, RD, true) KVC_CASE(128, 2, PG, RD, true) KVC_CASE(128, 4, PG, RD, true) \
+    KVC_CASE(256, 1, PG, RD, true) KVC_CASE(256, 2, PG, RD, true) KVC_CASE(256, 4, PG, RD, true)
     KVC_CASES(false, false)
     KVC_CASES(false, true)
     KVC_CASES(true, false)
-    KVC_CASES_Q8(false)
-    KVC_CASES_Q8(true)
+    KVC_CASES_Q8(false, false)
+    KVC_CASES_Q8(false, true)
+    KVC_CASES_Q8(true, false)
 #undef KVC_CASES_Q8
 #undef KVC_CASES
 #undef KVC_CASE

@@ -58,7 +58,8 @@ struct MmaShape {
     static constexpr int kNsub = kTokenGroups;                // sub-tiles per stage (one per token group)
     static constexpr int kStageBytes = 2 * kNsub * kSubBytes; // K and V of kNsub sub-tiles
     static constexpr int kCtasPerSm = decode_ctas_per_sm(Q8, PAGED, READ, D);
-    static constexpr int kStages = Q8 ? (kCtasPerSm >= 3 ? 3 : 5) : (D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3));
+    static constexpr int kStages =
+        Q8 ? (kCtasPerSm >= 3 ? 3 : ((READ && D < 256) ? 4 : 5)) : (D == 64 ? 6 : ((READ && D >= 256) ? 5 : 3));
     // INT8: row scales of each stage, one slot per sub-tile position (the
     // first sub-tile of a copy holds that copy's K and V scales)
     static constexpr int kScSlotBytes = Q8 ? 640 : 0;         // 2 x kScRunRows floats, 128-byte aligned
@@ -273,7 +274,12 @@ struct MmaSmem {
     static constexpr size_t kHdr = kMergeML + (size_t)S::kTokenGroups * GH * 8;   // the CTA's first segment header
     // 4 mbarriers: all compute warps, 2 warp pairs, first header published
     static constexpr size_t kCbar = kHdr + sizeof(MmaSegment);
-    static constexpr size_t kTotal = kCbar + 32 + 1024;   // + slack to align the base to 1024
+    // INT8 with read-time RoPE: each token group's K sub-tile, dequantised and
+    // rotated, in bf16 ([D/64 column blocks][16 rows][128 bytes], 16-byte
+    // chunks swizzled by row as the bf16 stages are)
+    static constexpr size_t kKrot = (kCbar + 32 + 127) / 128 * 128;
+    static constexpr size_t kTotal =
+        kKrot + ((Q8 && READ) ? (size_t)S::kTokenGroups * S::kSub * D * 2 : 0) + 1024;   // + slack to align the base
 };
 
 // Barrier among a fixed set of threads built on an mbarrier, so that waiting
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ KvTensorMaps maps) {
     using S = MmaShape<D, READ, Q8, PAGED>;
     using SM = MmaSmem<D, GH, READ, Q8, PAGED>;
-    static_assert(!(READ && Q8), "INT8 caches take no read-time RoPE");
+    static_assert(!(READ && Q8 && PAGED), "paged caches take no read-time RoPE");
     static_assert(!Q8 || D >= 128, "INT8 rows are whole 128-byte column blocks");
     constexpr int NST = S::kStages, NSUB = S::kNsub, HALF = S::kHalf;
 
@@ -586,6 +592,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
     float2* merge_ml = reinterpret_cast<float2*>(smem + SM::kMergeML);
     uint64_t* cbar = reinterpret_cast<uint64_t*>(smem + SM::kCbar);
     MmaSegment* first_hdr = reinterpret_cast<MmaSegment*>(smem + SM::kHdr);
+    unsigned char* krot = smem + SM::kKrot;           // INT8 + READ_INCACHE: rotated K sub-tiles
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -1432,7 +1439,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
         }
         csync.sync(p.err);
         float qf[S::kKsteps][4];
-        if (Q8 && g < GH) {
+        if (Q8 && !READ && g < GH) {
             // INT8: k-step ks takes columns q8_col0(ks) .. + 3 (see the Q K^T
             // product); each value is rotated with its pair column
 #pragma unroll
@@ -1482,7 +1489,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
 #pragma unroll
             for (int ks = 0; ks < S::kKsteps; ++ks) qf[ks][0] = qf[ks][1] = qf[ks][2] = qf[ks][3] = 0.f;
         }
-        if constexpr (Q8) {
+        if constexpr (Q8 && !READ) {
             float amax = 0.f;
 #pragma unroll
             for (int ks = 0; ks < S::kKsteps; ++ks)
@@ -1507,6 +1514,12 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             for (int ks = 0; ks < S::kKsteps; ++ks) {
                 qa[ks][0] = pack_bf16x2(qf[ks][0] * p.q_scale, qf[ks][1] * p.q_scale);
                 qa[ks][1] = pack_bf16x2(qf[ks][2] * p.q_scale, qf[ks][3] * p.q_scale);
+            }
+            if constexpr (Q8) {
+                // INT8 with read-time RoPE: bf16 q against the rotated bf16 K
+                qexp = 1.f;
+                S_run = 0.f;
+                rS = 0.f;
             }
         }
 #pragma unroll
@@ -1726,7 +1739,59 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 }
             }
 
-            if constexpr (READ) {
+            if constexpr (READ && Q8) {
+                // INT8: K of the sub-tile as code x row scale, rotated by
+                // R((ip0 + r) theta) as below, into the token group's bf16 tile;
+                // rows past nrows too (their scores are masked out)
+                const float4* rs4 = reinterpret_cast<const float4*>(rot + (s * NSUB + tg) * HALF);
+                const float* kscl = sc_base + (size_t)s * (S::kScStageBytes / 4) + meta[s].sbase[tg];
+                unsigned char* Kb = krot + (size_t)tg * S::kSub * D * 2;
+                float2 cc[4], ss[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 a = rs4[q * S::kCpr + rcp];
+                    const float2 ac = make_float2(a.x, a.z), as = make_float2(a.y, a.w);
+                    cc[q] = __ffma2_rn(ac, r0c[q], __fmul2_rn(as, make_float2(-r0s[q].x, -r0s[q].y)));
+                    ss[q] = __ffma2_rn(as, r0c[q], __fmul2_rn(ac, r0s[q]));
+                }
+                const int chi = rcp + S::kCpr;
+                const int clo = 8 * rcp, chc = 8 * chi;       // first columns of the two chunks
+#pragma unroll
+                for (int k = 0; k < S::kRowsPerLane; ++k) {
+                    const int r = rrow0 + k * kRowStep;
+                    const uint2 wl = *reinterpret_cast<const uint2*>(
+                        Ks + (clo >> 7) * bstride + r * 128 + ((((clo & 127) >> 4) ^ (r & 7)) << 4) + (clo & 8));
+                    const uint2 wh = *reinterpret_cast<const uint2*>(
+                        Ks + (chc >> 7) * bstride + r * 128 + ((((chc & 127) >> 4) ^ (r & 7)) << 4) + (chc & 8));
+                    const float sc = kscl[r];
+                    uint32_t ol[4], oh[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t lw = q < 2 ? wl.x : wl.y, hw = q < 2 ? wh.x : wh.y;
+                        const int sh = 16 * (q & 1);
+                        const float2 xl = make_float2((float)(int8_t)(lw >> sh) * sc, (float)(int8_t)(lw >> (sh + 8)) * sc);
+                        const float2 xh = make_float2((float)(int8_t)(hw >> sh) * sc, (float)(int8_t)(hw >> (sh + 8)) * sc);
+                        const float2 yl = __ffma2_rn(xl, cc[q], __fmul2_rn(xh, make_float2(-ss[q].x, -ss[q].y)));
+                        const float2 yh = __ffma2_rn(xl, ss[q], __fmul2_rn(xh, cc[q]));
+                        ol[q] = pack_bf16x2(yl.x, yl.y);
+                        oh[q] = pack_bf16x2(yh.x, yh.y);
+                    }
+                    *reinterpret_cast<uint4*>(Kb + (rcp >> 3) * (S::kSub * 128) + r * 128 + (((rcp & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(ol[0], ol[1], ol[2], ol[3]);
+                    *reinterpret_cast<uint4*>(Kb + (chi >> 3) * (S::kSub * 128) + r * 128 + (((chi & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(oh[0], oh[1], oh[2], oh[3]);
+                    if (k + 1 < S::kRowsPerLane) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 c0 = cc[q];
+                            cc[q] = __ffma2_rn(c0, stc[q], __fmul2_rn(ss[q], make_float2(-sts[q].x, -sts[q].y)));
+                            ss[q] = __ffma2_rn(ss[q], stc[q], __fmul2_rn(c0, sts[q]));
+                        }
+                    }
+                }
+                if constexpr (S::kDsplit == 2) psync.sync(p.err); else __syncwarp();
+            }
+            if constexpr (READ && !Q8) {
                 // rotate the stored (raw) K rows in place by R((ip0 + r) theta):
                 // R(ip0 theta) from the stage table times R(r theta), advanced
                 // from row to row by the step rotation.  Packed fp32 pairs; rows
@@ -1791,7 +1856,16 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             // ---- S = Q K^T over the 16 rows: two 8-token n-tiles --------------
             float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             uint4 vw[2][2];          // INT8: V code chunks of tokens 2c, 2c + 1, 2c + 8, 2c + 9
-            if constexpr (Q8) {
+            if constexpr (Q8 && READ) {
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int ta = 2 * c + 8 * hlf;
+                    vw[hlf][0] = *reinterpret_cast<const uint4*>(Vs + hd * bstride + ta * 128 + ((g ^ (ta & 7)) << 4));
+                    vw[hlf][1] = *reinterpret_cast<const uint4*>(Vs + hd * bstride + (ta + 1) * 128 +
+                                                                 ((g ^ ((ta + 1) & 7)) << 4));
+                }
+            }
+            if constexpr (Q8 && !READ) {
                 // INT8: lane (g, c) reads 8 code bytes of rows g and g + 8 at columns
                 // q8_col0(2 k2) .. + 7 and turns them into the B fragments of k-steps
                 // 2 k2 and 2 k2 + 1 (the 16-byte chunks k2 mod 4 and k2 mod 4 + 4 of a
@@ -1827,12 +1901,15 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             } else {
                 const int tok = ((lane >> 4) << 3) + (lane & 7);
                 const int chs = (lane >> 3) & 1;
+                // bf16 K: the stage's rows, or (INT8 + READ) the rotated tile
+                const uint32_t kbase = Q8 ? smem_u32(krot + (size_t)tg * S::kSub * D * 2) : ku;
+                const int kstride = Q8 ? S::kSub * 128 : bstride;
 #pragma unroll
                 for (int ks = 0; ks < S::kKsteps; ++ks) {
                     const int bx = ks >> 2;
                     const int ch = ((ks & 3) << 1) + chs;
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(ku + bx * bstride + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+                    ldsm_x4(kbase + bx * kstride + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
                     mma_bf16_16816(sa[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
                     mma_bf16_16816(sa[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
                 }
@@ -1850,7 +1927,7 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
                 const int tk[4] = {tk0, tk0 + 1, tk0 + 8, tk0 + 9};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    sv[e] *= scl[tk[e]] * qexp;
+                    if constexpr (!READ) sv[e] *= scl[tk[e]] * qexp;   // (READ: the K scale is in the tile)
                     vsc[e] = tk[e] < nrows ? vscl[tk[e]] : 0.f;
                 }
             }

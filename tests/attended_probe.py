@@ -150,13 +150,16 @@ class Probe:
         raise AssertionError(f"{what}: attended set differs\n" + "\n".join(msgs))
 
 
-def window_probe(kvc, *, dtype, B, Hq, Hkv, D, sinks, window, t, num_splits=0, fused=False):
+def window_probe(kvc, *, dtype, B, Hq, Hkv, D, sinks, window, t, num_splits=0, fused=False, rope="none"):
     """Ring / sink+ring cache: ids are slots.  Live rows: the attended slots at
-    t_b (at t_b without slot(t_b) for a decode step, whose kernel appends t_b)."""
+    t_b (at t_b without slot(t_b) for a decode step, whose kernel appends t_b).
+    K = 0 rotates to 0, so any RoPE mode leaves the expected sets unchanged;
+    read-time RoPE takes the kernels' rotating paths (runs cut at the
+    sink/window boundary and the ring's wrap)."""
     t = np.asarray(t, dtype=np.int64)
     C = sinks + window
     layout = "sink_ring" if sinks else "ring"
-    d = kvc.make_desc(layout, "none", dtype, 1, len(t), Hq, Hkv, D, window=window, sinks=sinks,
+    d = kvc.make_desc(layout, rope, dtype, 1, len(t), Hq, Hkv, D, window=window, sinks=sinks,
                       num_splits=num_splits)
     cache = kvc.alloc_cache(d, fill=NAN)
     ids = np.full((len(t), C), -1, dtype=np.int64)

@@ -57,14 +57,30 @@ def test_window_attended_sets_exact(kvc, dtype, D, sinks, num_splits, fused):
     run_decode(kvc, p, t)
 
 
-@pytest.mark.parametrize("name", ["ring_bf16", "sink_window_bf16", "ring_int8"])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("i8", 128), ("i8", 256)])
+@pytest.mark.parametrize("sinks", [0, 4])
+@pytest.mark.parametrize("num_splits,fused", [(0, False), (0, True), (7, False), (7, True)])
+def test_window_read_time_sets_exact(kvc, dtype, D, sinks, num_splits, fused):
+    """Read-time RoPE ([sink] "RoPE cache position shifting"): the rotating
+    paths (bf16 rows rotated in place, INT8 rows dequantised and rotated into
+    a bf16 tile) see exactly the attended sets."""
+    Hq, Hkv, C = GEOM[D]
+    W = C - sinks
+    t = _positions(sinks, C)
+    p = window_probe(kvc, dtype=dtype, B=len(t), Hq=Hq, Hkv=Hkv, D=D, sinks=sinks, window=W, t=t,
+                     num_splits=num_splits, fused=fused, rope="read_time")
+    run_decode(kvc, p, t)
+
+
+@pytest.mark.parametrize("name", ["ring_bf16", "sink_window_bf16", "ring_int8", "sink_window_int8"])
 @pytest.mark.parametrize("num_splits,fused", [(0, False), (0, True), (1, False), (7, True)])
 def test_window_workload_sets_exact(kvc, name, num_splits, fused):
-    """The full workload shapes and positions (bench.py's launch configuration at num_splits 0)."""
+    """The full workload shapes, positions and RoPE modes (bench.py's launch
+    configuration at num_splits 0)."""
     wl = kvc_synth.make_workload(name)
     t = wl.positions
     p = window_probe(kvc, dtype=wl.dtype, B=wl.batch, Hq=wl.q_heads, Hkv=wl.kv_heads, D=wl.head_dim,
-                     sinks=wl.sinks, window=wl.window, t=t, num_splits=num_splits, fused=fused)
+                     sinks=wl.sinks, window=wl.window, t=t, num_splits=num_splits, fused=fused, rope=wl.rope)
     run_decode(kvc, p, t)
 
 

@@ -4,7 +4,9 @@
   rows (both sides quantise the same bf16 values in fp32); with baked RoPE the
   two rotate with different sin/cos roundings, so codes may differ by one step;
 * decode outputs element by element at small sizes (ring before, at and after
-  the first wrap, no RoPE and baked; sink + ring; paged shared prefix; a
+  the first wrap, no RoPE, baked and read-time; sink + ring, baked and
+  read-time (raw keys dequantised and rotated at their in-cache positions);
+  paged shared prefix; a
   single-sequence pool at head_dim 256 with NaN scales in its non-resident
   slots) and on sampled sequences of the full ring_int8 workload in the launch
   configuration bench.py times, against the oracle over the rows as the INT8
@@ -46,6 +48,14 @@ def _small(case):
         return dataclasses.replace(kvc_synth.make_workload("ring_int8", small=True), rope="none")
     if case == "sink_baked":
         return kvc_synth.as_int8(kvc_synth.make_workload("sink_window_bf16", small=True), "sink_window_int8_small")
+    if case == "sink_read":
+        return kvc_synth.make_workload("sink_window_int8", small=True)
+    if case == "ring_read":
+        return dataclasses.replace(kvc_synth.make_workload("ring_int8", small=True), rope="read_time")
+    if case == "ring_d256_read":
+        return dataclasses.replace(kvc_synth.as_int8(kvc_synth.make_workload("ring_bf16", small=True),
+                                                     "ring_int8_d256_small"), rope="read_time", head_dim=256,
+                                   q_heads=8, kv_heads=2)
     if case == "paged":
         return kvc_synth.make_workload("paged_shared_prefix_int8", small=True)
     if case == "pool_d256":
@@ -54,7 +64,7 @@ def _small(case):
     raise ValueError(case)
 
 
-CASES = ["ring", "ring_none", "sink_baked", "paged", "pool_d256"]
+CASES = ["ring", "ring_none", "sink_baked", "sink_read", "ring_read", "ring_d256_read", "paged", "pool_d256"]
 
 
 def _maxerr(got, ref):
@@ -123,7 +133,7 @@ def test_int8_decode_full_size_sampled(kvc):
     assert kvc.get_error(st.ws) == 0
 
 
-@pytest.mark.parametrize("case", ["ring", "sink_baked", "paged"])
+@pytest.mark.parametrize("case", ["ring", "sink_baked", "sink_read", "paged"])
 def test_int8_decode_step_fused_append(kvc, case):
     """kvc_decode_step over consecutive positions: the fused INT8 append (in
     the decode kernel for ring layouts, in the plan kernel for paged) leaves

@@ -80,7 +80,8 @@ def test_invalid_descriptors_are_rejected(kvc):
         dict(layout="paged", block_size=0, num_blocks=4, max_blocks_per_seq=4),
         dict(layers=0),
         dict(dtype="i8", head_dim=64),                       # INT8: whole 128-byte column blocks
-        dict(dtype="i8", layout="sink_ring", sinks=4, window=96, rope="read_time"),   # INT8: no read-time RoPE
+        dict(dtype="i8", layout="paged", rope="read_time", block_size=16, num_blocks=4,
+             max_blocks_per_seq=4),                          # paged: no read-time RoPE
         dict(dtype="i8", batch=1, kv_heads=1, window=98),    # INT8: rows of a half not a multiple of 4
     ]
     for kw in bad:
@@ -108,7 +109,7 @@ def _documented_cache_bytes(f):
         if f["window"] < 1 or (layout == 0 and f["sinks"] != 0) or (layout == 1 and f["sinks"] < 1):
             return 0
         rows = f["batch"] * f["kv_heads"] * (f["sinks"] + f["window"])
-    if dtype == 2 and (f["head_dim"] < 128 or rope == 2 or rows % 4):
+    if dtype == 2 and (f["head_dim"] < 128 or rows % 4):
         return 0
     elems = f["layers"] * 2 * rows * f["head_dim"]
     if dtype == 2:
