@@ -773,15 +773,16 @@ def run_ours(args):
                 continue
             per_workload.append(measure_workload(name, pkw, PER_WORKLOAD_STEPS, args.loops))
         # chunked prefill (kvc_prefill), 128-token chunks ending at each
-        # sequence's position, on the three bf16 layouts
+        # sequence's position, on the three bf16 layouts and the INT8 paged batch
         prefill = []
-        for name in ("ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16"):
+        for name in ("ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16", "paged_shared_prefix_int8"):
             pa = argparse.Namespace(workload=name, chunk=128, steps=20, warmup=3)
             r = measure_prefill(pa)
             prefill.append({"workload": name, "chunk_tokens": 128, "ms_per_call": r["ms_per_call"],
                             "tokens_per_s": r["tokens_per_s"], "tflops": r["value"],
                             "roofline_frac": r["roofline"]["frac"], "peak_kind": r["roofline"]["peak_kind"],
-                            "rope": "read_time" if name == "sink_window_bf16" else "baked",
+                            "rope": "read_time" if name.startswith("sink_window") else "baked",
+                            "cache_dtype": "i8" if name.endswith("int8") else "bf16",
                             "device_errors": r["device_errors"]})
             torch.cuda.empty_cache()
     clk = clocks.stop()
@@ -1017,16 +1018,18 @@ def measure_pagein(args):
 
 def measure_prefill(args):
     """Chunked prefill (kvc_prefill) of T = --chunk tokens per sequence on a
-    bf16 workload (default ring_bf16: 8 sequences, 32 q / 8 kv heads, D 128,
-    a full 4096-slot ring; also sink_window_bf16, whose RoPE is applied at
-    read time, and paged_shared_prefix_bf16), each chunk ending at the workload's position t_b,
+    bf16 or INT8 workload (default ring_bf16: 8 sequences, 32 q / 8 kv heads,
+    D 128, a full 4096-slot ring; also sink_window_bf16, whose RoPE is applied
+    at read time, paged_shared_prefix_bf16, and their INT8 forms ring_int8,
+    sink_window_int8, paged_shared_prefix_int8), each chunk ending at the workload's position t_b,
     the cache holding every earlier position.  One call stages the chunk,
     runs the attention and appends the chunk.  L2 is flushed (a 256 MiB write)
     between timed calls; each call is timed with CUDA events.  Reports tokens/s
     and the attention's algorithmic TFLOP/s (4 D flops per (token, q head,
     attended key): q.k and p.v) against the measured bf16 tensor peak."""
     kvc = _kvc()
-    name = args.workload if args.workload in ("ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16") \
+    name = args.workload if args.workload in ("ring_bf16", "paged_shared_prefix_bf16", "sink_window_bf16",
+                                              "ring_int8", "paged_shared_prefix_int8", "sink_window_int8") \
         else "ring_bf16"
     wl = kvc_synth.make_workload(name)
     T = args.chunk

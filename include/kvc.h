@@ -240,10 +240,12 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
  *              followed by the chunk's staged rows.
  * READ_INCACHE: each token's window keys at distance t - p and its sinks at
  * min(t, C - 1) - p, as the decode step at t rotates them.
- * bf16 caches, head_dim 64, 128 or 256.  KVC_ERR_UNSUPPORTED: another cache
- * dtype; at head_dim 256, a ring or sink+ring chunk longer than the window,
- * paged blocks whose size is not a multiple of 8 dividing 64, or a GQA group
- * that does not divide 128.  Calls on one workspace must not overlap on the
+ * bf16 caches (head_dim 64, 128 or 256) and INT8 caches (128 or 256: cached
+ * rows are read back as code * scale, the chunk's own rows as the cache will
+ * read them back).  KVC_ERR_UNSUPPORTED: an fp32 cache; at head_dim 256 or on
+ * an INT8 cache, a ring or sink+ring chunk longer than the window, paged
+ * blocks whose size is not a multiple of 8 dividing 64, or a GQA group that
+ * does not divide 128.  Calls on one workspace must not overlap on the
  * GPU.  The attention runs on the tcgen05 tensor cores: a CTA of the
  * warp-specialised kernel (one per SM) holds all 512 tensor-memory columns
  * of its SM while it runs (the kernel for chunks longer than the window: 256

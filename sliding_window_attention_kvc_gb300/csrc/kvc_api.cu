@@ -325,6 +325,26 @@ int kv_maps_for(const kvc_desc* d, const Geo& g, const void* cache, KvTensorMaps
     return KVC_OK;
 }
 
+// INT8 caches, for the warp-specialised prefill: the codes as {D bytes, row,
+// K|V, layer}, boxes of 128 codes of `rows` rows (64 for slot tiles, a block
+// for paged tiles), no swizzle (rows land as 128 contiguous bytes).
+int encode_q8_code_map(const kvc_desc* d, const Geo& g, const void* cache, int rows, CUtensorMap* map) {
+    const unsigned long long half_rows = (unsigned long long)g.half_elems / d->head_dim;
+    if (half_rows >= (1ull << 31)) return KVC_ERR_UNSUPPORTED;
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return KVC_ERR_CUDA;
+    const cuuint64_t row_bytes = (cuuint64_t)d->head_dim, half_bytes = half_rows * row_bytes;
+    const cuuint64_t dims[4] = {(cuuint64_t)d->head_dim, half_rows, 2, (cuuint64_t)d->layers};
+    const cuuint64_t strides[3] = {row_bytes, half_bytes, 2 * half_bytes};
+    const cuuint32_t box[4] = {128, (cuuint32_t)rows, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(cache), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? KVC_OK
+               : KVC_ERR_CUDA;
+}
+
 // Paged caches, for the warp-specialised prefill: {column, row, K|V, layer}
 // with boxes of one block (bs rows) of K or of V, 64 columns.
 int encode_block_map(const kvc_desc* d, const Geo& g, const void* cache, CUtensorMap* map) {
@@ -639,13 +659,14 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     Geo g;
     int rc = check_desc(d, &g);
     if (rc) return rc;
-    if (d->dtype != KVC_BF16) return KVC_ERR_UNSUPPORTED;
+    if (d->dtype == KVC_F32) return KVC_ERR_UNSUPPORTED;
+    const bool q8 = d->dtype == KVC_I8;
     const bool paged_l = d->layout == KVC_LAYOUT_PAGED;
     // the warp-specialised kernel: 128-row Q tiles of whole GQA groups, paged
     // blocks that pack a 64-key tile, chunks no longer than the window
     const bool ws_kernel = 128 % g.G == 0 &&
                            (paged_l ? (d->block_size % 8 == 0 && 64 % d->block_size == 0) : T <= d->window);
-    if (!ws_kernel && ((d->head_dim != 64 && d->head_dim != 128) || g.G > 64)) return KVC_ERR_UNSUPPORTED;
+    if (!ws_kernel && (q8 || (d->head_dim != 64 && d->head_dim != 128) || g.G > 64)) return KVC_ERR_UNSUPPORTED;
     if (!cache || !q || !k_new || !v_new || !pos0 || !out || !workspace) return KVC_ERR_NULL;
     const bool paged = d->layout == KVC_LAYOUT_PAGED;
     if (paged && !block_table) return KVC_ERR_NULL;
@@ -682,7 +703,13 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     ap.maxb = d->max_blocks_per_seq;
     ap.rope = d->rope;
     if (d->rope == KVC_ROPE_BAKED) fill_theta(d->head_dim, d->rope_base, ap.theta, nullptr);
-    // 1. the chunk's rows as the cache will hold them
+    const long long half_rows = g.half_elems / d->head_dim;
+    if (q8) {
+        ap.scales = reinterpret_cast<float*>(static_cast<char*>(cache) + (size_t)d->layers * 2 * (size_t)g.half_elems);
+        ap.sc_layer_off = (long long)layer * 2 * half_rows;
+        ap.sc_kv_off = half_rows;
+    }
+    // 1. the chunk's rows as the cache will hold them (INT8: as it reads them back)
     if (launch_prefill_stage(ap, kst, vst, s) != cudaSuccess) return KVC_ERR_CUDA;
     // 2. attention: earlier keys from the cache as it stands, the chunk's from the stage
     PrefillParams pp{};
@@ -713,11 +740,18 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     pp.layer = layer;
     const float scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
     pp.q_scale = scale * 1.4426950408889634f;
+    pp.scales = ap.scales;
+    pp.sc_layer_off = ap.sc_layer_off;
+    pp.sc_kv_off = ap.sc_kv_off;
+    pp.half_rows = half_rows;
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
     if (ws_kernel) {
         PrefillMaps pm;
         std::memset(&pm, 0, sizeof(pm));
-        if (paged_l) {
+        if (q8) {
+            if ((rc = encode_q8_code_map(d, g, cache, paged_l ? d->block_size : 64, paged_l ? &pm.block : &pm.slot)))
+                return rc;
+        } else if (paged_l) {
             if ((rc = encode_block_map(d, g, cache, &pm.block))) return rc;
         } else {
             KvTensorMaps km;
@@ -725,7 +759,7 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
             pm.slot = km.run[kRunMaps - 1];                 // 64-row runs
         }
         if ((rc = encode_stage_map(d, kst, T, prefill_stage_bytes(d, T) / 2, &pm.stage))) return rc;
-        if (launch_prefill_ws(d->head_dim, pp, pm, s) != cudaSuccess) return KVC_ERR_CUDA;
+        if (launch_prefill_ws(d->head_dim, q8, pp, pm, s) != cudaSuccess) return KVC_ERR_CUDA;
     } else if (launch_prefill(d->head_dim, g.G, pp, s) != cudaSuccess) {
         return KVC_ERR_CUDA;
     }

@@ -132,9 +132,66 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
                                     p.theta);
 }
 
+// INT8 cache: the chunk's rows as the cache will read them back, bf16 of
+// code * row scale (the quantisation kvc_append applies: K rotated first when
+// BAKED), so the chunk's tokens attend one another as the decode steps would.
+// One warp per (token, kv head).
+template <int NP>
+__global__ void __launch_bounds__(256) prefill_stage_q8_kernel(const __grid_constant__ AppendParams p,
+                                                               __nv_bfloat16* kst, __nv_bfloat16* vst) {
+    constexpr int D = 64 * NP, HALF = 32 * NP;
+    const int i_tok = blockIdx.x, b = blockIdx.y;
+    const long long pos = (long long)p.pos[b] + i_tok;
+    if (pos < 0) return;
+    const int lane = threadIdx.x & 31;
+    for (int hk = threadIdx.x >> 5; hk < p.Hkv; hk += blockDim.x >> 5) {
+        const long long row = (((long long)b * p.n_new + i_tok) * p.Hkv + hk) * D;
+        const __nv_bfloat16* kr = static_cast<const __nv_bfloat16*>(p.k_new) + row;
+        const __nv_bfloat16* vr = static_cast<const __nv_bfloat16*>(p.v_new) + row;
+        float kx[2 * NP], vx[2 * NP];
+#pragma unroll
+        for (int m = 0; m < NP; ++m) {
+            const int i = lane + 32 * m;
+            float x1 = __bfloat162float(kr[i]), x2 = __bfloat162float(kr[i + HALF]);
+            if (p.rope == kRopeBaked) {
+                float c, sn;
+                rope_cos_sin(pos, p.theta[i], &c, &sn);
+                const float y1 = x1 * c - x2 * sn, y2 = x1 * sn + x2 * c;
+                x1 = y1;
+                x2 = y2;
+            }
+            kx[2 * m] = x1;
+            kx[2 * m + 1] = x2;
+            vx[2 * m] = __bfloat162float(vr[i]);
+            vx[2 * m + 1] = __bfloat162float(vr[i + HALF]);
+        }
+        int8_t kq[2 * NP], vq[2 * NP];
+        const float sk = q8_quantize_lane<2 * NP>(kx, kq);
+        const float sv = q8_quantize_lane<2 * NP>(vx, vq);
+#pragma unroll
+        for (int m = 0; m < NP; ++m) {
+            const int i = lane + 32 * m;
+            kst[row + i] = __float2bfloat16_rn((float)kq[2 * m] * sk);
+            kst[row + i + HALF] = __float2bfloat16_rn((float)kq[2 * m + 1] * sk);
+            vst[row + i] = __float2bfloat16_rn((float)vq[2 * m] * sv);
+            vst[row + i + HALF] = __float2bfloat16_rn((float)vq[2 * m + 1] * sv);
+        }
+    }
+}
+
 cudaError_t launch_prefill_stage(const AppendParams& p, void* kst, void* vst, cudaStream_t stream) {
-    prefill_stage_kernel<<<dim3(p.n_new, p.B), 256, 0, stream>>>(p, static_cast<__nv_bfloat16*>(kst),
-                                                                 static_cast<__nv_bfloat16*>(vst));
+    __nv_bfloat16* k = static_cast<__nv_bfloat16*>(kst);
+    __nv_bfloat16* v = static_cast<__nv_bfloat16*>(vst);
+    if (p.scales) {                       // INT8 cache
+        if (p.D == 128)
+            prefill_stage_q8_kernel<2><<<dim3(p.n_new, p.B), 256, 0, stream>>>(p, k, v);
+        else if (p.D == 256)
+            prefill_stage_q8_kernel<4><<<dim3(p.n_new, p.B), 256, 0, stream>>>(p, k, v);
+        else
+            return cudaErrorInvalidValue;
+    } else {
+        prefill_stage_kernel<<<dim3(p.n_new, p.B), 256, 0, stream>>>(p, k, v);
+    }
     return cudaGetLastError();
 }
 

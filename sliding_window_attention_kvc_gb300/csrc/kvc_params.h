@@ -178,6 +178,10 @@ struct PrefillParams {
     int rope;
     int layer;
     float q_scale;              // softmax scale * log2(e)
+    const float* scales;        // INT8 cache: row scales [layers][K|V][rows of a half]; else null
+    long long sc_layer_off;     // INT8: scales from `scales` to this layer's K half
+    long long sc_kv_off;        // INT8: from the K half's scales to the V half's (rows of a half)
+    long long half_rows;        // rows of a K (or V) half of a layer
     unsigned long long theta[kMaxHalfDim];   // theta_i / (2 pi) * 2^64 (see rope_cos_sin)
 };
 
@@ -190,6 +194,8 @@ struct PrefillParams {
 //          rows) of K or of V, one column block;
 //   stage  the chunk's staged rows [batch][T][kv head][D] (K, then V):
 //          {64 columns, kv head, batch * T, K|V, column block}, 64 tokens.
+// INT8 caches: slot and block are code maps {D bytes, row, K|V, layer} with
+// boxes of 128 codes of 64 rows (slot) or one block (block), no swizzle.
 struct PrefillMaps {
     CUtensorMap slot, block, stage;
     int slot_whole;
@@ -264,7 +270,8 @@ cudaError_t launch_prefill_stage(const AppendParams& p, void* kst, void* vst, cu
 cudaError_t launch_prefill(int head_dim, int g, const PrefillParams& p, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillParams& p, cudaStream_t stream);   // head_dim 128, tcgen05
 // head_dim 64 / 128 / 256, warp-specialised tcgen05 with TMA tiles
-cudaError_t launch_prefill_ws(int head_dim, const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream);
+cudaError_t launch_prefill_ws(int head_dim, bool q8, const PrefillParams& p, const PrefillMaps& maps,
+                              cudaStream_t stream);
 cudaError_t launch_valid_write(const TableParams& p, cudaStream_t stream);
 cudaError_t launch_block_prepare(int elt, const BlockParams& p, cudaStream_t stream);
 cudaError_t launch_block_share(const BlockParams& p, int n, cudaStream_t stream);

@@ -53,7 +53,12 @@ struct WsShape {
     static constexpr int OffQ = 0;
     static constexpr int OffStage = OffQ + NQ * QBytes;
     static constexpr int OffP = OffStage + STAGES * StageBytes;
-    static constexpr int OffMeta = OffP + NQ * PBytes;
+    // INT8 caches: row scales of each stage's cache tile, [stage][K|V][68]:
+    // copied from a row that is a multiple of 4 (whole 16-byte copies), the
+    // tile's first row sc_off after it
+    static constexpr int ScRows = kWsKeys + 4;
+    static constexpr int OffScale = OffP + NQ * PBytes;
+    static constexpr int OffMeta = OffScale + STAGES * 2 * ScRows * 4;
     static constexpr int TmemCols = 512;
     static constexpr int SCol0 = NQ * D;                       // S buffers after the O tiles
     static_assert(NQ * D + NQ * 2 * kWsKeys <= TmemCols, "TMEM columns");
@@ -66,17 +71,22 @@ struct WsShape {
 // test), or key by key from pos[].
 enum : int { kMaskNone = 0, kMaskRange = 1, kMaskKeys = 2 };
 
-struct WsStageMeta {
+struct alignas(16) WsStageMeta {
     int kind;
     int any_absent;          // some row has no key (its V is zeroed)
     int mask;                // kMaskNone / kMaskRange / kMaskKeys
     int kbase;               // kMaskRange: position of key 0
+    int sc_off;              // INT8 cache tile: row 0's scale in the stage's scale area
     int pos[kWsKeys];        // position of each row, -1 = none
 };
+
+// the barriers follow the stages' records: whole 16-byte records keep them aligned
+static_assert(sizeof(WsStageMeta) % 16 == 0, "stage records keep the barriers aligned");
 
 struct WsBars {
     uint64_t full[4], ready[4], empty[4];
     uint64_t s_full[2][2], s_free[2][2], p_full[2], o_done[2], q_ready[2], fin;
+    uint64_t fixb;           // INT8 with read-time RoPE: the fix-up threads, between expansion and rotation
     uint32_t tmem;
     int ntiles;              // set when the producer's end marker reaches the MMA thread
     int abort;
@@ -198,9 +208,10 @@ __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile
 
 }  // namespace
 
-template <int D, bool READ>
+template <int D, bool READ, bool Q8>
 __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
     prefill_ws_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ PrefillMaps maps) {
+    static_assert(!Q8 || D >= 128, "INT8 rows are whole 128-code boxes");
     using S = WsShape<D>;
     constexpr int NQ = S::NQ, NST = S::STAGES, CB = S::CB;
     extern __shared__ unsigned char ws_raw[];
@@ -243,6 +254,7 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
             mbar_init(&bars->q_ready[i], kWsRows);
         }
         mbar_init(&bars->fin, 1);
+        mbar_init(&bars->fixb, 64);
         bars->ntiles = 0x7fffffff;
         bars->abort = 0;
         mbar_fence_init();
@@ -263,6 +275,13 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
     ws_fence_after();
     const uint32_t tmem = bars->tmem;
     const long long unit = (long long)b * p.Hkv + h;
+    // INT8 cache tiles: the codes of 128 columns (hh) of K or V (kv) land in the
+    // stage's upper column blocks, 64 rows of 128 bytes, and are expanded in
+    // place (see the fix-up role); their row scales go to the scale area
+    auto code_at = [&](int s, int hh, int kv) -> unsigned char* {
+        return sm + S::OffStage + s * S::StageBytes + (CB / 2 + hh) * S::KVBlock + kv * (kWsKeys * 128);
+    };
+    float* sc_area = reinterpret_cast<float*>(sm + S::OffScale);
     auto give_up = [&]() {
         if (!*abort) {
             bars->abort = 1;
@@ -316,10 +335,27 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
                 meta[s].any_absent = absent;
                 meta[s].mask = (absent || partial) ? kMaskKeys : kMaskNone;
                 unsigned char* dst = sm + S::OffStage + s * S::StageBytes;
-                mbar_expect_tx(&bars->full[s], (uint32_t)S::StageBytes);
-                if (maps.slot_whole) {
+                if constexpr (Q8) {
+                    // codes by 128-column boxes; scales of the rows inside the half
+                    // (a multiple of 4: whole 16-byte copies)
+                    const long long urow = unit_base() + slot0, base4 = urow & ~3LL;
+                    const int nsc = (int)min((long long)S::ScRows, p.half_rows - base4);   // a multiple of 4
+                    meta[s].sc_off = (int)(urow - base4);
+                    mbar_expect_tx(&bars->full[s], (uint32_t)(2 * (D / 128) * kWsKeys * 128 + 2 * nsc * 4));
+#pragma unroll
+                    for (int hh = 0; hh < D / 128; ++hh)
+#pragma unroll
+                        for (int kv = 0; kv < 2; ++kv)
+                            tma_load_4d(code_at(s, hh, kv), &maps.slot, 128 * hh, (int)urow, kv, p.layer, &bars->full[s]);
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv)
+                        bulk_load(sc_area + (s * 2 + kv) * S::ScRows, p.scales + p.sc_layer_off + kv * p.sc_kv_off + base4,
+                                  (uint32_t)(nsc * 4), &bars->full[s]);
+                } else if (maps.slot_whole) {
+                    mbar_expect_tx(&bars->full[s], (uint32_t)S::StageBytes);
                     tma_load_5d(dst, &maps.slot, 0, (int)(unit_base() + slot0), 0, p.layer, 0, &bars->full[s]);
                 } else {
+                    mbar_expect_tx(&bars->full[s], (uint32_t)S::StageBytes);
 #pragma unroll
                     for (int cb = 0; cb < CB; ++cb)
                         tma_load_4d(dst + cb * S::KVBlock, &maps.slot, cb * 64, (int)(unit_base() + slot0), 0, p.layer,
@@ -364,21 +400,37 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
                         const int blb = base + src;
                         if (fill == 0) s = acquire();
                         if (!ok) break;
+                        if (Q8 && fill == 0 && lane == 0) meta[s].sc_off = 0;   // block rows: multiples of 8
                         // rows of this block: positions blb * bs + r, keys up to t0
                         for (int r = lane; r < bs; r += 32) {
                             const int q = blb * bs + r;
                             meta[s].pos[fill * bs + r] = q <= t0 ? q : -1;
                         }
                         if (lane == 0) {
-                            mbar_expect_tx(&bars->full[s], (uint32_t)(bs * D * 4));
-                            unsigned char* dst = sm + S::OffStage + s * S::StageBytes + fill * bs * 128;
                             const int row = (int)(((long long)ph * p.Hkv + h) * bs);
+                            if constexpr (Q8) {
+                                mbar_expect_tx(&bars->full[s], (uint32_t)(2 * (D / 128) * bs * 128 + 2 * bs * 4));
 #pragma unroll
-                            for (int cb = 0; cb < CB; ++cb)
+                                for (int hh = 0; hh < D / 128; ++hh)
+#pragma unroll
+                                    for (int kv = 0; kv < 2; ++kv)
+                                        tma_load_4d(code_at(s, hh, kv) + fill * bs * 128, &maps.block, 128 * hh, row, kv,
+                                                    p.layer, &bars->full[s]);
 #pragma unroll
                                 for (int kv = 0; kv < 2; ++kv)
-                                    tma_load_4d(dst + cb * S::KVBlock + kv * kWsKeys * 128, &maps.block, cb * 64, row, kv,
-                                                p.layer, &bars->full[s]);
+                                    bulk_load(sc_area + (s * 2 + kv) * S::ScRows + fill * bs,
+                                              p.scales + p.sc_layer_off + kv * p.sc_kv_off + row, (uint32_t)(bs * 4),
+                                              &bars->full[s]);
+                            } else {
+                                mbar_expect_tx(&bars->full[s], (uint32_t)(bs * D * 4));
+                                unsigned char* dst = sm + S::OffStage + s * S::StageBytes + fill * bs * 128;
+#pragma unroll
+                                for (int cb = 0; cb < CB; ++cb)
+#pragma unroll
+                                    for (int kv = 0; kv < 2; ++kv)
+                                        tma_load_4d(dst + cb * S::KVBlock + kv * kWsKeys * 128, &maps.block, cb * 64, row,
+                                                    kv, p.layer, &bars->full[s]);
+                            }
                         }
                         if (++fill == per) {
                             __syncwarp();
@@ -450,6 +502,7 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
     } else if (warp == 2 || warp == 3) {
         // ============================ fix-up ===============================
         const int ft = tid - 64;                       // 0 .. 63
+        uint32_t fix_phase = 0;
         for (int j = 0;; ++j) {
             const int s = j % NST;
             if (!ws_wait(&bars->full[s], (j / NST) & 1, abort)) {
@@ -460,6 +513,46 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
             unsigned char* st = sm + S::OffStage + s * S::StageBytes;
             if (kind != kTileEnd) {
                 bool wrote = false;
+                if constexpr (Q8) {
+                    if (kind != kTileStage) {
+                        // row ft of the cache tile: code x row scale to bf16, in the
+                        // stage's K / V layout.  Column boxes go in order: box hh
+                        // overwrites (in blocks 2 hh, 2 hh + 1) only this row's codes
+                        // of boxes < hh and its own, each already read.
+                        const float* scs = sc_area + s * 2 * S::ScRows + meta[s].sc_off;
+                        const float scl[2] = {scs[ft], scs[S::ScRows + ft]};
+#pragma unroll
+                        for (int hh = 0; hh < D / 128; ++hh) {
+#pragma unroll
+                            for (int kv = 0; kv < 2; ++kv) {
+                                const uint4* src = reinterpret_cast<const uint4*>(code_at(s, hh, kv) + ft * 128);
+                                uint4 cw[8];
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) cw[q] = src[q];
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    const uint32_t w4[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+#pragma unroll
+                                    for (int hf = 0; hf < 2; ++hf) {
+                                        uint32_t o[4];
+#pragma unroll
+                                        for (int e = 0; e < 2; ++e) {
+                                            const uint32_t w = w4[2 * hf + e];
+                                            o[2 * e] = pack_bf16x2((float)(int8_t)(w & 0xffu) * scl[kv],
+                                                                   (float)(int8_t)((w >> 8) & 0xffu) * scl[kv]);
+                                            o[2 * e + 1] = pack_bf16x2((float)(int8_t)((w >> 16) & 0xffu) * scl[kv],
+                                                                       (float)(int8_t)(w >> 24) * scl[kv]);
+                                        }
+                                        const int ch = 16 * hh + 2 * q + hf;     // 8-column chunk of the row
+                                        *reinterpret_cast<uint4*>(st + ws_off(ft, ch) + kv * (kWsKeys * 128)) =
+                                            make_uint4(o[0], o[1], o[2], o[3]);
+                                    }
+                                }
+                            }
+                        }
+                        wrote = true;
+                    }
+                }
                 if (meta[s].any_absent) {
                     // V rows of absent keys to zero: 64 threads, one row each
                     if (meta[s].pos[ft] < 0) {
@@ -471,6 +564,15 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
                                     make_uint4(0u, 0u, 0u, 0u);
                     }
                     wrote = true;
+                }
+                if constexpr (READ && Q8) {
+                    // the rotation below reads rows other threads expanded
+                    mbar_arrive(&bars->fixb);
+                    if (!ws_wait(&bars->fixb, fix_phase & 1, abort)) {
+                        give_up();
+                        break;
+                    }
+                    ++fix_phase;
                 }
                 if constexpr (READ) {
                     // raw K rows rotated at their positions: thread ft takes the
@@ -831,7 +933,7 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::TmemCols) : "memory");
 }
 
-template <int D, bool READ>
+template <int D, bool READ, bool Q8>
 static cudaError_t launch_prefill_ws_t(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream) {
     constexpr int kSmem = ws_smem_bytes<D>();
     static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
@@ -841,24 +943,26 @@ static cudaError_t launch_prefill_ws_t(const PrefillParams& p, const PrefillMaps
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_relaxed) & bit)) {
-        e = cudaFuncSetAttribute(prefill_ws_kernel<D, READ>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        e = cudaFuncSetAttribute(prefill_ws_kernel<D, READ, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_relaxed);
     }
     const int tok = kWsRows / p.G * WsShape<D>::NQ;
     dim3 grid((p.T + tok - 1) / tok, p.Hkv, p.B);
-    prefill_ws_kernel<D, READ><<<grid, WsShape<D>::Threads, kSmem, stream>>>(p, maps);
+    prefill_ws_kernel<D, READ, Q8><<<grid, WsShape<D>::Threads, kSmem, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_ws(int head_dim, const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream) {
+cudaError_t launch_prefill_ws(int head_dim, bool q8, const PrefillParams& p, const PrefillMaps& maps,
+                              cudaStream_t stream) {
     if (p.G < 1 || kWsRows % p.G) return cudaErrorInvalidValue;
     const bool rd = p.rope == kRopeRead;
-    if (head_dim == 64) return rd ? launch_prefill_ws_t<64, true>(p, maps, stream) : launch_prefill_ws_t<64, false>(p, maps, stream);
-    if (head_dim == 128)
-        return rd ? launch_prefill_ws_t<128, true>(p, maps, stream) : launch_prefill_ws_t<128, false>(p, maps, stream);
-    if (head_dim == 256)
-        return rd ? launch_prefill_ws_t<256, true>(p, maps, stream) : launch_prefill_ws_t<256, false>(p, maps, stream);
+#define KVC_WS(DD, RD, Q) \
+    if (head_dim == DD && rd == RD && q8 == Q) return launch_prefill_ws_t<DD, RD, Q>(p, maps, stream);
+    KVC_WS(64, false, false) KVC_WS(64, true, false)
+    KVC_WS(128, false, false) KVC_WS(128, true, false) KVC_WS(128, false, true) KVC_WS(128, true, true)
+    KVC_WS(256, false, false) KVC_WS(256, true, false) KVC_WS(256, false, true) KVC_WS(256, true, true)
+#undef KVC_WS
     return cudaErrorInvalidValue;
 }
 

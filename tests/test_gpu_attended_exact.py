@@ -214,6 +214,9 @@ def _run_prefill(kvc, p, pos0, T, table=None, valid_bits=None):
     q = torch.randn((B, T, Hq, D), generator=torch.Generator().manual_seed(9)).bfloat16().cuda()
     k = torch.zeros((B, T, Hkv, D), dtype=torch.bfloat16, device="cuda")
     pos = torch.from_numpy(np.asarray(pos0, dtype=np.int32)).cuda()
+    # the chunk's one-hot V: 127/128 on an INT8 cache, which stores it as the
+    # code 127 of scale 2^-7 and reads it back exactly, like the cached rows
+    one = 127.0 / 128.0 if p.dtype == "i8" else 1.0
     for ps in range(p.passes):
         p.fill(ps)
         v = torch.zeros((B, T, Hkv, D), dtype=torch.bfloat16)
@@ -224,15 +227,18 @@ def _run_prefill(kvc, p, pos0, T, table=None, valid_bits=None):
                     continue
                 h = e // D - ps * Hkv
                 if 0 <= h < Hkv:
-                    v[b, i, h, e % D] = 1.0
+                    v[b, i, h, e % D] = one
         out = kvc.prefill(d, p.cache, 0, q, k, v.cuda(), pos, ws, block_table=table, valid_bits=valid_bits)
         p.compare(out.view(B * T, Hq, D), ps, f"prefill pass {ps}")
     assert kvc.get_error(ws) == 0
 
 
-@pytest.mark.parametrize("D,rope,sinks", [(128, "baked", 0), (128, "read_time", 4), (64, "none", 0),
-                                          (64, "read_time", 4), (256, "baked", 0), (256, "read_time", 4)])
-def test_prefill_window_sets_exact(kvc, D, rope, sinks):
+@pytest.mark.parametrize("D,rope,sinks,dtype", [(128, "baked", 0, "bf16"), (128, "read_time", 4, "bf16"),
+                                                (64, "none", 0, "bf16"), (64, "read_time", 4, "bf16"),
+                                                (256, "baked", 0, "bf16"), (256, "read_time", 4, "bf16"),
+                                                (128, "baked", 0, "i8"), (128, "read_time", 4, "i8"),
+                                                (256, "read_time", 4, "i8")])
+def test_prefill_window_sets_exact(kvc, D, rope, sinks, dtype):
     """Ring and sink+ring chunks before, across and far past the first wrap,
     with left padding; ids: sinks keep their position, window positions count
     from the oldest one any chunk token can see."""
@@ -241,7 +247,7 @@ def test_prefill_window_sets_exact(kvc, D, rope, sinks):
     T = 128
     pos0 = np.array([-5, 0, 100, C - 64, C + 3, 3 * C + 77, 987654 - T], dtype=np.int64)
     B = len(pos0)
-    d = kvc.make_desc("sink_ring" if sinks else "ring", rope, "bf16", 1, B, Hq, Hkv, D, window=W, sinks=sinks)
+    d = kvc.make_desc("sink_ring" if sinks else "ring", rope, dtype, 1, B, Hq, Hkv, D, window=W, sinks=sinks)
     cache = kvc.alloc_cache(d, fill=NAN)
     ids = np.full((B, C), -1, dtype=np.int64)
     chunk_id = np.full((B, T), -1, dtype=np.int64)
@@ -270,8 +276,9 @@ def test_prefill_window_sets_exact(kvc, D, rope, sinks):
     _run_prefill(kvc, p, pos0, T)
 
 
-@pytest.mark.parametrize("D,bs", [(128, 16), (64, 16), (256, 64), (128, 32)])
-def test_prefill_paged_sets_exact(kvc, D, bs):
+@pytest.mark.parametrize("D,bs,dtype", [(128, 16, "bf16"), (64, 16, "bf16"), (256, 64, "bf16"), (128, 32, "bf16"),
+                                        (128, 16, "i8"), (256, 64, "i8")])
+def test_prefill_paged_sets_exact(kvc, D, bs, dtype):
     """Paged chunks over a table with a shared prefix, holes and invalid
     blocks; the chunk's own blocks mapped and resident; ids = positions."""
     rng = np.random.default_rng(21 + D + bs)
@@ -289,7 +296,7 @@ def test_prefill_paged_sets_exact(kvc, D, bs):
             if table[b, lb] < 0 or shared:
                 table[b, lb] = free.pop()
             valid[table[b, lb]] = True
-    d = kvc.make_desc("paged", "baked", "bf16", 1, B, Hq, Hkv, D, block_size=bs, num_blocks=nb,
+    d = kvc.make_desc("paged", "baked", dtype, 1, B, Hq, Hkv, D, block_size=bs, num_blocks=nb,
                       max_blocks_per_seq=maxb)
     cache = kvc.alloc_cache(d, fill=NAN)
     ids = np.full((nb, bs), -1, dtype=np.int64)

@@ -9,7 +9,9 @@ chunk overwrites were read before they were overwritten).  Cases: ring with a
 chunk across the first wrap and far past it, sink + ring, paged with shared
 prefix blocks, a chunk that starts at position 0, ragged chunk lengths (not a
 multiple of the 16 tokens a CTA takes), left padding, RoPE none, baked and read
-at in-cache positions.
+at in-cache positions; INT8 caches (ring, sink + ring with baked and read-time
+RoPE, paged, head_dim 128 and 256), whose keys and values are compared with the
+oracle as the cache reads them back.
 """
 
 import dataclasses
@@ -75,9 +77,15 @@ def _run(kvc, wl, pos0, T, layer=0):
 def _oracle(wl, b, pos0, T, q, layer=0):
     N = max(pos0 + T, 1)
     K, V = wl.kv_history(layer, b, np.arange(N))
+    K, V = K.double().numpy(), V.double().numpy()
+    if wl.dtype == "i8":
+        # rows as an INT8 cache reads them back; baked keys are quantised after
+        # rotation, inside the oracle
+        V = oracle.quant.store_i8(V)
+        if wl.rope != "baked":
+            K = oracle.quant.store_i8(K)
     spec = dict(rope=wl.rope, base=wl.rope_base, storage=wl.dtype, sinks=wl.sinks, window=wl.window)
-    return prefill_sequence(q[b].double().numpy(), K.double().numpy(), V.double().numpy(), pos0,
-                            _attended_fn(wl, b), **spec)
+    return prefill_sequence(q[b].double().numpy(), K, V, pos0, _attended_fn(wl, b), **spec)
 
 
 CASES = {
@@ -100,6 +108,17 @@ CASES = {
     "sink_read_d256": ("sink_window_bf16", "read_time", [3, 180, 987600], 45, {"head_dim": 256}),
     # a chunk longer than the window: the pre-tile kernels take it
     "ring_chunk_past_window": ("ring_bf16", "baked", [150, 190, 4300], 230),
+    # INT8 caches: cached keys expanded from codes in the kernel, the chunk's
+    # own rows staged as the cache reads them back
+    "ring_i8": ("ring_int8", "baked", [150, 190, 4300], 37),
+    "ring_i8_none": ("ring_int8", "none", [0, 64, 1000], 70),
+    "sink_i8_read": ("sink_window_int8", "read_time", [3, 180, 987600], 45),
+    "sink_i8_baked": ("sink_window_int8", "baked", [3, 180, 987600], 45),
+    "ring_i8_d256": ("ring_int8", "baked", [150, 190, 4300], 37, {"head_dim": 256}),
+    # a capacity that is not a multiple of 4: tiles' row scales start off a
+    # 16-byte boundary
+    "ring_i8_odd_capacity": ("ring_int8", "baked", [150, 190, 4300], 37, {"window": 198}),
+    "sink_i8_read_d256": ("sink_window_int8", "read_time", [3, 180, 987600], 45, {"head_dim": 256}),
 }
 
 
@@ -112,14 +131,15 @@ def test_prefill_window_layouts(kvc, case):
     for b in range(wl.batch):
         ref = _oracle(wl, b, pos0[b], T, q)
         err = float(np.abs(got[b] - ref).max())
-        assert err <= TOL["bf16"], (case, b, err)
+        assert err <= TOL[wl.dtype], (case, b, err)
     a, r = st.cache.float(), ref_cache.float()
     same = (a == r) | (torch.isnan(a) & torch.isnan(r))
     assert bool(same.all())
 
 
-def test_prefill_paged_shared_prefix(kvc):
-    wl = kvc_synth.make_workload("paged_shared_prefix_bf16", small=True)
+@pytest.mark.parametrize("name", ["paged_shared_prefix_bf16", "paged_shared_prefix_int8"])
+def test_prefill_paged_shared_prefix(kvc, name):
+    wl = kvc_synth.make_workload(name, small=True)
     T = 29
     pos0 = [max(int(t) - T + 1, 0) for t in wl.positions]     # the chunk ends at each sequence's mapped tail
     got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
@@ -128,7 +148,7 @@ def test_prefill_paged_shared_prefix(kvc):
         Tb = min(T, int(wl.positions[b]) + 1 - pos0[b])         # rows past the mapped tail are not compared
         ref = _oracle(wl, b, pos0[b], T, q)
         err = float(np.abs(got[b, :Tb] - ref[:Tb]).max())
-        assert err <= TOL["bf16"], (b, err)
+        assert err <= TOL[wl.dtype], (b, err)
 
 
 def test_prefill_left_padding(kvc):
@@ -152,3 +172,15 @@ def test_prefill_long_context_pool_d256(kvc):
     assert np.isfinite(got).all()
     ref = _oracle(wl, 0, pos0[0], T, q)
     assert float(np.abs(got[0] - ref).max()) <= TOL["bf16"]
+
+
+def test_prefill_long_context_pool_int8_d256(kvc):
+    """The pool's shape over an INT8 cache (head_dim 256, 64-token blocks, NaN
+    scales in the non-resident slots)."""
+    wl = kvc_synth.as_int8(kvc_synth.make_workload("long_context_pool_bf16", small=True), "long_context_pool_int8_small")
+    T = 96
+    pos0 = [int(wl.positions[0]) - T + 1]
+    got, st, ref_cache, q, _, _ = _run(kvc, wl, pos0, T)
+    assert np.isfinite(got).all()
+    ref = _oracle(wl, 0, pos0[0], T, q)
+    assert float(np.abs(got[0] - ref).max()) <= TOL["i8"]

@@ -181,8 +181,9 @@ def test_argument_errors_return_codes_without_launching(kvc):
     assert L.kvc_block_release(dg, A, None, A, A, A, -1, A, A, nws, None) == kvc.KVC_ERR_ARG
     assert L.kvc_block_release(dg, A, None, A, A, None, 1, A, A, nws, None) == kvc.KVC_ERR_NULL
     assert "free" in kvc.strerror(kvc.KVC_DEV_NO_FREE_BLOCK)
-    # chunked prefill: bf16 caches (fp32 and INT8 refused), head_dim 64 / 128 / 256; a
-    # head_dim 256 paged cache needs blocks that pack a 64-key tile; sizes checked first
+    # chunked prefill: bf16 and INT8 caches (fp32 refused), head_dim 64 / 128 / 256; a
+    # head_dim 256 paged cache needs blocks that pack a 64-key tile, an INT8 cache
+    # a chunk no longer than its window; sizes checked first
     pw = kvc.prefill_workspace_bytes(d, 16)
     assert pw > ws_n and kvc.prefill_workspace_bytes(d, 0) == 0
     assert L.kvc_prefill(dp, A, 0, A, A, A, 0, A, None, None, A, A, pw, None) == kvc.KVC_ERR_ARG
@@ -191,7 +192,7 @@ def test_argument_errors_return_codes_without_launching(kvc):
     df = _desc(kvc, dtype="f32")
     assert L.kvc_prefill(ctypes.byref(df), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
         kvc.KVC_ERR_UNSUPPORTED
-    d8 = _desc(kvc, dtype="i8")
+    d8 = _desc(kvc, dtype="i8", window=8)             # 3 * 2 * 8 rows per half: a multiple of 4
     assert L.kvc_prefill(ctypes.byref(d8), A, 0, A, A, A, 16, A, None, None, A, A, 1 << 30, None) == \
         kvc.KVC_ERR_UNSUPPORTED
     d256p = _desc(kvc, head_dim=256, layout="paged", rope="baked", block_size=12, num_blocks=10,
