@@ -119,8 +119,13 @@ struct SelfPlanArgs {
     int maxb, num_blocks, bs, nsplit;
 };
 
+// speculative: a plan made before the previous kernel in the stream has
+// finished, from the table as it stands, for prefetch hints only: it writes
+// nothing to global memory and reports no error.  `parity`: the phase of
+// `bar` this call's copies complete.
 static __device__ __noinline__ void self_plan_single(const SelfPlanArgs p, SelfPlan* sp, int* s_red,
-                                                     int32_t* s_tab, uint32_t* s_val, uint64_t* bar) {
+                                                     int32_t* s_tab, uint32_t* s_val, uint64_t* bar,
+                                                     uint32_t parity, bool speculative) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = kDecodeThreads / 32;
     constexpr int PER = kSelfPlanMax / kDecodeThreads;          // table entries per thread
@@ -144,9 +149,9 @@ static __device__ __noinline__ void self_plan_single(const SelfPlanArgs p, SelfP
         for (int i = tid; i < nvw; i += kDecodeThreads) s_val[i] = 0xffffffffu;
     }
     const int traw = __ldcg(p.pos);
-    if (!mbar_wait(bar, 0)) {
+    if (!mbar_wait(bar, parity)) {
         // the copies never landed: plan nothing (every share empty)
-        if (tid == 0) set_error(p.err, 0x8u /* KVC_DEV_TIMEOUT */);
+        if (tid == 0 && !speculative) set_error(p.err, 0x8u /* KVC_DEV_TIMEOUT */);
         for (int i = tid; i < maxb; i += kDecodeThreads) s_tab[i] = -1;
     }
     if (tid == 0) {
@@ -159,7 +164,7 @@ static __device__ __noinline__ void self_plan_single(const SelfPlanArgs p, SelfP
     const int t = clamp_paged_t(traw, maxb, p.bs);
     const int nb = t < 0 ? 0 : t / p.bs + 1;
     const int last_rows = t < 0 ? 0 : t - (nb - 1) * p.bs + 1;
-    const bool reporter = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    const bool reporter = !speculative && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
     bool bad = false;
     auto attended = [&](int e) -> bool {
         if (e >= nb) return false;
@@ -752,21 +757,50 @@ __global__ void __launch_bounds__(kDecodeThreads, decode_ctas_per_sm(Q8, PAGED, 
             }
         }
     }
-    // inputs written by earlier kernels (append, plan) are read only after this
-    pdl_wait();
-    pdl_launch_dependents();    // the combine kernel may start launching
-    __syncthreads();
     // one paged sequence: this CTA's share, planned here (no plan kernel)
     __shared__ SelfPlan s_plan;
     __shared__ int s_red[kDecodeThreads / 32];
+    int32_t* const s_tab = reinterpret_cast<int32_t*>(stage_base);
+    uint32_t* const s_val = reinterpret_cast<uint32_t*>(stage_base + kSelfPlanMax * 4);
     if constexpr (PAGED) {
         static_assert((size_t)NST * S::kStageBytes >= (size_t)(kSelfPlanMax + kSelfPlanValidWords) * 4,
                       "the stages hold the staged table and valid words");
         if (p.self_plan) {
+            // While the previous kernel finishes: the plan once on the table as
+            // it stands (its code and the table come into the SM's caches),
+            // and the first blocks of the share it gives prefetched into L2.
+            // Nothing of it is used after the wait, where the plan is made again.
+            __syncthreads();                     // the barriers above are set up
             const SelfPlanArgs a{p.table, p.valid, p.pos, p.err, const_cast<int2*>(p.seq_items),
                                  p.maxb, p.num_blocks, p.bs, p.nsplit};
-            self_plan_single(a, &s_plan, s_red, reinterpret_cast<int32_t*>(stage_base),
-                             reinterpret_cast<uint32_t*>(stage_base + kSelfPlanMax * 4), &s_plan_bar);
+            self_plan_single(a, &s_plan, s_red, s_tab, s_val, &s_plan_bar, 0, true);
+            if constexpr (!Q8) {
+                const int nblk = max(1, kSpecRows / p.bs);
+                if (warp == kConsumerWarps && lane < nblk && (int)blockIdx.x < s_plan.G && s_plan.rows > 0) {
+                    const int lbk = s_plan.lb + lane;
+                    const int phys = lane == 0 ? s_plan.phys : (lbk < p.maxb ? s_tab[lbk] : -1);
+                    if (phys >= 0 && phys < p.num_blocks) {
+                        const int r0 = lane == 0 ? s_plan.row : 0;
+                        const long long row = ((long long)phys * p.Hkv + kvh) * p.bs + r0;
+                        const char* k0 = static_cast<const char*>(p.cache) + (p.layer_off + row * D) * 2;
+                        bulk_prefetch_l2(k0, (uint32_t)((p.bs - r0) * D * 2));
+                        bulk_prefetch_l2(k0 + p.kv_off * 2, (uint32_t)((p.bs - r0) * D * 2));
+                    }
+                }
+            }
+            fence_proxy_async_smem();            // the staged table is read before it is copied again
+            __syncthreads();
+        }
+    }
+    // inputs written by earlier kernels (append, plan) are read only after this
+    pdl_wait();
+    pdl_launch_dependents();    // the combine kernel may start launching
+    __syncthreads();
+    if constexpr (PAGED) {
+        if (p.self_plan) {
+            const SelfPlanArgs a{p.table, p.valid, p.pos, p.err, const_cast<int2*>(p.seq_items),
+                                 p.maxb, p.num_blocks, p.bs, p.nsplit};
+            self_plan_single(a, &s_plan, s_red, s_tab, s_val, &s_plan_bar, 1, false);
         }
     }
 
