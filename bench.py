@@ -372,10 +372,10 @@ class ClockSampler:
 # capture per workload, and the digest of the kernel's sources
 # (KERNEL_TRAFFIC_FILES) they were taken on: reported only while those
 # sources are unchanged.
-KERNEL_TRAFFIC = {"ring_bf16": 137521664, "sink_window_bf16": 543171072,
-                  "paged_shared_prefix_bf16": 900302336, "long_context_pool_bf16": 153094144,
-                  "ring_int8": 69873408}
-KERNEL_TRAFFIC_SOURCES = "69ad45ef89365701209951fcb7e826d478c32492662b3cebbb062dced218d4b0"
+KERNEL_TRAFFIC = {"ring_bf16": 137733120, "sink_window_bf16": 543171072,
+                  "paged_shared_prefix_bf16": 835816960, "long_context_pool_bf16": 156326656,
+                  "ring_int8": 69896704}
+KERNEL_TRAFFIC_SOURCES = "1f057ea73a989aaf7bb3ecc95cb2521b7c4f353870ff5718cf4651c79eca2162"
 
 
 # the sources decode_mma_kernel and its launch are built from
