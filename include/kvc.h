@@ -154,9 +154,12 @@ KVC_API size_t kvc_cache_bytes(const kvc_desc* d);
 /* Bytes of workspace that kvc_append / kvc_decode_attention /
  * kvc_block_table_write / kvc_valid_write need for `d` (0 if `d` is invalid).
  * The workspace holds the device error word, split-K partial results and
- * per-(sequence, kv head) completion counters.  It must be zero-filled once
- * before first use (kvc_workspace_init); every call leaves it ready for the
- * next one.  Calls that share a workspace must not overlap on the GPU. */
+ * per-(sequence, kv head) completion counters, and for PAGED caches the
+ * step's plan (attended rows and an attended-block directory per sequence,
+ * the number of sequences reading each physical block) and the block
+ * manager's scratch.  It must be zero-filled once before first use
+ * (kvc_workspace_init); every call leaves it ready for the next one.  Calls
+ * that share a workspace must not overlap on the GPU. */
 KVC_API size_t kvc_workspace_bytes(const kvc_desc* d);
 
 /* Zero-fill `workspace` (cudaMemsetAsync on `stream`). */
