@@ -44,20 +44,19 @@ enum : int { kTileSlot = 0, kTileSink = 1, kTileBlocks = 2, kTileStage = 3, kTil
 template <int D>
 struct WsShape {
     static constexpr int NQ = D == 256 ? 1 : 2;
-    static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 2);
+    static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 4 : 2);
     static constexpr int CB = D / 64;                          // 64-column blocks of a row
     static constexpr int QBytes = kWsRows * D * 2;             // one Q tile
     static constexpr int KVBlock = 2 * kWsKeys * 128;          // one column block of K and V
     static constexpr int StageBytes = CB * KVBlock;            // K and V of 64 keys
-    static constexpr int PBytes = kWsRows * kWsKeys * 2;       // one P tile
     static constexpr int OffQ = 0;
     static constexpr int OffStage = OffQ + NQ * QBytes;
-    static constexpr int OffP = OffStage + STAGES * StageBytes;
+    static constexpr int OffP = OffStage + STAGES * StageBytes;   // (P lives in tensor memory)
     // INT8 caches: row scales of each stage's cache tile, [stage][K|V][68]:
     // copied from a row that is a multiple of 4 (whole 16-byte copies), the
     // tile's first row sc_off after it
     static constexpr int ScRows = kWsKeys + 4;
-    static constexpr int OffScale = OffP + NQ * PBytes;
+    static constexpr int OffScale = OffP;
     static constexpr int OffMeta = OffScale + STAGES * 2 * ScRows * 4;
     static constexpr int TmemCols = 512;
     static constexpr int SCol0 = NQ * D;                       // S buffers after the O tiles
@@ -118,6 +117,16 @@ __device__ __forceinline__ void ws_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// The same with A from tensor memory (a_tmem: lane = row, two 16-bit elements
+// along K per 32-bit column).
+__device__ __forceinline__ void ws_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -700,12 +709,14 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
                         break;
                     }
                     ws_fence_after();
-                    const uint32_t p_u = sm_u + S::OffP + i * S::PBytes;
+                    // P_i(j) in the S buffer it came from (bf16 pairs, 32 columns);
+                    // S of tile j + 2 reuses that buffer, issued after this P V
+                    const uint32_t p_t = tmem + S::SCol0 + (uint32_t)((i * 2 + (j & 1)) * kWsKeys);
                     const uint32_t v_u = stage_u(j) + kWsKeys * 128;
 #pragma unroll
                     for (int ks = 0; ks < kWsKeys / 16; ++ks)
-                        ws_mma(tmem + (uint32_t)(i * D), ws_sdesc(p_u + ks * 32, 16, 1024),
-                               ws_sdesc(v_u + ks * 16 * 128, S::KVBlock, 1024), kIdescO, (j > 0 || ks > 0));
+                        ws_mma_ts(tmem + (uint32_t)(i * D), p_t + (uint32_t)(ks * 8),
+                                  ws_sdesc(v_u + ks * 16 * 128, S::KVBlock, 1024), kIdescO, (j > 0 || ks > 0));
                     ws_commit(&bars->o_done[i]);
                 }
                 if (!ok) break;
@@ -783,7 +794,6 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
         write_q(sink_tile ? min(row_t, C - 1) : row_t);
 
         float m_run = -INFINITY, l_run = 0.f;
-        unsigned char* Ps = sm + S::OffP + qi * S::PBytes;
         int j = 0;
         bool ok = true;
         for (;; ++j) {
@@ -875,16 +885,15 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
                 }
                 ws_wait_st();
             }
-            // P row r: 64 keys = 8 chunks of 16 bytes, 128-byte swizzle
+            // P row r (bf16 pairs of the 64 keys) into the S buffer just read:
+            // the A operand of P V, in tensor memory
+            {
+                float pw[kWsKeys / 2];
 #pragma unroll
-            for (int ch = 0; ch < kWsKeys / 8; ++ch) {
-                const uint4 w = make_uint4(pack_bf16x2(sv[8 * ch], sv[8 * ch + 1]),
-                                           pack_bf16x2(sv[8 * ch + 2], sv[8 * ch + 3]),
-                                           pack_bf16x2(sv[8 * ch + 4], sv[8 * ch + 5]),
-                                           pack_bf16x2(sv[8 * ch + 6], sv[8 * ch + 7]));
-                *reinterpret_cast<uint4*>(Ps + r * 128 + (((ch ^ r) & 7) << 4)) = w;
+                for (int k2 = 0; k2 < kWsKeys / 2; ++k2) pw[k2] = __uint_as_float(pack_bf16x2(sv[2 * k2], sv[2 * k2 + 1]));
+                ws_st32(lane_base + scol, pw);
             }
-            fence_proxy_async_smem();
+            ws_wait_st();
             ws_fence_before();
             mbar_arrive(&bars->p_full[qi]);
         }
