@@ -16,12 +16,12 @@ constexpr int kStages = 4;                       // bulk-copy pipeline depth
 constexpr int kTargetCtas = 608;                 // 152 SMs x 2 CTAs x 2 waves
 constexpr int kStreamCtas = 304;                 // stream-K grid: 152 SMs x 2 CTAs
 // bf16 stream-K shares per persistent CTA (default).  Claiming several
-// shares in turn evens out CTAs that stream at different speeds (paged
-// batches: mixed lengths, shared-prefix blocks that hit in L2), at a fixed
-// cost per share (a segment start and a partial) that only long shares hide:
-// on the 64-sequence shared-prefix batch 2 shares per CTA measured 158.4 us,
-// 3 160.6, 4 166.6, 6 172.2.
-constexpr int kPagedShareFactor = 2;             // paged caches with >= kPagedShareBatch sequences
+// shares in turn would even out CTAs that stream at different speeds, but
+// every share costs a segment (a q load, a partial, a block walk): on the
+// 64-sequence shared-prefix batch one share per CTA measured 153.0 us, 2
+// 156.7, 3 160.6, 4 166.6, 6 172.2 -- so paged batches keep one, as the
+// other layouts do.
+constexpr int kPagedShareFactor = 1;             // paged caches with >= kPagedShareBatch sequences
 constexpr int kPagedShareBatch = 8;
 // bf16 ring / sink+ring stream-K partition: units charged to each sequence
 // for the start of its segment (a second segment costs a CTA a q load and a
