@@ -372,10 +372,10 @@ class ClockSampler:
 # capture per workload, and the digest of the kernel's sources
 # (KERNEL_TRAFFIC_FILES) they were taken on: reported only while those
 # sources are unchanged.
-KERNEL_TRAFFIC = {"ring_bf16": 137733120, "sink_window_bf16": 543171072,
-                  "paged_shared_prefix_bf16": 835816960, "long_context_pool_bf16": 156326656,
-                  "ring_int8": 69896704}
-KERNEL_TRAFFIC_SOURCES = "1f057ea73a989aaf7bb3ecc95cb2521b7c4f353870ff5718cf4651c79eca2162"
+KERNEL_TRAFFIC = {"ring_bf16": 137679616, "sink_window_bf16": 543395584,
+                  "paged_shared_prefix_bf16": 841479424, "long_context_pool_bf16": 156166144,
+                  "ring_int8": 70007552}
+KERNEL_TRAFFIC_SOURCES = "dcf56c7ec3c6a79febdb962c7d4ef07b95e6cf4c2075b4487a8ca60076ef4573"
 
 
 # the sources decode_mma_kernel and its launch are built from
