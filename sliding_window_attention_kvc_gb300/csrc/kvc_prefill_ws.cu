@@ -541,16 +541,23 @@ __global__ void __launch_bounds__(WsShape<D>::Threads, 1)
 #pragma unroll
                                 for (int q = 0; q < 8; ++q) {
                                     const uint32_t w4[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+                                    const float2 sc2 = make_float2(scl[kv], scl[kv]);
 #pragma unroll
                                     for (int hf = 0; hf < 2; ++hf) {
                                         uint32_t o[4];
 #pragma unroll
                                         for (int e = 0; e < 2; ++e) {
-                                            const uint32_t w = w4[2 * hf + e];
-                                            o[2 * e] = pack_bf16x2((float)(int8_t)(w & 0xffu) * scl[kv],
-                                                                   (float)(int8_t)((w >> 8) & 0xffu) * scl[kv]);
-                                            o[2 * e + 1] = pack_bf16x2((float)(int8_t)((w >> 16) & 0xffu) * scl[kv],
-                                                                       (float)(int8_t)(w >> 24) * scl[kv]);
+                                            // code c as the fp32 2^23 + (c + 128) (the byte under
+                                            // the exponent of 2^23), less 2^23 + 128: exact
+                                            const uint32_t x = w4[2 * hf + e] ^ 0x80808080u;
+#pragma unroll
+                                            for (int h2 = 0; h2 < 2; ++h2) {
+                                                float2 f = make_float2(
+                                                    __int_as_float(__byte_perm(x, 0x4B000000u, 0x7540u | (uint32_t)(2 * h2))),
+                                                    __int_as_float(__byte_perm(x, 0x4B000000u, 0x7540u | (uint32_t)(2 * h2 + 1))));
+                                                f = __fmul2_rn(__fadd2_rn(f, make_float2(-8388736.f, -8388736.f)), sc2);
+                                                o[2 * e + h2] = pack_bf16x2(f.x, f.y);
+                                            }
                                         }
                                         const int ch = 16 * hh + 2 * q + hf;     // 8-column chunk of the row
                                         *reinterpret_cast<uint4*>(st + ws_off(ft, ch) + kv * (kWsKeys * 128)) =
