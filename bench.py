@@ -263,14 +263,23 @@ class DecodeState:
                                out=self.out if out is None else out)
 
     def launches_per_step(self):
-        """Kernels one kvc_decode_step launches (fused append for bf16 / INT8 ring layouts)."""
-        bf16 = self.wl.dtype in ("bf16", "i8")     # the tensor-core kernel
-        paged = self.wl.layout == "paged"
-        n = 1                              # decode kernel
-        n += 1 if bf16 else 0              # combine kernel (bf16 stream-K)
-        n += 1 if paged else 0             # work plan
-        n += 1 if (paged or not bf16) else 0   # separate append kernel
-        return n
+        """Kernels one kvc_decode_step launches.  bf16 / INT8 caches: the
+        decode kernel (which writes the new token of window layouts) and its
+        combine kernel, plus a paged batch's plan kernel (which writes the new
+        tokens; a one-sequence paged cache whose table and valid words fit the
+        decode's shared memory, 5120 and 4096 words, is planned inside the
+        decode kernel).  fp32 caches: the decode kernel (its last CTA combines)
+        plus a separate append (window layouts) or the plan kernels (paged: one
+        for a single sequence of at most 4096 blocks, else two)."""
+        wl = self.wl
+        paged = wl.layout == "paged"
+        if wl.dtype in ("bf16", "i8"):
+            self_plan = (paged and wl.batch == 1 and wl.max_blocks_per_seq <= 5120
+                         and (wl.num_blocks + 31) // 32 <= 4096)
+            return 2 + (1 if paged and not self_plan else 0)
+        if paged:
+            return 1 + (1 if wl.batch == 1 and wl.max_blocks_per_seq <= 4096 else 2)
+        return 2
 
 
 class FastCalls:

@@ -50,3 +50,18 @@ def test_attended_count_matches_the_oracle_sets():
                     else:
                         ref = len(oracle.paged_attended(t, wl.block_table[b], wl.valid, wl.block_size))
                     assert bench.attended_count(wl, b, t) == ref, (name, b, t)
+
+
+def test_launches_per_step_follow_the_library():
+    """The launch count bench.py claims per kvc_decode_step, as the library's
+    host code launches them: a paged batch's plan kernel, the decode kernel and
+    its combine; window layouts and a one-sequence paged cache (planned in the
+    decode kernel): decode and combine; fp32 window caches: append and decode."""
+    class _St:
+        pass
+    want = {"paged_shared_prefix_bf16": 3, "paged_shared_prefix_int8": 3, "ring_bf16": 2, "sink_window_bf16": 2,
+            "ring_int8": 2, "sink_window_int8": 2, "long_context_pool_bf16": 2, "tiny_ring_sink_f32": 2}
+    for name, n in want.items():
+        st = _St()
+        st.wl = kvc_synth.make_workload(name)
+        assert bench.DecodeState.launches_per_step(st) == n, name
