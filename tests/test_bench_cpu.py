@@ -5,6 +5,7 @@ import argparse
 import json
 
 import bench
+import kvc_synth
 
 
 def test_reference_arm_line_keeps_the_contract():
