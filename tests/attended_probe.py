@@ -209,6 +209,7 @@ def paged_probe(kvc, *, dtype, Hq, Hkv, D, bs, num_blocks, table, valid, t, num_
         new_ids = []
         for b, tb in enumerate(t):
             ph, r = int(table[b, tb // bs]), int(tb % bs)
+            assert ph >= 0, f"sequence {b}: the new token's block is unmapped"
             new_ids.append(int(idmap[ph, r]))
             ids[ph, r] = -1                  # written by the call itself
     p = Probe(kvc, d, cache, ids, sets, new_ids)

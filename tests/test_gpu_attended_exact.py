@@ -351,6 +351,25 @@ def test_prefill_full_paged_workload_sets_exact(kvc):
     _run_prefill(kvc, p, pos0, T, table=torch.from_numpy(table).cuda())
 
 
+@pytest.mark.parametrize("num_splits,fused", [(0, False), (0, True), (7, False)])
+def test_paged_batch_over_64_sequences_sets_exact(kvc, num_splits, fused):
+    """A batch of more sequences than the decode CTAs keep rows for in
+    registers (64): the rest are reloaded per 32 when a CTA cuts its shares;
+    shared prefix, holes, invalid slots and an empty sequence as above."""
+    rng = np.random.default_rng(41)
+    B, bs, maxb = 70, 16, 64
+    nb = 3 + B * maxb
+    table, valid, t = _random_paged(rng, B, bs, maxb, nb, share=not fused, empty=not fused)
+    if fused:
+        for b in range(B):               # the new token's block: mapped and resident
+            if table[b, t[b] // bs] < 0:
+                t[b] = int(np.flatnonzero(table[b] >= 0)[-1]) * bs + bs // 2
+            valid[table[b, t[b] // bs]] = True
+    p = paged_probe(kvc, dtype="bf16", Hq=8, Hkv=2, D=128, bs=bs, num_blocks=nb, table=table, valid=valid, t=t,
+                    num_splits=num_splits, fused=fused)
+    run_decode(kvc, p, t)
+
+
 def test_paged_one_sequence_long_table_sets_exact(kvc):
     """One sequence whose table has more entries than the decode CTAs plan
     themselves (the plan kernel's single-sequence path): ids = row ranks."""
