@@ -213,12 +213,13 @@ KVC_API int kvc_decode_attention(const kvc_desc* d, const void* cache, int32_t l
 
 /* One decode step: kvc_append of the token at pos[b] (n_new = 1), then
  * kvc_decode_attention at pos[b], with the same arguments and results as
- * that pair of calls.  For bf16 and INT8 RING / SINK_RING caches, and PAGED
- * caches of one sequence, the append is fused into the attention kernel (the
- * CTA that reads the token's row writes it, with RoPE baked when BAKED, to the
- * cache and to its own copy of the tile); a PAGED batch's planning kernel
- * writes the tokens before the attention kernel reads; fp32 RING / SINK_RING
- * caches make the two calls in turn.
+ * that pair of calls.  For bf16 and INT8 caches, RING / SINK_RING and PAGED
+ * with one sequence (planned inside the attention kernel), the append is
+ * fused into the attention kernel (the CTA that reads the token's row writes
+ * it, with RoPE baked when BAKED, to the cache and to its own copy of the
+ * tile); on other PAGED caches the planning kernel writes the tokens before
+ * the attention kernel reads; fp32 RING / SINK_RING caches make the two calls
+ * in turn.
  *   k_new, v_new  [batch, kv_heads, head_dim], pre-RoPE, 16-byte aligned. */
 KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const void* q,
                             const void* k_new, const void* v_new, const int32_t* pos,
