@@ -382,9 +382,9 @@ class ClockSampler:
 # (KERNEL_TRAFFIC_FILES) they were taken on: reported only while those
 # sources are unchanged.
 KERNEL_TRAFFIC = {"ring_bf16": 137679616, "sink_window_bf16": 543395584,
-                  "paged_shared_prefix_bf16": 841479424, "long_context_pool_bf16": 156166144,
+                  "paged_shared_prefix_bf16": 842048256, "long_context_pool_bf16": 156166144,
                   "ring_int8": 70007552}
-KERNEL_TRAFFIC_SOURCES = "dcf56c7ec3c6a79febdb962c7d4ef07b95e6cf4c2075b4487a8ca60076ef4573"
+KERNEL_TRAFFIC_SOURCES = "f02be4f6134b2759b0e21e588a0edd73674ad22870749a437f767b62d27cc0d0"
 
 
 # the sources decode_mma_kernel and its launch are built from
