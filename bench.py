@@ -384,7 +384,7 @@ class ClockSampler:
 KERNEL_TRAFFIC = {"ring_bf16": 137679616, "sink_window_bf16": 543395584,
                   "paged_shared_prefix_bf16": 842048256, "long_context_pool_bf16": 156166144,
                   "ring_int8": 70007552}
-KERNEL_TRAFFIC_SOURCES = "f02be4f6134b2759b0e21e588a0edd73674ad22870749a437f767b62d27cc0d0"
+KERNEL_TRAFFIC_SOURCES = "24d88328106510f34575d45fb2800e534c79882dc6a5c05257f84bb13ded62e8"
 
 
 # the sources decode_mma_kernel and its launch are built from

@@ -128,7 +128,7 @@ static __device__ __noinline__ void self_plan_single(const SelfPlanArgs p, SelfP
                                                      uint32_t parity, bool speculative) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = kDecodeThreads / 32;
-    constexpr int PER = kSelfPlanMax / kDecodeThreads;          // table entries per thread
+    // warp w covers table entries [1024 w, 1024 w + 1024), one 32-entry group per step
     static_assert(NW * 1024 >= kSelfPlanMax, "the warps' ranges cover the table");
     const int maxb = p.maxb, nvw = (p.num_blocks + 31) >> 5;
     // the table and the valid words land in shared memory by bulk copies of
