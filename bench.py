@@ -1089,7 +1089,7 @@ def measure_prefill(args):
             "device_errors": kvc.get_error(ws)}
 
 
-def main(argv=None):
+def build_parser():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
@@ -1112,7 +1112,11 @@ def main(argv=None):
                     help="time a block-manager call instead of the decode step (separate JSON line)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per decode launch from an ncu capture of the current kernel")
-    args = ap.parse_args(argv)
+    return ap
+
+
+def main(argv=None):
+    args = build_parser().parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.measure == "block_prepare":

@@ -66,3 +66,42 @@ def test_launches_per_step_follow_the_library():
         st = _St()
         st.wl = kvc_synth.make_workload(name)
         assert bench.DecodeState.launches_per_step(st) == n, name
+
+
+def test_profile_commands_run_with_the_current_options_and_kernels():
+    """Every bench.py command quoted under profiles/ parses with the bench's
+    own options, and every ncu kernel filter there names a kernel defined in
+    the sources, so each summary can be re-made as written."""
+    import glob
+    import os
+    import re
+    import shlex
+
+    root = os.path.dirname(os.path.abspath(bench.__file__))
+    src = ""
+    for path in glob.glob(os.path.join(root, "sliding_window_attention_kvc_gb300", "csrc", "*")):
+        with open(path) as f:
+            src += f.read()
+    kernels = set()
+    for m in re.finditer(r"__global__", src):
+        # the first name followed by "(" that is not the launch-bounds qualifier
+        # or an expression inside it
+        for name in re.findall(r"\b(\w+)\s*\(", src[m.end():m.end() + 300]):
+            if name not in ("__launch_bounds__", "decode_ctas_per_sm"):
+                kernels.add(name)
+                break
+    assert {"decode_mma_kernel", "combine_streamk_kernel", "plan_rows_kernel", "prefill_ws_kernel"} <= kernels
+    ap = bench.build_parser()
+    commands = filters = 0
+    for path in sorted(glob.glob(os.path.join(root, "profiles", "*.md"))):
+        with open(path) as f:
+            text = f.read()
+        for m in re.finditer(r"python bench\.py([^`\n]*)", text):
+            argv = shlex.split(re.sub(r"\[[^\]]*\]", "", m.group(1)))   # drop optional parts in brackets
+            ap.parse_args(argv)
+            commands += 1
+        for m in re.finditer(r"-k regex:(\"[^\"]+\"|\S+)", text):
+            pat = re.compile(m.group(1).strip('"'))
+            assert any(pat.search(k) for k in kernels), (os.path.basename(path), m.group(1))
+            filters += 1
+    assert commands >= 10 and filters >= 5
