@@ -102,8 +102,8 @@ def lib() -> ctypes.CDLL:
         L.kvc_strerror.argtypes = [ctypes.c_int]
         L.kvc_strerror.restype = ctypes.c_char_p
         for name in ABI_FUNCTIONS:
-            if name not in ("kvc_cache_bytes", "kvc_workspace_bytes", "kvc_strerror", "kvc_pager_create",
-                            "kvc_pager_destroy"):
+            if name not in ("kvc_cache_bytes", "kvc_workspace_bytes", "kvc_prefill_workspace_bytes", "kvc_strerror",
+                            "kvc_pager_create", "kvc_pager_destroy"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib

@@ -50,6 +50,63 @@ def test_library_exports_every_declared_symbol(kvc):
         assert not [s for s in exported if s.startswith("cuda")], "CUDA runtime symbols leak out"
 
 
+def _header_without_comments():
+    with open(os.path.join(ROOT, "include", "kvc.h")) as f:
+        src = f.read()
+    return re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", src, flags=re.S))
+
+
+def test_binding_types_match_the_header(kvc):
+    """Every ctypes signature of the binding has the header's parameter count,
+    widths and pointer-ness, and the descriptor mirrors `kvc_desc` field by
+    field: a mismatch would pass the wrong bits through the ABI silently."""
+    src = _header_without_comments()
+    L = kvc.lib()
+    scalar = {"int32_t": ctypes.c_int32, "size_t": ctypes.c_size_t, "int": ctypes.c_int, "float": ctypes.c_float}
+    decls = re.findall(r"KVC_API\s+([\w\s\*]+?)\b(kvc_\w+)\s*\(([^)]*)\)\s*;", src)
+    assert {name for _, name, _ in decls} == set(kvc.ABI_FUNCTIONS)
+    for ret, name, params in decls:
+        fn = getattr(L, name)
+        ps = [" ".join(p.split()) for p in params.split(",") if p.strip()]
+        assert fn.argtypes is not None and len(fn.argtypes) == len(ps), (name, ps, fn.argtypes)
+        for p, t in zip(ps, fn.argtypes):
+            ctype = p.rsplit(" ", 1)[0].replace("const ", "").strip()
+            if "*" in p:
+                if ctype.startswith("kvc_desc"):
+                    assert t is ctypes.POINTER(kvc.KvcDesc), (name, p)
+                else:
+                    assert t is ctypes.c_void_p, (name, p, t)
+            else:
+                assert ctypes.sizeof(t) == ctypes.sizeof(scalar[ctype]) and t is not ctypes.c_void_p, (name, p, t)
+        ret = " ".join(ret.split())
+        want = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char*": ctypes.c_char_p,
+                "void": None, "kvc_pager*": ctypes.c_void_p}[ret]
+        assert fn.restype is want, (name, ret, fn.restype)
+    body = re.search(r"typedef struct\s*(?:\w+\s*)?\{(.*?)\}\s*kvc_desc\s*;", src, re.S).group(1)
+    fields = re.findall(r"(int32_t|float)\s+(\w+)\s*;", body)
+    assert [(n, scalar[t]) for t, n in fields] == list(kvc.KvcDesc._fields_)
+
+
+def test_sizes_above_2gib_come_back_whole(kvc):
+    """size_t results (cache, workspace and prefill workspace bytes) pass
+    through the binding without truncation to 32 bits."""
+    d = kvc.make_desc("paged", "baked", "bf16", 1, 4096, 32, 8, 128, block_size=16, num_blocks=1 << 20,
+                      max_blocks_per_seq=4096)
+    assert kvc.cache_bytes(d) == 2 * (1 << 20) * 8 * 16 * 128 * 2 > 2 ** 32
+    assert kvc.workspace_bytes(d) > 0
+    assert kvc.prefill_workspace_bytes(d, 256) > 2 ** 32
+
+
+def test_missing_library_fails_loudly(kvc, monkeypatch):
+    """Without libkvc.so every call raises: there is no CPU fallback."""
+    monkeypatch.setattr(kvc, "_lib", None)
+    monkeypatch.setattr(kvc, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libkvc.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        kvc.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        kvc.cache_bytes(_desc(kvc))
+
+
 def _desc(kvc, **kw):
     base = dict(layout="ring", rope="baked", dtype="bf16", layers=2, batch=3, q_heads=8, kv_heads=2,
                 head_dim=128, window=100)
