@@ -105,7 +105,10 @@ typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_I8 = 2 } kvc_dtype;
  * fp32 row scales, [layers, 2, batch, kv_heads, capacity] (or [layers, 2,
  * num_blocks, kv_heads, block_size]); kvc_cache_bytes counts both.
  * q_heads must be a multiple of kv_heads; q head h reads kv head
- * h / (q_heads / kv_heads) ([share] 2.2 and 4.1, grouped-query attention). */
+ * h / (q_heads / kv_heads) ([share] 2.2 and 4.1, grouped-query attention).
+ * Launch-grid limits (else KVC_ERR_DESC): batch <= 65535, P = q_heads / g4
+ * <= 65535 and batch * P < 2^31, where g4 is the largest of 4, 2, 1 that
+ * divides q_heads / kv_heads (q heads are processed in groups of g4). */
 typedef struct kvc_desc {
     int32_t layout;             /* kvc_layout */
     int32_t rope;               /* kvc_rope */

@@ -48,7 +48,10 @@ int check_desc(const kvc_desc* d, Geo* g) {
     g->G = d->q_heads / d->kv_heads;
     g->GH = (g->G % 4 == 0) ? 4 : ((g->G % 2 == 0) ? 2 : 1);
     g->nsub = g->G / g->GH;
-    if (d->batch > 65535 || d->kv_heads > 65535 || g->nsub > 65535) return KVC_ERR_DESC;
+    // launch-grid limits: sequences on x, (kv head, q-head group) pairs on y,
+    // and a 32-bit count of (sequence, pair) units
+    const long long pairs = (long long)d->kv_heads * g->nsub;
+    if (d->batch > 65535 || pairs > 65535 || d->batch * pairs > 0x7fffffffLL) return KVC_ERR_DESC;
     if (d->layout == KVC_LAYOUT_PAGED) {
         if (d->block_size < 1 || d->num_blocks < 1 || d->max_blocks_per_seq < 1) return KVC_ERR_DESC;
         if ((long long)d->block_size * d->max_blocks_per_seq > 0x7fffffffLL) return KVC_ERR_DESC;

@@ -156,6 +156,10 @@ def _documented_cache_bytes(f):
         return 0
     if f["head_dim"] not in (64, 128, 256) or f["num_splits"] < 0 or f["softmax_scale"] < 0:
         return 0
+    g = f["q_heads"] // f["kv_heads"]
+    pairs = f["q_heads"] // (4 if g % 4 == 0 else 2 if g % 2 == 0 else 1)
+    if f["batch"] > 65535 or pairs > 65535 or f["batch"] * pairs >= 2 ** 31:
+        return 0
     if rope != 0 and not f["rope_base"] > 0:
         return 0
     if layout == 2:                                   # PAGED
@@ -172,6 +176,24 @@ def _documented_cache_bytes(f):
     if dtype == 2:
         return elems + 4 * f["layers"] * 2 * rows     # codes, then one fp32 scale per row
     return elems * (4 if dtype == 0 else 2)
+
+
+def test_launch_grid_limits(kvc):
+    """Descriptors past the launch-grid limits of include/kvc.h are rejected
+    up front; those at the limits are accepted."""
+    L = kvc.lib()
+
+    def size(batch, q_heads, kv_heads):
+        d = kvc.make_desc("ring", "none", "bf16", 1, batch, q_heads, kv_heads, 64, window=1)
+        return L.kvc_cache_bytes(ctypes.byref(d))
+
+    assert size(1, 4 * 65535, 1) > 0                  # 65535 groups of 4 q heads
+    assert size(1, 4 * 65536, 1) == 0
+    assert size(1, 65535, 65535) > 0                  # one q head per kv head
+    assert size(1, 2 * 65536, 65536) == 0
+    assert size(65535, 8, 2) > 0 and size(65536, 8, 2) == 0
+    assert size(32768, 4 * 65535, 1) > 0              # 2^31 - 32768 units
+    assert size(32769, 4 * 65535, 1) == 0             # past 2^31
 
 
 def test_random_descriptors_follow_the_documented_rules(kvc):
