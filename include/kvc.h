@@ -306,7 +306,8 @@ KVC_API int kvc_valid_write(const kvc_desc* d, uint32_t* valid_bits, int32_t n,
  * and their valid bit (valid_bits may be NULL).  Errors (device bits): an
  * unmapped block entered mid-block (KVC_DEV_UNMAPPED_APPEND), a position past
  * the table (KVC_DEV_BAD_POSITION), an exhausted free list
- * (KVC_DEV_NO_FREE_BLOCK); the sequence is skipped. */
+ * (KVC_DEV_NO_FREE_BLOCK); the sequence is skipped.  Requires layers * 2 *
+ * kv_heads <= 65535 (the copy's launch grid), else KVC_ERR_UNSUPPORTED. */
 KVC_API int kvc_block_prepare(const kvc_desc* d, void* cache, const int32_t* pos, int32_t* block_table,
                               uint32_t* valid_bits, int32_t* refcount, int32_t* free_list, int32_t* free_count,
                               void* workspace, size_t workspace_bytes, void* stream);

@@ -858,6 +858,8 @@ KVC_API int kvc_block_prepare(const kvc_desc* d, void* cache, const int32_t* pos
     if (rc) return rc;
     if (!cache || !pos || !block_table || !refcount || !free_list || !free_count) return KVC_ERR_NULL;
     if (!aligned16(cache)) return KVC_ERR_ALIGN;
+    // the copy kernel's grid carries (layer, K|V, kv head) on y
+    if ((long long)d->layers * 2 * d->kv_heads > 65535) return KVC_ERR_UNSUPPORTED;
     kvc::BlockParams p;
     if ((rc = block_params(d, g, workspace, workspace_bytes, &p))) return rc;
     p.cache = cache;

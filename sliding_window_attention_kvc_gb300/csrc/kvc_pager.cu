@@ -181,6 +181,10 @@ KVC_API int kvc_pagein_issue(kvc_pager* pg, const kvc_desc* d, void* cache, cons
     if (d->dtype == KVC_I8) return KVC_ERR_UNSUPPORTED;   // host blocks hold no row scales
     if (n < 0) return KVC_ERR_ARG;
     if (n > 0 && (!cache || !host_kv || !in_block || !in_slot)) return KVC_ERR_NULL;
+    // every entry is checked before anything is recorded or copied
+    for (int i = 0; i < n; ++i)
+        if (in_block[i] < 0 || in_block[i] >= d->max_blocks_per_seq || in_slot[i] < 0 || in_slot[i] >= d->num_blocks)
+            return KVC_ERR_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVC_ERR_CUDA;
     if (pg->device != dev) {
@@ -200,8 +204,6 @@ KVC_API int kvc_pagein_issue(kvc_pager* pg, const kvc_desc* d, void* cache, cons
     if (cudaEventRecord(pg->after_compute, ks) != cudaSuccess) return KVC_ERR_CUDA;
     if (cudaStreamWaitEvent(cs, pg->after_compute, 0) != cudaSuccess) return KVC_ERR_CUDA;
     for (int i = 0; i < n; ++i) {
-        if (in_block[i] < 0 || in_block[i] >= d->max_blocks_per_seq || in_slot[i] < 0 || in_slot[i] >= d->num_blocks)
-            return KVC_ERR_ARG;
         // host: [logical block][layer][K|V][kv head][row][D]; device: [layer][K|V][slot][kv head][row][D]
         const char* src = static_cast<const char*>(host_kv) + (size_t)in_block[i] * d->layers * 2 * block_bytes;
         char* dst = static_cast<char*>(cache) + (size_t)in_slot[i] * block_bytes;

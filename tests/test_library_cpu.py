@@ -254,6 +254,10 @@ def test_argument_errors_return_codes_without_launching(kvc):
     assert L.kvc_block_prepare(dg, A, A, None, None, A, A, A, A, nws, None) == kvc.KVC_ERR_NULL
     assert L.kvc_block_prepare(dg, A + 8, A, A, None, A, A, A, A, nws, None) == kvc.KVC_ERR_ALIGN
     assert L.kvc_block_prepare(dg, A, A, A, None, A, A, A, A, nws - 1, None) == kvc.KVC_ERR_WORKSPACE
+    deep = _desc(kvc, layout="paged", rope="baked", layers=128, q_heads=256, kv_heads=256, block_size=16,
+                 num_blocks=10, max_blocks_per_seq=4)   # 128 * 2 * 256 copy rows: past the launch grid
+    assert L.kvc_block_prepare(ctypes.byref(deep), A, A, A, None, A, A, A, A, 1 << 40, None) == \
+        kvc.KVC_ERR_UNSUPPORTED
     assert L.kvc_block_share(dg, A, A, -1, A, A, A, A, nws, None) == kvc.KVC_ERR_ARG
     assert L.kvc_block_share(dg, A, A, 0, None, None, None, None, 0, None) == kvc.KVC_OK
     assert L.kvc_block_share(dg, A, A, 1, A, None, A, A, nws, None) == kvc.KVC_ERR_NULL

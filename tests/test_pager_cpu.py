@@ -89,3 +89,21 @@ def test_lru_random_steps_match_the_model(lib):
                     pg.plan(need, pinned)
                 continue
             assert pg.plan(need, pinned) == want
+
+
+def test_pagein_issue_rejects_bad_entries_before_any_copy(lib):
+    """A bad (block, slot) anywhere in the list is refused before any CUDA
+    call, so no copy of the list's good entries is issued either."""
+    import ctypes
+    d = kvc.make_desc("paged", "baked", "bf16", 2, 1, 8, 2, 128, block_size=16, num_blocks=8,
+                      max_blocks_per_seq=32)
+    pg = kvc.Pager(8)
+    A = 1 << 20                                   # fake addresses: never dereferenced on this path
+    arr = ctypes.c_int32 * 2
+    for blocks, slots in (([0, 32], [1, 2]), ([0, 3], [1, 8]), ([0, -1], [1, 2]), ([0, 3], [-1, 2])):
+        rc = lib.kvc_pagein_issue(pg._p, ctypes.byref(d), A, A, 2, arr(*blocks), arr(*slots), None, None)
+        assert rc == kvc.KVC_ERR_ARG, (blocks, slots, rc)
+    d8 = kvc.make_desc("paged", "baked", "i8", 2, 1, 8, 2, 128, block_size=16, num_blocks=8, max_blocks_per_seq=32)
+    assert lib.kvc_pagein_issue(pg._p, ctypes.byref(d8), A, A, 1, arr(0, 0), arr(1, 0), None, None) == \
+        kvc.KVC_ERR_UNSUPPORTED
+    pg.close()
