@@ -395,6 +395,17 @@ extern "C" KVC_API int kvc_append(const kvc_desc* d, void* cache, int32_t layer,
                                   int32_t n_new, const int32_t* pos, const int32_t* block_table, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+// The attention's pointer, alignment and layer checks (kvc_decode_attention,
+// kvc_decode_step, kvc_decode_attention_noalloc), made before anything is issued.
+static int decode_args(const kvc_desc* d, const void* cache, int32_t layer, const void* q, const int32_t* pos,
+                       const int32_t* block_table, const void* out) {
+    if (!cache || !q || !pos || !out) return KVC_ERR_NULL;
+    if (d->layout == KVC_LAYOUT_PAGED && !block_table) return KVC_ERR_NULL;
+    if (!aligned16(cache) || !aligned16(q) || !aligned16(out)) return KVC_ERR_ALIGN;
+    if (layer < 0 || layer >= d->layers) return KVC_ERR_ARG;
+    return KVC_OK;
+}
+
 static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, const void* q, const void* k_new,
                        const void* v_new, const int32_t* pos, const int32_t* block_table,
                        const uint32_t* valid_bits, void* out, void* workspace, size_t workspace_bytes,
@@ -402,11 +413,10 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     Geo g;
     int rc = check_desc(d, &g);
     if (rc) return rc;
-    if (!cache || !q || !pos || !out || !workspace) return KVC_ERR_NULL;
+    if ((rc = decode_args(d, cache, layer, q, pos, block_table, out))) return rc;
+    if (!workspace) return KVC_ERR_NULL;
+    if (!aligned16(workspace)) return KVC_ERR_ALIGN;
     const bool paged = d->layout == KVC_LAYOUT_PAGED;
-    if (paged && !block_table) return KVC_ERR_NULL;
-    if (!aligned16(cache) || !aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVC_ERR_ALIGN;
-    if (layer < 0 || layer >= d->layers) return KVC_ERR_ARG;
     const WorkspaceLayout w = ws_layout(d, g);
     if (workspace_bytes < w.total) return KVC_ERR_WORKSPACE;
     char* ws = static_cast<char*>(workspace);
@@ -454,6 +464,10 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, p.theta, p.theta_f);
 
     dim3 grid(d->dtype != KVC_F32 ? w.ctas : w.items, d->kv_heads, g.nsub);
+    // the tensor-core kernel's maps, encoded before anything is launched (a
+    // failure leaves the cache and the workspace untouched)
+    KvTensorMaps maps;
+    if (d->dtype != KVC_F32 && (rc = kv_maps_for(d, g, cache, &maps, &p.tma_whole))) return rc;
     // one paged sequence on the tensor-core kernel: its CTAs plan their own
     // shares from the block table and write the step's token themselves
     // (the CTAs bulk-copy the table and the valid words: 16-byte aligned buffers)
@@ -523,9 +537,6 @@ static int decode_impl(const kvc_desc* d, const void* cache, int32_t layer, cons
     }
     const bool rd = d->rope == KVC_ROPE_READ_INCACHE;
     if (d->dtype != KVC_F32) {
-        KvTensorMaps maps;
-        rc = kv_maps_for(d, g, cache, &maps, &p.tma_whole);
-        if (rc) return rc;
         if (launch_decode_mma(d->head_dim, g.GH, paged, rd, d->dtype == KVC_I8, p, maps, grid, s) != cudaSuccess)
             return KVC_ERR_CUDA;
         return KVC_OK;
@@ -712,6 +723,22 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
         ap.sc_layer_off = (long long)layer * 2 * half_rows;
         ap.sc_kv_off = half_rows;
     }
+    // the warp-specialised kernel's maps, encoded before anything is launched
+    PrefillMaps pm;
+    std::memset(&pm, 0, sizeof(pm));
+    if (ws_kernel) {
+        if (q8) {
+            if ((rc = encode_q8_code_map(d, g, cache, paged_l ? d->block_size : 64, paged_l ? &pm.block : &pm.slot)))
+                return rc;
+        } else if (paged_l) {
+            if ((rc = encode_block_map(d, g, cache, &pm.block))) return rc;
+        } else {
+            KvTensorMaps km;
+            if ((rc = kv_maps_for(d, g, cache, &km, &pm.slot_whole))) return rc;
+            pm.slot = km.run[kRunMaps - 1];                 // 64-row runs
+        }
+        if ((rc = encode_stage_map(d, kst, T, prefill_stage_bytes(d, T) / 2, &pm.stage))) return rc;
+    }
     // 1. the chunk's rows as the cache will hold them (INT8: as it reads them back)
     if (launch_prefill_stage(ap, kst, vst, s) != cudaSuccess) return KVC_ERR_CUDA;
     // 2. attention: earlier keys from the cache as it stands, the chunk's from the stage
@@ -749,19 +776,6 @@ KVC_API int kvc_prefill(const kvc_desc* d, void* cache, int32_t layer, const voi
     pp.half_rows = half_rows;
     if (d->rope != KVC_ROPE_NONE) fill_theta(d->head_dim, d->rope_base, pp.theta, nullptr);
     if (ws_kernel) {
-        PrefillMaps pm;
-        std::memset(&pm, 0, sizeof(pm));
-        if (q8) {
-            if ((rc = encode_q8_code_map(d, g, cache, paged_l ? d->block_size : 64, paged_l ? &pm.block : &pm.slot)))
-                return rc;
-        } else if (paged_l) {
-            if ((rc = encode_block_map(d, g, cache, &pm.block))) return rc;
-        } else {
-            KvTensorMaps km;
-            if ((rc = kv_maps_for(d, g, cache, &km, &pm.slot_whole))) return rc;
-            pm.slot = km.run[kRunMaps - 1];                 // 64-row runs
-        }
-        if ((rc = encode_stage_map(d, kst, T, prefill_stage_bytes(d, T) / 2, &pm.stage))) return rc;
         if (launch_prefill_ws(d->head_dim, q8, pp, pm, s) != cudaSuccess) return KVC_ERR_CUDA;
     } else if (launch_prefill(d->head_dim, g.G, pp, s) != cudaSuccess) {
         return KVC_ERR_CUDA;
@@ -793,6 +807,11 @@ KVC_API int kvc_decode_step(const kvc_desc* d, void* cache, int32_t layer, const
         return decode_impl(d, cache, layer, q, k_new, v_new, pos, block_table, valid_bits, out, workspace,
                            workspace_bytes, stream);
     }
+    // the attention's own arguments are checked before the append launches
+    if ((rc = decode_args(d, cache, layer, q, pos, block_table, out))) return rc;
+    if (!workspace) return KVC_ERR_NULL;
+    if (!aligned16(workspace)) return KVC_ERR_ALIGN;
+    if (workspace_bytes < ws_layout(d, g).total) return KVC_ERR_WORKSPACE;
     rc = kvc_append(d, cache, layer, k_new, v_new, 1, pos, block_table, workspace, workspace_bytes, stream);
     if (rc) return rc;
     return decode_impl(d, cache, layer, q, nullptr, nullptr, pos, block_table, valid_bits, out, workspace,
@@ -1024,6 +1043,7 @@ extern "C" KVC_API int kvc_decode_attention_noalloc(const kvc_desc* d, const voi
     Geo g;
     int rc = check_desc(d, &g);
     if (rc) return rc;
+    if ((rc = decode_args(d, cache, layer, q, pos, block_table, out))) return rc;
     const WorkspaceLayout w = ws_layout(d, g);
     if (w.total > (size_t)KVC_NOALLOC_SCRATCH_BYTES) return KVC_ERR_TOO_LARGE;
     void* scratch = nullptr;

@@ -284,6 +284,33 @@ def test_argument_errors_return_codes_without_launching(kvc):
         kvc.KVC_ERR_UNSUPPORTED
 
 
+def test_decode_arguments_are_checked_before_anything_is_issued(kvc):
+    """With no GPU any launch or copy fails with KVC_ERR_CUDA, so getting the
+    argument's own error code shows nothing was issued before the check: the
+    fp32 step's append, the no-allocation call's scratch clear."""
+    L = kvc.lib()
+    A = 1 << 20   # fake, 16-byte aligned "device" addresses: never dereferenced on these paths
+    for dtype in ("f32", "bf16"):
+        d = _desc(kvc, dtype=dtype)
+        dp, n = ctypes.byref(d), kvc.workspace_bytes(d)
+        step = lambda cache=A, layer=0, q=A, pos=A, out=A, ws=A, ws_n=n: L.kvc_decode_step(
+            dp, cache, layer, q, A, A, pos, None, None, out, ws, ws_n, None)
+        assert step(q=None) == kvc.KVC_ERR_NULL
+        assert step(out=None) == kvc.KVC_ERR_NULL
+        assert step(ws=None) == kvc.KVC_ERR_NULL
+        assert step(out=A + 4) == kvc.KVC_ERR_ALIGN
+        assert step(ws=A + 8) == kvc.KVC_ERR_ALIGN
+        assert step(layer=2) == kvc.KVC_ERR_ARG
+        assert step(ws_n=n - 1) == kvc.KVC_ERR_WORKSPACE
+        noalloc = lambda q=A, out=A, layer=0: L.kvc_decode_attention_noalloc(dp, A, layer, q, A, None, None, out,
+                                                                             None)
+        assert noalloc(q=None) == kvc.KVC_ERR_NULL
+        assert noalloc(out=A + 2) == kvc.KVC_ERR_ALIGN
+        assert noalloc(layer=-1) == kvc.KVC_ERR_ARG
+    dpg = _desc(kvc, layout="paged", rope="baked", block_size=16, num_blocks=10, max_blocks_per_seq=4)
+    assert L.kvc_decode_attention_noalloc(ctypes.byref(dpg), A, 0, A, A, None, None, A, None) == kvc.KVC_ERR_NULL
+
+
 def test_int8_views_cover_the_buffer(kvc):
     d = _desc(kvc, dtype="i8", window=100)
     buf = torch.zeros(kvc.cache_bytes(d), dtype=torch.uint8)
