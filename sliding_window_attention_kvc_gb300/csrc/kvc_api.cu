@@ -948,7 +948,9 @@ KVC_API const char* kvc_strerror(int code) {
         case KVC_OK: return "ok";
         case KVC_ERR_NULL: return "a required pointer is NULL";
         case KVC_ERR_DESC: return "inconsistent cache descriptor";
-        case KVC_ERR_UNSUPPORTED: return "unsupported combination (head_dim not 64/128/256, or PAGED with READ_INCACHE)";
+        case KVC_ERR_UNSUPPORTED:
+            return "unsupported combination of head_dim, cache dtype, layout and RoPE mode for this call, "
+                   "or past one of its launch limits";
         case KVC_ERR_ALIGN: return "pointer not 16-byte aligned";
         case KVC_ERR_WORKSPACE: return "workspace smaller than kvc_workspace_bytes()";
         case KVC_ERR_ARG: return "argument out of range";
