@@ -183,6 +183,31 @@ def test_tiny_ring_sink_f32_all_256_steps(kvc):
     assert worst <= TOL["f32"], worst
 
 
+def test_decode_step_f32_through_the_first_wrap(kvc):
+    """kvc_decode_step on an fp32 cache (kvc_append, then the attention, on
+    the same stream) from an empty cache past the first wrap of the window:
+    outputs within the fp32 tolerance of the oracle at every step, and the
+    cache bit-identical to one filled by kvc_append alone."""
+    wl = kvc_synth.make_workload("tiny_ring_sink_f32")
+    d = bench.workload_desc(wl, layers=1)
+    cache = kvc.alloc_cache(d, fill=float("nan"))
+    ref_cache = kvc.alloc_cache(d, fill=float("nan"))
+    ws = kvc.alloc_workspace(d)
+    worst = 0.0
+    for t in range(72):
+        k, v = wl.kv_history(0, 0, [t])                     # [1, kv_heads, D]
+        k, v = k.contiguous().cuda(), v.contiguous().cuda()
+        pos = torch.tensor([t], dtype=torch.int32, device="cuda")
+        q = wl.query(0, 0, t)[None].contiguous().cuda()
+        out = kvc.decode_step(d, cache, 0, q, k, v, pos, ws)
+        kvc.append(d, ref_cache, 0, k[None], v[None], pos, ws)
+        ref = oracle_outputs(wl, 0, positions=np.array([t]))[0]
+        worst = max(worst, _maxerr(out[0].float().cpu().numpy(), ref))
+    assert worst <= TOL["f32"], worst
+    assert torch.equal(torch.nan_to_num(cache, nan=7.0), torch.nan_to_num(ref_cache, nan=7.0))
+    assert kvc.get_error(ws) == 0
+
+
 @pytest.mark.parametrize("name", SMALL)
 @pytest.mark.parametrize("num_splits", [0, 1, 7])
 def test_decode_small_elementwise(kvc, name, num_splits):
