@@ -187,6 +187,15 @@ def _need(t: torch.Tensor, name: str, dtype=None, numel=None):
         raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
 
 
+def _need_cache(d: KvcDesc, cache: torch.Tensor):
+    """The cache tensor: the descriptor's element type and at least
+    kvc_cache_bytes(d) bytes (the library sees only its address)."""
+    need = cache_bytes(d)
+    if isinstance(cache, torch.Tensor) and cache.numel() * cache.element_size() < need:
+        raise ValueError(f"cache holds {cache.numel() * cache.element_size()} bytes, the descriptor needs {need}")
+    _need(cache, "cache", cache_dtype(d))
+
+
 def alloc_cache(d: KvcDesc, device="cuda", fill=None) -> torch.Tensor:
     """Caller-owned cache tensor of the layout's shape (uninitialised unless `fill`).
 
@@ -235,7 +244,7 @@ def append(d: KvcDesc, cache: torch.Tensor, layer: int, k_new: torch.Tensor, v_n
            pos: torch.Tensor, workspace: torch.Tensor, block_table: torch.Tensor | None = None, stream=None):
     """kvc_append: k_new / v_new [batch, n_new, kv_heads, D] (or [batch, kv_heads, D] for one token)."""
     dt = desc_dtype(d)
-    _need(cache, "cache", cache_dtype(d))
+    _need_cache(d, cache)
     _need(k_new, "k_new", dt)
     _need(v_new, "v_new", dt)
     _need(pos, "pos", torch.int32, d.batch)
@@ -257,7 +266,7 @@ def decode_attention(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tenso
                      stream=None) -> torch.Tensor:
     """kvc_decode_attention: q [batch, q_heads, D] -> out [batch, q_heads, D]."""
     dt = desc_dtype(d)
-    _need(cache, "cache", cache_dtype(d))
+    _need_cache(d, cache)
     _need(q, "q", dt, d.batch * d.q_heads * d.head_dim)
     _need(pos, "pos", torch.int32, d.batch)
     _need(workspace, "workspace", torch.uint8)
@@ -281,7 +290,7 @@ def decode_step(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, k_
                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """kvc_decode_step: append the token at pos (k_new / v_new [batch, kv_heads, D]) and attend."""
     dt = desc_dtype(d)
-    _need(cache, "cache", cache_dtype(d))
+    _need_cache(d, cache)
     _need(q, "q", dt, d.batch * d.q_heads * d.head_dim)
     _need(k_new, "k_new", dt, d.batch * d.kv_heads * d.head_dim)
     _need(v_new, "v_new", dt, d.batch * d.kv_heads * d.head_dim)
@@ -319,7 +328,7 @@ def prefill(d: KvcDesc, cache: torch.Tensor, layer: int, q: torch.Tensor, k_new:
             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """kvc_prefill: q [batch, T, q_heads, D], k_new / v_new [batch, T, kv_heads, D] -> out [batch, T, q_heads, D]."""
     dt = desc_dtype(d)
-    _need(cache, "cache", cache_dtype(d))
+    _need_cache(d, cache)
     _need(q, "q", dt)
     if q.numel() % (d.batch * d.q_heads * d.head_dim):
         raise ValueError("q must be [batch, T, q_heads, head_dim]")
@@ -386,6 +395,7 @@ class BlockState:
 
 def block_prepare(d: KvcDesc, cache: torch.Tensor, pos: torch.Tensor, state: BlockState,
                   workspace: torch.Tensor, stream=None):
+    _need_cache(d, cache)
     _need(pos, "pos", torch.int32, d.batch)
     _need(workspace, "workspace", torch.uint8)
     _check(lib().kvc_block_prepare(ctypes.byref(d), _ptr(cache), _ptr(pos), _ptr(state.table),
@@ -456,7 +466,16 @@ class Pager:
                "kvc_pager_evict")
 
     def issue(self, d: KvcDesc, cache, host_kv, pageins, copy_stream, compute_stream=None):
+        """Copy each (logical block, slot) of `pageins` from host_kv, pinned host memory laid out
+        [logical block][layer][K|V][kv head][row][D], into its slot of the cache."""
         n = len(pageins)
+        if n:
+            elt = 4 if d.dtype == 0 else 2
+            need = (max(b for b, _ in pageins) + 1) * d.layers * 2 * d.kv_heads * d.block_size * d.head_dim * elt
+            if host_kv.numel() * host_kv.element_size() < need:
+                raise ValueError(f"host_kv holds {host_kv.numel() * host_kv.element_size()} bytes, "
+                                 f"the listed blocks need {need}")
+        _need_cache(d, cache)
         arr = ctypes.c_int32 * max(1, n)
         _check(lib().kvc_pagein_issue(self._p, ctypes.byref(d), _ptr(cache), ctypes.c_void_p(host_kv.data_ptr()), n,
                                       arr(*[b for b, _ in pageins]), arr(*[s for _, s in pageins]),

@@ -374,3 +374,29 @@ def test_step_bytes_match_the_oracle_attended_sets(name):
     nb = bench.step_bytes(wl)
     assert nb["kv_logical"] == logical * row
     assert nb["kv_unique"] == (logical if wl.layout == "window" else len(cells)) * row
+
+
+def test_binding_refuses_buffers_smaller_than_the_descriptor(kvc):
+    """The library sees only addresses, so the binding checks sizes: a cache
+    tensor below kvc_cache_bytes, or a host page-in buffer too short for the
+    listed blocks, raises before anything is passed on."""
+    z = lambda n, dt=torch.bfloat16: torch.zeros(n, dtype=dt)
+    for dtype in ("f32", "bf16", "i8"):
+        d = _desc(kvc, dtype=dtype, window=104)
+        short = z(kvc.cache_bytes(d) - 1, torch.uint8).view(torch.uint8)
+        with pytest.raises(ValueError, match="cache holds"):
+            kvc.decode_step(d, short, 0, z(1), z(1), z(1), z(1, torch.int32), z(1, torch.uint8))
+        with pytest.raises(ValueError, match="cache holds"):
+            kvc.decode_attention(d, short, 0, z(1), z(1, torch.int32), z(1, torch.uint8))
+        with pytest.raises(ValueError, match="cache holds"):
+            kvc.append(d, short, 0, z(1), z(1), z(1, torch.int32), z(1, torch.uint8))
+        with pytest.raises(ValueError, match="cache holds"):
+            kvc.prefill(d, short, 0, z(1), z(1), z(1), z(1, torch.int32), z(1, torch.uint8))
+    dp = _desc(kvc, layout="paged", rope="baked", layers=2, block_size=16, num_blocks=8, max_blocks_per_seq=32)
+    with pytest.raises(ValueError, match="cache holds"):
+        kvc.block_prepare(dp, z(10), z(1, torch.int32), None, z(1, torch.uint8))
+    pg = kvc.Pager(8)
+    per_block = 2 * 2 * 2 * 16 * 128 * 2                # layers, K|V, kv heads, rows, D, bf16
+    with pytest.raises(ValueError, match="host_kv holds"):
+        pg.issue(dp, z(1), z(4 * per_block // 2 - 1), [(0, 1), (3, 2)], None)
+    pg.close()
