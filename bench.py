@@ -384,7 +384,7 @@ class ClockSampler:
 KERNEL_TRAFFIC = {"ring_bf16": 137679616, "sink_window_bf16": 543395584,
                   "paged_shared_prefix_bf16": 842048256, "long_context_pool_bf16": 156166144,
                   "ring_int8": 70007552}
-KERNEL_TRAFFIC_SOURCES = "fa195ecdf51faf141447ec522ba633984674ac83921e963d0d55c571ad9c8cc1"
+KERNEL_TRAFFIC_SOURCES = "24d6eacb67dbe03dc8e15f6823c3bd723a1a13f551c9d31eef08d159a6fe4904"
 
 
 # the sources decode_mma_kernel and its launch are built from

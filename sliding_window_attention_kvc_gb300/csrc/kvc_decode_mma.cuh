@@ -368,7 +368,7 @@ __device__ __forceinline__ void paged_partition(const DecodeParams& p, int b, lo
 
 // ---------------------------------------------------------------------------
 // Combine kernel for the stream-K decode: one CTA per (sequence, kv head,
-// q-head group, 32-column chunk).  out = sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)
+// q-head group, COLS-column chunk).  out = sum_i o_i 2^(m_i - M) / sum_i l_i 2^(m_i - M)
 // over the sequence's partials, M = max m_i; an empty attended set gives 0.
 // One warp per q head finds M and L; threads then split the partials into
 // groups (four loads in flight each) and reduce through shared memory.
