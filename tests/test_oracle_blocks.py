@@ -42,11 +42,11 @@ def visible(bm, pool, b, t):
     return out
 
 
-def test_worked_scenario_share_cow_release():
+def _worked_scenario(cls):
     # block size 4, pool of 8; sequence 0 writes 6 tokens, sequence 1 takes
     # its 6-token prefix (2 blocks), then both write token 6 into the shared,
     # partly filled second block
-    bm, pool = BlockManager(8, 4, batch=2, max_blocks=4), Pool(8, 4)
+    bm, pool = cls(8, 4, batch=2, max_blocks=4), Pool(8, 4)
     hist = [{}, {}]
     for t in range(6):
         step(bm, pool, hist, [t, -1], lambda b, p: 100 * b + p)
@@ -75,8 +75,12 @@ def test_worked_scenario_share_cow_release():
     assert not bm.valid.any()
 
 
-def test_new_block_only_at_a_block_start_and_exhaustion():
-    bm = BlockManager(2, 4, batch=3, max_blocks=2)
+def test_worked_scenario_share_cow_release():
+    _worked_scenario(BlockManager)
+
+
+def _new_block_rule(cls):
+    bm = cls(2, 4, batch=3, max_blocks=2)
     bm.prepare([0, 5, -1])
     assert bm.errors == [(1, blocks.ERR_UNMAPPED)] and bm.table[0, 0] == 1
     bm.prepare([4, 0, 0])
@@ -86,10 +90,14 @@ def test_new_block_only_at_a_block_start_and_exhaustion():
     assert bm.check_invariants()
 
 
-def test_three_sharers_two_copies():
+def test_new_block_only_at_a_block_start_and_exhaustion():
+    _new_block_rule(BlockManager)
+
+
+def _three_sharers(cls):
     # a block shared by 3 sequences, all three writing: the first two copy,
     # the third writes in place (count r - k seen by the k-th)
-    bm, pool = BlockManager(6, 4, batch=3, max_blocks=2), Pool(6, 4)
+    bm, pool = cls(6, 4, batch=3, max_blocks=2), Pool(6, 4)
     hist = [{}, {}, {}]
     for t in range(2):
         step(bm, pool, hist, [t, -1, -1], lambda b, p: p)
@@ -99,6 +107,10 @@ def test_three_sharers_two_copies():
     copies = bm.prepare([2, 2, 2], copy=pool.copy)
     assert [c[0] for c in copies] == [0, 1] and bm.table[2, 0] == 5
     assert bm.check_invariants()
+
+
+def test_three_sharers_two_copies():
+    _three_sharers(BlockManager)
 
 
 def _churn(bm, pool, rng, steps, do_cow=True, careful_release=True):
@@ -185,3 +197,79 @@ def test_planted_mistakes_are_caught(mistake):
         if caught:
             break
     assert caught
+
+
+# Mistakes planted in copies of the oracle (subclasses, on the CPU): each is a
+# plausible slip in the block manager, and each must fail one of the pins above.
+class _ShortCopy(BlockManager):            # copy-on-write brings one row too few
+    def prepare(self, positions, copy=None):
+        short = (lambda s, d, r: copy(s, d, max(r - 1, 0))) if copy else None
+        return super().prepare(positions, copy=short)
+
+
+class _CopyKeepsCount(BlockManager):       # the shared block's count not dropped after its copy
+    def prepare(self, positions, copy=None):
+        copies = super().prepare(positions, copy=copy)
+        for _, src, _, _ in copies:
+            self.ref[src] += 1
+        return copies
+
+
+class _FifoFreeList(BlockManager):         # free list taken from the bottom, not the top
+    def _take(self):
+        if not self.free:
+            return None
+        f = self.free.pop(0)
+        self.ref[f] = 1
+        self.valid[f] = True
+        return f
+
+
+class _MidBlockAllocation(BlockManager):   # a new block taken mid-block instead of an error
+    def prepare(self, positions, copy=None):
+        for b, t in enumerate(positions):
+            if t >= 0 and t // self.bs < self.table.shape[1] and self.table[b, t // self.bs] < 0 and t % self.bs:
+                f = self._take()
+                if f is not None:
+                    self.table[b, t // self.bs] = f
+        return super().prepare(positions, copy=copy)
+
+
+class _ShareWithoutCounts(BlockManager):   # prefix sharing maps blocks without raising counts
+    def share(self, src, dst, nblocks):
+        before = self.ref.copy()
+        super().share(src, dst, nblocks)
+        self.ref[:] = before
+
+
+class _ReleaseDescending(BlockManager):    # freed blocks pushed in descending id
+    def release(self, seqs):
+        n = len(self.free)
+        super().release(seqs)
+        self.free[n:] = sorted(self.free[n:], reverse=True)
+
+
+def _churn_catches(cls):
+    rng = np.random.default_rng(7)
+    bm, pool = cls(64, 4, batch=6, max_blocks=8), Pool(64, 4)
+    for t, hist in _churn(bm, pool, rng, 400):
+        if not bm.check_invariants():
+            return True
+        for b in range(len(t)):
+            if t[b] >= 0 and visible(bm, pool, b, t[b]) != {p: v for p, v in hist[b].items() if p <= t[b]}:
+                return True
+    return False
+
+
+@pytest.mark.parametrize("cls", [_ShortCopy, _CopyKeepsCount, _FifoFreeList, _MidBlockAllocation,
+                                 _ShareWithoutCounts, _ReleaseDescending], ids=lambda c: c.__name__.strip("_"))
+def test_planted_block_manager_mistakes_fail_a_pin(cls):
+    failed = []
+    for pin in (_worked_scenario, _new_block_rule, _three_sharers):
+        try:
+            pin(cls)
+        except AssertionError:
+            failed.append(pin.__name__)
+    if _churn_catches(cls):
+        failed.append("churn")
+    assert failed, cls.__name__
