@@ -154,7 +154,10 @@ def test_incache_positions_match_compacted_cache():
     assert check_incache(layouts.incache_position)
 
 
-def test_paged_attended_matches_pool_model():
+def check_paged(attended_fn) -> bool:
+    """The attended set of a paged sequence against the block-pool model
+    (mapped and resident blocks, positions up to t) on random tables with
+    unmapped entries and non-resident blocks."""
     rng = np.random.default_rng(0)
     bs, maxb, nb = 4, 6, 20
     for trial in range(20):
@@ -169,8 +172,14 @@ def test_paged_attended_matches_pool_model():
                 if table[b][p // bs] >= 0:
                     pool.append(b, None, None, p)
             for t in range(bs * maxb):
-                got = layouts.paged_attended(t, table[b], valid, bs)
-                assert list(got) == [e["position"] for e in pool.visible(b, t)]
+                got = attended_fn(t, table[b], valid, bs)
+                if list(got) != [e["position"] for e in pool.visible(b, t)]:
+                    return False
+    return True
+
+
+def test_paged_attended_matches_pool_model():
+    assert check_paged(layouts.paged_attended)
 
 
 # ---------------------------------------------------------------------------
@@ -219,16 +228,23 @@ def test_rope_scores_depend_only_on_distance():
 # storage rounding
 # ---------------------------------------------------------------------------
 
-def test_round_bf16_matches_torch_on_fp32_values():
+def check_round_bf16(round_fn) -> bool:
+    """Round-to-nearest-even to bf16: torch's fp32 -> bf16 conversion on fp32
+    values over 17 decades, and the tie cases written out."""
     rng = np.random.default_rng(3)
     x32 = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
     ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
-    assert np.array_equal(storage.round_bf16(x32.astype(np.float64)), ref)
+    ok = np.array_equal(round_fn(x32.astype(np.float64)), ref)
     # ties go to the even significand
-    assert storage.round_bf16(1 + 2.0 ** -8) == 1.0
-    assert storage.round_bf16(1 + 3 * 2.0 ** -8) == 1 + 2.0 ** -6
-    assert storage.round_bf16(-(1 + 2.0 ** -8)) == -1.0
-    assert storage.round_bf16(0.0) == 0.0
+    ok &= round_fn(1 + 2.0 ** -8) == 1.0
+    ok &= round_fn(1 + 3 * 2.0 ** -8) == 1 + 2.0 ** -6
+    ok &= round_fn(-(1 + 2.0 ** -8)) == -1.0
+    ok &= round_fn(0.0) == 0.0
+    return bool(ok)
+
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    assert check_round_bf16(storage.round_bf16)
 
 
 # ---------------------------------------------------------------------------
@@ -509,3 +525,37 @@ def test_planted_mistakes_fail_a_pin():
     assert not check_attention(no_scale)
     assert not check_attention(gqa_modulo)
     assert not check_attention(v_wrong_head)
+
+
+def test_planted_paged_and_rounding_mistakes_fail_a_pin():
+    # paged attended set: residency ignored, the whole block of t attended,
+    # unmapped entries read as physical block 0
+    def ignores_valid(t, row, valid, bs):
+        return layouts.paged_attended(t, row, np.ones_like(valid), bs)
+
+    def whole_last_block(t, row, valid, bs):
+        end = (t // bs + 1) * bs
+        return np.array([p for p in range(end) if row[p // bs] >= 0 and valid[row[p // bs]]], dtype=np.int64)
+
+    def unmapped_as_block0(t, row, valid, bs):
+        return layouts.paged_attended(t, np.where(np.asarray(row) < 0, 0, row), valid, bs)
+
+    for fn in (ignores_valid, whole_last_block, unmapped_as_block0):
+        assert not check_paged(fn), fn.__name__
+
+    # bf16 storage: truncation toward zero, ties away from zero
+    def bits(x):
+        return np.atleast_1d(np.asarray(x, dtype=np.float64)).astype(np.float32).view(np.uint32)
+
+    def from_bits(u, like):
+        out = (u & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+        return out if np.ndim(like) else float(out[0])
+
+    def truncate(x):
+        return from_bits(bits(x), x)
+
+    def ties_away(x):
+        return from_bits(bits(x) + np.uint32(0x8000), x)
+
+    for fn in (truncate, ties_away):
+        assert not check_round_bf16(fn), fn.__name__
