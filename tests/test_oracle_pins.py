@@ -559,3 +559,51 @@ def test_planted_paged_and_rounding_mistakes_fail_a_pin():
 
     for fn in (truncate, ties_away):
         assert not check_round_bf16(fn), fn.__name__
+
+
+def check_read_time(decode_fn) -> bool:
+    """[sink] "RoPE cache position shifting", written out: keep the compacting
+    StreamingLLM cache of (key, value) pairs, rotate each kept key at its index
+    in that cache and the query at the last index, and take fp64 SDPA. The
+    read-time decode over the same attended positions must match, before and
+    long after the cache first shifts (S = 0 and S = 4)."""
+    rng = np.random.default_rng(21)
+    D, n = 16, 60
+    K_all, V_all = rng.standard_normal((n, D)), rng.standard_normal((n, D))
+    q = rng.standard_normal((2, D))
+    ok = True
+    for S, W in ((4, 7), (0, 9)):
+        comp = layouts.StreamingKV(S, W)
+        for t in range(n):
+            comp.append(K_all[t], V_all[t], t)
+            kept = comp.visible()
+            Kr = rope.rotate(np.stack([e["key"] for e in kept]), np.arange(len(kept)))
+            V = np.stack([e["value"] for e in kept])
+            ref = _sdpa(rope.rotate(q, len(kept) - 1), Kr[:, None, :], V[:, None, :])
+            pos = np.array([e["position"] for e in kept])
+            got = decode_fn(q, K_all[pos], V_all[pos], pos, t, rope="read_time", storage="f32", sinks=S, window=W)
+            ok &= bool(np.allclose(got, ref, rtol=0, atol=1e-12))
+    return ok
+
+
+def test_read_time_rope_equals_attention_over_the_compacted_cache():
+    assert check_read_time(decode_reference)
+    # the layout-model route: one kv head, K and V [n, 1, D]
+    assert check_read_time(lambda q, K, V, pos, t, **kw: decode_sequence(q, K[:, None], V[:, None], pos, t, **kw))
+
+
+def test_planted_read_time_mistakes_fail_a_pin():
+    def q_at_absolute(q, K, V, positions, t, *, sinks, window, **kw):
+        # keys at their in-cache positions, the query left at t
+        ip = layouts.incache_position(positions, t, sinks, window)
+        out, _ = attend(rope.rotate(q, t), rope.rotate(K, ip), V, 1.0 / math.sqrt(q.shape[-1]))
+        return out
+
+    def keys_at_absolute(q, K, V, positions, t, *, sinks, window, **kw):
+        # the query at its in-cache position, keys left at their absolute positions
+        iq = int(layouts.incache_position(t, t, sinks, window))
+        out, _ = attend(rope.rotate(q, iq), rope.rotate(K, positions), V, 1.0 / math.sqrt(q.shape[-1]))
+        return out
+
+    for fn in (q_at_absolute, keys_at_absolute):
+        assert not check_read_time(fn), fn.__name__
