@@ -607,3 +607,47 @@ def test_planted_read_time_mistakes_fail_a_pin():
 
     for fn in (q_at_absolute, keys_at_absolute):
         assert not check_read_time(fn), fn.__name__
+
+
+def check_baked_shift_invariance(decode_fn) -> bool:
+    """Baked RoPE scores depend only on t - p ([primer] 4.5, [pool] rows
+    rotated at their absolute positions): moving every attended position and
+    t by the same offset leaves the output unchanged, and at distance 0 from
+    the query a key scores as without RoPE.  Tolerance 1e-6: keys are stored
+    as fp32 after rotation (relative rounding 2^-24), so the output moves by
+    ~3e-8 with the angles; a misplaced rotation moves it by O(1)."""
+    rng = np.random.default_rng(22)
+    D = 32
+    q = rng.standard_normal((3, D))
+    K, V = rng.standard_normal((9, D)), rng.standard_normal((9, D))
+    pos = np.array([0, 3, 4, 5, 9, 10, 11, 12, 13])
+    base = decode_fn(q, K, V, pos, 13, rope="baked", storage="f32")
+    ok = True
+    for shift in (1, 1000, 262131, 999986):
+        got = decode_fn(q, K, V, pos + shift, 13 + shift, rope="baked", storage="f32")
+        ok &= bool(np.allclose(got, base, rtol=0, atol=1e-6))
+    one = decode_fn(q, K[-1:], V[-1:], pos[-1:], 13, rope="baked", storage="f32")
+    ok &= bool(np.allclose(one, V[-1:].repeat(3, axis=0), rtol=0, atol=1e-12))   # a single key: its value
+    two = decode_fn(q, K[-2:], V[-2:], pos[-2:] + 500, 513, rope="baked", storage="f32")
+    ok &= bool(np.allclose(two, decode_fn(q, rope.rotate(K[-2:], [-1, 0]), V[-2:], pos[-2:], 13, rope="none",
+                                          storage="f32"), rtol=0, atol=1e-6))
+    return ok
+
+
+def test_baked_rope_depends_only_on_distance():
+    assert check_baked_shift_invariance(decode_reference)
+
+
+def test_planted_baked_mistakes_fail_a_pin():
+    def q_unrotated(q, K, V, positions, t, **kw):
+        out, _ = attend(np.asarray(q, dtype=np.float64), rope.rotate(K, positions), V, 1.0 / math.sqrt(q.shape[-1]))
+        return out if kw.get("rope") == "baked" else decode_reference(q, K, V, positions, t, **kw)
+
+    def keys_reversed(q, K, V, positions, t, **kw):
+        if kw.get("rope") != "baked":
+            return decode_reference(q, K, V, positions, t, **kw)
+        out, _ = attend(rope.rotate(q, t), rope.rotate(K, t - np.asarray(positions)), V, 1.0 / math.sqrt(q.shape[-1]))
+        return out
+
+    for fn in (q_unrotated, keys_reversed):
+        assert not check_baked_shift_invariance(fn), fn.__name__
