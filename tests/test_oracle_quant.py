@@ -104,6 +104,31 @@ def test_baked_keys_are_quantised_after_rotation():
     assert math.isclose(float(s[0]), float(np.abs(R.astype(np.float32)).max()) / 127, rel_tol=1e-6)
 
 
+def test_read_time_keys_are_quantised_before_rotation():
+    # read-time RoPE on an INT8 cache: the raw key is stored and the value read
+    # back (code * scale) is rotated at its in-cache position.  Integer rows
+    # holding +-127 are stored losslessly, so the INT8 result equals the
+    # unquantised one exactly, past the cache's first shift; quantising the
+    # rotated key instead (the baked rule) would not.
+    rng = np.random.default_rng(12)
+    S, W, t, D = 4, 7, 30, 16
+    pos = np.concatenate([np.arange(S), np.arange(t - W + 1, t + 1)])
+    K = rng.integers(-127, 128, size=(len(pos), D)).astype(np.float64)
+    V = rng.integers(-127, 128, size=(len(pos), D)).astype(np.float64)
+    K[:, 5] = -127
+    V[:, 2] = 127
+    q = rng.standard_normal((2, D)) * 0.05
+    spec = dict(rope="read_time", sinks=S, window=W)
+    want = attention.decode_reference(q, K, V, pos, t, storage="f32", **spec)
+    got = attention.decode_reference(q, quant.store_i8(K), quant.store_i8(V), pos, t, storage="i8", **spec)
+    assert (got == want).all()
+    from oracle.layouts import incache_position
+    from oracle.rope import rotate
+    ip = incache_position(pos, t, S, W)
+    rotated_then_stored = quant.store_i8(rotate(K, ip, 10000.0))
+    assert not np.allclose(rotated_then_stored, rotate(K, ip, 10000.0), rtol=0, atol=1e-6)
+
+
 @pytest.mark.parametrize("D", [128, 256])
 def test_store_i8_matches_quantize_then_dequantize(D):
     rng = np.random.default_rng(D)
