@@ -69,3 +69,18 @@ def test_scripts_import_the_oracle_only_in_their_cpu_legs():
         uses = [fn for m, fn in _imports(os.path.join(ROOT, name)) if m in ("oracle", "tests")]
         assert uses, name
         assert set(uses) <= fns, (name, uses)
+
+
+def test_generators_hold_none_of_the_methods_arithmetic():
+    """kvc_synth draws seeded values and positions only: no rotation,
+    exponential, square root, quantisation or contraction appears in it."""
+    import re
+    banned = re.compile(r"\b(exp2?|cos|sin|sqrt|softmax|rint|clip|clamp|einsum|matmul|rotate|quantize\w*)\s*\("
+                        r"|\b127\b|[\w\)\]]\s*@\s*[\w\(]")
+    for path in _py("kvc_synth"):
+        with open(path) as f:
+            for n, line in enumerate(f, 1):
+                code = line.split("#", 1)[0]
+                if code.strip().startswith(("\"", "'")) or not code.strip():
+                    continue
+                assert not banned.search(code), f"{os.path.basename(path)}:{n}: {line.strip()}"
